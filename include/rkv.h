@@ -1,0 +1,221 @@
+/*
+ * rkv.h -- C ABI of librkv, a GB300 (sm_103a) implementation of RocketKV's
+ * decode-time hot path: stage-1 SnapKV++ eviction at prefill and stage-2 Hybrid
+ * Sparse Attention (HSA) at every decode step.
+ *
+ * Sources, cited by short name:
+ *   [summary]  "RocketKV: Accelerating Long-Context LLM Inference via Two-Stage
+ *              KV Cache Compression", research-map summary, sections Problem,
+ *              Approach, Key results.
+ *   [abstract] the same paper's abstract (arXiv 2502.14051).
+ *   [adapted]  "RocketKV-adapted -- Two-Stage Compression (SnapKV Eviction +
+ *              Hybrid Sparse Attention)", VeloxQuant-MLX docs, sections "Where
+ *              it sits -- the mechanism gap", "The one setting worth tuning:
+ *              rocketkv_compression_ratio", "Adaptation notes", "Evidence".
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers, 16-byte aligned, owned by
+ *     the caller.  The library never allocates or frees device memory and keeps no
+ *     per-cache state; scratch lives in a caller-provided workspace.
+ *   - Pointers marked "host" are read during the call only.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and returns without synchronising, except rkv_get_device_status.
+ *   - Arguments are validated on the host before anything is enqueued; a failed
+ *     check returns RKV_ERR_INVALID_ARG / RKV_ERR_UNSUPPORTED / RKV_ERR_WORKSPACE
+ *     with no side effect and a message in rkv_last_error().
+ *   - A failed kernel launch returns RKV_ERR_CUDA.
+ *   - Errors found on the device (a page id out of range, a sequence longer than
+ *     its pages, a bounded wait that ran out) are OR-ed into cache->error_word as
+ *     RKV_DEVERR_* bits; the kernel skips the offending access and carries on.
+ *     rkv_get_device_status reads and clears the word.
+ *   - head_dim must be 128; page_size 16, 32 or 64; Hq a multiple of Hkv with
+ *     G = Hq / Hkv in {1, 2, 4, 8}.
+ *   - bf16 data is passed as IEEE bfloat16 bit patterns (rkv_bf16).
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t rkv_bf16;
+
+typedef enum {
+  RKV_OK = 0,
+  RKV_ERR_INVALID_ARG = 1,
+  RKV_ERR_UNSUPPORTED = 2,
+  RKV_ERR_WORKSPACE = 3,
+  RKV_ERR_CUDA = 4,
+  RKV_ERR_DEVICE_DATA = 5,
+  RKV_ERR_TIMEOUT = 6
+} rkv_status;
+
+/* bits of cache->error_word */
+#define RKV_DEVERR_PAGE_ID   0x1  /* page_table entry outside [0, num_phys_pages) */
+#define RKV_DEVERR_CAPACITY  0x2  /* seq_len (+ appended tokens) beyond max_pages * page_size */
+#define RKV_DEVERR_TIMEOUT   0x4  /* a bounded wait on an mbarrier ran out */
+
+#define RKV_HEAD_DIM 128
+#define RKV_MAX_BATCH 256
+
+/* Result of the adaptive ratio split. */
+typedef struct {
+  double c;          /* overall ratio prompt_len / budget */
+  double r;          /* stage-1 share of log c */
+  double c1;         /* stage-1 (eviction) ratio c^r */
+  double c2;         /* stage-2 (HSA) ratio c^(1-r) */
+  int32_t keep1;     /* stage-1 survivors per KV head, window included */
+  int32_t k1;        /* HSA channels per KV head */
+  int32_t k2;        /* HSA pages per KV head per step */
+  int32_t pool_kernel; /* default stage-1 max-pool kernel for this prompt length */
+} rkv_split;
+
+/*
+ * The compressed, paged KV cache of one attention layer (all device memory,
+ * caller-owned).
+ *   k_pages, v_pages : [num_phys_pages][Hkv][page_size][head_dim] bf16.  Token i of
+ *                      sequence b sits in physical page page_table[b][i / page_size],
+ *                      slot i % page_size.  Survivors are stored in ascending
+ *                      original position, decode tokens after them.
+ *   page_table       : [B][max_pages] int32 physical page ids.
+ *   seq_len          : [B] int32, current compressed length n of each sequence.
+ *   kmax, kmin       : [B][Hkv][head_dim][max_pages] bf16, channel-major paged
+ *                      element-wise max / min of the keys ([adapted], "Where it
+ *                      sits": Quest-style paged max/min summaries).  Only pages
+ *                      below ceil(n / page_size) are meaningful.
+ *   error_word       : one device int32 receiving RKV_DEVERR_* bits.
+ * max_pages must be a multiple of 8.
+ */
+typedef struct {
+  rkv_bf16* k_pages;
+  rkv_bf16* v_pages;
+  int32_t* page_table;
+  int32_t* seq_len;
+  rkv_bf16* kmax;
+  rkv_bf16* kmin;
+  int32_t* error_word;
+  int32_t B, Hkv, head_dim, page_size, max_pages, num_phys_pages;
+} rkv_cache;
+
+/*
+ * Adaptive split of the overall ratio c = prompt_len / budget between the stages
+ * ([adapted], "The one setting worth tuning"): r = clip(0.2 + 0.06*log2(c), 0.2,
+ * 0.8), stage 1 compresses by c^r and stage 2 by c^(1-r) (c = 64 -> 10.3x / 6.2x).
+ * Sizes (readings; the pages leave them open): keep1 = round(prompt_len / c^r)
+ * clamped to [max(budget, window), prompt_len]; k2 = budget / page_size;
+ * k1 = 16*round(head_dim / (16*sqrt(c2))) in [16, head_dim] unless k1_override > 0;
+ * pool_kernel = 7 / 31 / 63 for prompts up to 8K / 48K / longer.
+ * Host only.  Returns RKV_ERR_INVALID_ARG for non-positive sizes or out == NULL.
+ */
+rkv_status rkv_split_ratio(int32_t prompt_len, int32_t budget, int32_t head_dim,
+                           int32_t page_size, int32_t window, int32_t k1_override,
+                           rkv_split* out);
+
+/* Bytes of workspace rkv_prefill_evict needs for these sizes. */
+size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t window,
+                                  int32_t max_prompt_len);
+
+/*
+ * Stage 1, SnapKV++ eviction ([abstract]; [summary], Approach: SnapKV with a
+ * large pooling kernel and GQA-group-level selection).  Per sequence b and KV
+ * head g:
+ *   S[t]  = sum over the G query heads of group g and the w window rows j of
+ *           softmax(q_win . k^T * scale)[j, t], row j (prompt position L-w+j)
+ *           normalised over the keys t <= L-w+j; scored for t < L-w;
+ *   S'    = centred max-pool of S with kernel pool_kernel[b] (out-of-range
+ *           positions ignored);
+ *   kept  = the top keep1[b]-w positions by (S' desc, position asc) plus the w
+ *           window positions, ascending;
+ * then the kept tokens' K and V are written into the cache pages (positions
+ * 0..keep1-1), their Kmax/Kmin summaries are built and seq_len[b] = keep1[b].
+ *   q_win  : device [B][Hq][window][128] bf16, the last `window` queries.
+ *   k, v   : device [B][Hkv][max_prompt_len][128] bf16; rows >= prompt_len[b]
+ *            are never read.
+ *   prompt_len, keep1, pool_kernel : host [B]; window <= keep1[b] <= prompt_len[b]
+ *            <= max_prompt_len; pool_kernel odd in [1, 255]; G * window <= 128.
+ *   scale  : softmax scale (1/sqrt(128) for the standard one).
+ *   cache  : destination; its pages must hold keep1[b] tokens of every sequence.
+ *   kept_idx : device [B][Hkv][kept_stride] int32, receives the kept positions.
+ *   pooled_scores : device [B][Hkv][max_prompt_len] fp32 receiving S' for
+ *            t < L-w, or NULL.
+ */
+rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv_bf16* v,
+                             int32_t B, int32_t Hq, int32_t window, int32_t max_prompt_len,
+                             const int32_t* prompt_len, const int32_t* keep1,
+                             const int32_t* pool_kernel, float scale,
+                             const rkv_cache* cache, int32_t* kept_idx, int32_t kept_stride,
+                             float* pooled_scores, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * Append n_new tokens to every sequence and bring the page summaries up to date
+ * ([adapted], "Evidence": the incremental update equals a rebuild, bit for bit).
+ * For each b the tokens go to positions [seq_len[b], seq_len[b] + n_new): when
+ * k_new is not NULL they are first copied from k_new / v_new (device
+ * [B][Hkv][n_new][128] bf16) into their page slots, otherwise they must already
+ * be there.  Every touched page's Kmax/Kmin is recomputed from its valid tokens,
+ * then seq_len[b] += n_new.  With seq_len = 0 and n_new = n this is a full
+ * rebuild.  A sequence that would outgrow its pages is left unchanged and flags
+ * RKV_DEVERR_CAPACITY.
+ */
+rkv_status rkv_append_page_summary(const rkv_cache* cache, const rkv_bf16* k_new,
+                                   const rkv_bf16* v_new, int32_t n_new, void* stream);
+
+/* Bytes of workspace rkv_decode_hsa needs. */
+size_t rkv_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_pages);
+
+/*
+ * Stage 2, one Hybrid Sparse Attention step over the current cache ([adapted],
+ * "Where it sits" and "Adaptation notes"; [abstract]).  Per sequence b and KV
+ * head g, with n = seq_len[b] and NP = ceil(n / page_size):
+ *   1. channels S = top-k1[b] of a_i = sum over the group's heads of |q_h,i|
+ *      (ties: lower channel);
+ *   2. page bound s_p = sum_h sum_{i in S} max(q_h,i*Kmax_i,p, q_h,i*Kmin_i,p);
+ *   3. pages = top-min(k2[b], NP) by (s_p desc, page asc);
+ *   4. out_h = softmax(q_h . k_t * scale) . v_t over all 128 channels of every
+ *      valid token t < n of the selected pages, for each head h of the group.
+ *   q            : device [B][Hq][128] bf16 decode queries.
+ *   k1, k2       : host [B]; 1 <= k1 <= 128, k2 >= 1.
+ *   out          : device [B][Hq][128] fp32.
+ *   sel_channels : device [B][Hkv][128] int32 or NULL; receives the channel set,
+ *                  ascending, in the first k1[b] entries.
+ *   sel_pages    : device [B][Hkv][sel_pages_stride] int32 or NULL; receives the
+ *                  page set, ascending, in the first min(k2[b], NP) entries and -1
+ *                  in the next entry if there is room.
+ */
+rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
+                          const int32_t* k1, const int32_t* k2, float scale, float* out,
+                          int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, read and clear cache->error_word.  RKV_OK when it was 0,
+ * RKV_ERR_TIMEOUT when the timeout bit was set, else RKV_ERR_DEVICE_DATA; *bits
+ * (if not NULL) receives the raw word. */
+rkv_status rkv_get_device_status(const rkv_cache* cache, void* stream, int32_t* bits);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* rkv_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+int64_t rkv_launch_count(void);
+
+/*
+ * Per-kernel timing for measurement.  While enabled, every kernel launch is
+ * bracketed by CUDA events recorded on its own stream.  rkv_profile_read
+ * synchronises those events and returns, for kernel kind `kind`, the number of
+ * launches and their summed device time (ms) since the last reset; it returns
+ * the kind's name, or NULL past the last kind.
+ */
+void rkv_profile_enable(int32_t enable);
+void rkv_profile_reset(void);
+const char* rkv_profile_read(int32_t kind, int64_t* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RKV_H */

@@ -1,0 +1,339 @@
+"""Plain CPU oracle for the RocketKV decode-time hot path (test infrastructure only).
+
+This module is the slow, obviously-correct statement of what the CUDA library
+computes.  It is TEST INFRASTRUCTURE: only the tests, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or
+call it.  The CUDA product path never imports it and shares no code with it.
+
+Everything here is numpy in float64.  bf16 inputs arrive already widened to
+float64 (the widening is exact), so every step below works on the exact input
+values.  No step is blocked, fused or reordered beyond what the definition
+states; library routines (matmul, sort, exp) serve as single steps.
+
+Sources (cited by short name below):
+
+* [summary]  "RocketKV: Accelerating Long-Context LLM Inference via Two-Stage KV
+  Cache Compression", research-map summary (atlas.scime.ai), sections
+  Problem / Approach / Key results.
+* [abstract] the same paper's abstract (papers.pytorch.kr, arXiv 2502.14051).
+* [adapted]  "RocketKV-adapted -- Two-Stage Compression (SnapKV Eviction +
+  Hybrid Sparse Attention)", VeloxQuant-MLX docs, sections "The problem this
+  solves", "Where it sits -- the mechanism gap", "The one setting worth tuning:
+  rocketkv_compression_ratio", "Adaptation notes", "Evidence".
+
+Where the pages leave a step open the plainest reading is taken; each such
+reading is marked READING below and listed in the design doc.
+
+Parity status per function (what pins it, in tests/test_oracle_pins.py):
+  split_ratio ............ worked example c=64 -> 10.3x / 6.2x, clip ends, c1*c2=c
+  window_column_scores ... row-sum invariant, zero-query closed form,
+                           causal decomposition, pure-Python brute force
+  max_pool ............... scipy.ndimage.maximum_filter1d
+  select_kept ............ single-query special case == top-k of raw logits
+  page_summaries ......... append == rebuild, membership + bound properties
+  channel_select ......... top-k property with planted ties
+  page_scores ............ per-token bound (brute force), P=1 closed form
+  topk_pages ............. top-k property with planted ties
+  sparse_attention ....... k1=d, k2=all pages == torch SDPA (library)
+  default_pool_kernel .... PARITY UNPINNED (the pages give no rule)
+  derived k1 in split .... PARITY UNPINNED (the pages give no rule)
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "split_ratio",
+    "default_pool_kernel",
+    "window_column_scores",
+    "window_scores",
+    "max_pool",
+    "select_kept",
+    "prefill_evict_unit",
+    "page_summaries",
+    "append_summaries",
+    "channel_select",
+    "page_scores",
+    "topk_pages",
+    "sparse_attention",
+    "hsa_decode_unit",
+]
+
+
+# --------------------------------------------------------------------------
+# a1: adaptive split of the compression ratio
+# --------------------------------------------------------------------------
+def default_pool_kernel(prompt_len: int) -> int:
+    """Default stage-1 pooling kernel size.
+
+    [abstract] says SnapKV++ uses an "adaptive pooling size"; [summary, Approach]
+    says "large pooling kernel".  Neither gives the rule.  READING: the kernel
+    grows with prompt length, 7 up to 8K tokens, 31 up to 48K, 63 beyond.  This
+    reproduces the three sizes the workloads fix (4K->7, 32K->31, 109K->63).
+    PARITY UNPINNED.
+    """
+    if prompt_len <= 8192:
+        return 7
+    if prompt_len <= 49152:
+        return 31
+    return 63
+
+
+def split_ratio(prompt_len: int, budget: int, head_dim: int, page_size: int,
+                window: int, k1_override: int = 0) -> dict:
+    """Split the overall ratio c between the two stages.
+
+    [adapted, "The one setting worth tuning"]: r = clip(0.2 + 0.06*log2(c), 0.2,
+    0.8); stage 1 compresses by c**r and stage 2 by c**(1-r); c=64 gives 10.3x and
+    6.2x.  c is the prompt length over the token budget.
+
+    READINGS (the pages do not say how the stage ratios become sizes):
+      keep1 = round(L / c1), clamped to [max(budget, window), L]  (stage-1 survivors
+              including the observation window);
+      k2    = budget // page_size (pages attended per step, so k2*P = budget);
+      k1    = 16*round(d / (16*sqrt(c2))) clamped to [16, d]: stage 2's ratio is split
+              evenly between the head and sequence dimensions (PARITY UNPINNED);
+              k1_override replaces it ([adapted] exposes rocketkv_head_topk1).
+    """
+    c = prompt_len / budget
+    r = 0.2 + 0.06 * math.log2(c)
+    r = min(max(r, 0.2), 0.8)
+    c1 = c ** r
+    c2 = c ** (1.0 - r)
+    keep1 = int(math.floor(prompt_len / c1 + 0.5))
+    keep1 = min(max(keep1, budget, window), prompt_len)
+    if k1_override > 0:
+        k1 = int(k1_override)
+    else:
+        k1 = 16 * int(math.floor(head_dim / (16.0 * math.sqrt(c2)) + 0.5))
+        k1 = min(max(k1, 16), head_dim)
+    k2 = max(1, budget // page_size)
+    return dict(c=c, r=r, c1=c1, c2=c2, keep1=keep1, k1=k1, k2=k2,
+                pool_kernel=default_pool_kernel(prompt_len))
+
+
+# --------------------------------------------------------------------------
+# a2-a5: stage 1, SnapKV++ eviction at prefill (one sequence)
+# --------------------------------------------------------------------------
+def window_column_scores(q_win: np.ndarray, k: np.ndarray, scale: float | None = None) -> np.ndarray:
+    """Column sums of the observation window's attention weights, per KV head.
+
+    q_win: [Hq, w, d] queries at prompt positions L-w .. L-1.
+    k:     [Hkv, L, d] prompt keys.
+    Returns A: [Hkv, L] with A[g, t] = sum over query heads h of group g and window
+    rows j of softmax_t(q[h, j] . k[g, t] * scale), the softmax taken over the keys
+    row j may see.
+
+    [abstract]: SnapKV++ scores the input tokens with full GQA compatibility;
+    [summary, Approach]: selection is GQA-group-level; [adapted, "The one setting
+    worth tuning"] calls it exact-attention selection.
+    READINGS: the score is the softmax attention weight with scale 1/sqrt(d); row j
+    (position L-w+j) sees keys t <= L-w+j (causal) and is normalised over exactly
+    those; query head h belongs to KV head h // (Hq/Hkv); the group's heads and
+    rows are summed.
+    """
+    Hq, w, d = q_win.shape
+    Hkv, L, _ = k.shape
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pos = (L - w) + np.arange(w)                       # query positions
+    visible = np.arange(L)[None, :] <= pos[:, None]    # [w, L]
+    A = np.zeros((Hkv, L), dtype=np.float64)
+    for h in range(Hq):
+        g = h // G
+        z = (q_win[h] @ k[g].T) * scale                # [w, L] logits
+        z = np.where(visible, z, -np.inf)
+        z = z - z.max(axis=1, keepdims=True)
+        e = np.exp(z)                                  # masked entries -> 0
+        p = e / e.sum(axis=1, keepdims=True)
+        A[g] += p.sum(axis=0)
+    return A
+
+
+def window_scores(q_win: np.ndarray, k: np.ndarray, scale: float | None = None) -> np.ndarray:
+    """Stage-1 score S[g, t] of each prefix token t < L - w (the window is always kept)."""
+    w = q_win.shape[1]
+    L = k.shape[1]
+    return window_column_scores(q_win, k, scale)[:, : L - w]
+
+
+def max_pool(S: np.ndarray, kernel: int) -> np.ndarray:
+    """1-D max pooling along the sequence, stride 1, centred, odd kernel.
+
+    [summary, Approach]: SnapKV with a large pooling kernel.  READING: max pooling;
+    positions outside [0, len) are ignored (padding never wins).
+    S: [..., n].  Returns the same shape.
+    """
+    assert kernel % 2 == 1 and kernel >= 1
+    half = kernel // 2
+    n = S.shape[-1]
+    out = S.copy()
+    for s in range(1, min(half, n - 1) + 1):
+        # neighbour on the right: out[t] vs S[t+s]
+        out[..., : n - s] = np.maximum(out[..., : n - s], S[..., s:])
+        # neighbour on the left: out[t] vs S[t-s]
+        out[..., s:] = np.maximum(out[..., s:], S[..., : n - s])
+    return out
+
+
+def select_kept(S_pooled: np.ndarray, keep1: int, prompt_len: int, window: int) -> np.ndarray:
+    """Kept prompt positions for one KV head, ascending.
+
+    The top (keep1 - w) prefix positions by (pooled score desc, position asc),
+    plus the w window positions.  [adapted, "The problem this solves"]: stage 1
+    keeps only a small surviving set and evicts the rest permanently ([summary,
+    Problem]).  READING: keep1 counts the window; ties go to the lower position.
+    """
+    n_prefix = prompt_len - window
+    n_pick = keep1 - window
+    assert S_pooled.shape == (n_prefix,)
+    assert 0 <= n_pick <= n_prefix
+    order = np.lexsort((np.arange(n_prefix), -S_pooled))   # primary: -score, then index
+    picked = np.sort(order[:n_pick])
+    return np.concatenate([picked, np.arange(n_prefix, prompt_len)]).astype(np.int64)
+
+
+def prefill_evict_unit(q_win: np.ndarray, k: np.ndarray, keep1: int, pool_kernel: int,
+                       scale: float | None = None) -> dict:
+    """Stage 1 for one sequence: scores, pooled scores and kept positions per KV head.
+
+    q_win [Hq, w, d], k [Hkv, L, d].  Returns dict(scores [Hkv, L-w],
+    pooled [Hkv, L-w], kept [Hkv, keep1]).
+    """
+    w = q_win.shape[1]
+    Hkv, L, _ = k.shape
+    S = window_scores(q_win, k, scale)
+    Sp = max_pool(S, pool_kernel)
+    kept = np.stack([select_kept(Sp[g], keep1, L, w) for g in range(Hkv)])
+    return dict(scores=S, pooled=Sp, kept=kept)
+
+
+# --------------------------------------------------------------------------
+# a6: paged element-wise Kmax / Kmin summaries
+# --------------------------------------------------------------------------
+def page_summaries(Kc: np.ndarray, n: int, page_size: int) -> tuple[np.ndarray, np.ndarray]:
+    """Kmax, Kmin of every page of one head's compressed keys.
+
+    [adapted, "Where it sits -- the mechanism gap"]: Quest-style paged element-wise
+    max/min summaries along the sequence dimension.  READING: a page holds
+    page_size consecutive compressed tokens; a partial last page summarises only
+    its valid tokens.
+    Kc: [>= n, d].  Returns (kmax, kmin), each [d, ceil(n / P)] (channel-major).
+    """
+    d = Kc.shape[1]
+    NP = -(-n // page_size)
+    kmax = np.empty((d, NP))
+    kmin = np.empty((d, NP))
+    for p in range(NP):
+        tok = Kc[p * page_size: min(n, (p + 1) * page_size)]
+        kmax[:, p] = tok.max(axis=0)
+        kmin[:, p] = tok.min(axis=0)
+    return kmax, kmin
+
+
+def append_summaries(kmax: np.ndarray, kmin: np.ndarray, Kc: np.ndarray, n_old: int,
+                     n_new: int, page_size: int) -> tuple[np.ndarray, np.ndarray]:
+    """Incremental update after tokens [n_old, n_old + n_new) were appended.
+
+    [adapted, "Evidence"]: the incremental update must equal a rebuild from
+    scratch.  The oracle recomputes every touched page from its tokens.
+    """
+    n = n_old + n_new
+    NP = -(-n // page_size)
+    d = Kc.shape[1]
+    out_max = np.empty((d, NP))
+    out_min = np.empty((d, NP))
+    first_touched = n_old // page_size
+    out_max[:, :first_touched] = kmax[:, :first_touched]
+    out_min[:, :first_touched] = kmin[:, :first_touched]
+    for p in range(first_touched, NP):
+        tok = Kc[p * page_size: min(n, (p + 1) * page_size)]
+        out_max[:, p] = tok.max(axis=0)
+        out_min[:, p] = tok.min(axis=0)
+    return out_max, out_min
+
+
+# --------------------------------------------------------------------------
+# a7-a10: stage 2, Hybrid Sparse Attention at one decode step (one KV head)
+# --------------------------------------------------------------------------
+def channel_select(q_group: np.ndarray, k1: int) -> tuple[np.ndarray, np.ndarray]:
+    """Top-k1 channels by |q| summed over the GQA group.
+
+    [adapted, "Where it sits"]: SparQ-style top-magnitude channel selection along
+    the head dimension.  READING: one channel set per KV head from
+    a_i = sum_h |q[h, i]|; ties go to the lower channel.
+    q_group: [G, d].  Returns (channels ascending [k1], a [d]).
+    """
+    d = q_group.shape[1]
+    a = np.abs(q_group).sum(axis=0)
+    order = np.lexsort((np.arange(d), -a))
+    return np.sort(order[:k1]), a
+
+
+def page_scores(q_group: np.ndarray, kmax: np.ndarray, kmin: np.ndarray,
+                channels: np.ndarray, per_head: bool = False) -> np.ndarray:
+    """Page score bound over the selected channels.
+
+    s_page = sum over i in S of max(q_i * Kmax_i, q_i * Kmin_i), an upper bound on
+    every token's partial dot product in the page ([adapted, "Where it sits" and
+    "Evidence"]).  READING for GQA: the group's per-head bounds are summed.
+    q_group [G, d]; kmax/kmin [d, NP].  Returns [NP] (or [G, NP] if per_head).
+    """
+    qs = q_group[:, channels]                  # [G, k1]
+    hi = kmax[channels, :]                     # [k1, NP]
+    lo = kmin[channels, :]
+    terms = np.maximum(qs[:, :, None] * hi[None, :, :], qs[:, :, None] * lo[None, :, :])
+    per = terms.sum(axis=1)                    # [G, NP]
+    return per if per_head else per.sum(axis=0)
+
+
+def topk_pages(scores: np.ndarray, k2: int) -> np.ndarray:
+    """Top-k2 pages by (score desc, page asc); every page when there are <= k2.
+
+    [adapted, "Adaptation notes"]: the selection takes whole pages, k2 of them.
+    Returns page indices ascending.
+    """
+    NP = scores.shape[0]
+    k = min(k2, NP)
+    order = np.lexsort((np.arange(NP), -scores))
+    return np.sort(order[:k])
+
+
+def sparse_attention(q_group: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, n: int,
+                     pages: np.ndarray, page_size: int, scale: float | None = None) -> np.ndarray:
+    """Exact softmax attention over every channel of the selected pages' tokens.
+
+    [abstract]: the second stage is fine-grain top-k sparse attention; [adapted,
+    "Adaptation notes"]: a selected page contributes all its tokens.  Tokens at or
+    beyond n (the unfilled tail of the last page) are not part of the sequence.
+    q_group [G, d]; Kc, Vc [>= n, d].  Returns [G, d].
+    """
+    d = q_group.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    tok = np.concatenate([np.arange(p * page_size, (p + 1) * page_size) for p in pages])
+    tok = tok[tok < n]
+    z = (q_group @ Kc[tok].T) * scale          # [G, ntok]
+    z = z - z.max(axis=1, keepdims=True)
+    e = np.exp(z)
+    p = e / e.sum(axis=1, keepdims=True)
+    return p @ Vc[tok]
+
+
+def hsa_decode_unit(q_group: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, n: int,
+                    kmax: np.ndarray, kmin: np.ndarray, page_size: int, k1: int, k2: int,
+                    scale: float | None = None, pages_override: np.ndarray | None = None) -> dict:
+    """One HSA decode step for one KV head (steps 1-4 of stage 2, in order).
+
+    pages_override replaces the oracle's own page choice in step 4 (used when the
+    two sides legitimately pick different pages at a tie).
+    """
+    chans, a = channel_select(q_group, k1)
+    sig = page_scores(q_group, kmax, kmin, chans)
+    pages = topk_pages(sig, k2)
+    use = pages if pages_override is None else np.asarray(pages_override)
+    out = sparse_attention(q_group, Kc, Vc, n, use, page_size, scale)
+    return dict(channels=chans, channel_score=a, page_score=sig, pages=pages, out=out)
