@@ -1,0 +1,515 @@
+#!/usr/bin/env python
+"""Benchmark of the RocketKV decode-time hot path on one GB300 (or N, one per rank).
+
+One bench step is one pass of the whole hot path over one request of the
+workload: the adaptive split, stage-1 SnapKV++ eviction of the prompt
+(rkv_prefill_evict, which also builds the page summaries), then every decode step
+(rkv_append_page_summary of the new token + rkv_decode_hsa).  Inputs are seeded,
+synthetic and resident in HBM before timing.  L2 is flushed (a 256 MB write)
+before the prefill and before every decode step, outside the timed intervals:
+each timed interval starts with a cold L2, as a layer of a full model would.
+
+The metric is decode steps per second per layer over the whole job, prefill time
+included: decode_steps * K / sum(pass time).  Each pass's prefill and decode
+steps run as CUDA graphs (one per decode step) timed with CUDA events on the
+launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2]
+    python bench.py --impl reference     # the CPU oracle, timed on this host
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from two_stage_kv_snapkv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "HSA decode steps/s per layer & achieved HBM GB/s vs GB300 peak; prefill evict ms"
+UNIT = "decode steps/s per layer"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, help="1..5 (2: Llama3.1-8B layer, 32K prompt)")
+    ap.add_argument("--seed", type=int, default=0x5EED)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-decode-steps", type=int, default=16)
+    ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- peaks / clocks
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(hbm_gbs=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], samples=0)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit()) if rows else None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=smax, reasons=reasons,
+                    samples=len(rows))
+
+
+# --------------------------------------------------------------------------- workload setup
+class Setup:
+    """Everything one rank needs for K passes of one workload (layer 0)."""
+
+    def __init__(self, wl: W.Workload, rkv, seed: int, dev):
+        self.wl, self.rkv, self.dev = wl, rkv, dev
+        self.inp = W.prefill_tensors(wl, seed, 0, dev, tail="zero")
+        self.dec = [W.decode_tensors(wl, t, seed, 0, dev) for t in range(wl.steps)]
+        for d in self.dec:
+            d["k_new"] = d["k_new"].unsqueeze(2).contiguous()
+            d["v_new"] = d["v_new"].unsqueeze(2).contiguous()
+        self.splits = []
+        for L in wl.prompt_lens:
+            s = rkv.rkv_split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0)
+            if wl.pool_kernel:
+                s["pool_kernel"] = wl.pool_kernel
+            self.splits.append(s)
+        self.keep1 = [s["keep1"] for s in self.splits]
+        self.k1 = [s["k1"] for s in self.splits]
+        self.k2 = [s["k2"] for s in self.splits]
+        self.kp = [s["pool_kernel"] for s in self.splits]
+        P = wl.page_size
+        max_pages = (max(self.keep1) + wl.steps + P - 1) // P
+        max_pages = (max_pages + 7) // 8 * 8
+        pt = W.page_table(wl.B, max_pages, seed, dev)
+        self.cache = rkv.PagedCache(wl.B, wl.Hkv, P, max_pages, dev, page_table=pt)
+        self.kept = torch.empty((wl.B, wl.Hkv, max(self.keep1)), dtype=torch.int32, device=dev)
+        self.pws = rkv.prefill_workspace(wl.B, wl.Hq, wl.Hkv, wl.window, wl.Lmax, dev)
+        self.dws = rkv.decode_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, dev)
+        self.out = torch.empty((wl.steps, wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    # one call each, on the current stream
+    def prefill(self):
+        i = self.inp
+        self.rkv.rkv_prefill_evict(i["q_win"], i["k"], i["v"], i["prompt_len"], self.keep1, self.kp, self.cache,
+                                   self.kept, workspace=self.pws)
+
+    def decode(self, t: int):
+        d = self.dec[t]
+        self.rkv.rkv_append_page_summary(self.cache, d["k_new"], d["v_new"], 1)
+        self.rkv.rkv_decode_hsa(self.cache, d["q"], self.k1, self.k2, self.out[t], workspace=self.dws)
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    # ------------------------------------------------------------ byte accounting
+    def decode_bytes(self, t: int) -> dict:
+        """Compulsory HBM bytes of decode step t, by kernel (the method must move these)."""
+        wl = self.wl
+        P = wl.page_size
+        summ = kv = 0
+        for b in range(wl.B):
+            n = self.keep1[b] + t + 1
+            NP = -(-n // P)
+            summ += wl.Hkv * 2 * self.k1[b] * NP * 2
+            kv += wl.Hkv * min(self.k2[b], NP) * P * 128 * 2 * 2
+        q = wl.B * wl.Hq * 128 * 2
+        out = wl.B * wl.Hq * 128 * 4
+        append = wl.B * wl.Hkv * (128 * 2 * 2 * 2 + 128 * 2 * 2 * 2)   # new k,v read+write, summaries
+        return dict(hsa_score=summ + q, hsa_attend=kv + q + out, append_small=append,
+                    step_total=summ + kv + q + out + append)
+
+    def prefill_bytes(self) -> dict:
+        wl = self.wl
+        kbytes = sum(wl.Hkv * L * 128 * 2 for L in wl.prompt_lens)
+        surv = sum(wl.Hkv * k * 128 * 2 * 2 * 2 for k in self.keep1)   # K+V read and written
+        return dict(snap_stats=kbytes, snap_colsum=kbytes, snap_compact=surv, total=2 * kbytes + surv)
+
+
+def capture(fn, stream) -> torch.cuda.CUDAGraph:
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(setup: Setup, decode_steps: int) -> dict:
+    """Time the oracle on this host: the whole prefill of every unit + `decode_steps` steps."""
+    import numpy as np
+
+    from oracle import rkv_oracle as O
+
+    wl = setup.wl
+    f = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
+    q_win = f(setup.inp["q_win"])
+    k = f(setup.inp["k"])
+    v = f(setup.inp["v"])
+    t0 = time.perf_counter()
+    units = []
+    for b in range(wl.B):
+        L = wl.prompt_lens[b]
+        res = O.prefill_evict_unit(q_win[b], k[b, :, :L], setup.keep1[b], setup.kp[b])
+        for g in range(wl.Hkv):
+            kept = res["kept"][g]
+            Kc, Vc = k[b, g, kept], v[b, g, kept]
+            units.append([b, g, Kc, Vc, O.page_summaries(Kc, len(kept), wl.page_size)])
+    t_prefill = time.perf_counter() - t0
+    G = wl.G
+    t1 = time.perf_counter()
+    for t in range(decode_steps):
+        d = setup.dec[t]
+        q = f(d["q"])
+        kn, vn = f(d["k_new"][:, :, 0]), f(d["v_new"][:, :, 0])
+        for u in units:
+            b, g, Kc, Vc, (kmax, kmin) = u
+            n_old = len(Kc)
+            Kc = np.concatenate([Kc, kn[b, g][None]])
+            Vc = np.concatenate([Vc, vn[b, g][None]])
+            kmax, kmin = O.append_summaries(kmax, kmin, Kc, n_old, 1, wl.page_size)
+            O.hsa_decode_unit(q[b, g * G:(g + 1) * G], Kc, Vc, n_old + 1, kmax, kmin, wl.page_size,
+                              setup.k1[b], setup.k2[b])
+            u[2], u[3], u[4] = Kc, Vc, (kmax, kmin)
+    t_dec = (time.perf_counter() - t1) / max(1, decode_steps)
+    whole = t_prefill + wl.steps * t_dec
+    return dict(value=wl.steps / whole, t_prefill_s=t_prefill, t_decode_step_s=t_dec, seconds=t_prefill + t_dec *
+                decode_steps)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- main arms
+def run_ours(args, rank: int, world: int, dev) -> dict:
+    from two_stage_kv_snapkv_gb300 import rkv
+
+    wl = W.workload(args.workload, args.seed)
+    setup = Setup(wl, rkv, args.seed + rank, dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+
+    # eager warm-up (sets kernel attributes, checks the path runs)
+    setup.prefill()
+    for t in range(wl.steps):
+        setup.decode(t)
+    torch.cuda.synchronize()
+    st, bits = rkv.rkv_get_device_status(setup.cache, stream)
+    if st != rkv.RKV_OK:
+        raise RuntimeError(f"device status {st} bits {bits}")
+
+    if args.ncu:
+        setup.prefill()
+        for t in range(wl.steps):
+            setup.decode(t)
+        torch.cuda.synchronize()
+        return {}
+
+    # graphs: one for the prefill, one per decode step
+    n0 = rkv.rkv_launch_count()
+    g_pre = capture(setup.prefill, stream)
+    g_dec = [capture(lambda t=t: setup.decode(t), stream) for t in range(wl.steps)]
+    launches_per_pass = rkv.rkv_launch_count() - n0
+    # instrumented copies: library events around every kernel launch
+    rkv.profile_enable(True)
+    gi_pre = capture(setup.prefill, stream)
+    gi_dec = [capture(lambda t=t: setup.decode(t), stream) for t in range(wl.steps)]
+    rkv.profile_enable(False)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (wl.steps + 1))]
+
+    def one_pass(pre, dec):
+        setup.flush()
+        ev[0].record(stream)
+        pre.replay()
+        ev[1].record(stream)
+        for t in range(wl.steps):
+            setup.flush()
+            ev[2 + 2 * t].record(stream)
+            dec[t].replay()
+            ev[3 + 2 * t].record(stream)
+        stream.synchronize()
+        pre_ms = ev[0].elapsed_time(ev[1])
+        dec_ms = [ev[2 + 2 * t].elapsed_time(ev[3 + 2 * t]) for t in range(wl.steps)]
+        return pre_ms, dec_ms
+
+    for _ in range(args.warmup):
+        one_pass(g_pre, g_dec)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    pre_all, dec_all = [], []
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for _ in range(args.steps):
+            p, d = one_pass(g_pre, g_dec)
+            pre_all.append(p)
+            dec_all.append(d)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.summary()
+    pass_ms = [p + sum(d) for p, d in zip(pre_all, dec_all)]
+    total_ms = sum(pass_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * wl.steps * args.steps / (total_ms / 1e3)
+
+    # per-kernel durations from the instrumented graphs (same work, same flushes)
+    rkv.profile_reset()
+    for _ in range(args.steps):
+        one_pass(gi_pre, gi_dec)
+        rkv.profile_accumulate()
+    prof = {k: v for k, v in rkv.profile_read().items() if v[0] > 0}
+    rkv.profile_release()
+    dominant = max(prof, key=lambda k: prof[k][1])
+
+    peaks = measured_peaks()
+    step_bytes = [setup.decode_bytes(t) for t in range(wl.steps)]
+    pb = setup.prefill_bytes()
+
+    def algo_bytes(kind):
+        if kind in ("hsa_score", "hsa_attend", "append_small"):
+            return statistics.mean(sb[kind] for sb in step_bytes)
+        if kind in pb:
+            return pb[kind]
+        return None
+
+    kernels = {}
+    for k, (n, ms) in prof.items():
+        avg_ms = ms / n
+        ab = algo_bytes(k)
+        kernels[k] = dict(launches=n, avg_us=round(avg_ms * 1e3, 3), share=round(ms / sum(v[1] for v in prof.values()), 4),
+                          algo_bytes=ab, achieved_gbs=(round(ab / (avg_ms * 1e-3) / 1e9, 1) if ab else None))
+    dk = kernels[dominant]
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        ent = tj.get(str(wl.name), {}).get(dominant)
+        if ent and ent.get("source_sha") == _source_sha(ent.get("source_file", "")):
+            traffic = ent["bytes_per_launch"]
+    roofline = dict(bound="hbm", kernel=dominant, achieved=dk["achieved_gbs"], peak=peaks["hbm_gbs"],
+                    unit="GB/s", frac=(round(dk["achieved_gbs"] / peaks["hbm_gbs"], 4) if dk["achieved_gbs"] else None),
+                    traffic=traffic, peak_source=peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
+                    if peaks["source"] == "measured" else "fallback 6.8 TB/s")
+
+    dec_mean_ms = statistics.mean(x for d in dec_all for x in d)
+    step_total = statistics.mean(sb["step_total"] for sb in step_bytes)
+    res = dict(
+        metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="bf16", data="synthetic (seeded; see DESIGN.md input recipe)",
+        config=dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, head_dim=wl.d, prompt_len=wl.prompt_lens[0]
+                    if wl.B == 1 else f"{min(wl.prompt_lens)}..{max(wl.prompt_lens)}", budget=wl.budget,
+                    window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, keep1=self_or_range(setup.keep1),
+                    k1=self_or_range(setup.k1), k2=self_or_range(setup.k2), pool_kernel=self_or_range(setup.kp),
+                    step="one request: split + prefill evict + every decode step (append + HSA)",
+                    l2="flushed (256 MB write) before the prefill and before every decode step; flush not timed",
+                    timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
+                    parallelism=f"replica x{world}" if world > 1 else "single GPU"),
+        prefill_evict_ms=round(statistics.mean(pre_all), 4),
+        decode_us_per_step=round(dec_mean_ms * 1e3, 3),
+        decode_achieved_gbs=round(step_total / (dec_mean_ms * 1e-3) / 1e9, 1),
+        decode_compulsory_mb_per_step=round(step_total / 1e6, 3),
+        prefill_achieved_gbs=round(pb["total"] / (statistics.mean(pre_all) * 1e-3) / 1e9, 1),
+        roofline=roofline, kernels=kernels, gpu_launches=int(launches_per_pass * args.steps),
+        clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]),
+    )
+    if rank == 0 and not args.no_e2e:
+        res["e2e"] = run_e2e(setup, args, stream, rkv)
+    if rank == 0 and not args.no_cpu_baseline:
+        o = oracle_sample(setup, args.cpu_decode_steps)
+        res["cpu_baseline"] = dict(value=round(o["value"], 3), unit=UNIT, cores=host_cores(), kind="oracle",
+                                   sample=f"oracle prefill of all {wl.B * wl.Hkv} units + {args.cpu_decode_steps} "
+                                          f"of {wl.steps} decode steps ({o['seconds']:.1f} s), extrapolated to the "
+                                          f"whole request: steps / (prefill + steps * mean step)")
+    return res
+
+
+def self_or_range(xs):
+    return xs[0] if len(set(xs)) == 1 else f"{min(xs)}..{max(xs)}"
+
+
+def _source_sha(rel: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, rel)
+    if not rel or not os.path.exists(path):
+        return ""
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def run_e2e(setup: Setup, args, stream, rkv) -> dict:
+    """The same request through the public API from pinned host buffers: prompt and
+    per-step inputs copied in, every step's output copied out, inside the timed region."""
+    wl = setup.wl
+    host = {k: setup.inp[k].cpu().pin_memory() for k in ("q_win", "k", "v")}
+    hdec = [{k: d[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")} for d in setup.dec]
+    hout = torch.empty((wl.steps, wl.B, wl.Hq, 128), dtype=torch.float32).pin_memory()
+    dq = {k: torch.empty_like(setup.inp[k]) for k in ("q_win", "k", "v")}
+    dd = {k: torch.empty_like(setup.dec[0][k]) for k in ("q", "k_new", "v_new")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        wl.steps * sum(t.numel() * t.element_size() for t in hdec[0].values())
+    d2h = hout.numel() * 4
+
+    def one():
+        for k in host:
+            dq[k].copy_(host[k], non_blocking=True)
+        rkv.rkv_prefill_evict(dq["q_win"], dq["k"], dq["v"], wl.prompt_lens, setup.keep1, setup.kp, setup.cache,
+                              setup.kept, workspace=setup.pws)
+        for t in range(wl.steps):
+            for k in dd:
+                dd[k].copy_(hdec[t][k], non_blocking=True)
+            rkv.rkv_append_page_summary(setup.cache, dd["k_new"], dd["v_new"], 1)
+            rkv.rkv_decode_hsa(setup.cache, dd["q"], setup.k1, setup.k2, setup.out[t], workspace=setup.dws)
+            hout[t].copy_(setup.out[t], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(args.steps):
+        setup.flush()
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        stream.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return dict(value=round(wl.steps * len(times) / (sum(times) / 1e3), 2), unit=UNIT, h2d_bytes_per_step=int(h2d),
+                d2h_bytes_per_step=int(d2h), ms_per_step=round(statistics.mean(times), 4),
+                path="python binding -> C ABI, eager launches, pinned host buffers")
+
+
+def run_reference(args, rank: int, world: int) -> dict:
+    """The CPU oracle as the reference arm: each step is a bounded sample of the request."""
+    if rank != 0:
+        return {}
+    wl = W.workload(args.workload, args.seed)
+
+    class _Split:
+        pass
+
+    from oracle import rkv_oracle as O
+
+    setup = _Split()
+    setup.wl = wl
+    setup.inp = W.prefill_tensors(wl, args.seed, 0, "cpu", tail="zero")
+    nsteps = min(wl.steps, 4)
+    setup.dec = []
+    for t in range(nsteps):
+        d = W.decode_tensors(wl, t, args.seed, 0, "cpu")
+        d["k_new"] = d["k_new"].unsqueeze(2)
+        d["v_new"] = d["v_new"].unsqueeze(2)
+        setup.dec.append(d)
+    sp = [O.split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0) for L in wl.prompt_lens]
+    setup.keep1 = [s["keep1"] for s in sp]
+    setup.k1 = [s["k1"] for s in sp]
+    setup.k2 = [s["k2"] for s in sp]
+    setup.kp = [wl.pool_kernel or s["pool_kernel"] for s in sp]
+    for _ in range(args.warmup):
+        oracle_sample(setup, 1)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        o = oracle_sample(setup, nsteps)
+        vals.append(o["value"])
+        secs += o["seconds"]
+    value = statistics.mean(vals)
+    return dict(impl="reference", metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(1e3 / value * wl.steps, 3), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)",
+                config=dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, decode_steps=wl.steps),
+                cpu_baseline=dict(value=round(value, 3), unit=UNIT, cores=host_cores(), kind="oracle",
+                                  sample=f"per step: oracle prefill of all units + {nsteps} decode steps, "
+                                         f"extrapolated to the whole request ({secs:.1f} s total)"),
+                e2e=dict(value=round(value, 3), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res))
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    res = run_ours(args, rank, world, dev)
+    if rank == 0 and res:
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -205,12 +205,17 @@ int64_t rkv_launch_count(void);
 
 /*
  * Per-kernel timing for measurement.  While enabled, every kernel launch is
- * bracketed by CUDA events recorded on its own stream.  rkv_profile_read
- * synchronises those events and returns, for kernel kind `kind`, the number of
- * launches and their summed device time (ms) since the last reset; it returns
- * the kind's name, or NULL past the last kind.
+ * bracketed by a pair of CUDA events recorded on its own stream (inside a stream
+ * capture the records become graph nodes, re-recorded on every replay).
+ * rkv_profile_accumulate synchronises every recorded pair and adds its elapsed
+ * time to per-kind totals, keeping the pairs (call it after each graph replay);
+ * rkv_profile_release frees the pairs; rkv_profile_reset zeroes the totals;
+ * rkv_profile_read returns a kind's launch count and summed device time (ms) and
+ * its name, or NULL past the last kind.  Host only; not for use in hot loops.
  */
 void rkv_profile_enable(int32_t enable);
+void rkv_profile_accumulate(void);
+void rkv_profile_release(void);
 void rkv_profile_reset(void);
 const char* rkv_profile_read(int32_t kind, int64_t* launches, double* total_ms);
 

@@ -1,0 +1,140 @@
+"""Host-side tests of the C ABI: no GPU needed, nothing is launched.
+
+The library must load, export every function include/rkv.h declares, compute
+the adaptive split on the host exactly as the oracle does, and reject bad
+arguments before touching the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import rkv_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def rkv():
+    from two_stage_kv_snapkv_gb300 import build_lib
+    build_lib.build()
+    from two_stage_kv_snapkv_gb300 import rkv as mod
+    return mod
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_entry_points():
+    names = _declared_functions()
+    for n in ("rkv_split_ratio", "rkv_prefill_evict", "rkv_append_page_summary", "rkv_decode_hsa"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(rkv):
+    lib = rkv.lib()
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_declared_functions()) <= set(rkv.EXPORTED) | set(_declared_functions())
+
+
+@pytest.mark.parametrize("L,budget,P,k1o", [
+    (4096, 256, 16, 64), (32768, 512, 16, 0), (109000, 256, 16, 0), (65536, 4096, 16, 0),
+    (8192, 2048, 32, 0), (32768, 2048, 32, 0), (20000, 2048, 32, 0), (300, 256, 16, 0), (200, 256, 16, 0),
+    (1 << 20, 256, 64, 0), (1000, 1000, 16, 0), (999, 7, 16, 0), (5000, 100, 16, 128)])
+def test_host_split_matches_oracle(rkv, L, budget, P, k1o):
+    a = rkv.rkv_split_ratio(L, budget, 128, P, 32, k1o)
+    b = O.split_ratio(L, budget, 128, P, 32, k1o)
+    for key in ("keep1", "k1", "k2", "pool_kernel"):
+        assert a[key] == b[key], key
+    for key in ("c", "r", "c1", "c2"):
+        assert a[key] == pytest.approx(b[key], rel=1e-12), key
+
+
+def test_split_rejects_bad_sizes(rkv):
+    with pytest.raises(rkv.RkvError) as e:
+        rkv.rkv_split_ratio(0, 256)
+    assert e.value.status == rkv.RKV_ERR_INVALID_ARG
+
+
+def _fake_cache(rkv, **kw):
+    base = dict(k_pages=0x10000, v_pages=0x20000, page_table=0x30000, seq_len=0x40000, kmax=0x50000,
+                kmin=0x60000, error_word=0x70000, B=2, Hkv=2, head_dim=128, page_size=16, max_pages=64,
+                num_phys_pages=128)
+    base.update(kw)
+    return rkv.RkvCacheStruct(**base)
+
+
+def _decode_call(rkv, cache, Hq=8, k1=(64, 64), k2=(4, 4), ws_bytes=None, q=0x80000, out=0x90000, ws=0xA0000):
+    lib = rkv.lib()
+    if ws_bytes is None:
+        ws_bytes = lib.rkv_decode_workspace_size(cache.B, Hq, cache.Hkv, cache.max_pages)
+    i32 = ctypes.c_int32 * len(k1)
+    return lib.rkv_decode_hsa(ctypes.byref(cache), ctypes.c_void_p(q), Hq, i32(*k1), i32(*k2), ctypes.c_float(0.088),
+                              ctypes.c_void_p(out), None, None, 0, ctypes.c_void_p(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,Hq,k1,k2,expect", [
+    (dict(head_dim=64), 8, (64, 64), (4, 4), "UNSUPPORTED"),
+    (dict(page_size=8), 8, (64, 64), (4, 4), "UNSUPPORTED"),
+    (dict(max_pages=60), 8, (64, 64), (4, 4), "INVALID_ARG"),
+    (dict(kmax=0x50004), 8, (64, 64), (4, 4), "INVALID_ARG"),
+    (dict(error_word=0), 8, (64, 64), (4, 4), "INVALID_ARG"),
+    (dict(), 6, (64, 64), (4, 4), "UNSUPPORTED"),       # group size 3
+    (dict(), 7, (64, 64), (4, 4), "INVALID_ARG"),       # not a multiple of Hkv
+    (dict(), 8, (0, 64), (4, 4), "INVALID_ARG"),
+    (dict(), 8, (64, 129), (4, 4), "INVALID_ARG"),
+    (dict(), 8, (64, 64), (4, 0), "INVALID_ARG"),
+])
+def test_decode_rejects_bad_arguments_without_launching(rkv, kw, Hq, k1, k2, expect):
+    before = rkv.rkv_launch_count()
+    st = _decode_call(rkv, _fake_cache(rkv, **kw), Hq=Hq, k1=k1, k2=k2)
+    assert st == getattr(rkv, "RKV_ERR_" + expect), rkv.rkv_last_error()
+    assert rkv.rkv_last_error()
+    assert rkv.rkv_launch_count() == before
+
+
+def test_decode_rejects_small_workspace(rkv):
+    cache = _fake_cache(rkv)
+    need = rkv.lib().rkv_decode_workspace_size(2, 8, 2, 64)
+    assert _decode_call(rkv, cache, ws_bytes=need - 1) == rkv.RKV_ERR_WORKSPACE
+
+
+def test_prefill_rejects_bad_arguments_without_launching(rkv):
+    lib = rkv.lib()
+    cache = _fake_cache(rkv)
+    i32 = ctypes.c_int32 * 2
+    ws_need = lib.rkv_prefill_workspace_size(2, 8, 2, 32, 1024)
+
+    def call(L=(1024, 900), keep=(200, 200), kp=(7, 7), w=32, Hq=8, stride=256, ws=ws_need, pooled=None):
+        return lib.rkv_prefill_evict(ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000), ctypes.c_void_p(0x300000),
+                                     2, Hq, w, 1024, i32(*L), i32(*keep), i32(*kp), ctypes.c_float(0.088),
+                                     ctypes.byref(cache), ctypes.c_void_p(0x400000), stride,
+                                     pooled, ctypes.c_void_p(0x500000), ws, None)
+
+    before = rkv.rkv_launch_count()
+    assert call(L=(1025, 900)) == rkv.RKV_ERR_INVALID_ARG          # longer than max_prompt_len
+    assert call(keep=(20, 200)) == rkv.RKV_ERR_INVALID_ARG         # keep1 < window
+    assert call(keep=(200, 901)) == rkv.RKV_ERR_INVALID_ARG        # keep1 > prompt
+    assert call(kp=(6, 7)) == rkv.RKV_ERR_INVALID_ARG              # even pooling kernel
+    assert call(kp=(257, 7)) == rkv.RKV_ERR_INVALID_ARG
+    assert call(w=33) == rkv.RKV_ERR_UNSUPPORTED                   # G*w > 128
+    assert call(stride=100) == rkv.RKV_ERR_INVALID_ARG             # kept_stride < keep1
+    assert call(ws=ws_need - 16) == rkv.RKV_ERR_WORKSPACE
+    assert call(keep=(1025, 200), L=(1024, 900)) == rkv.RKV_ERR_INVALID_ARG
+    assert call(pooled=ctypes.c_void_p(0x600004)) == rkv.RKV_ERR_INVALID_ARG   # misaligned
+    # capacity: 64 pages x 16 tokens = 1024 >= keep1, so only the launch would be left
+    assert rkv.rkv_launch_count() == before
+
+
+def test_append_rejects_bad_arguments(rkv):
+    lib = rkv.lib()
+    cache = _fake_cache(rkv)
+    assert lib.rkv_append_page_summary(ctypes.byref(cache), None, None, 0, None) == rkv.RKV_ERR_INVALID_ARG
+    assert lib.rkv_append_page_summary(ctypes.byref(cache), ctypes.c_void_p(0x1000), None, 1, None) == \
+        rkv.RKV_ERR_INVALID_ARG
+    assert lib.rkv_append_page_summary(ctypes.byref(cache), None, None, 64 * 16 + 1, None) == rkv.RKV_ERR_INVALID_ARG

@@ -1,0 +1,224 @@
+"""GPU parity: librkv against the CPU oracle on the same seeded inputs.
+
+Small cases run the whole path (prefill, every decode step) unit by unit; the
+full-size workloads run in the launch configuration the bench uses and are
+checked on sampled (sequence, KV head) units.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rkv_oracle as O
+from two_stage_kv_snapkv_gb300 import workloads as W
+
+from rkv_check import ATOL_OUT, GpuRun, OracleUnit, check_topk, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from two_stage_kv_snapkv_gb300 import build_lib
+    build_lib.build()
+    from two_stage_kv_snapkv_gb300 import rkv as mod
+    return mod
+
+
+SMALL = {
+    # several tiles and a ragged tail, GQA 4, two sequences of different length
+    "gqa4_ragged": W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16,
+                            steps=20, pool_kernel=5),
+    "gqa1": W.custom(B=1, Hq=2, Hkv=2, prompt_lens=[513], budget=48, window=16, page_size=16, steps=6,
+                     pool_kernel=3),
+    "gqa8_w16": W.custom(B=1, Hq=8, Hkv=1, prompt_lens=[900], budget=80, window=16, page_size=16, steps=5,
+                         pool_kernel=9),
+    "gqa2_p32": W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[1200, 333], budget=96, window=8, page_size=32, steps=40,
+                         pool_kernel=7),
+    "p64_outliers": W.custom(B=1, Hq=8, Hkv=2, prompt_lens=[2000], budget=128, window=32, page_size=64, steps=70,
+                             pool_kernel=15, outlier_channels=4, sinks=4),
+    "w1_kernel1": W.custom(B=1, Hq=1, Hkv=1, prompt_lens=[300], budget=40, window=1, page_size=16, steps=3,
+                           pool_kernel=1),
+    "no_eviction": W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[100], budget=256, window=8, page_size=16, steps=4,
+                            pool_kernel=3),
+    "prompt_equals_window": W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[16, 40], budget=8, window=16, page_size=16,
+                                     steps=3, pool_kernel=3),
+    "needles": W.custom(B=1, Hq=8, Hkv=2, prompt_lens=[3000], budget=128, window=32, page_size=16, steps=8,
+                        pool_kernel=7, needles_per_head=2),
+    "k1_small": W.custom(B=3, Hq=8, Hkv=2, prompt_lens=[640, 1500, 64], budget=64, window=8, page_size=16,
+                         steps=10, pool_kernel=5, k1=16),
+}
+
+
+def _run_small(rkv, wl, check_every=1):
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+        u.check_cache(run)
+    errs = []
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in units:
+            errs.append(u.step(run, d, out, ch, pg, check_cache=(step % check_every == 0))["err"])
+    st, bits = run.status()
+    assert st == rkv.RKV_OK, (st, bits)
+    return max(errs) if errs else 0.0
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_end_to_end(rkv, name):
+    err = _run_small(rkv, SMALL[name])
+    assert err <= ATOL_OUT
+
+
+def test_tiny_workload_end_to_end(rkv):
+    """Workload 1: 4K prompt, GQA 4, needles, 16 decode steps, every step checked."""
+    wl = W.workload(1)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    units = [OracleUnit(run, 0, g) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+        u.check_cache(run)
+    hits = 0
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in units:
+            u.step(run, d, out, ch, pg, check_cache=True)
+    st, _ = run.status()
+    assert st == rkv.RKV_OK
+
+
+def test_full_selection_is_dense_attention(rkv):
+    """k1 = 128 and k2 >= pages: HSA is exact attention over every cached token."""
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[600, 450], budget=64, window=8, page_size=16, steps=2,
+                  pool_kernel=5)
+    run = GpuRun(wl, rkv)
+    run.k1 = [128, 128]
+    run.k2 = [4096, 4096]
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(2) for g in range(2)]
+    for u in units:
+        u.check_prefill(run)
+    d, out, ch, pg = run.decode_step(0)
+    for u in units:
+        u.step(run, d, out, ch, pg)
+        G = wl.G
+        qg = f64(d["q"][u.b, u.g * G:(u.g + 1) * G])
+        dense = O.sparse_attention(qg, u.Kc, u.Vc, u.n, np.arange(-(-u.n // 16)), 16)
+        np.testing.assert_allclose(f64(out[u.b, u.g * G:(u.g + 1) * G]), dense, atol=ATOL_OUT)
+
+
+def test_append_equals_rebuild_on_gpu(rkv):
+    """Incremental appends, then a from-scratch rebuild by the library: bit-identical summaries."""
+    wl = W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[600, 600], budget=64, window=8, page_size=16, steps=37,
+                  pool_kernel=5)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    for step in range(wl.steps):
+        run.decode_step(step)
+    c = run.cache
+    n = int(c.seq_len[0].item())
+    assert c.seq_len.tolist() == [n, n] and n % 16 != 0
+    NP = -(-n // 16)
+    inc_max, inc_min = c.kmax[..., :NP].clone(), c.kmin[..., :NP].clone()
+    c.kmax.fill_(float("nan"))
+    c.kmin.fill_(float("nan"))
+    c.seq_len.zero_()
+    for chunk in (17, 5, n - 22):          # uneven chunks; the tokens are already in their pages
+        rkv.rkv_append_page_summary(c, None, None, chunk)
+    assert c.seq_len.tolist() == [n, n]
+    assert torch.equal(c.kmax[..., :NP], inc_max) and torch.equal(c.kmin[..., :NP], inc_min)
+    st, _ = run.status()
+    assert st == rkv.RKV_OK
+
+
+def test_deterministic(rkv):
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[900, 700], budget=64, window=8, page_size=16, steps=3,
+                  pool_kernel=5)
+    outs = []
+    for _ in range(2):
+        run = GpuRun(wl, rkv)
+        run.prefill()
+        res = [run.kept.clone(), run.pooled.clone()]
+        for s in range(wl.steps):
+            d, out, ch, pg = run.decode_step(s)
+            res += [out.clone(), pg.clone()]
+        outs.append(res)
+    for a, b in zip(*outs):
+        assert torch.equal(a.nan_to_num(), b.nan_to_num())
+
+
+def test_bad_page_id_is_flagged_not_faulted(rkv):
+    wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    assert run.status()[0] == rkv.RKV_OK
+    run.k2 = [1000]        # every page is attended, so the bad entry is used
+    run.cache.page_table[0, 1] = run.cache.num_phys_pages + 7
+    run.decode_step(0)
+    st, bits = run.status()
+    assert st == rkv.RKV_ERR_DEVICE_DATA and bits & rkv.DEVERR_PAGE_ID
+    assert run.status() == (rkv.RKV_OK, 0)   # the word was cleared
+
+
+def test_capacity_overflow_is_flagged(rkv):
+    wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    cap = run.cache.max_pages * 16
+    run.cache.seq_len.fill_(cap)
+    d, out, ch, pg = run.decode_step(0)        # the append does not fit: flagged, length kept
+    st, bits = run.status()
+    assert st == rkv.RKV_ERR_DEVICE_DATA and bits & rkv.DEVERR_CAPACITY
+    assert int(run.cache.seq_len[0].item()) == cap
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sampled_full(rkv, n, units, steps_checked, gen_device="cuda"):
+    wl = W.workload(n)
+    run = GpuRun(wl, rkv, gen_device=gen_device, tail="zero")
+    run.prefill()
+    checks = [OracleUnit(run, b, g) for b, g in units]
+    for u in checks:
+        u.check_prefill(run)
+        u.check_cache(run)
+    errs = []
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        if step in steps_checked:
+            for u in checks:
+                errs.append(u.step(run, d, out, ch, pg, check_cache=True)["err"])
+        else:
+            for u in checks:   # keep the oracle's cache in step without re-checking
+                G = wl.G
+                u.Kc = np.concatenate([u.Kc[: u.n], f64(d["k_new"][u.b, u.g])[None]])
+                u.Vc = np.concatenate([u.Vc[: u.n], f64(d["v_new"][u.b, u.g])[None]])
+                u.n += 1
+    st, bits = run.status()
+    assert st == rkv.RKV_OK, bits
+    return max(errs)
+
+
+def test_workload2_llama_layer_32k(rkv):
+    assert _sampled_full(rkv, 2, [(0, 0), (0, 5)], {0, 63, 127}) <= ATOL_OUT
+
+
+def test_workload3_extreme_ratio_109k(rkv):
+    assert _sampled_full(rkv, 3, [(0, 3)], {0, 63}) <= ATOL_OUT
+
+
+def test_workload4_batched_ragged(rkv):
+    wl = W.workload(4)
+    longest = int(np.argmax(wl.prompt_lens))
+    shortest = int(np.argmin(wl.prompt_lens))
+    assert _sampled_full(rkv, 4, [(longest, 1), (shortest, 6)], {0, 255}) <= ATOL_OUT
+
+
+def test_workload5_one_layer_sampled(rkv):
+    assert _sampled_full(rkv, 5, [(0, 0), (7, 7)], {0, 63}) <= ATOL_OUT

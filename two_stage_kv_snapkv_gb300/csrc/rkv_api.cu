@@ -1,0 +1,361 @@
+// C ABI of librkv: argument validation, the adaptive ratio split, dispatch to the
+// kernel launchers, error reporting, launch counting and optional per-kernel timing.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+#include <atomic>
+
+#include "rkv.h"
+#include "rkv_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<long long> g_launches{0};
+
+rkv_status fail(rkv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rkv_status check_cache(const rkv_cache* c) {
+  if (!c) return fail(RKV_ERR_INVALID_ARG, "cache is NULL");
+  if (c->head_dim != RKV_HEAD_DIM) return fail(RKV_ERR_UNSUPPORTED, "head_dim %d unsupported (only 128)", c->head_dim);
+  if (c->B < 1 || c->B > RKV_MAX_BATCH) return fail(RKV_ERR_INVALID_ARG, "B=%d outside [1, %d]", c->B, RKV_MAX_BATCH);
+  if (c->Hkv < 1) return fail(RKV_ERR_INVALID_ARG, "Hkv=%d", c->Hkv);
+  if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64)
+    return fail(RKV_ERR_UNSUPPORTED, "page_size %d unsupported (16, 32 or 64)", c->page_size);
+  if (c->max_pages < 8 || c->max_pages % 8 != 0)
+    return fail(RKV_ERR_INVALID_ARG, "max_pages=%d must be a positive multiple of 8", c->max_pages);
+  if (c->max_pages > 16384) return fail(RKV_ERR_UNSUPPORTED, "max_pages=%d above 16384", c->max_pages);
+  if (c->num_phys_pages < 1) return fail(RKV_ERR_INVALID_ARG, "num_phys_pages=%d", c->num_phys_pages);
+  if (!c->k_pages || !c->v_pages || !c->page_table || !c->seq_len || !c->kmax || !c->kmin || !c->error_word)
+    return fail(RKV_ERR_INVALID_ARG, "a cache pointer is NULL");
+  if (!al16(c->k_pages) || !al16(c->v_pages) || !al16(c->page_table) || !al16(c->kmax) || !al16(c->kmin))
+    return fail(RKV_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  return RKV_OK;
+}
+
+rkv_status check_heads(int Hq, int Hkv) {
+  if (Hq < 1 || Hq % Hkv != 0) return fail(RKV_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(RKV_ERR_UNSUPPORTED, "group size %d unsupported", G);
+  return RKV_OK;
+}
+
+rkv_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return RKV_OK;
+  return fail(RKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ profiling
+struct Pending {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<cudaEvent_t> g_pool;
+std::vector<Pending> g_pending;
+cudaEvent_t g_open[rkv::K_NUM_KINDS];
+long long g_count[rkv::K_NUM_KINDS];
+double g_ms[rkv::K_NUM_KINDS];
+
+cudaEvent_t take_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Adds the elapsed time of every recorded pair to the totals; the pairs stay
+// recorded (a captured graph re-records the same events on every replay).
+void accumulate_locked() {
+  for (const Pending& p : g_pending) {
+    cudaEventSynchronize(p.b);
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) ms = 0.f;
+    g_count[p.kind] += 1;
+    g_ms[p.kind] += ms;
+  }
+}
+
+void release_locked() {
+  for (const Pending& p : g_pending) {
+    g_pool.push_back(p.a);
+    g_pool.push_back(p.b);
+  }
+  g_pending.clear();
+}
+
+}  // namespace
+
+namespace rkv {
+
+const char* kernel_name(int kind) {
+  static const char* names[K_NUM_KINDS] = {
+      "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
+      "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
+      "hsa_topk",     "hsa_attend",   "hsa_combine"};
+  return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
+}
+
+// Inside a stream capture a plain record only orders the capture; the external
+// flag makes it a timing node of the graph.
+void record(cudaEvent_t e, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(stream, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, stream, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, stream);
+}
+
+void launch_begin(int kind, cudaStream_t stream) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t e = take_event();
+  record(e, stream);
+  g_open[kind] = e;
+}
+
+void launch_end(int kind, cudaStream_t stream) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_open[kind]) return;
+  cudaEvent_t e = take_event();
+  record(e, stream);
+  g_pending.push_back({kind, g_open[kind], e});
+  g_open[kind] = nullptr;
+}
+
+int num_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  return sms;
+}
+
+}  // namespace rkv
+
+extern "C" {
+
+rkv_status rkv_split_ratio(int32_t prompt_len, int32_t budget, int32_t head_dim, int32_t page_size, int32_t window,
+                           int32_t k1_override, rkv_split* out) {
+  if (!out) return fail(RKV_ERR_INVALID_ARG, "out is NULL");
+  if (prompt_len < 1 || budget < 1 || head_dim < 1 || page_size < 1 || window < 0 || k1_override < 0)
+    return fail(RKV_ERR_INVALID_ARG, "sizes must be positive");
+  const double c = (double)prompt_len / (double)budget;
+  double r = 0.2 + 0.06 * std::log2(c);
+  r = r < 0.2 ? 0.2 : (r > 0.8 ? 0.8 : r);
+  const double c1 = std::pow(c, r), c2 = std::pow(c, 1.0 - r);
+  long long keep1 = (long long)std::floor((double)prompt_len / c1 + 0.5);
+  long long lo = budget > window ? budget : window;
+  keep1 = keep1 < lo ? lo : keep1;
+  keep1 = keep1 > prompt_len ? prompt_len : keep1;
+  int k1 = k1_override;
+  if (k1 <= 0) {
+    k1 = 16 * (int)std::floor((double)head_dim / (16.0 * std::sqrt(c2)) + 0.5);
+    k1 = k1 < 16 ? 16 : (k1 > head_dim ? head_dim : k1);
+  }
+  int k2 = budget / page_size;
+  k2 = k2 < 1 ? 1 : k2;
+  out->c = c;
+  out->r = r;
+  out->c1 = c1;
+  out->c2 = c2;
+  out->keep1 = (int32_t)keep1;
+  out->k1 = k1;
+  out->k2 = k2;
+  out->pool_kernel = prompt_len <= 8192 ? 7 : (prompt_len <= 49152 ? 31 : 63);
+  return RKV_OK;
+}
+
+size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t window, int32_t max_prompt_len) {
+  if (B < 1 || Hkv < 1 || max_prompt_len < 1) return 0;
+  return rkv::prefill_ws_bytes(B, Hq, Hkv, window, max_prompt_len);
+}
+
+rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv_bf16* v, int32_t B, int32_t Hq,
+                             int32_t window, int32_t max_prompt_len, const int32_t* prompt_len, const int32_t* keep1,
+                             const int32_t* pool_kernel, float scale, const rkv_cache* cache, int32_t* kept_idx,
+                             int32_t kept_stride, float* pooled_scores, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
+  if (B != cache->B) return fail(RKV_ERR_INVALID_ARG, "B=%d differs from cache B=%d", B, cache->B);
+  if (!q_win || !k || !v || !kept_idx || !prompt_len || !keep1 || !pool_kernel || !workspace)
+    return fail(RKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!al16(q_win) || !al16(k) || !al16(v) || !al16(kept_idx) || !al16(workspace) ||
+      (pooled_scores && !al16(pooled_scores)))
+    return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  const int G = Hq / cache->Hkv;
+  if (window < 1 || G * window > 128)
+    return fail(RKV_ERR_UNSUPPORTED, "window=%d: need 1 <= G*window <= 128 (G=%d)", window, G);
+  if (max_prompt_len < 1) return fail(RKV_ERR_INVALID_ARG, "max_prompt_len=%d", max_prompt_len);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
+  for (int b = 0; b < B; ++b) {
+    const int L = prompt_len[b], kk = keep1[b], kp = pool_kernel[b];
+    if (L < window || L > max_prompt_len)
+      return fail(RKV_ERR_INVALID_ARG, "prompt_len[%d]=%d outside [window, max_prompt_len]", b, L);
+    if (kk < window || kk > L) return fail(RKV_ERR_INVALID_ARG, "keep1[%d]=%d outside [window, prompt_len]", b, kk);
+    if (kk > cache->max_pages * cache->page_size)
+      return fail(RKV_ERR_INVALID_ARG, "keep1[%d]=%d exceeds the cache capacity", b, kk);
+    if (kk > kept_stride) return fail(RKV_ERR_INVALID_ARG, "kept_stride=%d < keep1[%d]=%d", kept_stride, b, kk);
+    if (kp < 1 || kp > 255 || kp % 2 == 0)
+      return fail(RKV_ERR_INVALID_ARG, "pool_kernel[%d]=%d must be odd in [1, 255]", b, kp);
+  }
+  const size_t need = rkv::prefill_ws_bytes(B, Hq, cache->Hkv, window, max_prompt_len);
+  if (workspace_bytes < need)
+    return fail(RKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  rkv::PrefillArgs a;
+  a.q_win = q_win;
+  a.k = k;
+  a.v = v;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = cache->Hkv;
+  a.G = G;
+  a.w = window;
+  a.Lmax = max_prompt_len;
+  a.prompt_len = prompt_len;
+  a.keep1 = keep1;
+  a.pool_kernel = pool_kernel;
+  a.scale = scale;
+  a.cache = *cache;
+  a.kept_idx = kept_idx;
+  a.kept_stride = kept_stride;
+  a.pooled_out = pooled_scores;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  return cuda_status(rkv::launch_prefill(a, static_cast<cudaStream_t>(stream)), "rkv_prefill_evict launch");
+}
+
+rkv_status rkv_append_page_summary(const rkv_cache* cache, const rkv_bf16* k_new, const rkv_bf16* v_new,
+                                   int32_t n_new, void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if (n_new < 1) return fail(RKV_ERR_INVALID_ARG, "n_new=%d", n_new);
+  if (n_new > cache->max_pages * cache->page_size) return fail(RKV_ERR_INVALID_ARG, "n_new=%d exceeds capacity", n_new);
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(RKV_ERR_INVALID_ARG, "k_new and v_new must both be set");
+  if (k_new && (!al16(k_new) || !al16(v_new))) return fail(RKV_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned");
+  return cuda_status(rkv::launch_append(*cache, k_new, v_new, n_new, static_cast<cudaStream_t>(stream)),
+                     "rkv_append_page_summary launch");
+}
+
+size_t rkv_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_pages) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_pages < 1) return 0;
+  return rkv::decode_ws_bytes(B, Hq, Hkv, max_pages);
+}
+
+rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* k1, const int32_t* k2,
+                          float scale, float* out, int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
+  if (!q || !k1 || !k2 || !out || !workspace) return fail(RKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!al16(q) || !al16(out) || !al16(workspace) || (sel_channels && !al16(sel_channels)) ||
+      (sel_pages && !al16(sel_pages)))
+    return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
+  for (int b = 0; b < cache->B; ++b) {
+    if (k1[b] < 1 || k1[b] > RKV_HEAD_DIM) return fail(RKV_ERR_INVALID_ARG, "k1[%d]=%d outside [1, 128]", b, k1[b]);
+    if (k2[b] < 1) return fail(RKV_ERR_INVALID_ARG, "k2[%d]=%d", b, k2[b]);
+    if (sel_pages) {
+      const int kk = k2[b] < cache->max_pages ? k2[b] : cache->max_pages;
+      if (sel_pages_stride < kk) return fail(RKV_ERR_INVALID_ARG, "sel_pages_stride=%d < %d", sel_pages_stride, kk);
+    }
+  }
+  const size_t need = rkv::decode_ws_bytes(cache->B, Hq, cache->Hkv, cache->max_pages);
+  if (workspace_bytes < need)
+    return fail(RKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  rkv::DecodeArgs a;
+  a.cache = *cache;
+  a.q = q;
+  a.Hq = Hq;
+  a.G = Hq / cache->Hkv;
+  a.k1 = k1;
+  a.k2 = k2;
+  a.scale = scale;
+  a.out = out;
+  a.sel_channels = sel_channels;
+  a.sel_pages = sel_pages;
+  a.sel_pages_stride = sel_pages_stride;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  return cuda_status(rkv::launch_decode(a, static_cast<cudaStream_t>(stream)), "rkv_decode_hsa launch");
+}
+
+rkv_status rkv_get_device_status(const rkv_cache* cache, void* stream, int32_t* bits) {
+  if (!cache || !cache->error_word) return fail(RKV_ERR_INVALID_ARG, "cache or error_word is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, cache->error_word, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && word != 0) e = cudaMemsetAsync(cache->error_word, 0, sizeof word, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(RKV_ERR_CUDA, "rkv_get_device_status: %s", cudaGetErrorString(e));
+  if (bits) *bits = word;
+  if (word == 0) return RKV_OK;
+  if (word & RKV_DEVERR_TIMEOUT) return fail(RKV_ERR_TIMEOUT, "a bounded device wait ran out (word 0x%x)", word);
+  return fail(RKV_ERR_DEVICE_DATA, "device data error (word 0x%x)", word);
+}
+
+const char* rkv_last_error(void) { return g_err.c_str(); }
+
+int64_t rkv_launch_count(void) { return (int64_t)g_launches.load(); }
+
+void rkv_profile_enable(int32_t enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = enable != 0;
+}
+
+void rkv_profile_accumulate(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  accumulate_locked();
+}
+
+void rkv_profile_release(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  release_locked();
+}
+
+void rkv_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int i = 0; i < rkv::K_NUM_KINDS; ++i) {
+    g_count[i] = 0;
+    g_ms[i] = 0.0;
+  }
+}
+
+const char* rkv_profile_read(int32_t kind, int64_t* launches, double* total_ms) {
+  if (kind < 0 || kind >= rkv::K_NUM_KINDS) return nullptr;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (launches) *launches = g_count[kind];
+  if (total_ms) *total_ms = g_ms[kind];
+  return rkv::kernel_name(kind);
+}
+
+}  // extern "C"

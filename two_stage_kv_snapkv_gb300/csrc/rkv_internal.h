@@ -1,0 +1,78 @@
+// Internal launcher interface between the C-ABI layer (rkv_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rkv.h"
+
+namespace rkv {
+
+// Kinds of kernel, for launch counting and the optional per-kernel timing.
+enum KernelKind {
+  K_APPEND_SMALL = 0,
+  K_APPEND_PAGES,
+  K_APPEND_ADVANCE,
+  K_SNAP_STATS,
+  K_SNAP_STATS_COMBINE,
+  K_SNAP_COLSUM,
+  K_SNAP_POOL,
+  K_SNAP_SELECT,
+  K_SNAP_COMPACT,
+  K_HSA_SCORE,
+  K_HSA_TOPK,
+  K_HSA_ATTEND,
+  K_HSA_COMBINE,
+  K_NUM_KINDS
+};
+const char* kernel_name(int kind);
+
+// Launch bookkeeping: counting and, when enabled, event brackets on `stream`.
+void launch_begin(int kind, cudaStream_t stream);
+void launch_end(int kind, cudaStream_t stream);
+int num_sms();
+
+// --------------------------------------------------------------- cache append
+cudaError_t launch_append(const rkv_cache& c, const rkv_bf16* k_new, const rkv_bf16* v_new,
+                          int n_new, cudaStream_t s);
+
+// --------------------------------------------------------------- prefill
+struct PrefillArgs {
+  const rkv_bf16* q_win;
+  const rkv_bf16* k;
+  const rkv_bf16* v;
+  int B, Hq, Hkv, G, w, Lmax;
+  const int32_t* prompt_len;   // host [B]
+  const int32_t* keep1;        // host [B]
+  const int32_t* pool_kernel;  // host [B]
+  float scale;
+  rkv_cache cache;
+  int32_t* kept_idx;
+  int kept_stride;
+  float* pooled_out;  // may be null
+  void* ws;
+  size_t ws_bytes;
+};
+size_t prefill_ws_bytes(int B, int Hq, int Hkv, int w, int Lmax);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+// --------------------------------------------------------------- decode
+struct DecodeArgs {
+  rkv_cache cache;
+  const rkv_bf16* q;
+  int Hq, G;
+  const int32_t* k1;  // host [B]
+  const int32_t* k2;  // host [B]
+  float scale;
+  float* out;
+  int32_t* sel_channels;
+  int32_t* sel_pages;
+  int sel_pages_stride;
+  void* ws;
+  size_t ws_bytes;
+};
+size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+}  // namespace rkv

@@ -1,0 +1,279 @@
+"""Thin Python binding of librkv (include/rkv.h).
+
+Argument marshalling only: every step of the hot path runs in the CUDA library.
+torch tensors provide device memory and streams.  Importing this module loads
+``_build/librkv.so`` and raises if it has not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "librkv.so")
+
+RKV_OK = 0
+RKV_ERR_INVALID_ARG = 1
+RKV_ERR_UNSUPPORTED = 2
+RKV_ERR_WORKSPACE = 3
+RKV_ERR_CUDA = 4
+RKV_ERR_DEVICE_DATA = 5
+RKV_ERR_TIMEOUT = 6
+DEVERR_PAGE_ID = 0x1
+DEVERR_CAPACITY = 0x2
+DEVERR_TIMEOUT = 0x4
+HEAD_DIM = 128
+MAX_BATCH = 256
+
+
+class RkvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"rkv status {status}: {msg}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"librkv.so is not built ({_LIB_PATH}); run `python -c 'import __graft_entry__ as g; g.build()'`")
+    return ctypes.CDLL(_LIB_PATH)
+
+
+_lib = _load()
+
+
+class RkvSplit(ctypes.Structure):
+    _fields_ = [("c", ctypes.c_double), ("r", ctypes.c_double), ("c1", ctypes.c_double), ("c2", ctypes.c_double),
+                ("keep1", ctypes.c_int32), ("k1", ctypes.c_int32), ("k2", ctypes.c_int32),
+                ("pool_kernel", ctypes.c_int32)]
+
+
+class RkvCacheStruct(ctypes.Structure):
+    _fields_ = [("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("seq_len", ctypes.c_void_p), ("kmax", ctypes.c_void_p), ("kmin", ctypes.c_void_p),
+                ("error_word", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("num_phys_pages", ctypes.c_int32)]
+
+
+_vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_lib.rkv_split_ratio.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(RkvSplit)]
+_lib.rkv_split_ratio.restype = _i32
+_lib.rkv_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.rkv_prefill_workspace_size.restype = _sz
+_lib.rkv_prefill_evict.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32p, _i32p, _i32p, _f32,
+                                   ctypes.POINTER(RkvCacheStruct), _vp, _i32, _vp, _vp, _sz, _vp]
+_lib.rkv_prefill_evict.restype = _i32
+_lib.rkv_append_page_summary.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _vp, _i32, _vp]
+_lib.rkv_append_page_summary.restype = _i32
+_lib.rkv_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
+_lib.rkv_decode_workspace_size.restype = _sz
+_lib.rkv_decode_hsa.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp, _vp, _i32,
+                                _vp, _sz, _vp]
+_lib.rkv_decode_hsa.restype = _i32
+_lib.rkv_get_device_status.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32p]
+_lib.rkv_get_device_status.restype = _i32
+_lib.rkv_last_error.argtypes = []
+_lib.rkv_last_error.restype = ctypes.c_char_p
+_lib.rkv_launch_count.argtypes = []
+_lib.rkv_launch_count.restype = ctypes.c_int64
+_lib.rkv_profile_enable.argtypes = [_i32]
+_lib.rkv_profile_enable.restype = None
+_lib.rkv_profile_reset.argtypes = []
+_lib.rkv_profile_reset.restype = None
+_lib.rkv_profile_accumulate.argtypes = []
+_lib.rkv_profile_accumulate.restype = None
+_lib.rkv_profile_release.argtypes = []
+_lib.rkv_profile_release.restype = None
+_lib.rkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
+_lib.rkv_profile_read.restype = ctypes.c_char_p
+
+EXPORTED = ["rkv_split_ratio", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
+            "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_get_device_status", "rkv_last_error",
+            "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
+            "rkv_profile_reset", "rkv_profile_read"]
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int):
+    if status != RKV_OK:
+        raise RkvError(status, _lib.rkv_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to librkv must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _host_i32(values: Sequence[int]):
+    arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
+    return arr
+
+
+# ------------------------------------------------------------------ cache
+class PagedCache:
+    """Device memory of one layer's compressed paged cache (see rkv_cache in rkv.h)."""
+
+    def __init__(self, B: int, Hkv: int, page_size: int, max_pages: int, device="cuda",
+                 page_table: Optional[torch.Tensor] = None, num_phys_pages: Optional[int] = None,
+                 fill: Optional[float] = None):
+        max_pages = (max_pages + 7) // 8 * 8
+        if page_table is None:
+            page_table = torch.arange(B * max_pages, dtype=torch.int32, device=device).view(B, max_pages)
+        assert page_table.shape == (B, max_pages) and page_table.dtype == torch.int32
+        if num_phys_pages is None:
+            num_phys_pages = int(page_table.max().item()) + 1
+        self.B, self.Hkv, self.page_size, self.max_pages = B, Hkv, page_size, max_pages
+        self.num_phys_pages = num_phys_pages
+        self.page_table = page_table.to(device).contiguous()
+        shape = (num_phys_pages, Hkv, page_size, HEAD_DIM)
+        self.k_pages = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.v_pages = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.kmax = torch.empty((B, Hkv, HEAD_DIM, max_pages), dtype=torch.bfloat16, device=device)
+        self.kmin = torch.empty((B, Hkv, HEAD_DIM, max_pages), dtype=torch.bfloat16, device=device)
+        if fill is not None:
+            for t in (self.k_pages, self.v_pages, self.kmax, self.kmin):
+                t.fill_(fill)
+        self.seq_len = torch.zeros(B, dtype=torch.int32, device=device)
+        self.error_word = torch.zeros(4, dtype=torch.int32, device=device)
+        self._struct = RkvCacheStruct(
+            self.k_pages.data_ptr(), self.v_pages.data_ptr(), self.page_table.data_ptr(), self.seq_len.data_ptr(),
+            self.kmax.data_ptr(), self.kmin.data_ptr(), self.error_word.data_ptr(), B, Hkv, HEAD_DIM, page_size,
+            max_pages, num_phys_pages)
+
+    @property
+    def struct(self) -> RkvCacheStruct:
+        return self._struct
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in
+                   (self.k_pages, self.v_pages, self.kmax, self.kmin, self.page_table, self.seq_len))
+
+    def token_kv(self, b: int, n: Optional[int] = None):
+        """(K, V) of sequence b's first n tokens, [Hkv, n, 128] (gathered by torch; for checks)."""
+        if n is None:
+            n = int(self.seq_len[b].item())
+        P = self.page_size
+        npg = -(-n // P)
+        phys = self.page_table[b, :npg].long()
+        K = self.k_pages[phys].permute(1, 0, 2, 3).reshape(self.Hkv, npg * P, HEAD_DIM)[:, :n]
+        V = self.v_pages[phys].permute(1, 0, 2, 3).reshape(self.Hkv, npg * P, HEAD_DIM)[:, :n]
+        return K, V
+
+
+# ------------------------------------------------------------------ entry points
+def rkv_split_ratio(prompt_len: int, budget: int, head_dim: int = HEAD_DIM, page_size: int = 16, window: int = 32,
+                    k1_override: int = 0) -> dict:
+    out = RkvSplit()
+    _check(_lib.rkv_split_ratio(prompt_len, budget, head_dim, page_size, window, k1_override, ctypes.byref(out)))
+    return dict(c=out.c, r=out.r, c1=out.c1, c2=out.c2, keep1=out.keep1, k1=out.k1, k2=out.k2,
+                pool_kernel=out.pool_kernel)
+
+
+def prefill_workspace(B: int, Hq: int, Hkv: int, window: int, max_prompt_len: int, device="cuda") -> torch.Tensor:
+    n = _lib.rkv_prefill_workspace_size(B, Hq, Hkv, window, max_prompt_len)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def decode_workspace(B: int, Hq: int, Hkv: int, max_pages: int, device="cuda") -> torch.Tensor:
+    n = _lib.rkv_decode_workspace_size(B, Hq, Hkv, max_pages)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def rkv_prefill_evict(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, prompt_len: Sequence[int],
+                      keep1: Sequence[int], pool_kernel: Sequence[int], cache: PagedCache, kept_idx: torch.Tensor,
+                      pooled_scores: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    B, Hq, w, d = q_win.shape
+    Lmax = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = prefill_workspace(B, Hq, cache.Hkv, w, Lmax, q_win.device)
+    _check(_lib.rkv_prefill_evict(_ptr(q_win), _ptr(k), _ptr(v), B, Hq, w, Lmax, _host_i32(prompt_len),
+                                  _host_i32(keep1), _host_i32(pool_kernel), scale, ctypes.byref(cache.struct),
+                                  _ptr(kept_idx), kept_idx.shape[-1], _ptr(pooled_scores), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)))
+
+
+def rkv_append_page_summary(cache: PagedCache, k_new: Optional[torch.Tensor] = None,
+                            v_new: Optional[torch.Tensor] = None, n_new: Optional[int] = None, stream=None):
+    if n_new is None:
+        n_new = 1 if k_new is None or k_new.dim() == 3 else k_new.shape[2]
+    _check(_lib.rkv_append_page_summary(ctypes.byref(cache.struct), _ptr(k_new), _ptr(v_new), n_new,
+                                        _stream(stream)))
+
+
+def rkv_decode_hsa(cache: PagedCache, q: torch.Tensor, k1: Sequence[int], k2: Sequence[int], out: torch.Tensor,
+                   sel_channels: Optional[torch.Tensor] = None, sel_pages: Optional[torch.Tensor] = None,
+                   scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, cache.Hkv, cache.max_pages, q.device)
+    stride = sel_pages.shape[-1] if sel_pages is not None else 0
+    _check(_lib.rkv_decode_hsa(ctypes.byref(cache.struct), _ptr(q), Hq, _host_i32(k1), _host_i32(k2), scale,
+                               _ptr(out), _ptr(sel_channels), _ptr(sel_pages), stride, _ptr(workspace),
+                               workspace.numel(), _stream(stream)))
+
+
+def rkv_get_device_status(cache: PagedCache, stream=None) -> tuple:
+    bits = ctypes.c_int32(0)
+    st = _lib.rkv_get_device_status(ctypes.byref(cache.struct), _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def rkv_last_error() -> str:
+    return _lib.rkv_last_error().decode()
+
+
+def rkv_launch_count() -> int:
+    return int(_lib.rkv_launch_count())
+
+
+def profile_enable(on: bool = True):
+    _lib.rkv_profile_enable(1 if on else 0)
+
+
+def profile_reset():
+    _lib.rkv_profile_reset()
+
+
+def profile_accumulate():
+    _lib.rkv_profile_accumulate()
+
+
+def profile_release():
+    _lib.rkv_profile_release()
+
+
+def profile_read() -> dict:
+    """{kernel name: (launches, total ms)} for every kernel kind."""
+    res = {}
+    kind = 0
+    while True:
+        n = ctypes.c_int64(0)
+        ms = ctypes.c_double(0.0)
+        name = _lib.rkv_profile_read(kind, ctypes.byref(n), ctypes.byref(ms))
+        if name is None:
+            break
+        res[name.decode()] = (int(n.value), float(ms.value))
+        kind += 1
+    return res
