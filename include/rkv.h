@@ -192,6 +192,30 @@ rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
                           int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
                           void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * rkv_decode_hsa without a workspace argument, for callers that cannot allocate
+ * device memory when they call (for instance a plug-in inside an engine that owns
+ * every device allocation, or a latency-critical loop that must never reach
+ * cudaMalloc and its device-wide synchronisation).  The pages describe no such
+ * call; it exists for those callers only.  It computes exactly what
+ * rkv_decode_hsa computes, using as scratch one array of 32 MiB compiled into the
+ * library (held on every GPU that loads the library until the process exits).
+ *   - It allocates nothing and frees nothing.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call outside any stream
+ *     capture.
+ *   - A cache whose rkv_decode_workspace_size exceeds 32 MiB is rejected with
+ *     RKV_ERR_WORKSPACE and nothing is launched.
+ *   - All calls share the one array: two calls whose work overlaps on the GPU (on
+ *     different streams, or from different threads) race and corrupt each other;
+ *     order them on one stream.  Nothing in the array needs to start at zero.
+ * Arguments, layouts and other statuses as for rkv_decode_hsa.
+ */
+rkv_status rkv_decode_hsa_noalloc(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
+                                  const int32_t* k1, const int32_t* k2, float scale, float* out,
+                                  int32_t* sel_channels, int32_t* sel_pages,
+                                  int32_t sel_pages_stride, void* stream);
+
 /* Synchronise `stream`, read and clear cache->error_word.  RKV_OK when it was 0,
  * RKV_ERR_TIMEOUT when the timeout bit was set, else RKV_ERR_DEVICE_DATA; *bits
  * (if not NULL) receives the raw word. */

@@ -145,6 +145,8 @@ void launch_end(int kind, cudaStream_t stream) {
   g_open[kind] = nullptr;
 }
 
+void set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
 int num_sms() {
   static int sms = 0;
   if (sms == 0) {

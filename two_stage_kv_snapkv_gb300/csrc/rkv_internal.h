@@ -32,6 +32,8 @@ const char* kernel_name(int kind);
 void launch_begin(int kind, cudaStream_t stream);
 void launch_end(int kind, cudaStream_t stream);
 int num_sms();
+// Sets the message rkv_last_error() returns on this thread.
+void set_last_error(const char* msg);
 
 // --------------------------------------------------------------- cache append
 cudaError_t launch_append(const rkv_cache& c, const rkv_bf16* k_new, const rkv_bf16* v_new,

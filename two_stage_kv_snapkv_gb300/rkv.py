@@ -75,6 +75,9 @@ _lib.rkv_decode_workspace_size.restype = _sz
 _lib.rkv_decode_hsa.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp, _vp, _i32,
                                 _vp, _sz, _vp]
 _lib.rkv_decode_hsa.restype = _i32
+_lib.rkv_decode_hsa_noalloc.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp,
+                                        _vp, _i32, _vp]
+_lib.rkv_decode_hsa_noalloc.restype = _i32
 _lib.rkv_get_device_status.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32p]
 _lib.rkv_get_device_status.restype = _i32
 _lib.rkv_last_error.argtypes = []
@@ -93,7 +96,7 @@ _lib.rkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.P
 _lib.rkv_profile_read.restype = ctypes.c_char_p
 
 EXPORTED = ["rkv_split_ratio", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
-            "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_get_device_status", "rkv_last_error",
+            "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
             "rkv_profile_reset", "rkv_profile_read"]
 
