@@ -4,7 +4,7 @@
 One bench step is one pass of the whole hot path over one request of the
 workload: the adaptive split, stage-1 SnapKV++ eviction of the prompt
 (rkv_prefill_evict, which also builds the page summaries), then every decode step
-(rkv_append_page_summary of the new token + rkv_decode_hsa).  Inputs are seeded,
+(rkv_decode_step: append the new token + the HSA step, one launch).  Inputs are seeded,
 synthetic and resident in HBM before timing.  L2 is flushed (a 256 MB write)
 before the prefill and before every decode step, outside the timed intervals:
 each timed interval starts with a cold L2, as a layer of a full model would.
@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-decode-steps", type=int, default=16)
     ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
+    ap.add_argument("--decode-path", choices=["auto", "split", "fused"], default="auto",
+                    help="decode implementation: one fused launch per step (auto/fused) or four kernels")
     return ap.parse_args()
 
 
@@ -154,8 +156,8 @@ class Setup:
 
     def decode(self, t: int):
         d = self.dec[t]
-        self.rkv.rkv_append_page_summary(self.cache, d["k_new"], d["v_new"], 1)
-        self.rkv.rkv_decode_hsa(self.cache, d["q"], self.k1, self.k2, self.out[t], workspace=self.dws)
+        self.rkv.rkv_decode_step(self.cache, d["q"], d["k_new"], d["v_new"], self.k1, self.k2, self.out[t],
+                                 workspace=self.dws)
 
     def flush(self):
         self.flush_buf.zero_()
@@ -174,8 +176,9 @@ class Setup:
         q = wl.B * wl.Hq * 128 * 2
         out = wl.B * wl.Hq * 128 * 4
         append = wl.B * wl.Hkv * (128 * 2 * 2 * 2 + 128 * 2 * 2 * 2)   # new k,v read+write, summaries
-        return dict(hsa_score=summ + q, hsa_attend=kv + q + out, append_small=append,
-                    step_total=summ + kv + q + out + append)
+        total = summ + kv + q + out + append
+        return dict(hsa_score=summ + q, hsa_attend=kv + q + out, append_small=append, hsa_step=total,
+                    step_total=total)
 
     def prefill_bytes(self) -> dict:
         wl = self.wl
@@ -246,6 +249,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     from two_stage_kv_snapkv_gb300 import rkv
 
     wl = W.workload(args.workload, args.seed)
+    rkv.rkv_decode_path({"auto": 0, "split": 1, "fused": 2}[args.decode_path])
     setup = Setup(wl, rkv, args.seed + rank, dev)
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
@@ -331,7 +335,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     pb = setup.prefill_bytes()
 
     def algo_bytes(kind):
-        if kind in ("hsa_score", "hsa_attend", "append_small"):
+        if kind in ("hsa_score", "hsa_attend", "append_small", "hsa_step"):
             return statistics.mean(sb[kind] for sb in step_bytes)
         if kind in pb:
             return pb[kind]
@@ -370,6 +374,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
                     step="one request: split + prefill evict + every decode step (append + HSA)",
                     l2="flushed (256 MB write) before the prefill and before every decode step; flush not timed",
                     timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
+                    decode_path=args.decode_path,
                     parallelism=f"replica x{world}" if world > 1 else "single GPU"),
         prefill_evict_ms=round(statistics.mean(pre_all), 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),
@@ -423,8 +428,8 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         for t in range(wl.steps):
             for k in dd:
                 dd[k].copy_(hdec[t][k], non_blocking=True)
-            rkv.rkv_append_page_summary(setup.cache, dd["k_new"], dd["v_new"], 1)
-            rkv.rkv_decode_hsa(setup.cache, dd["q"], setup.k1, setup.k2, setup.out[t], workspace=setup.dws)
+            rkv.rkv_decode_step(setup.cache, dd["q"], dd["k_new"], dd["v_new"], setup.k1, setup.k2, setup.out[t],
+                                workspace=setup.dws)
             hout[t].copy_(setup.out[t], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):

@@ -88,6 +88,9 @@ typedef struct {
  *                      sits": Quest-style paged max/min summaries).  Only pages
  *                      below ceil(n / page_size) are meaningful.
  *   error_word       : one device int32 receiving RKV_DEVERR_* bits.
+ *   step_sync        : [B] int32, zero when the cache is created; rkv_decode_step
+ *                      uses it to advance seq_len exactly once per sequence and
+ *                      leaves it at zero.  May be NULL if rkv_decode_step is not used.
  * max_pages must be a multiple of 8.
  */
 typedef struct {
@@ -98,6 +101,7 @@ typedef struct {
   rkv_bf16* kmax;
   rkv_bf16* kmin;
   int32_t* error_word;
+  int32_t* step_sync;
   int32_t B, Hkv, head_dim, page_size, max_pages, num_phys_pages;
 } rkv_cache;
 
@@ -165,7 +169,7 @@ rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv
 rkv_status rkv_append_page_summary(const rkv_cache* cache, const rkv_bf16* k_new,
                                    const rkv_bf16* v_new, int32_t n_new, void* stream);
 
-/* Bytes of workspace rkv_decode_hsa needs. */
+/* Bytes of workspace rkv_decode_hsa and rkv_decode_step need. */
 size_t rkv_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_pages);
 
 /*
@@ -191,6 +195,33 @@ rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
                           const int32_t* k1, const int32_t* k2, float scale, float* out,
                           int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One whole decode step: append one token to every sequence, then the HSA step of
+ * rkv_decode_hsa over the grown cache (the new token is a candidate like any
+ * other).  Equivalent to rkv_append_page_summary(cache, k_new, v_new, 1) followed
+ * by rkv_decode_hsa, but while max_pages <= 4096 it runs as one kernel launch:
+ * one thread-block cluster per (sequence, KV head) shares its page scores and its
+ * partial softmax states through distributed shared memory.
+ *   k_new, v_new : device [B][Hkv][128] bf16, the new token's key and value.
+ *   cache->step_sync must be set (zero-initialised with the cache).
+ * Other arguments as for rkv_decode_hsa; the workspace is used only by the
+ * multi-kernel path for larger caches.
+ */
+rkv_status rkv_decode_step(const rkv_cache* cache, const rkv_bf16* q, const rkv_bf16* k_new,
+                           const rkv_bf16* v_new, int32_t Hq, const int32_t* k1, const int32_t* k2,
+                           float scale, float* out, int32_t* sel_channels, int32_t* sel_pages,
+                           int32_t sel_pages_stride, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Which implementation rkv_decode_hsa / rkv_decode_step use, process-wide:
+ * 0 = automatic (the fused one-launch kernel whenever max_pages <= 4096),
+ * 1 = always the four-kernel path, 2 = fused when possible (as 0).  Any other
+ * value leaves the setting unchanged.  Returns the setting in force.  Both paths
+ * compute the same result; this exists for testing and measurement.
+ */
+int32_t rkv_decode_path(int32_t path);
 
 /*
  * rkv_decode_hsa without a workspace argument, for callers that cannot allocate

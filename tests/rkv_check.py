@@ -60,8 +60,9 @@ class GpuRun:
     """One layer of a workload on the GPU: inputs, cache, prefill, decode steps."""
 
     def __init__(self, wl: W.Workload, rkv, seed: int = 0x5EED, layer: int = 0, gen_device="cpu",
-                 tail="nan", fill=float("nan")):
+                 tail="nan", fill=float("nan"), api: str = "step"):
         self.wl, self.rkv, self.seed, self.layer = wl, rkv, seed, layer
+        self.api = api   # "step": rkv_decode_step; "separate": rkv_append_page_summary + rkv_decode_hsa
         self.dev = torch.device("cuda")
         self.inputs = W.prefill_tensors(wl, seed, layer, gen_device, tail=tail)
         self.gpu_in = {k: (v.to(self.dev) if torch.is_tensor(v) else v) for k, v in self.inputs.items()}
@@ -92,10 +93,14 @@ class GpuRun:
         out = torch.full((wl.B, wl.Hq, 128), float("nan"), dtype=torch.float32, device=self.dev)
         ch = torch.full((wl.B, wl.Hkv, 128), -9, dtype=torch.int32, device=self.dev)
         pg = torch.full((wl.B, wl.Hkv, max(self.k2) + 1), -9, dtype=torch.int32, device=self.dev)
-        self.rkv.rkv_append_page_summary(self.cache, d["k_new"].unsqueeze(2).contiguous(),
-                                         d["v_new"].unsqueeze(2).contiguous(), 1)
-        self.rkv.rkv_decode_hsa(self.cache, d["q"], self.k1, self.k2, out, sel_channels=ch, sel_pages=pg,
-                                workspace=self.dws)
+        if self.api == "step":
+            self.rkv.rkv_decode_step(self.cache, d["q"], d["k_new"], d["v_new"], self.k1, self.k2, out,
+                                     sel_channels=ch, sel_pages=pg, workspace=self.dws)
+        else:
+            self.rkv.rkv_append_page_summary(self.cache, d["k_new"].unsqueeze(2).contiguous(),
+                                             d["v_new"].unsqueeze(2).contiguous(), 1)
+            self.rkv.rkv_decode_hsa(self.cache, d["q"], self.k1, self.k2, out, sel_channels=ch, sel_pages=pg,
+                                    workspace=self.dws)
         return d, out, ch, pg
 
     def status(self):

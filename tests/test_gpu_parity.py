@@ -53,8 +53,17 @@ SMALL = {
 }
 
 
-def _run_small(rkv, wl, check_every=1):
-    run = GpuRun(wl, rkv)
+@pytest.fixture(params=["fused", "split"])
+def path(rkv, request):
+    """Run a test on each decode implementation (one fused launch / four kernels)."""
+    old = rkv.rkv_decode_path(-1)
+    rkv.rkv_decode_path(2 if request.param == "fused" else 1)
+    yield request.param
+    rkv.rkv_decode_path(old)
+
+
+def _run_small(rkv, wl, check_every=1, api="step"):
+    run = GpuRun(wl, rkv, api=api)
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     for u in units:
@@ -70,13 +79,14 @@ def _run_small(rkv, wl, check_every=1):
     return max(errs) if errs else 0.0
 
 
+@pytest.mark.parametrize("api", ["step", "separate"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_small_end_to_end(rkv, name):
-    err = _run_small(rkv, SMALL[name])
+def test_small_end_to_end(rkv, path, name, api):
+    err = _run_small(rkv, SMALL[name], api=api)
     assert err <= ATOL_OUT
 
 
-def test_tiny_workload_end_to_end(rkv):
+def test_tiny_workload_end_to_end(rkv, path):
     """Workload 1: 4K prompt, GQA 4, needles, 16 decode steps, every step checked."""
     wl = W.workload(1)
     run = GpuRun(wl, rkv)
@@ -94,7 +104,7 @@ def test_tiny_workload_end_to_end(rkv):
     assert st == rkv.RKV_OK
 
 
-def test_full_selection_is_dense_attention(rkv):
+def test_full_selection_is_dense_attention(rkv, path):
     """k1 = 128 and k2 >= pages: HSA is exact attention over every cached token."""
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[600, 450], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
@@ -114,7 +124,7 @@ def test_full_selection_is_dense_attention(rkv):
         np.testing.assert_allclose(f64(out[u.b, u.g * G:(u.g + 1) * G]), dense, atol=ATOL_OUT)
 
 
-def test_append_equals_rebuild_on_gpu(rkv):
+def test_append_equals_rebuild_on_gpu(rkv, path):
     """Incremental appends, then a from-scratch rebuild by the library: bit-identical summaries."""
     wl = W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[600, 600], budget=64, window=8, page_size=16, steps=37,
                   pool_kernel=5)
@@ -138,7 +148,7 @@ def test_append_equals_rebuild_on_gpu(rkv):
     assert st == rkv.RKV_OK
 
 
-def test_deterministic(rkv):
+def test_deterministic(rkv, path):
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[900, 700], budget=64, window=8, page_size=16, steps=3,
                   pool_kernel=5)
     outs = []
@@ -154,7 +164,7 @@ def test_deterministic(rkv):
         assert torch.equal(a.nan_to_num(), b.nan_to_num())
 
 
-def test_bad_page_id_is_flagged_not_faulted(rkv):
+def test_bad_page_id_is_flagged_not_faulted(rkv, path):
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
     run = GpuRun(wl, rkv)
     run.prefill()
@@ -167,7 +177,7 @@ def test_bad_page_id_is_flagged_not_faulted(rkv):
     assert run.status() == (rkv.RKV_OK, 0)   # the word was cleared
 
 
-def test_capacity_overflow_is_flagged(rkv):
+def test_capacity_overflow_is_flagged(rkv, path):
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
     run = GpuRun(wl, rkv)
     run.prefill()
@@ -213,7 +223,7 @@ def test_workload3_extreme_ratio_109k(rkv):
     assert _sampled_full(rkv, 3, [(0, 3)], {0, 63}) <= ATOL_OUT
 
 
-def test_workload4_batched_ragged(rkv):
+def test_workload4_batched_ragged(rkv, path):
     wl = W.workload(4)
     longest = int(np.argmax(wl.prompt_lens))
     shortest = int(np.argmin(wl.prompt_lens))

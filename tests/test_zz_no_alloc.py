@@ -42,6 +42,15 @@ def _noalloc(rkv, cache, q, k1, k2, out, ch, pg):
 
 
 def test_noalloc_matches_workspace_decode_two_calls(rkv):
+    # the four-kernel path is the one that keeps its scratch in the workspace
+    old = rkv.rkv_decode_path(1)
+    try:
+        _compare_two_calls(rkv)
+    finally:
+        rkv.rkv_decode_path(old)
+
+
+def _compare_two_calls(rkv):
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
     run = GpuRun(wl, rkv)
@@ -74,7 +83,7 @@ def test_noalloc_matches_workspace_decode_two_calls(rkv):
 
 def test_noalloc_rejects_caches_beyond_its_scratch(rkv):
     # 256 sequences x 8 query heads need 2048 x 64 split partials of 512 B: > 32 MiB
-    c = rkv.RkvCacheStruct(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000,
+    c = rkv.RkvCacheStruct(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000, 0x78000,
                            256, 1, 128, 16, 64, 256 * 64)
     k = (ctypes.c_int32 * 256)(*([32] * 256))
     before = rkv.rkv_launch_count()

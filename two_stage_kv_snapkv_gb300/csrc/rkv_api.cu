@@ -16,6 +16,7 @@ namespace {
 
 thread_local std::string g_err;
 std::atomic<long long> g_launches{0};
+std::atomic<int> g_decode_path{0};
 
 rkv_status fail(rkv_status s, const char* fmt, ...) {
   char buf[512];
@@ -111,7 +112,7 @@ const char* kernel_name(int kind) {
   static const char* names[K_NUM_KINDS] = {
       "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
       "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
-      "hsa_topk",     "hsa_attend",   "hsa_combine"};
+      "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
 }
 
@@ -271,9 +272,10 @@ size_t rkv_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max
   return rkv::decode_ws_bytes(B, Hq, Hkv, max_pages);
 }
 
-rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* k1, const int32_t* k2,
-                          float scale, float* out, int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+static rkv_status decode_common(const rkv_cache* cache, const rkv_bf16* q, const rkv_bf16* k_new,
+                                const rkv_bf16* v_new, int32_t Hq, const int32_t* k1, const int32_t* k2, float scale,
+                                float* out, int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
+                                void* workspace, size_t workspace_bytes, void* stream, const char* who) {
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -281,6 +283,11 @@ rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
   if (!al16(q) || !al16(out) || !al16(workspace) || (sel_channels && !al16(sel_channels)) ||
       (sel_pages && !al16(sel_pages)))
     return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if (k_new) {
+    if (!v_new) return fail(RKV_ERR_INVALID_ARG, "k_new and v_new must both be set");
+    if (!al16(k_new) || !al16(v_new)) return fail(RKV_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned");
+    if (!cache->step_sync) return fail(RKV_ERR_INVALID_ARG, "cache->step_sync is NULL");
+  }
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
   for (int b = 0; b < cache->B; ++b) {
     if (k1[b] < 1 || k1[b] > RKV_HEAD_DIM) return fail(RKV_ERR_INVALID_ARG, "k1[%d]=%d outside [1, 128]", b, k1[b]);
@@ -296,6 +303,9 @@ rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
   rkv::DecodeArgs a;
   a.cache = *cache;
   a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.mode = g_decode_path.load();
   a.Hq = Hq;
   a.G = Hq / cache->Hkv;
   a.k1 = k1;
@@ -307,7 +317,28 @@ rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
   a.sel_pages_stride = sel_pages_stride;
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
-  return cuda_status(rkv::launch_decode(a, static_cast<cudaStream_t>(stream)), "rkv_decode_hsa launch");
+  return cuda_status(rkv::launch_decode(a, static_cast<cudaStream_t>(stream)), who);
+}
+
+rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* k1, const int32_t* k2,
+                          float scale, float* out, int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common(cache, q, nullptr, nullptr, Hq, k1, k2, scale, out, sel_channels, sel_pages, sel_pages_stride,
+                       workspace, workspace_bytes, stream, "rkv_decode_hsa launch");
+}
+
+rkv_status rkv_decode_step(const rkv_cache* cache, const rkv_bf16* q, const rkv_bf16* k_new, const rkv_bf16* v_new,
+                           int32_t Hq, const int32_t* k1, const int32_t* k2, float scale, float* out,
+                           int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!k_new || !v_new) return fail(RKV_ERR_INVALID_ARG, "rkv_decode_step needs k_new and v_new");
+  return decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, sel_channels, sel_pages, sel_pages_stride,
+                       workspace, workspace_bytes, stream, "rkv_decode_step launch");
+}
+
+int32_t rkv_decode_path(int32_t path) {
+  if (path >= 0 && path <= 2) g_decode_path.store(path);
+  return g_decode_path.load();
 }
 
 rkv_status rkv_get_device_status(const rkv_cache* cache, void* stream, int32_t* bits) {

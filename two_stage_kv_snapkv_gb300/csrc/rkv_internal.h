@@ -24,6 +24,7 @@ enum KernelKind {
   K_HSA_TOPK,
   K_HSA_ATTEND,
   K_HSA_COMBINE,
+  K_HSA_STEP,
   K_NUM_KINDS
 };
 const char* kernel_name(int kind);
@@ -60,9 +61,13 @@ size_t prefill_ws_bytes(int B, int Hq, int Hkv, int w, int Lmax);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 
 // --------------------------------------------------------------- decode
+enum DecodePath { DECODE_AUTO = 0, DECODE_SPLIT = 1, DECODE_FUSED = 2 };
 struct DecodeArgs {
   rkv_cache cache;
   const rkv_bf16* q;
+  const rkv_bf16* k_new;  // null: no append (rkv_decode_hsa)
+  const rkv_bf16* v_new;
+  int mode;               // DecodePath
   int Hq, G;
   const int32_t* k1;  // host [B]
   const int32_t* k2;  // host [B]
@@ -75,6 +80,7 @@ struct DecodeArgs {
   size_t ws_bytes;
 };
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages);
+bool decode_fused_ok(const rkv_cache& c);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 }  // namespace rkv

@@ -54,7 +54,7 @@ class RkvSplit(ctypes.Structure):
 class RkvCacheStruct(ctypes.Structure):
     _fields_ = [("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
                 ("seq_len", ctypes.c_void_p), ("kmax", ctypes.c_void_p), ("kmin", ctypes.c_void_p),
-                ("error_word", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("error_word", ctypes.c_void_p), ("step_sync", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32), ("max_pages", ctypes.c_int32),
                 ("num_phys_pages", ctypes.c_int32)]
 
@@ -75,6 +75,11 @@ _lib.rkv_decode_workspace_size.restype = _sz
 _lib.rkv_decode_hsa.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp, _vp, _i32,
                                 _vp, _sz, _vp]
 _lib.rkv_decode_hsa.restype = _i32
+_lib.rkv_decode_step.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _vp, _vp, _i32, _i32p, _i32p, _f32, _vp, _vp,
+                                 _vp, _i32, _vp, _sz, _vp]
+_lib.rkv_decode_step.restype = _i32
+_lib.rkv_decode_path.argtypes = [_i32]
+_lib.rkv_decode_path.restype = _i32
 _lib.rkv_decode_hsa_noalloc.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp,
                                         _vp, _i32, _vp]
 _lib.rkv_decode_hsa_noalloc.restype = _i32
@@ -96,7 +101,8 @@ _lib.rkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.P
 _lib.rkv_profile_read.restype = ctypes.c_char_p
 
 EXPORTED = ["rkv_split_ratio", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
-            "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_get_device_status", "rkv_last_error",
+            "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
+            "rkv_decode_path", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
             "rkv_profile_reset", "rkv_profile_read"]
 
@@ -155,10 +161,11 @@ class PagedCache:
                 t.fill_(fill)
         self.seq_len = torch.zeros(B, dtype=torch.int32, device=device)
         self.error_word = torch.zeros(4, dtype=torch.int32, device=device)
+        self.step_sync = torch.zeros(B, dtype=torch.int32, device=device)
         self._struct = RkvCacheStruct(
             self.k_pages.data_ptr(), self.v_pages.data_ptr(), self.page_table.data_ptr(), self.seq_len.data_ptr(),
-            self.kmax.data_ptr(), self.kmin.data_ptr(), self.error_word.data_ptr(), B, Hkv, HEAD_DIM, page_size,
-            max_pages, num_phys_pages)
+            self.kmax.data_ptr(), self.kmin.data_ptr(), self.error_word.data_ptr(), self.step_sync.data_ptr(), B, Hkv,
+            HEAD_DIM, page_size, max_pages, num_phys_pages)
 
     @property
     def struct(self) -> RkvCacheStruct:
@@ -235,6 +242,27 @@ def rkv_decode_hsa(cache: PagedCache, q: torch.Tensor, k1: Sequence[int], k2: Se
     _check(_lib.rkv_decode_hsa(ctypes.byref(cache.struct), _ptr(q), Hq, _host_i32(k1), _host_i32(k2), scale,
                                _ptr(out), _ptr(sel_channels), _ptr(sel_pages), stride, _ptr(workspace),
                                workspace.numel(), _stream(stream)))
+
+
+def rkv_decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                    k1: Sequence[int], k2: Sequence[int], out: torch.Tensor,
+                    sel_channels: Optional[torch.Tensor] = None, sel_pages: Optional[torch.Tensor] = None,
+                    scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Append one token ([B, Hkv, 128] k_new / v_new) and run the HSA step, as one launch."""
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, cache.Hkv, cache.max_pages, q.device)
+    stride = sel_pages.shape[-1] if sel_pages is not None else 0
+    _check(_lib.rkv_decode_step(ctypes.byref(cache.struct), _ptr(q), _ptr(k_new), _ptr(v_new), Hq, _host_i32(k1),
+                                _host_i32(k2), scale, _ptr(out), _ptr(sel_channels), _ptr(sel_pages), stride,
+                                _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def rkv_decode_path(path: int = -1) -> int:
+    """0 auto (fused when it fits), 1 four-kernel path, 2 fused; -1 only reads the setting."""
+    return int(_lib.rkv_decode_path(path))
 
 
 def rkv_get_device_status(cache: PagedCache, stream=None) -> tuple:
