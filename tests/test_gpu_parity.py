@@ -148,6 +148,25 @@ def test_append_equals_rebuild_on_gpu(rkv, path):
     assert st == rkv.RKV_OK
 
 
+@pytest.mark.parametrize("L", [3000, 700])
+def test_prefill_select_with_large_tie_groups(rkv, L):
+    """Prompt keys take only two values, so hundreds of scores tie exactly at the top-k
+    boundary: the kept set must be exactly the oracle's (ties go to lower positions)."""
+    wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[L], budget=128, window=8, page_size=16, steps=1, pool_kernel=1)
+    run = GpuRun(wl, rkv)
+    k = run.inputs["k"]
+    a, bvec = k[0, 0, 0].clone(), k[0, 0, 1].clone()
+    pattern = (torch.arange(L) % 3 == 0)
+    k[0, 0, :L][pattern] = a
+    k[0, 0, :L][~pattern] = bvec
+    run.gpu_in["k"] = k.to(run.dev)
+    run.prefill()
+    u = OracleUnit(run, 0, 0)
+    kept = run.kept[0, 0, : run.keep1[0]].cpu().numpy()
+    np.testing.assert_array_equal(kept, u.res["kept"][0])
+    assert run.status()[0] == rkv.RKV_OK
+
+
 def test_deterministic(rkv, path):
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[900, 700], budget=64, window=8, page_size=16, steps=3,
                   pool_kernel=5)

@@ -20,14 +20,17 @@
 //   caller's workspace) for larger caches.
 //
 // Attention in both: the selected pages are cut into 16-token chunks; each warp
-// streams chunks through a ring of shared-memory stages filled by bulk copies
-// (cp.async.bulk, TMA engine; one 256-B row per lane, 16 K rows + 16 V rows) that
-// complete on an mbarrier; q.K^T and P.V are m16n8k16 bf16 tensor-core MMAs with
-// the GQA group's heads as the M rows; fp32 online softmax; P split into bf16 hi +
-// lo so the P.V product keeps ~16 bits of the probabilities.
+// streams chunks through a ring of shared-memory stages filled by tiled TMA loads
+// (cp.async.bulk.tensor, 128-byte swizzle: four 16 x 64 boxes per chunk, K and V
+// halves) that complete on an mbarrier; q.K^T and P.V are m16n8k16 bf16 tensor-core
+// MMAs fed by ldmatrix from the swizzled rows, with the GQA group's heads as the M
+// rows; fp32 online softmax; P split into bf16 hi + lo so the P.V product keeps
+// ~16 bits of the probabilities.
 #include <climits>
 
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "rkv_device.cuh"
 #include "rkv_internal.h"
@@ -45,20 +48,23 @@ constexpr int kAtWarps = 4;
 constexpr int kThreads = kAtWarps * 32;
 constexpr int kSplitStages = 3;
 constexpr int kFusedStages = 2;
-constexpr int kChunkTok = 16;                           // tokens per pipeline stage
-constexpr int kRowBytes = 272;                          // 256 B token row + 16 B pad
-constexpr int kStageBytes = 2 * kChunkTok * kRowBytes;  // K rows then V rows
+constexpr int kChunkTok = 16;                 // tokens per pipeline stage
+constexpr int kHalfBytes = kChunkTok * 128;   // one 16-token x 64-channel box (128-B rows)
+constexpr int kStageBytes = 4 * kHalfBytes;   // K lo, K hi, V lo, V hi
 constexpr int kWarpCombineBytes = kAtWarps * 8 * (2 + 128) * 4;
 constexpr int kFusedMaxPages = 4096;
 constexpr int kMaxCluster = 8;
 
 constexpr int ring_bytes(int stages) { return kAtWarps * stages * kStageBytes; }
-constexpr int kSplitSmem = ring_bytes(kSplitStages) > kWarpCombineBytes ? ring_bytes(kSplitStages) : kWarpCombineBytes;
+constexpr int kSplitSmem =
+    1024 + (ring_bytes(kSplitStages) > kWarpCombineBytes ? ring_bytes(kSplitStages) : kWarpCombineBytes);
 static_assert(ring_bytes(kFusedStages) >= kWarpCombineBytes, "the ring doubles as the warp-combine buffer");
 // the summary staging tile must hold at least 8 pages of all 128 channels (Kmax + Kmin)
 static_assert(ring_bytes(kFusedStages) >= 2 * 128 * 8 * 2, "staging tile too small");
 
 struct HsaParams {
+  CUtensorMap tmk;         // k_pages as [num_phys*Hkv*P rows][128] bf16, 16x64 boxes, 128-B swizzle
+  CUtensorMap tmv;         // v_pages, same
   rkv_bf16* k_pages;
   rkv_bf16* v_pages;
   const int32_t* page_table;
@@ -78,7 +84,7 @@ struct HsaParams {
   int32_t* sel_channels;
   int32_t* sel_pages;
   int sel_pages_stride;
-  int B, Hkv, Hq, G, P, max_pages, num_phys, nsplit, cluster;
+  int B, Hkv, Hq, G, P, max_pages, num_phys, nsplit, cluster, region_bytes;
   float scale_log2;
   int32_t k1[RKV_MAX_BATCH];
   int32_t k2[RKV_MAX_BATCH];
@@ -97,38 +103,44 @@ __device__ __forceinline__ int seq_length(const HsaParams& p, int b) {
 
 // Shared-memory state of the channel selection (one KV head).
 struct ChanSmem {
-  float qf[8][128];
-  unsigned long long akey[128];
+  alignas(16) unsigned long long akey[128];
   int chan[128];
   float qpos[128], qneg[128];
-  int warp_cnt[4];
+  int warp_cnt[8];  // also the scratch of a 128-thread block scan (5 ints)
 };
 
 // Top-k1 channels of a_i = sum_h |q_h,i| (ties: lower channel), ascending, with the
 // per-channel sums of the positive and negative parts of q over the group.  The
 // channel score is summed in fp64, where a sum of <= 8 bf16 magnitudes is exact, and
 // ranked on its bit pattern (order-preserving for non-negative doubles).
-// Every thread of a block of >= 128 threads calls this after filling qf.
-__device__ void select_channels(ChanSmem& cs, int G, int k1) {
+// Every thread of a block of >= 128 threads calls this after filling qf[G][128].
+__device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int k1) {
   const int tid = threadIdx.x;
   __syncthreads();
   if (tid < 128) {
     double s = 0.0;
-    for (int h = 0; h < G; ++h) s += fabs((double)cs.qf[h][tid]);
+    for (int h = 0; h < G; ++h) s += fabs((double)qf[h][tid]);
     cs.akey[tid] = (unsigned long long)__double_as_longlong(s);
   }
   __syncthreads();
   bool sel = false;
   unsigned bal = 0;
   if (tid < 128) {
+    // rank = #greater + #equal at a lower channel; four independent counters keep the
+    // shared-memory loads in flight
     const unsigned long long ai = cs.akey[tid];
-    int rank = 0;
-#pragma unroll 8
-    for (int j = 0; j < 128; ++j) {
-      const unsigned long long aj = cs.akey[j];
-      rank += (aj > ai) || (aj == ai && j < tid);
+    const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(cs.akey);
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 4
+    for (int j2 = 0; j2 < 64; j2 += 2) {
+      const ulonglong2 u = a2[j2], v = a2[j2 + 1];
+      const int j = 2 * j2;
+      r0 += (u.x > ai) | ((u.x == ai) & (j < tid));
+      r1 += (u.y > ai) | ((u.y == ai) & (j + 1 < tid));
+      r2 += (v.x > ai) | ((v.x == ai) & (j + 2 < tid));
+      r3 += (v.y > ai) | ((v.y == ai) & (j + 3 < tid));
     }
-    sel = rank < k1;
+    sel = (r0 + r1) + (r2 + r3) < k1;
     bal = __ballot_sync(0xffffffffu, sel);
     if ((tid & 31) == 0) cs.warp_cnt[tid >> 5] = __popc(bal);
   }
@@ -139,7 +151,7 @@ __device__ void select_channels(ChanSmem& cs, int G, int k1) {
     cs.chan[pos] = tid;
     float sp = 0.f, sn = 0.f;
     for (int h = 0; h < G; ++h) {
-      const float x = cs.qf[h][tid];
+      const float x = qf[h][tid];
       sp += fmaxf(x, 0.f);
       sn += fminf(x, 0.f);
     }
@@ -207,23 +219,46 @@ __device__ void topk_ascending(const uint32_t* keys, int n, int k, uint32_t* his
   }
 }
 
-// Shared-memory state of one CTA's attention.
+// Shared-memory address of 16-byte piece `piece` (channels 8*piece .. 8*piece+7) of
+// token row `row` in a TMA-written K or V block: two 16 x 64 boxes (channels 0-63,
+// 64-127) of 128-byte rows, each 16-byte piece XOR-ed with row % 8 (128-B swizzle;
+// the block is 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int piece) {
+  return base + (piece >> 3) * kHalfBytes + row * 128 + ((((piece & 7) ^ (row & 7))) << 4);
+}
+
+// Dynamic shared memory rounded up to a 1024-byte boundary (the TMA swizzle atom).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// Barriers of one CTA's attention ring.
 template <int STAGES>
 struct AttnSmem {
   uint64_t bars[kAtWarps][STAGES];
   int tstart[kAtWarps][STAGES];
-  float ctaM[8], ctaL[8];
-  float ctaO[8][128];
 };
+
+// A CTA's merged softmax state per head (unnormalised), left in its ring.
+struct CtaPart {
+  float M[8], L[8];
+  float O[8][128];
+};
+constexpr int kCtaPartOffset = (kWarpCombineBytes + 255) & ~255;
+static_assert(kCtaPartOffset + (int)sizeof(CtaPart) <= ring_bytes(kFusedStages), "ring too small for the partials");
 
 // Attention of one CTA (4 warps) over items [it0, it1) of the unit's selected pages
 // `sel` (ascending page ids; item i = chunk i % cpp of page sel[i / cpp]); `ptab` is
-// the sequence's page-table row.  Leaves the CTA's merged softmax state per head in
-// a.ctaM / a.ctaL / a.ctaO (unnormalised) and returns 1 when a bounded wait ran out.
-// `ring` is ring_bytes(STAGES) of shared memory, at least kWarpCombineBytes.
+// the sequence's page-table row.  When new_pos >= 0, token new_pos is taken from
+// new_kv (shared memory: its 128 K then 128 V bf16 values) instead of its cache slot,
+// which may still be being written.  Leaves the CTA's merged state in the returned
+// CtaPart (inside `ring`, ring_bytes(STAGES) of 1024-aligned shared memory) and sets
+// *timed_out when a bounded wait ran out.
 template <int STAGES>
-__device__ int attend_cta(const HsaParams& p, const int32_t* sel, const int32_t* ptab, int b, int g, int n, int it0,
-                          int it1, uint8_t* ring, AttnSmem<STAGES>& a) {
+__device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int32_t* ptab, int b, int g, int n,
+                               int it0, int it1, uint8_t* ring, AttnSmem<STAGES>& a, int new_pos,
+                               const uint8_t* new_kv, int* timed_out_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = p.P, G = p.G;
   const int NP = (n + P - 1) / P;
@@ -262,14 +297,17 @@ __device__ int attend_cta(const HsaParams& p, const int32_t* sel, const int32_t*
       phys = 0;
       t0 = INT_MAX / 2;  // every token of this chunk is masked
     }
-    const size_t off = (((size_t)phys * p.Hkv + g) * P + (size_t)chunk * kChunkTok) * 128;
+    const int y = (phys * p.Hkv + g) * P + chunk * kChunkTok;
     if (lane == 0) {
       a.tstart[warp][s] = t0;
-      mbar_arrive_expect_tx(&a.bars[warp][s], 2 * kChunkTok * 256);
+      uint8_t* st = wbuf + s * kStageBytes;
+      mbar_arrive_expect_tx(&a.bars[warp][s], kStageBytes);
+      tma_load_2d(st, &p.tmk, 0, y, &a.bars[warp][s]);
+      tma_load_2d(st + kHalfBytes, &p.tmk, 64, y, &a.bars[warp][s]);
+      tma_load_2d(st + 2 * kHalfBytes, &p.tmv, 0, y, &a.bars[warp][s]);
+      tma_load_2d(st + 3 * kHalfBytes, &p.tmv, 64, y, &a.bars[warp][s]);
     }
     __syncwarp();
-    const rkv_bf16* src = lane < 16 ? p.k_pages + off + lane * 128 : p.v_pages + off + (lane - 16) * 128;
-    bulk_g2s(wbuf + s * kStageBytes + lane * kRowBytes, src, 256, &a.bars[warp][s]);
   };
 
   float m_run = -1e30f, l_run = 0.f;
@@ -289,35 +327,52 @@ __device__ int attend_cta(const HsaParams& p, const int32_t* sel, const int32_t*
       break;
     }
     uint8_t* kb = wbuf + s * kStageBytes;
-    uint8_t* vb = kb + kChunkTok * kRowBytes;
-    const int nvalid = n - a.tstart[warp][s];
-    if (nvalid < kChunkTok) {
-      // rows past the end of the sequence hold stale data: zero their V rows
-      const int nv = max(nvalid, 0);
-      for (int w16 = lane; w16 < (kChunkTok - nv) * 16; w16 += 32)
-        *reinterpret_cast<uint4*>(vb + (nv + (w16 >> 4)) * kRowBytes + (w16 & 15) * 16) = make_uint4(0, 0, 0, 0);
+    uint8_t* vb = kb + 2 * kHalfBytes;
+    const int t0 = a.tstart[warp][s];
+    const int nvalid = n - t0;
+    const bool has_new = new_pos >= t0 && new_pos < t0 + kChunkTok;
+    if (nvalid < kChunkTok || has_new) {
+      if (nvalid < kChunkTok) {
+        // rows past the end of the sequence hold stale data: zero their V rows (both
+        // halves; the swizzle only permutes 16-B pieces within a 128-B row)
+        const int nv = max(nvalid, 0);
+        for (int w16 = lane; w16 < (kChunkTok - nv) * 16; w16 += 32) {
+          const int row = nv + (w16 >> 4), piece = w16 & 15;
+          *reinterpret_cast<uint4*>(vb + (piece >> 3) * kHalfBytes + row * 128 + (piece & 7) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (has_new) {
+        // the appended token: lanes 0-15 write its K pieces, lanes 16-31 its V pieces
+        const int row = new_pos - t0, piece = lane & 15;
+        uint8_t* dst = (lane < 16 ? kb : vb) + (piece >> 3) * kHalfBytes + row * 128 + (((piece & 7) ^ (row & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(new_kv + lane * 16);
+      }
       fence_proxy_async_smem();
       __syncwarp();
     }
-    float sacc[2][4];
+    // q.K^T for 16 tokens; two accumulators per n-tile shorten the MMA chains
+    float sacc[2][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) sacc[nt][e][0] = sacc[nt][e][1] = sacc[nt][e][2] = sacc[nt][e][3] = 0.f;
     const uint32_t kb32 = smem_u32(kb), vb32 = smem_u32(vb);
 #pragma unroll
     for (int kk2 = 0; kk2 < 4; ++kk2) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, kb32 + (nt * 8 + (lane & 7)) * kRowBytes + (kk2 * 32 + (lane >> 3) * 8) * 2);
-        mma_16816(sacc[nt], qa0[2 * kk2], 0u, qa2[2 * kk2], 0u, b0, b1);
-        mma_16816(sacc[nt], qa0[2 * kk2 + 1], 0u, qa2[2 * kk2 + 1], 0u, b2, b3);
+        ldsm_x4(b0, b1, b2, b3, swz(kb32, nt * 8 + (lane & 7), kk2 * 4 + (lane >> 3)));
+        mma_16816(sacc[nt][0], qa0[2 * kk2], 0u, qa2[2 * kk2], 0u, b0, b1);
+        mma_16816(sacc[nt][1], qa0[2 * kk2 + 1], 0u, qa2[2 * kk2 + 1], 0u, b2, b3);
       }
     }
     const int c0 = 2 * q4;
-    const float z0 = (c0 < nvalid) ? sacc[0][0] * sl : -INFINITY;
-    const float z1 = (c0 + 1 < nvalid) ? sacc[0][1] * sl : -INFINITY;
-    const float z2 = (c0 + 8 < nvalid) ? sacc[1][0] * sl : -INFINITY;
-    const float z3 = (c0 + 9 < nvalid) ? sacc[1][1] * sl : -INFINITY;
+    const float z0 = (c0 < nvalid) ? (sacc[0][0][0] + sacc[0][1][0]) * sl : -INFINITY;
+    const float z1 = (c0 + 1 < nvalid) ? (sacc[0][0][1] + sacc[0][1][1]) * sl : -INFINITY;
+    const float z2 = (c0 + 8 < nvalid) ? (sacc[1][0][0] + sacc[1][1][0]) * sl : -INFINITY;
+    const float z3 = (c0 + 9 < nvalid) ? (sacc[1][0][1] + sacc[1][1][1]) * sl : -INFINITY;
     float mx = fmaxf(fmaxf(z0, z1), fmaxf(z2, z3));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -338,11 +393,10 @@ __device__ int attend_cta(const HsaParams& p, const int32_t* sel, const int32_t*
 #pragma unroll
     for (int nt2 = 0; nt2 < 8; ++nt2) {
       uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(v0, v1, v2, v3,
-                vb32 + ((lane & 7) + ((lane >> 3) & 1) * 8) * kRowBytes + (nt2 * 16 + (lane >> 4) * 8) * 2);
+      ldsm_x4_t(v0, v1, v2, v3, swz(vb32, (lane & 7) + ((lane >> 3) & 1) * 8, nt2 * 2 + (lane >> 4)));
       mma_16816(o[2 * nt2], ph0, 0u, ph2, 0u, v0, v1);
-      mma_16816(o[2 * nt2], pl0, 0u, pl2, 0u, v0, v1);
       mma_16816(o[2 * nt2 + 1], ph0, 0u, ph2, 0u, v2, v3);
+      mma_16816(o[2 * nt2], pl0, 0u, pl2, 0u, v0, v1);
       mma_16816(o[2 * nt2 + 1], pl0, 0u, pl2, 0u, v2, v3);
     }
     __syncwarp();
@@ -356,13 +410,14 @@ __device__ int attend_cta(const HsaParams& p, const int32_t* sel, const int32_t*
     // wait (bounded) for this warp's copies still in flight before the ring is reused
     for (int j = consumed; j < issued; ++j) mbar_wait(&a.bars[warp][j % STAGES], (uint32_t)((j / STAGES) & 1));
   }
-  const int any_to = __syncthreads_or(timed_out);
+  *timed_out_out = __syncthreads_or(timed_out);
 
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
   float* cm = reinterpret_cast<float*>(ring);  // the ring is free now
   float* cl = cm + kAtWarps * 8;
   float* co = cl + kAtWarps * 8;
+  CtaPart* part = reinterpret_cast<CtaPart*>(ring + kCtaPartOffset);
   if (hv) {
     if (q4 == 0) {
       cm[warp * 8 + hrow] = m_run;
@@ -387,28 +442,39 @@ __device__ int attend_cta(const HsaParams& p, const int32_t* sel, const int32_t*
       L += cl[w * 8 + h] * f;
       O += co[(w * 8 + h) * 128 + c] * f;
     }
-    a.ctaO[h][c] = O;
+    part->O[h][c] = O;
     if (c == 0) {
-      a.ctaM[h] = M;
-      a.ctaL[h] = L;
+      part->M[h] = M;
+      part->L[h] = L;
     }
   }
   __syncthreads();
-  return any_to;
+  return part;
 }
 
 // ---------------------------------------------------------------------------
 // Fused decode step.  grid (C, B*Hkv), cluster (C, 1, 1), 128 threads.
-// Dynamic shared memory: ring (2 stages x 4 warps; first used to stage summaries) |
-// keys [max_pages] | sel [max_pages] | page-table row [max_pages].
+// Dynamic shared memory (1024-aligned start):
+//   region [region_bytes]: the query, then the staged summaries, then the K/V ring
+//                          (STAGES x 4 warps x 8 KB) and the warp partials;
+//   keys [max_pages] | sel [max_pages] | page-table row [max_pages];
+//   inbox [C][ceil(G/C)][130] floats: the other CTAs' partial states of the heads
+//                          this CTA finishes.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
+
+template <int STAGES>
 __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constant__ HsaParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ChanSmem cs;
-  __shared__ AttnSmem<kFusedStages> as;
-  __shared__ uint32_t hist[258];
-  __shared__ int scan[kAtWarps + 1];
+  __shared__ AttnSmem<STAGES> as;
   __shared__ uint64_t sbar, pbar;
+  __shared__ __align__(16) uint8_t new_kv[512];
+  __shared__ uint32_t hist[258];
+  __shared__ int scan[kThreads / 32 + 1];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = p.cluster;
@@ -416,12 +482,27 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv;
   const int tid = threadIdx.x;
   const int G = p.G, P = p.P;
-  uint8_t* ring = smem;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + ring_bytes(kFusedStages));
+  uint8_t* ring = align1024(smem);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(ring + p.region_bytes);
   int32_t* sel = reinterpret_cast<int32_t*>(keys + p.max_pages);
   int32_t* ptab = sel + p.max_pages;
+  float* inbox = reinterpret_cast<float*>(ptab + p.max_pages);
+  const int hpc = (G + C - 1) / C;  // heads finished per CTA
+  float(*qf)[128] = reinterpret_cast<float(*)[128]>(ring);  // until the summaries are staged
 
-  // 1. length before this step; the append makes it n0 + 1
+  // every CTA of the cluster must be running before anyone stores into its shared
+  // memory: arrive now, wait just before the first remote store
+  cluster_arrive_relaxed();
+
+  // 1. loads that depend on nothing: the group's query (16 bytes per thread), the new
+  // token's K and V rows, the sequence length (one round trip for all of them)
+  const rkv_bf16* qg = p.q + ((size_t)b * p.Hq + (size_t)g * G) * 128;
+  uint4 qv = make_uint4(0, 0, 0, 0), nkv = make_uint4(0, 0, 0, 0);
+  if (tid < G * 16) qv = *reinterpret_cast<const uint4*>(qg + tid * 8);
+  if (p.k_new && tid < 32)
+    nkv = *reinterpret_cast<const uint4*>((tid < 16 ? p.k_new : p.v_new) + ((size_t)b * p.Hkv + g) * 128 +
+                                          (tid & 15) * 8);
+  // the length before this step; the append makes it n0 + 1
   const int cap = p.max_pages * P;
   int n0 = p.seq_len[b];
   bool do_append = p.k_new != nullptr;
@@ -450,65 +531,53 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     }
   }
 
-  // 3. query of the group
-  const rkv_bf16* qg = p.q + ((size_t)b * p.Hq + (size_t)g * G) * 128;
-  for (int i = tid; i < G * 128; i += kThreads) cs.qf[i >> 7][i & 127] = bf16_f(qg[i]);
+  // 3. query of the group and the new token's rows into shared memory
+  if (tid < G * 16) {  // 8 channels per thread
+    float* dst = &qf[tid >> 4][(tid & 15) * 8];
+    dst[0] = bf16_lo(qv.x); dst[1] = bf16_hi(qv.x); dst[2] = bf16_lo(qv.y); dst[3] = bf16_hi(qv.y);
+    dst[4] = bf16_lo(qv.z); dst[5] = bf16_hi(qv.z); dst[6] = bf16_lo(qv.w); dst[7] = bf16_hi(qv.w);
+  }
+  if (do_append && tid < 32) *reinterpret_cast<uint4*>(new_kv + tid * 16) = nkv;
 
-  // 4. append (rank 0): token into its slot, its page's Kmax/Kmin folded
-  if (do_append && rank == 0 && tid < 64) {
-    const int page = n0 / P, slot = n0 % P;
-    const int phys = p.page_table[(size_t)b * p.max_pages + page];
-    if (phys >= 0 && phys < p.num_phys) {
-      const size_t src = ((size_t)b * p.Hkv + g) * 128 + 2 * tid;
-      const size_t dst = (((size_t)phys * p.Hkv + g) * P + slot) * 128 + 2 * tid;
-      const uint32_t ku = *reinterpret_cast<const uint32_t*>(p.k_new + src);
-      *reinterpret_cast<uint32_t*>(p.k_pages + dst) = ku;
-      *reinterpret_cast<uint32_t*>(p.v_pages + dst) = *reinterpret_cast<const uint32_t*>(p.v_new + src);
-      const size_t row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + page;
-      float mx0 = bf16_lo(ku), mx1 = bf16_hi(ku), mn0 = mx0, mn1 = mx1;
-      if (slot > 0) {
-        mx0 = fmaxf(bf16_f(p.kmax[row]), mx0);
-        mx1 = fmaxf(bf16_f(p.kmax[row + p.max_pages]), mx1);
-        mn0 = fminf(bf16_f(p.kmin[row]), mn0);
-        mn1 = fminf(bf16_f(p.kmin[row + p.max_pages]), mn1);
-      }
-      p.kmax[row] = (rkv_bf16)(__float_as_uint(mx0) >> 16);
-      p.kmax[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mx1) >> 16);
-      p.kmin[row] = (rkv_bf16)(__float_as_uint(mn0) >> 16);
-      p.kmin[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mn1) >> 16);
-      // the new K/V row and summaries are read back by bulk copies (async proxy)
-      asm volatile("fence.proxy.async.global;\n" ::: "memory");
-    } else {
-      flag_error(p.err, RKV_DEVERR_PAGE_ID);
-    }
+  // 4. append (rank 0): the token goes into its slot and its page's Kmax/Kmin are
+  // folded.  Within this step every CTA takes the token from new_kv, so nothing waits
+  // for these writes: the loads are issued here, the stores after the scoring.
+  const bool appender = do_append && rank == 0 && tid < 64;
+  uint32_t app_k = 0, app_v = 0, app_mx = 0, app_mn = 0;
+  int app_phys = -1;
+  size_t app_row = 0;
+  if (appender) {
+    const int page = n0 / P;
+    const size_t src = ((size_t)b * p.Hkv + g) * 128 + 2 * tid;
+    app_row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + page;
+    app_phys = p.page_table[(size_t)b * p.max_pages + page];
+    app_k = *reinterpret_cast<const uint32_t*>(p.k_new + src);
+    app_v = *reinterpret_cast<const uint32_t*>(p.v_new + src);
+    app_mx = (uint32_t)p.kmax[app_row] | ((uint32_t)p.kmax[app_row + p.max_pages] << 16);
+    app_mn = (uint32_t)p.kmin[app_row] | ((uint32_t)p.kmin[app_row + p.max_pages] << 16);
   }
 
   // 5. channels (every CTA)
   const int k1 = p.k1[b];
-  select_channels(cs, G, k1);
-  cluster.sync();  // the append is visible; every CTA of the cluster has read seq_len
+  select_channels(qf, cs, G, k1);
 
-  // 6. the last cluster of sequence b to get here advances seq_len
-  if (do_append && rank == 0 && tid == 0) {
-    __threadfence();
-    if (atomicAdd(&p.sync[b], 1) == p.Hkv - 1) {
-      p.sync[b] = 0;
-      p.seq_len[b] = n;
-    }
-  }
-
-  // 7. page bounds of this CTA's slice [p0, p1) (8-page aligned).  The k1 Kmax and
-  // k1 Kmin row pieces of a tile are bulk-copied into the ring at once (one round
-  // trip), then every thread bounds pages from shared memory.
+  // 6. page bounds of this CTA's slice [p0, p1) (8-page aligned).  The k1 Kmax and
+  // k1 Kmin row pieces of a tile (the region holds the whole slice whenever it fits)
+  // are bulk-copied at once (one round trip); the appended token is folded into its
+  // page's staged summary (a fold that the append may already have done changes
+  // nothing: max and min are idempotent); then every thread bounds pages from shared
+  // memory, and the scores go to every CTA's key array.
   const int per = ((NP + C - 1) / C + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
-  const int tcap = (ring_bytes(kFusedStages) / (4 * k1)) & ~7;
-  const rkv_bf16* smax = reinterpret_cast<const rkv_bf16*>(ring);
+  const int tcap = (p.region_bytes / (4 * k1)) & ~7;
+  rkv_bf16* stg = reinterpret_cast<rkv_bf16*>(ring);
+  const int pnew = do_append ? n0 / P : -1;
+  bool waited = false;
   for (int t0 = p0, tile = 0; t0 < p1; t0 += tcap, ++tile) {
     const int cnt = min(tcap, p1 - t0);
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
     fence_proxy_async_smem();
-    __syncthreads();  // the previous tile is consumed
+    __syncthreads();  // the previous tile (or the query) is consumed
     if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
     __syncthreads();
     for (int i = tid; i < 2 * k1; i += kThreads) {
@@ -518,62 +587,187 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
                (uint32_t)cnt8 * 2, &sbar);
     }
     if (!mbar_wait(&sbar, (uint32_t)(tile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
-    for (int j = tid; j < cnt; j += kThreads) {
-      float s = 0.f;
-      for (int kk = 0; kk < k1; ++kk) {
-        s = fmaf(cs.qpos[kk], bf16_f(smax[kk * cnt8 + j]), s);
-        s = fmaf(cs.qneg[kk], bf16_f(smax[(k1 + kk) * cnt8 + j]), s);
+    if (pnew >= t0 && pnew < t0 + cnt) {
+      const int j = pnew - t0;
+      const bool first = (n0 % P) == 0;
+      const rkv_bf16* kn = reinterpret_cast<const rkv_bf16*>(new_kv);
+      for (int kk = tid; kk < k1; kk += kThreads) {
+        const float x = bf16_f(kn[cs.chan[kk]]);
+        const float hi = first ? x : fmaxf(bf16_f(stg[kk * cnt8 + j]), x);
+        const float lo = first ? x : fminf(bf16_f(stg[(k1 + kk) * cnt8 + j]), x);
+        stg[kk * cnt8 + j] = (rkv_bf16)(__float_as_uint(hi) >> 16);
+        stg[(k1 + kk) * cnt8 + j] = (rkv_bf16)(__float_as_uint(lo) >> 16);
       }
-      keys[t0 + j] = float_key(s);
+      __syncthreads();
+    }
+    if (!waited) {  // peers are running: their key arrays can take our scores
+      cluster_wait();
+      waited = true;
+    }
+    for (int j = tid; j < cnt; j += kThreads) {
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // independent chains
+      int kk = 0;
+      for (; kk + 1 < k1; kk += 2) {
+        s0 = fmaf(cs.qpos[kk], bf16_f(stg[kk * cnt8 + j]), s0);
+        s1 = fmaf(cs.qneg[kk], bf16_f(stg[(k1 + kk) * cnt8 + j]), s1);
+        s2 = fmaf(cs.qpos[kk + 1], bf16_f(stg[(kk + 1) * cnt8 + j]), s2);
+        s3 = fmaf(cs.qneg[kk + 1], bf16_f(stg[(k1 + kk + 1) * cnt8 + j]), s3);
+      }
+      if (kk < k1) {
+        s0 = fmaf(cs.qpos[kk], bf16_f(stg[kk * cnt8 + j]), s0);
+        s1 = fmaf(cs.qneg[kk], bf16_f(stg[(k1 + kk) * cnt8 + j]), s1);
+      }
+      const uint32_t key = float_key((s0 + s2) + (s1 + s3));
+      for (int r = 0; r < C; ++r) cluster.map_shared_rank(keys, r)[t0 + j] = key;
     }
   }
-  fence_proxy_async_smem();  // generic reads of the ring before the attention's bulk copies
-  cluster.sync();            // every slice is written
+  if (!waited) cluster_wait();
+  fence_proxy_async_smem();  // generic accesses to the region before the attention's TMA loads
+  cluster.sync();            // every CTA holds every page's key
 
-  // 8. gather the other slices, then the same top-k2 in every CTA
-  for (int r = 0; r < C; ++r) {
-    if (r == rank) continue;
-    const uint32_t* remote = cluster.map_shared_rank(keys, r);
-    const int r0 = min(NP, r * per), r1 = min(NP, r0 + per);
-    for (int i = r0 + tid; i < r1; i += kThreads) keys[i] = remote[i];
-  }
-  __syncthreads();
-  const int k = min(p.k2[b], NP);
-  int32_t* user_pages = (rank == 0 && p.sel_pages) ? p.sel_pages + (size_t)unit * p.sel_pages_stride : nullptr;
-  if (k >= NP) {
-    for (int i = tid; i < NP; i += kThreads) {
-      sel[i] = i;
-      if (user_pages) user_pages[i] = i;
+  // the append's stores: their loads completed long ago, and nothing in this step
+  // waits for them
+  if (appender) {
+    if (app_phys >= 0 && app_phys < p.num_phys) {
+      const int slot = n0 % P;
+      const size_t dst = (((size_t)app_phys * p.Hkv + g) * P + slot) * 128 + 2 * tid;
+      *reinterpret_cast<uint32_t*>(p.k_pages + dst) = app_k;
+      *reinterpret_cast<uint32_t*>(p.v_pages + dst) = app_v;
+      float mx0 = bf16_lo(app_k), mx1 = bf16_hi(app_k), mn0 = mx0, mn1 = mx1;
+      if (slot > 0) {
+        mx0 = fmaxf(bf16_lo(app_mx), mx0);
+        mx1 = fmaxf(bf16_hi(app_mx), mx1);
+        mn0 = fminf(bf16_lo(app_mn), mn0);
+        mn1 = fminf(bf16_hi(app_mn), mn1);
+      }
+      p.kmax[app_row] = (rkv_bf16)(__float_as_uint(mx0) >> 16);
+      p.kmax[app_row + p.max_pages] = (rkv_bf16)(__float_as_uint(mx1) >> 16);
+      p.kmin[app_row] = (rkv_bf16)(__float_as_uint(mn0) >> 16);
+      p.kmin[app_row + p.max_pages] = (rkv_bf16)(__float_as_uint(mn1) >> 16);
+    } else {
+      flag_error(p.err, RKV_DEVERR_PAGE_ID);
     }
-  } else {
-    topk_ascending<kThreads>(keys, NP, k, hist, scan, sel, user_pages);
   }
-  if (user_pages && tid == 0 && k < p.sel_pages_stride) user_pages[k] = -1;
+  // 7. top-k2.  Small page counts: each CTA ranks the pages of its own slice against
+  // all keys (rank = #greater + #equal with a lower index: the order (score desc, page
+  // asc)) and stores each page ranked below k into slot `rank` of every CTA's list.
+  // Larger counts: every CTA runs the same block radix select over all keys.
+  const int k = min(p.k2[b], NP);
+  const bool by_rank = NP <= 512;
+  if (k >= NP) {
+    for (int i = tid; i < NP; i += kThreads) sel[i] = i;
+  } else if (by_rank) {
+    const int np4k = (NP + 3) & ~3;  // keys are read four at a time; the padding never ranks
+    if (tid < np4k - NP) keys[NP + tid] = 0u;
+    __syncthreads();
+    const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+    // two pages per thread share every key load; counters stay independent
+    for (int i0 = p0 + tid; i0 < p1; i0 += 2 * kThreads) {
+      const int i1 = i0 + kThreads;
+      const bool has1 = i1 < p1;
+      const uint32_t ka = keys[i0], kb = has1 ? keys[i1] : 0xffffffffu;
+      int ga0 = 0, ga1 = 0, ea0 = 0, ea1 = 0, gb0 = 0, gb1 = 0, eb0 = 0, eb1 = 0;
+#pragma unroll 2
+      for (int j4 = 0; j4 < (np4k >> 2); j4 += 2) {
+        const uint4 u = k4[j4];
+        const uint4 v = (j4 + 1 < (np4k >> 2)) ? k4[j4 + 1] : make_uint4(0, 0, 0, 0);
+        ga0 += (u.x > ka) + (u.y > ka) + (u.z > ka) + (u.w > ka);
+        ga1 += (v.x > ka) + (v.y > ka) + (v.z > ka) + (v.w > ka);
+        ea0 += (u.x == ka) + (u.y == ka) + (u.z == ka) + (u.w == ka);
+        ea1 += (v.x == ka) + (v.y == ka) + (v.z == ka) + (v.w == ka);
+        gb0 += (u.x > kb) + (u.y > kb) + (u.z > kb) + (u.w > kb);
+        gb1 += (v.x > kb) + (v.y > kb) + (v.z > kb) + (v.w > kb);
+        eb0 += (u.x == kb) + (u.y == kb) + (u.z == kb) + (u.w == kb);
+        eb1 += (v.x == kb) + (v.y == kb) + (v.z == kb) + (v.w == kb);
+      }
+      for (int e = 0; e < 2; ++e) {
+        const int i = e == 0 ? i0 : i1;
+        if (e == 1 && !has1) break;
+        const uint32_t ki = e == 0 ? ka : kb;
+        int rk = e == 0 ? ga0 + ga1 : gb0 + gb1;
+        if ((e == 0 ? ea0 + ea1 : eb0 + eb1) > 1) {  // other pages share this score: lower indices rank first
+          int t0 = 0, t1 = 0;
+          for (int j = 0; j + 1 < i; j += 2) {
+            t0 += keys[j] == ki;
+            t1 += keys[j + 1] == ki;
+          }
+          if (i & 1) t0 += keys[i - 1] == ki;
+          rk += t0 + t1;
+        }
+        if (rk < k)
+          for (int r = 0; r < C; ++r) cluster.map_shared_rank(sel, r)[rk] = i;
+      }
+    }
+    cluster.sync();  // every CTA's list is complete
+  } else {
+    topk_ascending<kThreads>(keys, NP, k, hist, scan, sel, nullptr);
+  }
+  int32_t* user_pages = (rank == 0 && p.sel_pages) ? p.sel_pages + (size_t)unit * p.sel_pages_stride : nullptr;
+  if (user_pages) {  // the caller's copy, ascending (CTA 0 only)
+    __syncthreads();
+    uint8_t* flag = ring;
+    for (int i = tid; i < NP; i += kThreads) flag[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < k; i += kThreads) flag[sel[i]] = 1;
+    __syncthreads();
+    const int seg = (NP + kThreads - 1) / kThreads;
+    const int s0 = min(NP, tid * seg), s1 = min(NP, s0 + seg);
+    int cnt = 0;
+    for (int i = s0; i < s1; ++i) cnt += flag[i];
+    int total;
+    int o = block_exclusive_scan<kThreads>(cnt, scan, &total);
+    for (int i = s0; i < s1; ++i)
+      if (flag[i]) user_pages[o++] = i;
+    if (tid == 0 && k < p.sel_pages_stride) user_pages[k] = -1;
+    fence_proxy_async_smem();  // generic writes to the region before the attention's TMA loads
+  }
   if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   if (!mbar_wait(&pbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
   __syncthreads();
 
-  // 9. attention over this CTA's share of the selected chunks
+  // 8. attention over this CTA's share of the selected chunks
   const int items = k * (P / kChunkTok);
   const int ips = (items + C - 1) / C;
   const int it0 = min(items, rank * ips), it1 = min(items, it0 + ips);
-  attend_cta<kFusedStages>(p, sel, ptab, b, g, n, it0, it1, ring, as);
-  cluster.sync();  // every CTA's partial state is in its shared memory
+  int to = 0;
+  const CtaPart* part = attend_cta<STAGES>(p, sel, ptab, b, g, n, it0, it1, ring, as, do_append ? n0 : -1, new_kv, &to);
 
-  // 10. merge the CTAs' states; CTA r finishes heads r, r + C, ...
+  // 9. each head's partial state goes to the CTA that finishes the head (h % C), slot
+  // [rank][h / C] of its inbox
+  for (int h = 0; h < G; ++h) {
+    float* dst = cluster.map_shared_rank(inbox, h % C) + ((size_t)rank * hpc + h / C) * 130;
+    dst[2 + tid] = part->O[h][tid];
+    if (tid == 0) {
+      dst[0] = part->M[h];
+      dst[1] = part->L[h];
+    }
+  }
+
+  cluster.sync();  // every inbox is filled; no shared memory is touched remotely after this
+
+  // 10. merge this CTA's heads
   for (int h = rank; h < G; h += C) {
     float M = -1e30f;
-    for (int r = 0; r < C; ++r) M = fmaxf(M, cluster.map_shared_rank(&as, r)->ctaM[h]);
+    for (int r = 0; r < C; ++r) M = fmaxf(M, inbox[((size_t)r * hpc + h / C) * 130]);
     float L = 0.f, O = 0.f;
     for (int r = 0; r < C; ++r) {
-      const AttnSmem<kFusedStages>* ra = cluster.map_shared_rank(&as, r);
-      const float f = exp2f(ra->ctaM[h] - M);
-      L += ra->ctaL[h] * f;
-      O += ra->ctaO[h][tid] * f;
+      const float* src = inbox + ((size_t)r * hpc + h / C) * 130;
+      const float f = exp2f(src[0] - M);
+      L += src[1] * f;
+      O += src[2 + tid] * f;
     }
     p.out[((size_t)b * p.Hq + (size_t)g * G + h) * 128 + tid] = L > 0.f ? O / L : 0.f;
   }
-  cluster.sync();  // no CTA leaves while others still read its shared memory
+
+  // 11. the last cluster of sequence b to get here advances seq_len (every CTA of every
+  // cluster of b read it at the start, before its cluster's first barrier)
+  if (do_append && rank == 0 && tid == 0) {
+    __threadfence();
+    if (atomicAdd(&p.sync[b], 1) == p.Hkv - 1) {
+      p.sync[b] = 0;
+      p.seq_len[b] = n;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -582,6 +776,7 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kScoreThreads) hsa_score_kernel(const __grid_constant__ HsaParams p) {
   __shared__ ChanSmem cs;
+  __shared__ float qf[8][128];
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv;
   const int tid = threadIdx.x;
   const int n = seq_length(p, b);
@@ -591,9 +786,9 @@ __global__ void __launch_bounds__(kScoreThreads) hsa_score_kernel(const __grid_c
   if (page0 >= NP && !write_ch) return;
   const int G = p.G;
   const rkv_bf16* qg = p.q + ((size_t)b * p.Hq + (size_t)g * G) * 128;
-  for (int i = tid; i < G * 128; i += kScoreThreads) cs.qf[i >> 7][i & 127] = bf16_f(qg[i]);
+  for (int i = tid; i < G * 128; i += kScoreThreads) qf[i >> 7][i & 127] = bf16_f(qg[i]);
   const int k1 = p.k1[b];
-  select_channels(cs, G, k1);
+  select_channels(qf, cs, G, k1);
   if (write_ch && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   const int pg = page0 + 2 * tid;
   if (pg < NP) {
@@ -643,17 +838,19 @@ __global__ void __launch_bounds__(kThreads) hsa_attend_kernel(const __grid_const
   const int items = k * (p.P / kChunkTok);
   const int ips = (items + p.nsplit - 1) / p.nsplit;
   const int it0 = min(items, split * ips), it1 = min(items, it0 + ips);
-  if (attend_cta<kSplitStages>(p, p.selp + (size_t)unit * p.max_pages, p.page_table + (size_t)b * p.max_pages, b, g,
-                               n, it0, it1, smem, as))
-    return;
+  int to = 0;
+  const CtaPart* part = attend_cta<kSplitStages>(p, p.selp + (size_t)unit * p.max_pages,
+                                                 p.page_table + (size_t)b * p.max_pages, b, g, n, it0, it1,
+                                                 align1024(smem), as, -1, nullptr, &to);
+  if (to) return;
   const int c = threadIdx.x;
   for (int h = 0; h < p.G; ++h) {
     const size_t bh = (size_t)b * p.Hq + (size_t)g * p.G + h;
     if (p.nsplit == 1) {
-      p.out[bh * 128 + c] = as.ctaL[h] > 0.f ? as.ctaO[h][c] / as.ctaL[h] : 0.f;
+      p.out[bh * 128 + c] = part->L[h] > 0.f ? part->O[h][c] / part->L[h] : 0.f;
     } else {
-      p.part_o[(bh * p.nsplit + split) * 128 + c] = as.ctaO[h][c];
-      if (c == 0) p.part_ml[bh * p.nsplit + split] = make_float2(as.ctaM[h], as.ctaL[h]);
+      p.part_o[(bh * p.nsplit + split) * 128 + c] = part->O[h][c];
+      if (c == 0) p.part_ml[bh * p.nsplit + split] = make_float2(part->M[h], part->L[h]);
     }
   }
 }
@@ -676,9 +873,40 @@ __global__ void __launch_bounds__(128) hsa_combine_kernel(const __grid_constant_
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-HsaParams make_params(const DecodeArgs& a) {
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// A [rows][128] bf16 page pool as a 2-D tensor map with 16-row x 64-channel boxes
+// and 128-byte swizzle (box rows are 128 B, so the pieces of row r are XOR-ed with r % 8).
+bool encode_pool_map(CUtensorMap* m, const rkv_bf16* base, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, (cuuint32_t)kChunkTok};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<rkv_bf16*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+HsaParams make_params(const DecodeArgs& a, bool* ok) {
   const rkv_cache& c = a.cache;
   HsaParams p;
+  const uint64_t rows = (uint64_t)c.num_phys_pages * c.Hkv * c.page_size;
+  *ok = encode_pool_map(&p.tmk, c.k_pages, rows) && encode_pool_map(&p.tmv, c.v_pages, rows);
   p.k_pages = c.k_pages;
   p.v_pages = c.v_pages;
   p.page_table = c.page_table;
@@ -724,48 +952,84 @@ int max_items(const DecodeArgs& a) {
   return (k2max < a.cache.max_pages ? k2max : a.cache.max_pages) * (a.cache.page_size / kChunkTok);
 }
 
-size_t fused_smem_bytes(int max_pages) { return (size_t)ring_bytes(kFusedStages) + 3 * (size_t)max_pages * 4; }
+// Dynamic shared memory of the fused kernel: 1024 (alignment) + region + key, list
+// and page-table arrays + the partials inbox.
+size_t fused_smem_bytes(int region, int max_pages) {
+  return 1024 + (size_t)region + 3 * (size_t)max_pages * 4 + (size_t)(8 + kMaxCluster) * 130 * 4;
+}
+
+template <int STAGES>
+int fused_blocks_per_sm(size_t smem) {
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(hsa_step_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr = true;
+  }
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, hsa_step_kernel<STAGES>, kThreads, smem) != cudaSuccess)
+    nb = 0;
+  return nb;
+}
 
 cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
-  static bool attrs = false;
-  if (!attrs) {
-    cudaFuncSetAttribute(hsa_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)fused_smem_bytes(kFusedMaxPages));
-    attrs = true;
-  }
-  const size_t smem = fused_smem_bytes(a.cache.max_pages);
-  // CTAs per unit: enough to give every unit a share of one wave of resident CTAs,
-  // at most one CTA per 4 attention chunks and at most 8 (a portable cluster)
-  static size_t occ_smem = 0;
-  static int occ_blocks = 0;
-  if (occ_smem != smem) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, hsa_step_kernel, kThreads, smem) != cudaSuccess || nb < 1)
-      nb = 1;
-    occ_blocks = nb;
-    occ_smem = smem;
-  }
   const int units = a.cache.B * a.cache.Hkv;
-  const int slots = occ_blocks * num_sms();
-  int C = units < slots ? slots / units : 1;
+  int k1max = 1;
+  for (int b = 0; b < a.cache.B; ++b) k1max = a.k1[b] > k1max ? a.k1[b] : k1max;
+  // The region must hold the ring, and should hold a whole slice of staged summaries.
+  auto region_for = [&](int stages, int C) {
+    const int per = ((a.cache.max_pages + C - 1) / C + 7) & ~7;
+    int stage_bytes = 4 * k1max * per;
+    stage_bytes = stage_bytes < 128 * 1024 ? stage_bytes : 128 * 1024;  // larger slices take several tiles
+    int r = ring_bytes(stages) > stage_bytes ? ring_bytes(stages) : stage_bytes;
+    return (r + 1023) & ~1023;
+  };
+  // CTAs per unit: enough to give every unit a share of one wave of resident CTAs, at
+  // most one CTA per 4 attention chunks and at most 8 (a portable cluster); three ring
+  // stages while two CTAs still fit on an SM, else two.
   const int by_items = (max_items(a) + kAtWarps - 1) / kAtWarps;
-  C = C < by_items ? C : by_items;
-  C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
-  p.cluster = C;
+  int best_C = 1, best_st = 2;
+  size_t best_smem = 0;
+  for (int st = 3; st >= 2; --st) {
+    int C = kMaxCluster;
+    for (int it = 0; it < 4; ++it) {  // C and the occupancy depend on each other
+      const size_t smem = fused_smem_bytes(region_for(st, C), a.cache.max_pages);
+      const int occ = st == 3 ? fused_blocks_per_sm<3>(smem) : fused_blocks_per_sm<2>(smem);
+      const int slots = (occ > 0 ? occ : 1) * num_sms();
+      int Cn = units < slots ? slots / units : 1;
+      Cn = Cn < by_items ? Cn : by_items;
+      Cn = Cn < 1 ? 1 : (Cn > kMaxCluster ? kMaxCluster : Cn);
+      if (Cn == C) break;
+      C = Cn;
+    }
+    const size_t smem = fused_smem_bytes(region_for(st, C), a.cache.max_pages);
+    const int occ = st == 3 ? fused_blocks_per_sm<3>(smem) : fused_blocks_per_sm<2>(smem);
+    if (st == 3 && occ < 2 && units * C > num_sms()) continue;  // prefer two CTAs per SM
+    best_C = C;
+    best_st = st;
+    best_smem = smem;
+    break;
+  }
+  if (best_smem == 0) {
+    best_st = 2;
+    best_smem = fused_smem_bytes(region_for(2, best_C), a.cache.max_pages);
+  }
+  p.cluster = best_C;
+  p.region_bytes = region_for(best_st, best_C);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, (unsigned)units, 1);
+  cfg.gridDim = dim3(best_C, (unsigned)units, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = best_smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.x = best_C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   launch_begin(K_HSA_STEP, s);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, hsa_step_kernel, p);
+  const cudaError_t e = best_st == 3 ? cudaLaunchKernelEx(&cfg, hsa_step_kernel<3>, p)
+                                     : cudaLaunchKernelEx(&cfg, hsa_step_kernel<2>, p);
   launch_end(K_HSA_STEP, s);
   return e;
 }
@@ -813,7 +1077,12 @@ size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages) {
 bool decode_fused_ok(const rkv_cache& c) { return c.max_pages <= kFusedMaxPages; }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  HsaParams p = make_params(a);
+  bool ok = false;
+  HsaParams p = make_params(a, &ok);
+  if (!ok) {
+    set_last_error("cuTensorMapEncodeTiled failed for the K/V page pools");
+    return cudaErrorInvalidValue;
+  }
   if (a.mode != DECODE_SPLIT && decode_fused_ok(a.cache)) {
     const cudaError_t e = launch_fused(p, a, s);
     if (e != cudaSuccess) return e;

@@ -123,6 +123,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Tiled TMA load of one box of a 2-D tensor map into this CTA's shared memory;
+// completion is signalled on `bar` as transaction bytes.  `map` must live in
+// parameter, constant or global memory (a __grid_constant__ kernel parameter).
+// The innermost coordinate x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ errors
 __device__ __forceinline__ void flag_error(int32_t* word, int32_t bit) {
   if (word) atomicOr(word, bit);
