@@ -250,7 +250,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
 
     wl = W.workload(args.workload, args.seed)
     rkv.rkv_decode_path({"auto": 0, "split": 1, "fused": 2}[args.decode_path])
-    setup = Setup(wl, rkv, args.seed + rank, dev)
+    setup = Setup(wl, rkv, rank_seed(args.seed, rank), dev)
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
 
@@ -314,12 +314,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         torch.distributed.barrier()
     clocks = clk.summary()
     pass_ms = [p + sum(d) for p, d in zip(pre_all, dec_all)]
-    total_ms = sum(pass_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * wl.steps * args.steps / (total_ms / 1e3)
+    total_ms, value = whole_job_value(sum(pass_ms), wl.steps, args.steps, world, dev)
 
     # per-kernel durations from the instrumented graphs (same work, same flushes)
     rkv.profile_reset()
@@ -393,6 +388,24 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
                                           f"of {wl.steps} decode steps ({o['seconds']:.1f} s), extrapolated to the "
                                           f"whole request: steps / (prefill + steps * mean step)")
     return res
+
+
+def whole_job_value(total_ms: float, decode_steps: int, passes: int, world: int, device) -> tuple:
+    """Max timed total over the ranks, and the whole-job decode steps/s it gives.
+
+    Every rank runs its own independent request (weak scaling, no data exchange), so
+    the job processed world * decode_steps * passes decode steps in the slowest rank's
+    time.  Returns (max total ms, decode steps per second)."""
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total = float(t.item())
+    return total, world * decode_steps * passes / (total / 1e3)
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own request: the shards are independent sequences."""
+    return seed + rank
 
 
 def self_or_range(xs):
