@@ -87,9 +87,12 @@ class GpuRun:
         self.rkv.rkv_prefill_evict(g["q_win"], g["k"], g["v"], g["prompt_len"], self.keep1, self.kp, self.cache,
                                    self.kept, pooled_scores=self.pooled)
 
-    def decode_step(self, step: int):
+    def decode_step(self, step: int, edit=None):
+        """One decode step; `edit(d)` may change the step's tensors before the call."""
         wl = self.wl
         d = W.decode_tensors(wl, step, self.seed, self.layer, self.dev)
+        if edit is not None:
+            edit(d)
         out = torch.full((wl.B, wl.Hq, 128), float("nan"), dtype=torch.float32, device=self.dev)
         ch = torch.full((wl.B, wl.Hkv, 128), -9, dtype=torch.int32, device=self.dev)
         pg = torch.full((wl.B, wl.Hkv, max(self.k2) + 1), -9, dtype=torch.int32, device=self.dev)
@@ -184,4 +187,4 @@ class OracleUnit:
         got = f64(out[b, g * G:(g + 1) * G])
         err = float(np.abs(got - ref).max())
         assert err <= ATOL_OUT, f"attention max-abs error {err}"
-        return dict(err=err, swaps=swaps)
+        return dict(err=err, swaps=swaps, sig=sig, pages=gpages)

@@ -167,6 +167,57 @@ def test_prefill_select_with_large_tie_groups(rkv, L):
     assert run.status()[0] == rkv.RKV_OK
 
 
+@pytest.mark.parametrize("L,budget", [(1500, 256), (6000, 4096)])
+def test_decode_select_with_tied_page_scores(rkv, path, L, budget):
+    """Every prompt key is the same vector, so every page of the compressed cache but the
+    one taking the new tokens has the same Kmax/Kmin and the same bound.  The top-k2
+    boundary then falls inside a group of equal scores (about 50 pages, or about 340)
+    and the tied pages must go to the lowest page indices, as in the oracle."""
+    wl = W.custom(B=1, Hq=8, Hkv=2, prompt_lens=[L], budget=budget, window=16, page_size=16, steps=2,
+                  pool_kernel=3)
+    run = GpuRun(wl, rkv)
+    k = run.inputs["k"]
+    k[0, :, :L] = k[0, :, :1].clone()
+    run.gpu_in["k"] = k.to(run.dev)
+    run.prefill()
+    units = [OracleUnit(run, 0, g) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in units:
+            r = u.step(run, d, out, ch, pg)
+            sig, kk = r["sig"], len(r["pages"])
+            desc = np.sort(sig)[::-1]
+            assert kk < len(sig) and desc[kk - 1] == desc[kk], "no tie at the boundary"
+            ref = np.sort(np.lexsort((np.arange(len(sig)), -sig))[:kk])
+            np.testing.assert_array_equal(r["pages"], ref)
+    assert run.status()[0] == rkv.RKV_OK
+
+
+def test_channel_ties_go_to_lower_channels(rkv, path):
+    """Every channel of the decode query has the same magnitude (signs vary), so all
+    128 channel scores tie exactly: the channel set must be channels 0 .. k1-1."""
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 900], budget=64, window=8, page_size=16, steps=2,
+                  pool_kernel=5)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+
+    def flat_q(d):
+        d["q"] = torch.where(d["q"] >= 0, 0.75, -0.75).to(d["q"].dtype)
+
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step, edit=flat_q)
+        for u in units:
+            u.step(run, d, out, ch, pg)
+            k1 = run.k1[u.b]
+            np.testing.assert_array_equal(ch[u.b, u.g, :k1].cpu().numpy(), np.arange(k1))
+    assert run.status()[0] == rkv.RKV_OK
+
+
 def test_deterministic(rkv, path):
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[900, 700], budget=64, window=8, page_size=16, steps=3,
                   pool_kernel=5)

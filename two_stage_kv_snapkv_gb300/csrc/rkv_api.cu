@@ -9,6 +9,8 @@
 #include <vector>
 #include <atomic>
 
+#include <cudaTypedefs.h>
+
 #include "rkv.h"
 #include "rkv_internal.h"
 
@@ -157,6 +159,28 @@ int num_sms() {
     if (sms <= 0) sms = 1;
   }
   return sms;
+}
+
+
+bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  // cuTensorMapEncodeTiled from the driver, looked up once per process
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace rkv

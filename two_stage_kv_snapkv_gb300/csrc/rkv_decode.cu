@@ -103,44 +103,56 @@ __device__ __forceinline__ int seq_length(const HsaParams& p, int b) {
 
 // Shared-memory state of the channel selection (one KV head).
 struct ChanSmem {
-  alignas(16) unsigned long long akey[128];
+  alignas(16) uint32_t ahi[128];  // high and low words of the fp64 channel scores
+  uint32_t alo[128];
   int chan[128];
   float qpos[128], qneg[128];
-  int warp_cnt[8];  // also the scratch of a 128-thread block scan (5 ints)
+  int warp_cnt[8];
 };
 
 // Top-k1 channels of a_i = sum_h |q_h,i| (ties: lower channel), ascending, with the
 // per-channel sums of the positive and negative parts of q over the group.  The
 // channel score is summed in fp64, where a sum of <= 8 bf16 magnitudes is exact, and
-// ranked on its bit pattern (order-preserving for non-negative doubles).
+// ranked on its bit pattern (order-preserving for non-negative doubles): the high
+// words decide unless another channel shares this one's high word.
 // Every thread of a block of >= 128 threads calls this after filling qf[G][128].
 __device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int k1) {
   const int tid = threadIdx.x;
   __syncthreads();
+  uint32_t hi = 0, lo = 0;
   if (tid < 128) {
     double s = 0.0;
     for (int h = 0; h < G; ++h) s += fabs((double)qf[h][tid]);
-    cs.akey[tid] = (unsigned long long)__double_as_longlong(s);
+    const unsigned long long u = (unsigned long long)__double_as_longlong(s);
+    hi = (uint32_t)(u >> 32);
+    lo = (uint32_t)u;
+    cs.ahi[tid] = hi;
+    cs.alo[tid] = lo;
   }
   __syncthreads();
   bool sel = false;
   unsigned bal = 0;
   if (tid < 128) {
-    // rank = #greater + #equal at a lower channel; four independent counters keep the
-    // shared-memory loads in flight
-    const unsigned long long ai = cs.akey[tid];
-    const ulonglong2* a2 = reinterpret_cast<const ulonglong2*>(cs.akey);
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 4
-    for (int j2 = 0; j2 < 64; j2 += 2) {
-      const ulonglong2 u = a2[j2], v = a2[j2 + 1];
-      const int j = 2 * j2;
-      r0 += (u.x > ai) | ((u.x == ai) & (j < tid));
-      r1 += (u.y > ai) | ((u.y == ai) & (j + 1 < tid));
-      r2 += (v.x > ai) | ((v.x == ai) & (j + 2 < tid));
-      r3 += (v.y > ai) | ((v.y == ai) & (j + 3 < tid));
+    // rank = #greater + #equal at a lower channel
+    const uint4* h4 = reinterpret_cast<const uint4*>(cs.ahi);
+    int g0 = 0, g1 = 0, e0 = 0, e1 = 0;
+#pragma unroll 8
+    for (int j4 = 0; j4 < 32; ++j4) {
+      const uint4 u = h4[j4];
+      g0 += (u.x > hi) + (u.y > hi);
+      g1 += (u.z > hi) + (u.w > hi);
+      e0 += (u.x == hi) + (u.y == hi);
+      e1 += (u.z == hi) + (u.w == hi);
     }
-    sel = (r0 + r1) + (r2 + r3) < k1;
+    int rank = g0 + g1;
+    if (e0 + e1 > 1) {  // another channel has the same high word: the low words decide
+      for (int j = 0; j < 128; ++j) {
+        if (cs.ahi[j] != hi || j == tid) continue;
+        const uint32_t l = cs.alo[j];
+        rank += (l > lo) | ((l == lo) & (j < tid));
+      }
+    }
+    sel = rank < k1;
     bal = __ballot_sync(0xffffffffu, sel);
     if ((tid & 31) == 0) cs.warp_cnt[tid >> 5] = __popc(bal);
   }
@@ -185,52 +197,12 @@ __device__ __forceinline__ float2 page_pair_bound(const HsaParams& p, int unit, 
   return make_float2(s0, s1);
 }
 
-// Writes the ascending indices of the top-k of keys[0..n) (1 <= k < n) to out[0..k):
-// every key > T, and keys == T by ascending index until k are taken.
-template <int NT>
-__device__ void topk_ascending(const uint32_t* keys, int n, int k, uint32_t* hist, int* scan, int32_t* out,
-                               int32_t* out2) {
-  uint32_t T;
-  int need;
-  block_radix_threshold<NT>(n, k, [&](int i) { return keys[i]; }, hist, &T, &need);
-  const int tid = threadIdx.x;
-  const int seg = (n + NT - 1) / NT;
-  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
-  int ceq = 0;
-  for (int i = s0; i < s1; ++i) ceq += keys[i] == T;
-  int total;
-  const int eq_base = block_exclusive_scan<NT>(ceq, scan, &total);
-  int csel = 0;
-  for (int i = s0, er = eq_base; i < s1; ++i) {
-    const uint32_t u = keys[i];
-    if (u > T) ++csel;
-    else if (u == T) { csel += er < need; ++er; }
-  }
-  const int out_base = block_exclusive_scan<NT>(csel, scan, &total);
-  for (int i = s0, er = eq_base, o = out_base; i < s1; ++i) {
-    const uint32_t u = keys[i];
-    bool take = u > T;
-    if (u == T) { take = er < need; ++er; }
-    if (take && o < k) {
-      out[o] = i;
-      if (out2) out2[o] = i;
-      ++o;
-    }
-  }
-}
-
 // Shared-memory address of 16-byte piece `piece` (channels 8*piece .. 8*piece+7) of
 // token row `row` in a TMA-written K or V block: two 16 x 64 boxes (channels 0-63,
 // 64-127) of 128-byte rows, each 16-byte piece XOR-ed with row % 8 (128-B swizzle;
 // the block is 1024-byte aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int piece) {
   return base + (piece >> 3) * kHalfBytes + row * 128 + ((((piece & 7) ^ (row & 7))) << 4);
-}
-
-// Dynamic shared memory rounded up to a 1024-byte boundary (the TMA swizzle atom).
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  const uint32_t a = smem_u32(p);
-  return p + (((a + 1023u) & ~1023u) - a);
 }
 
 // Barriers of one CTA's attention ring.
@@ -247,6 +219,7 @@ struct CtaPart {
 };
 constexpr int kCtaPartOffset = (kWarpCombineBytes + 255) & ~255;
 static_assert(kCtaPartOffset + (int)sizeof(CtaPart) <= ring_bytes(kFusedStages), "ring too small for the partials");
+static_assert((int)sizeof(TopkSmem<kThreads>) <= ring_bytes(kFusedStages), "ring too small for the top-k scratch");
 
 // Attention of one CTA (4 warps) over items [it0, it1) of the unit's selected pages
 // `sel` (ascending page ids; item i = chunk i % cpp of page sel[i / cpp]); `ptab` is
@@ -473,8 +446,6 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   __shared__ AttnSmem<STAGES> as;
   __shared__ uint64_t sbar, pbar;
   __shared__ __align__(16) uint8_t new_kv[512];
-  __shared__ uint32_t hist[258];
-  __shared__ int scan[kThreads / 32 + 1];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = p.cluster;
@@ -648,79 +619,23 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
       flag_error(p.err, RKV_DEVERR_PAGE_ID);
     }
   }
-  // 7. top-k2.  Small page counts: each CTA ranks the pages of its own slice against
-  // all keys (rank = #greater + #equal with a lower index: the order (score desc, page
-  // asc)) and stores each page ranked below k into slot `rank` of every CTA's list.
-  // Larger counts: every CTA runs the same block radix select over all keys.
+  // 7. top-k2: every CTA runs the same select over all keys (no exchange needed); the
+  // list is ascending.  Its scratch lives in the region, free between the scoring and
+  // the attention.
   const int k = min(p.k2[b], NP);
-  const bool by_rank = NP <= 512;
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
-  } else if (by_rank) {
-    const int np4k = (NP + 3) & ~3;  // keys are read four at a time; the padding never ranks
-    if (tid < np4k - NP) keys[NP + tid] = 0u;
-    __syncthreads();
-    const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-    // two pages per thread share every key load; counters stay independent
-    for (int i0 = p0 + tid; i0 < p1; i0 += 2 * kThreads) {
-      const int i1 = i0 + kThreads;
-      const bool has1 = i1 < p1;
-      const uint32_t ka = keys[i0], kb = has1 ? keys[i1] : 0xffffffffu;
-      int ga0 = 0, ga1 = 0, ea0 = 0, ea1 = 0, gb0 = 0, gb1 = 0, eb0 = 0, eb1 = 0;
-#pragma unroll 2
-      for (int j4 = 0; j4 < (np4k >> 2); j4 += 2) {
-        const uint4 u = k4[j4];
-        const uint4 v = (j4 + 1 < (np4k >> 2)) ? k4[j4 + 1] : make_uint4(0, 0, 0, 0);
-        ga0 += (u.x > ka) + (u.y > ka) + (u.z > ka) + (u.w > ka);
-        ga1 += (v.x > ka) + (v.y > ka) + (v.z > ka) + (v.w > ka);
-        ea0 += (u.x == ka) + (u.y == ka) + (u.z == ka) + (u.w == ka);
-        ea1 += (v.x == ka) + (v.y == ka) + (v.z == ka) + (v.w == ka);
-        gb0 += (u.x > kb) + (u.y > kb) + (u.z > kb) + (u.w > kb);
-        gb1 += (v.x > kb) + (v.y > kb) + (v.z > kb) + (v.w > kb);
-        eb0 += (u.x == kb) + (u.y == kb) + (u.z == kb) + (u.w == kb);
-        eb1 += (v.x == kb) + (v.y == kb) + (v.z == kb) + (v.w == kb);
-      }
-      for (int e = 0; e < 2; ++e) {
-        const int i = e == 0 ? i0 : i1;
-        if (e == 1 && !has1) break;
-        const uint32_t ki = e == 0 ? ka : kb;
-        int rk = e == 0 ? ga0 + ga1 : gb0 + gb1;
-        if ((e == 0 ? ea0 + ea1 : eb0 + eb1) > 1) {  // other pages share this score: lower indices rank first
-          int t0 = 0, t1 = 0;
-          for (int j = 0; j + 1 < i; j += 2) {
-            t0 += keys[j] == ki;
-            t1 += keys[j + 1] == ki;
-          }
-          if (i & 1) t0 += keys[i - 1] == ki;
-          rk += t0 + t1;
-        }
-        if (rk < k)
-          for (int r = 0; r < C; ++r) cluster.map_shared_rank(sel, r)[rk] = i;
-      }
-    }
-    cluster.sync();  // every CTA's list is complete
   } else {
-    topk_ascending<kThreads>(keys, NP, k, hist, scan, sel, nullptr);
+    topk_adaptive<kThreads>(NP, k, [&](int i) { return keys[i]; }, *reinterpret_cast<TopkSmem<kThreads>*>(ring),
+                            sel, nullptr);
   }
-  int32_t* user_pages = (rank == 0 && p.sel_pages) ? p.sel_pages + (size_t)unit * p.sel_pages_stride : nullptr;
-  if (user_pages) {  // the caller's copy, ascending (CTA 0 only)
-    __syncthreads();
-    uint8_t* flag = ring;
-    for (int i = tid; i < NP; i += kThreads) flag[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < k; i += kThreads) flag[sel[i]] = 1;
-    __syncthreads();
-    const int seg = (NP + kThreads - 1) / kThreads;
-    const int s0 = min(NP, tid * seg), s1 = min(NP, s0 + seg);
-    int cnt = 0;
-    for (int i = s0; i < s1; ++i) cnt += flag[i];
-    int total;
-    int o = block_exclusive_scan<kThreads>(cnt, scan, &total);
-    for (int i = s0; i < s1; ++i)
-      if (flag[i]) user_pages[o++] = i;
+  __syncthreads();
+  if (rank == 0 && p.sel_pages) {  // the caller's copy (CTA 0 only)
+    int32_t* user_pages = p.sel_pages + (size_t)unit * p.sel_pages_stride;
+    for (int i = tid; i < k; i += kThreads) user_pages[i] = sel[i];
     if (tid == 0 && k < p.sel_pages_stride) user_pages[k] = -1;
-    fence_proxy_async_smem();  // generic writes to the region before the attention's TMA loads
   }
+  fence_proxy_async_smem();  // generic writes to the region before the attention's TMA loads
   if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   if (!mbar_wait(&pbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
   __syncthreads();
@@ -803,8 +718,7 @@ __global__ void __launch_bounds__(kScoreThreads) hsa_score_kernel(const __grid_c
 // dynamic shared memory = max_pages keys.
 __global__ void __launch_bounds__(kTopkThreads) hsa_topk_kernel(const __grid_constant__ HsaParams p) {
   extern __shared__ uint32_t keys[];
-  __shared__ uint32_t hist[258];
-  __shared__ int scan_scratch[kTopkThreads / 32 + 1];
+  __shared__ TopkSmem<kTopkThreads> ts;
   const int unit = blockIdx.x, b = unit / p.Hkv;
   const int tid = threadIdx.x;
   const int n = seq_length(p, b);
@@ -823,7 +737,7 @@ __global__ void __launch_bounds__(kTopkThreads) hsa_topk_kernel(const __grid_con
   const float* sg = p.sigma + (size_t)unit * p.max_pages;
   for (int i = tid; i < NP; i += kTopkThreads) keys[i] = float_key(sg[i]);
   __syncthreads();
-  topk_ascending<kTopkThreads>(keys, NP, k, hist, scan_scratch, out, user);
+  topk_adaptive<kTopkThreads>(NP, k, [&](int i) { return keys[i]; }, ts, out, user);
 }
 
 // Split path, step 4: attention over a range of the selected chunks.
@@ -873,33 +787,9 @@ __global__ void __launch_bounds__(128) hsa_combine_kernel(const __grid_constant_
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// cuTensorMapEncodeTiled from the driver, looked up once.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    cudaDriverEntryPointQueryResult q;
-    void* f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-// A [rows][128] bf16 page pool as a 2-D tensor map with 16-row x 64-channel boxes
-// and 128-byte swizzle (box rows are 128 B, so the pieces of row r are XOR-ed with r % 8).
+// A [rows][128] bf16 page pool as a 2-D tensor map with 16-row x 64-channel boxes.
 bool encode_pool_map(CUtensorMap* m, const rkv_bf16* base, uint64_t rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {128, rows};
-  cuuint64_t strides[1] = {256};
-  cuuint32_t box[2] = {64, (cuuint32_t)kChunkTok};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<rkv_bf16*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_rows_map(m, base, rows, kChunkTok);
 }
 
 HsaParams make_params(const DecodeArgs& a, bool* ok) {
@@ -983,36 +873,57 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
     int r = ring_bytes(stages) > stage_bytes ? ring_bytes(stages) : stage_bytes;
     return (r + 1023) & ~1023;
   };
-  // CTAs per unit: enough to give every unit a share of one wave of resident CTAs, at
-  // most one CTA per 4 attention chunks and at most 8 (a portable cluster); three ring
-  // stages while two CTAs still fit on an SM, else two.
+  // CTAs per unit (the cluster size C, at most 8 and at most one per 4 attention
+  // chunks) and ring stages: among the configurations whose CTAs all fit in one wave
+  // of resident CTAs (C = 1 always qualifies), the one with the most CTAs, then the
+  // fewest summary tiles per CTA, then the most stages.
   const int by_items = (max_items(a) + kAtWarps - 1) / kAtWarps;
-  int best_C = 1, best_st = 2;
+  // the choice depends on nothing else, so the last one is kept per host thread
+  struct Choice {
+    int units, max_pages, k1max, by_items, dev, C, st;
+    size_t smem;
+  };
+  static thread_local Choice last = {-1, -1, -1, -1, -1, 0, 0, 0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int best_C = 1, best_st = 2, best_tiles = 0;
+  long best_ctas = -1;
   size_t best_smem = 0;
-  for (int st = 3; st >= 2; --st) {
-    int C = kMaxCluster;
-    for (int it = 0; it < 4; ++it) {  // C and the occupancy depend on each other
-      const size_t smem = fused_smem_bytes(region_for(st, C), a.cache.max_pages);
+  const bool cached = last.units == units && last.max_pages == a.cache.max_pages && last.k1max == k1max &&
+                      last.by_items == by_items && last.dev == dev;
+  if (cached) {
+    best_C = last.C;
+    best_st = last.st;
+    best_smem = last.smem;
+  }
+  for (int st = 3; st >= 2 && !cached; --st) {
+    for (int C = 1; C <= kMaxCluster; ++C) {
+      if (C > 1 && C > by_items) break;
+      const int region = region_for(st, C);
+      const size_t smem = fused_smem_bytes(region, a.cache.max_pages);
       const int occ = st == 3 ? fused_blocks_per_sm<3>(smem) : fused_blocks_per_sm<2>(smem);
-      const int slots = (occ > 0 ? occ : 1) * num_sms();
-      int Cn = units < slots ? slots / units : 1;
-      Cn = Cn < by_items ? Cn : by_items;
-      Cn = Cn < 1 ? 1 : (Cn > kMaxCluster ? kMaxCluster : Cn);
-      if (Cn == C) break;
-      C = Cn;
+      if (occ < 1) continue;
+      const long ctas = (long)units * C;
+      if (C > 1 && ctas > (long)occ * num_sms()) continue;
+      const int per = ((a.cache.max_pages + C - 1) / C + 7) & ~7;
+      const int tcap = (region / (4 * k1max)) & ~7;
+      const int tiles = tcap > 0 ? (per + tcap - 1) / tcap : 1 << 20;
+      const bool better = ctas > best_ctas || (ctas == best_ctas && tiles < best_tiles);
+      if (better) {
+        best_C = C;
+        best_st = st;
+        best_tiles = tiles;
+        best_ctas = ctas;
+        best_smem = smem;
+      }
     }
-    const size_t smem = fused_smem_bytes(region_for(st, C), a.cache.max_pages);
-    const int occ = st == 3 ? fused_blocks_per_sm<3>(smem) : fused_blocks_per_sm<2>(smem);
-    if (st == 3 && occ < 2 && units * C > num_sms()) continue;  // prefer two CTAs per SM
-    best_C = C;
-    best_st = st;
-    best_smem = smem;
-    break;
   }
   if (best_smem == 0) {
+    best_C = 1;
     best_st = 2;
-    best_smem = fused_smem_bytes(region_for(2, best_C), a.cache.max_pages);
+    best_smem = fused_smem_bytes(region_for(2, 1), a.cache.max_pages);
   }
+  if (!cached) last = {units, a.cache.max_pages, k1max, by_items, dev, best_C, best_st, best_smem};
   p.cluster = best_C;
   p.region_bytes = region_for(best_st, best_C);
   cudaLaunchConfig_t cfg = {};

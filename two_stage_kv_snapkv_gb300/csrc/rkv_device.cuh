@@ -86,6 +86,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -133,6 +136,76 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Dynamic shared memory rounded up to a 1024-byte boundary (the 128-byte swizzle atom).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// ------------------------------------------------------------------ tcgen05 (5th-gen tensor cores)
+// Tensor memory (TMEM): 128 lanes x 512 columns of 32-bit cells per SM.  Addresses are
+// (lane << 16) | column.  One warp allocates and frees; the base lands in shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 in, fp32 accumulate; issued by one thread.
+// adesc / bdesc: shared-memory matrix descriptors; idesc: instruction descriptor.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 32 consecutive columns of this thread's TMEM lane (the warp covers 32 lanes), with
+// the wait for the load in the same statement so no use of r can move above it.
+__device__ __forceinline__ void tc_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 operand stored as TMA writes it with
+// 128-byte swizzle: rows of 128 B (64 elements of K), 8-row groups 1024 B apart, the
+// atom 1024-byte aligned.  Fields: start address >> 4 (bits 0-13), leading byte offset
+// >> 4 (16-29, unused by swizzled K-major layouts), stride byte offset >> 4 (32-45),
+// the fixed 0b001 of bits 46-48, swizzle mode 2 = 128 B (61-63).  A K step of 16
+// elements inside the 128-B row is a +32 B start address.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both K-major:
+// D format (bits 4-5) = 1 (f32), A format (7-9) = 1 (bf16), B format (10-12) = 1 (bf16),
+// N >> 3 (17-22), M >> 4 (24-28).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // ------------------------------------------------------------------ errors
@@ -229,6 +302,204 @@ __device__ void block_radix_threshold(int n, int k, KeyFn key, uint32_t* hist, u
   }
   *T_out = prefix;
   *need_out = remaining;
+}
+
+// ------------------------------------------------------------------ adaptive-bin top-k
+// Top k of n uint32 keys, ordered by (key descending, index ascending), for
+// 1 <= k < n: the ascending indices go to out[0..k) (and out2, when not null).
+//
+// The key interval [lo, hi] that holds the k-th key shrinks by histograms of 1024
+// bins laid linearly over it (the first over [min key, max key]); a round ends with
+// the bin holding the k-th key.  Once that bin holds at most kTkCand keys, the
+// boundary key and index (T, t) come from ranking the bin's keys among themselves,
+// and the selection is {key > hi} + {key in [lo, hi] with (key, -index) >= (T, -t)}.
+// If the interval has shrunk to a single key value with more keys than that, the
+// equal keys are taken by ascending index.  Keys are order-preserving images of
+// floats in practice, so one round usually leaves a handful of candidates.
+// `key(i)` is called several times for each i in [0, n); every thread calls this.
+constexpr int kTkBins = 1024;
+constexpr int kTkCand = 32;
+template <int NT>
+struct TopkSmem {
+  uint32_t hist[kTkBins];
+  int cand[kTkCand];
+  uint32_t ckey[kTkCand];
+  uint32_t wlo[NT / 32], whi[NT / 32];
+  int wa[NT / 32], wb[NT / 32];
+  int ncand, bstar, need, nb, tidx;
+  uint32_t tkey;
+};
+
+template <int NT, class KeyFn>
+__device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t* out, int32_t* out2) {
+  static_assert(NT % 32 == 0 && kTkBins % NT == 0, "bins must split evenly over the threads");
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kTkBins / NT;  // bins per thread
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+
+  // 1. the key range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int i = tid; i < n; i += NT) {
+    const uint32_t u = key(i);
+    lo = min(lo, u);
+    hi = max(hi, u);
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    ts.wlo[warp] = lo;
+    ts.whi[warp] = hi;
+  }
+  if (tid == 0) ts.ncand = 0;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, ts.wlo[w]);
+    hi = max(hi, ts.whi[w]);
+  }
+
+  // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
+  int need = k, nin = n;
+  while (nin > kTkCand && lo != hi) {
+    const uint32_t range = hi - lo;
+    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;  // (range >> shift) < 1024
+    for (int i = tid; i < kTkBins; i += NT) ts.hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t u = key(i);
+      if (u >= lo && u <= hi) atomicAdd(&ts.hist[(u - lo) >> shift], 1u);
+    }
+    __syncthreads();
+    uint32_t c[BPT];
+    int s = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      c[j] = ts.hist[tid * BPT + j];
+      s += (int)c[j];
+    }
+    int incl = s;  // sum over the lanes >= this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) ts.wa[warp] = incl;
+    __syncthreads();
+    int above = incl - s;  // keys in the bins above this thread's
+    for (int w = warp + 1; w < NW; ++w) above += ts.wa[w];
+    if (above < need && above + s >= need) {
+      int acc = above;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (acc + (int)c[j] >= need) {
+          ts.bstar = tid * BPT + j;
+          ts.need = need - acc;
+          ts.nb = (int)c[j];
+          break;
+        }
+        acc += (int)c[j];
+      }
+    }
+    __syncthreads();
+    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
+    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
+    lo = nlo;
+    need = ts.need;
+    nin = ts.nb;
+    // the next round's first barrier orders these reads before the next writes
+  }
+
+  // 3. the boundary pair (T, t) among at most kTkCand candidates (one atomic per warp
+  // and pass gathers them; the ranking reads a contiguous copy of their keys)
+  const bool by_index = nin > kTkCand;  // then lo == hi
+  if (!by_index) {
+    for (int i0 = 0; i0 < n; i0 += NT) {
+      const int i = i0 + tid;
+      uint32_t u = 0;
+      const bool in = i < n && (u = key(i), u >= lo && u <= hi);
+      const unsigned m = __ballot_sync(0xffffffffu, in);
+      int slot0 = 0;
+      if (m && lane == 0) slot0 = atomicAdd(&ts.ncand, __popc(m));
+      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+      if (in) {
+        const int slot = slot0 + __popc(m & lt);
+        if (slot < kTkCand) {
+          ts.cand[slot] = i;
+          ts.ckey[slot] = u;
+        }
+      }
+    }
+    __syncthreads();
+    const int nc = min(ts.ncand, kTkCand);
+    for (int j = tid; j < nc; j += NT) {
+      const int ci = ts.cand[j];
+      const uint32_t cu = ts.ckey[j];
+      int r0 = 0, r1 = 0;
+      int m = 0;
+      for (; m + 1 < nc; m += 2) {
+        const uint32_t a0 = ts.ckey[m], a1 = ts.ckey[m + 1];
+        const int c0 = ts.cand[m], c1 = ts.cand[m + 1];
+        r0 += (a0 > cu) | ((a0 == cu) & (c0 < ci));
+        r1 += (a1 > cu) | ((a1 == cu) & (c1 < ci));
+      }
+      if (m < nc) r0 += (ts.ckey[m] > cu) | ((ts.ckey[m] == cu) & (ts.cand[m] < ci));
+      if (r0 + r1 == need - 1) {
+        ts.tkey = cu;
+        ts.tidx = ci;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t T = by_index ? lo : ts.tkey;
+  const int tI = by_index ? 0 : ts.tidx;
+  // 0: not taken, 1: taken, 2: a boundary key, taken by ascending index
+  auto pick = [&](int i) -> int {
+    const uint32_t u = key(i);
+    if (u > hi) return 1;
+    if (u < lo) return 0;
+    if (by_index) return 2;
+    return (u > T || (u == T && i <= tI)) ? 1 : 0;
+  };
+
+  // 4. ascending compaction: warp w owns a contiguous span of indices
+  const int span = (((n + NW - 1) / NW) + 31) & ~31;
+  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
+  int cnt = 0, bcnt = 0;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const int t = i < w1 ? pick(i) : 0;
+    cnt += __popc(__ballot_sync(0xffffffffu, t == 1));
+    bcnt += __popc(__ballot_sync(0xffffffffu, t == 2));
+  }
+  if (lane == 0) {
+    ts.wa[warp] = cnt;
+    ts.wb[warp] = bcnt;
+  }
+  __syncthreads();
+  int base = 0, bseen = 0;
+  for (int w = 0; w < warp; ++w) {
+    base += ts.wa[w];
+    bseen += ts.wb[w];
+  }
+  int o = base + min(need, bseen);
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const int t = i < w1 ? pick(i) : 0;
+    const unsigned m2 = __ballot_sync(0xffffffffu, t == 2);
+    const bool take = t == 1 || (t == 2 && bseen + __popc(m2 & lt) < need);
+    const unsigned mt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int pos = o + __popc(mt & lt);
+      if (pos < k) {
+        out[pos] = i;
+        if (out2) out2[pos] = i;
+      }
+    }
+    o += __popc(mt);
+    bseen += __popc(m2);
+  }
+  __syncthreads();  // the scratch may be reused right after
 }
 
 }  // namespace rkv

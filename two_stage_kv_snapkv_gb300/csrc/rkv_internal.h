@@ -1,6 +1,7 @@
 // Internal launcher interface between the C-ABI layer (rkv_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -35,6 +36,11 @@ void launch_end(int kind, cudaStream_t stream);
 int num_sms();
 // Sets the message rkv_last_error() returns on this thread.
 void set_last_error(const char* msg);
+
+// A [rows][128] bf16 array as a 2-D tensor map of box_rows x 64-element boxes with
+// 128-byte swizzle (a box row is 128 B; its 16-byte pieces are XOR-ed with row % 8).
+// False when the driver's encoder is unavailable or rejects the map.
+bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
 
 // --------------------------------------------------------------- cache append
 cudaError_t launch_append(const rkv_cache& c, const rkv_bf16* k_new, const rkv_bf16* v_new,

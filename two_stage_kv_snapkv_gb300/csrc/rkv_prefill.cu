@@ -17,18 +17,26 @@
 //                       (value desc, position asc) + the window, ascending
 //   snap_compact        gather of the survivors' K/V into the cache pages, their
 //                       Kmax/Kmin summaries, seq_len = keep1
-// The logits are m16n8k16 bf16 tensor-core MMAs with fp32 accumulation; K tiles are
-// staged in shared memory with cp.async, Q fragments stay in registers.
+// The logits are tcgen05 MMAs (5th-generation tensor cores, bf16 in, fp32 out in
+// tensor memory): each CTA scores a run of 128-key tiles of one unit, the tiles
+// streamed in by TMA, with the unit's query rows resident in shared memory.  Pass 1
+// puts the query rows on the TMEM lanes (one row per epilogue thread: the row's
+// running max and sum stay in that thread); pass 2 swaps the operands so the keys
+// are the lanes (one key per thread: its column sum over the rows is a private loop).
 #include "rkv_device.cuh"
 #include "rkv_internal.h"
 
 namespace rkv {
 namespace {
 
-constexpr int kSnapThreads = 128;  // 4 warps x 32 query rows
-constexpr int kSnapTile = 64;      // keys per shared-memory tile
-constexpr int kRowB = 272;         // 256 B key row + 16 B pad
-constexpr int kSnapSmem = 128 * kRowB + 2 * kSnapTile * kRowB + 4 * kSnapTile * 4;
+constexpr int kTcTile = 128;                      // keys per tile (the MMA's M or N)
+constexpr int kTcTilesPerItem = 16;               // tiles per CTA
+constexpr int kTcItemKeys = kTcTile * kTcTilesPerItem;
+constexpr int kTcStages = 2;                      // K tiles in flight per CTA
+constexpr int kTcThreads = 192;                   // warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr int kTcOperandBytes = 128 * 256;        // 128 rows x 128 bf16: two 128 x 64 boxes
+constexpr int kTcSmem = 1024 + kTcOperandBytes * (1 + kTcStages);
+constexpr int kTcTmemCols = 256;                  // two 128-column fp32 accumulators
 constexpr int kMaxSnapSplit = 256;
 constexpr int kPoolTile = 2048;
 constexpr int kPoolThreads = 256;
@@ -36,10 +44,11 @@ constexpr int kMaxPool = 255;
 constexpr int kSelectThreads = 1024;
 
 struct SnapParams {
+  CUtensorMap tmk;        // k as [B*Hkv*Lmax rows][128] bf16, 128-row x 64-channel boxes, 128-B swizzle
   const rkv_bf16* q_win;
   const rkv_bf16* k;
   const rkv_bf16* v;
-  int B, Hq, Hkv, G, w, R, Lmax, nsplit, tiles_per_split;
+  int B, Hq, Hkv, G, w, R, Lmax, nsplit;
   float scale_log2;
   float2* part;           // [units][nsplit][128] (m, l)
   float2* rowstat;        // [units][128] (M, 1/l)
@@ -60,190 +69,202 @@ struct SnapParams {
   int32_t kp[RKV_MAX_BATCH];
 };
 
+// Byte offset of 16-byte piece `piece` (channels 8*piece .. +7) of row `row` in an
+// operand laid out as TMA writes it: two 128-row x 64-channel boxes (channels 0-63,
+// 64-127) of 128-byte rows, each piece XOR-ed with row % 8.
+__device__ __forceinline__ uint32_t tc_swz(int row, int piece) {
+  return (uint32_t)((piece >> 3) * (kTcOperandBytes / 2) + row * 128 + ((((piece & 7) ^ (row & 7))) << 4));
+}
+
 // ---------------------------------------------------------------------------
-// Both passes.  grid (nsplit, B*Hkv), 128 threads, dynamic smem kSnapSmem.
-// Warp w owns query rows [32w, 32w+32) as two m16 tiles; a 64-key tile is 8 n8
-// tiles; the 128 channels are 8 k16 steps.
+// Both passes.  grid (nsplit, B*Hkv), 192 threads, dynamic smem kTcSmem; CTA
+// `split` scores keys [split * 2048, ...) of its unit (pass 1: all L keys; pass 2:
+// the L - w prefix keys).
+//   warp 4 (one lane): TMA loads of the K tiles into a two-stage ring;
+//   warp 5 (one lane): per tile, eight K=16 MMAs into accumulator (tile % 2) of TMEM;
+//   warps 0-3: read the accumulator (thread = TMEM lane) and fold it.
+// Barriers: full[s] (TMA -> MMA, transaction bytes), empty[s] (MMA commit -> TMA),
+// tfull[d] (MMA commit -> epilogue), tempty[d] (128 epilogue arrivals -> MMA).  Every
+// wait is bounded; a wait that runs out flags RKV_DEVERR_TIMEOUT, stops every role
+// and the CTA drains what it issued before freeing TMEM.
 // ---------------------------------------------------------------------------
 template <bool kStats>
-__global__ void __launch_bounds__(kSnapThreads) snap_score_kernel(const __grid_constant__ SnapParams p) {
+__global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_constant__ SnapParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* qs = smem;
-  uint8_t* ks = smem + 128 * kRowB;
-  float* colbuf = reinterpret_cast<float*>(ks + 2 * kSnapTile * kRowB);
+  __shared__ uint64_t full_b[kTcStages], empty_b[kTcStages], tfull_b[2], tempty_b[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ volatile int abort_flag;
+  __shared__ float2 rs[128];  // pass 2: (M_r, 1/l_r)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv, split = blockIdx.x;
   const int L = p.L[b];
   const int col_end = kStats ? L : L - p.w;  // keys scored by this pass
-  const int t_begin = split * p.tiles_per_split * kSnapTile;
-  const int t_end = min(col_end, t_begin + p.tiles_per_split * kSnapTile);
-  const int ntiles = t_end > t_begin ? (t_end - t_begin + kSnapTile - 1) / kSnapTile : 0;
-
-  // rows of this thread: idx = mt*2 + h -> r = 32*warp + 16*mt + lane/4 + 8*h
-  int rows[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) rows[i] = 32 * warp + 16 * (i >> 1) + (lane >> 2) + 8 * (i & 1);
-
+  const int t_begin = split * kTcItemKeys;
+  const int t_end = min(col_end, t_begin + kTcItemKeys);
+  const int ntiles = t_end > t_begin ? (t_end - t_begin + kTcTile - 1) / kTcTile : 0;
   if (ntiles == 0) {
-    if (kStats && (lane & 3) == 0) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        p.part[((size_t)unit * p.nsplit + split) * 128 + rows[i]] = make_float2(-1e30f, 0.f);
-    }
+    if (kStats && tid < 128) p.part[((size_t)unit * p.nsplit + split) * 128 + tid] = make_float2(-1e30f, 0.f);
     return;
   }
+  uint8_t* qs = align1024(smem);
+  uint8_t* ks = qs + kTcOperandBytes;
 
-  const rkv_bf16* kbase = p.k + ((size_t)b * p.Hkv + g) * p.Lmax * 128;
-  auto load_tile = [&](int ti, int buf) {
-    const int t0 = t_begin + ti * kSnapTile;
-    for (int e = tid; e < kSnapTile * 16; e += kSnapThreads) {
-      const int row = e >> 4, c16 = e & 15;
-      const int t = t0 + row;
-      const bool ok = t < t_end;
-      cp_async16(ks + (buf * kSnapTile + row) * kRowB + c16 * 16, ok ? kbase + (size_t)t * 128 + c16 * 8 : p.k,
-                 ok ? 16u : 0u);
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full_b[s], 1);
+      mbar_init(&empty_b[s], 1);
     }
-  };
-  // Q rows (zero beyond R)
-  for (int e = tid; e < 128 * 16; e += kSnapThreads) {
-    const int r = e >> 4, c16 = e & 15;
-    const bool ok = r < p.R;
-    const rkv_bf16* src =
-        ok ? p.q_win + (((size_t)b * p.Hq + (size_t)g * p.G + r / p.w) * p.w + r % p.w) * 128 + c16 * 8 : p.q_win;
-    cp_async16(qs + r * kRowB + c16 * 16, src, ok ? 16u : 0u);
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&tfull_b[d], 1);
+      mbar_init(&tempty_b[d], 128);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
   }
-  load_tile(0, 0);
-  cp_async_commit();
-  if (ntiles > 1) load_tile(1, 1);
-  cp_async_commit();
-
-  // per-row state
-  float st_a[4], st_b[4];   // stats: (m, l); colsum: (M, 1/l)
-  int lim[4];               // stats: last visible key position of the row
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = rows[i];
-    if (kStats) {
-      st_a[i] = -1e30f;
-      st_b[i] = 0.f;
-      lim[i] = r < p.R ? L - p.w + (r % p.w) : -1;
-    } else {
-      const float2 rs = p.rowstat[(size_t)unit * 128 + r];
-      st_a[i] = rs.x;
-      st_b[i] = rs.y;
-      lim[i] = 0;
-    }
+  if (warp == 5) {
+    tmem_alloc(&tmem_base, kTcTmemCols);
+    tmem_relinquish();
   }
+  // the unit's query rows (row r = head * w + j), zero from row R on
+  for (int e = tid; e < 128 * 16; e += kTcThreads) {
+    const int r = e >> 4, piece = e & 15;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < p.R)
+      v = *reinterpret_cast<const uint4*>(
+          p.q_win + (((size_t)b * p.Hq + (size_t)g * p.G + r / p.w) * p.w + r % p.w) * 128 + piece * 8);
+    *reinterpret_cast<uint4*>(qs + tc_swz(r, piece)) = v;
+  }
+  if (!kStats)
+    for (int r = tid; r < 128; r += kTcThreads) rs[r] = p.rowstat[(size_t)unit * 128 + r];
+  fence_proxy_async_smem();  // the generic writes of Q, before the MMAs read it
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  int issued = 0, committed = -1;  // TMA tiles issued (warp 4); last tile committed (warp 5)
 
-  uint32_t af[2][8][4];
-  const float sl = p.scale_log2;
-  for (int ti = 0; ti < ntiles; ++ti) {
-    const int buf = ti & 1;
-    cp_async_wait<1>();
-    __syncthreads();
-    if (ti == 0) {
-      const uint32_t q32 = smem_u32(qs);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ldsm_x4(af[mt][kk][0], af[mt][kk][1], af[mt][kk][2], af[mt][kk][3],
-                  q32 + (warp * 32 + mt * 16 + (lane & 15)) * kRowB + (kk * 16 + (lane >> 4) * 8) * 2);
-    }
-    float acc[2][8][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-    const uint32_t k32 = smem_u32(ks + buf * kSnapTile * kRowB);
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int kk2 = 0; kk2 < 4; ++kk2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, k32 + (nt * 8 + (lane & 7)) * kRowB + (kk2 * 32 + (lane >> 3) * 8) * 2);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const uint32_t* a0 = af[mt][2 * kk2];
-          const uint32_t* a1 = af[mt][2 * kk2 + 1];
-          mma_16816(acc[mt][nt], a0[0], a0[1], a0[2], a0[3], b0, b1);
-          mma_16816(acc[mt][nt], a1[0], a1[1], a1[2], a1[3], b2, b3);
+  if (warp == 4) {
+    if (lane == 0) {
+      const int row0 = unit * p.Lmax + t_begin;  // rows past the unit are masked, past the array zero
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % kTcStages;
+        if (i >= kTcStages && !mbar_wait(&empty_b[s], (uint32_t)((i / kTcStages - 1) & 1))) {
+          flag_error(p.err, RKV_DEVERR_TIMEOUT);
+          abort_flag = 1;
         }
+        if (abort_flag) break;
+        uint8_t* st = ks + s * kTcOperandBytes;
+        mbar_arrive_expect_tx(&full_b[s], kTcOperandBytes);
+        tma_load_2d(st, &p.tmk, 0, row0 + i * kTcTile, &full_b[s]);
+        tma_load_2d(st + kTcOperandBytes / 2, &p.tmk, 64, row0 + i * kTcTile, &full_b[s]);
+        issued = i + 1;
       }
     }
-    __syncthreads();  // every warp is done with this buffer
-    if (ti + 2 < ntiles) load_tile(ti + 2, buf);
-    cp_async_commit();
-
-    const int t0 = t_begin + ti * kSnapTile + 2 * (lane & 3);
-    if (kStats) {
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      const uint32_t q32 = smem_u32(qs), k32 = smem_u32(ks);
+      for (int i = 0; i < ntiles; ++i) {
+        const int s = i % kTcStages, d = i & 1;
+        bool ok = mbar_wait(&full_b[s], (uint32_t)((i / kTcStages) & 1));
+        if (ok && i >= 2) ok = mbar_wait(&tempty_b[d], (uint32_t)(((i >> 1) - 1) & 1));
+        if (!ok) {
+          flag_error(p.err, RKV_DEVERR_TIMEOUT);
+          abort_flag = 1;
+        }
+        if (abort_flag) break;
+        tc_fence_after();
+        const uint32_t kt = k32 + s * kTcOperandBytes;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int mt = i >> 1, h = i & 1;
-        float z[16];
-        float mx = -INFINITY;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTcOperandBytes / 2) + (kk & 3) * 32;
+          const uint64_t qd = sw128_kmajor_desc(q32 + off), kd = sw128_kmajor_desc(kt + off);
+          tc_mma_bf16(tmem + d * 128, kStats ? qd : kd, kStats ? kd : qd, idesc, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&empty_b[s]);
+        tc_commit(&tfull_b[d]);
+        committed = i;
+      }
+      // the last tile's stage release lands before the CTA may exit
+      if (committed >= 0 && !abort_flag)
+        mbar_wait(&empty_b[committed % kTcStages], (uint32_t)((committed / kTcStages) & 1));
+    }
+  } else {
+    // epilogue: thread tid owns TMEM lane tid (pass 1: query row tid; pass 2: key t0 + tid)
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl = p.scale_log2;
+    float m_run = -1e30f, l_run = 0.f;
+    const int lim = (kStats && tid < p.R) ? L - p.w + tid % p.w : -1;  // last key row tid sees
+    for (int i = 0; i < ntiles; ++i) {
+      const int d = i & 1;
+      const bool late = !mbar_wait(&tfull_b[d], (uint32_t)((i >> 1) & 1));
+      if (late) {
+        flag_error(p.err, RKV_DEVERR_TIMEOUT);
+        abort_flag = 1;
+      }
+      if (__any_sync(0xffffffffu, late || abort_flag)) break;  // warp-uniform: the TMEM loads are .aligned
+      tc_fence_after();
+      const int t0 = t_begin + i * kTcTile;
+      if (kStats) {
+        const int vis = min(t_end, lim + 1) - t0;  // keys of this tile the row sees: [0, vis)
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tc_ld32_wait(lane_addr + d * 128 + c * 32, v);
+          float z[32];
+          float mx = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int t = t0 + nt * 8 + c;
-            const float v = (t <= lim[i] && t < t_end) ? acc[mt][nt][2 * h + c] * sl : -INFINITY;
-            z[nt * 2 + c] = v;
-            mx = fmaxf(mx, v);
+          for (int j = 0; j < 32; ++j) {
+            z[j] = (c * 32 + j < vis) ? __uint_as_float(v[j]) * sl : -INFINITY;
+            mx = fmaxf(mx, z[j]);
           }
-        const float m_new = fmaxf(st_a[i], mx);
-        float sum = 0.f;
+          const float m_new = fmaxf(m_run, mx);
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sum += exp2f(z[e] - m_new);
-        st_b[i] = st_b[i] * exp2f(st_a[i] - m_new) + sum;
-        st_a[i] = m_new;
-      }
-    } else {
-      float cs[8][2];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) cs[nt][0] = cs[nt][1] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int mt = i >> 1, h = i & 1;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) cs[nt][c] += exp2f(acc[mt][nt][2 * h + c] * sl - st_a[i]) * st_b[i];
-      }
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float x = cs[nt][c];
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          x += __shfl_xor_sync(0xffffffffu, x, 8);
-          x += __shfl_xor_sync(0xffffffffu, x, 16);
-          if (lane < 4) colbuf[warp * kSnapTile + nt * 8 + 2 * lane + c] = x;
+          for (int j = 0; j < 32; j += 2) {
+            s0 += exp2f(z[j] - m_new);
+            s1 += exp2f(z[j + 1] - m_new);
+          }
+          l_run = l_run * exp2f(m_run - m_new) + (s0 + s1);
+          m_run = m_new;
         }
-      __syncthreads();
-      if (tid < kSnapTile) {
-        const int t = t_begin + ti * kSnapTile + tid;
-        if (t < t_end)
-          p.S[(size_t)unit * p.Lmax + t] =
-              (colbuf[tid] + colbuf[kSnapTile + tid]) + (colbuf[2 * kSnapTile + tid] + colbuf[3 * kSnapTile + tid]);
+      } else {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4 && c * 32 < p.R; ++c) {
+          uint32_t v[32];
+          tc_ld32_wait(lane_addr + d * 128 + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 a0 = rs[c * 32 + j], a1 = rs[c * 32 + j + 1];
+            s0 = fmaf(exp2f(__uint_as_float(v[j]) * sl - a0.x), a0.y, s0);
+            s1 = fmaf(exp2f(__uint_as_float(v[j + 1]) * sl - a1.x), a1.y, s1);
+          }
+        }
+        const int t = t0 + tid;
+        if (t < t_end) p.S[(size_t)unit * p.Lmax + t] = s0 + s1;
       }
+      tc_fence_before();
+      mbar_arrive(&tempty_b[d]);
     }
+    if (kStats) p.part[((size_t)unit * p.nsplit + split) * 128 + tid] = make_float2(m_run, l_run);
   }
 
-  if (kStats) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, st_a[i], o);
-        const float lo = __shfl_xor_sync(0xffffffffu, st_b[i], o);
-        const float M = fmaxf(st_a[i], mo);
-        st_b[i] = st_b[i] * exp2f(st_a[i] - M) + lo * exp2f(mo - M);
-        st_a[i] = M;
-      }
-      if ((lane & 3) == 0) p.part[((size_t)unit * p.nsplit + split) * 128 + rows[i]] = make_float2(st_a[i], st_b[i]);
-    }
+  // teardown: after a timeout, wait (bounded) for the copies and MMAs still in flight
+  tc_fence_before();
+  __syncthreads();
+  if (abort_flag) {
+    if (warp == 4 && lane == 0)
+      for (int i = max(0, issued - kTcStages); i < issued; ++i)
+        mbar_wait(&full_b[i % kTcStages], (uint32_t)((i / kTcStages) & 1));
+    if (warp == 5 && lane == 0 && committed >= 0)
+      mbar_wait(&tfull_b[committed & 1], (uint32_t)((committed >> 1) & 1));
+    __syncthreads();
+  }
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
   }
 }
 
@@ -434,30 +455,31 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     Lmax_seen = a.prompt_len[b] > Lmax_seen ? a.prompt_len[b] : Lmax_seen;
     keep_max = a.keep1[b] > keep_max ? a.keep1[b] : keep_max;
   }
-  // splits along L: one wave of 2 resident CTAs per SM (the register count allows 2)
-  const int tiles = (Lmax_seen + kSnapTile - 1) / kSnapTile;
-  const int slots = 2 * num_sms();
-  int nsplit = (int)units < slots ? slots / (int)units : 1;
-  nsplit = nsplit < 1 ? 1 : (nsplit > kMaxSnapSplit ? kMaxSnapSplit : nsplit);
-  nsplit = nsplit > tiles ? tiles : nsplit;
-  p.tiles_per_split = (tiles + nsplit - 1) / nsplit;
-  p.nsplit = (tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-
+  // one CTA per 2048 keys of a unit
+  p.nsplit = (Lmax_seen + kTcItemKeys - 1) / kTcItemKeys;
+  if (p.nsplit > kMaxSnapSplit) {
+    set_last_error("prompt longer than the scoring kernels' split table (524288 tokens)");
+    return cudaErrorInvalidValue;
+  }
+  if (!encode_rows_map(&p.tmk, a.k, (uint64_t)a.B * a.Hkv * a.Lmax, kTcTile)) {
+    set_last_error("cuTensorMapEncodeTiled failed for the prompt keys");
+    return cudaErrorInvalidValue;
+  }
   static bool attrs = false;
   if (!attrs) {
-    cudaFuncSetAttribute(snap_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSnapSmem);
-    cudaFuncSetAttribute(snap_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSnapSmem);
+    cudaFuncSetAttribute(snap_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    cudaFuncSetAttribute(snap_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     attrs = true;
   }
   const dim3 sgrid(p.nsplit, (unsigned)units);
   launch_begin(K_SNAP_STATS, s);
-  snap_score_kernel<true><<<sgrid, kSnapThreads, kSnapSmem, s>>>(p);
+  snap_score_kernel<true><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
   launch_end(K_SNAP_STATS, s);
   launch_begin(K_SNAP_STATS_COMBINE, s);
   snap_stats_combine_kernel<<<(unsigned)units, 128, 0, s>>>(p);
   launch_end(K_SNAP_STATS_COMBINE, s);
   launch_begin(K_SNAP_COLSUM, s);
-  snap_score_kernel<false><<<sgrid, kSnapThreads, kSnapSmem, s>>>(p);
+  snap_score_kernel<false><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
   launch_end(K_SNAP_COLSUM, s);
   launch_begin(K_SNAP_POOL, s);
   snap_pool_kernel<<<dim3((Lmax_seen + kPoolTile - 1) / kPoolTile, (unsigned)units), kPoolThreads, 0, s>>>(p);
