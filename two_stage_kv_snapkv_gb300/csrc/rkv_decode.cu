@@ -11,7 +11,7 @@
 // * hsa_step_kernel (fused, one launch): one thread-block cluster per (sequence, KV
 //   head).  Optionally appends the new token first.  Every CTA selects the
 //   channels; each CTA stages the summaries of its slice of pages into shared
-//   memory with bulk copies (one round trip) and bounds those pages; the page
+//   memory (cp.async, one round trip) and bounds those pages; the page
 //   scores are shared through distributed shared memory; every CTA runs the same
 //   top-k2 select, attends over its share of the selected pages, and the CTAs'
 //   partial softmax states are merged through distributed shared memory.  Used
@@ -103,53 +103,92 @@ __device__ __forceinline__ int seq_length(const HsaParams& p, int b) {
 
 // Shared-memory state of the channel selection (one KV head).
 struct ChanSmem {
-  alignas(16) uint32_t ahi[128];  // high and low words of the fp64 channel scores
-  uint32_t alo[128];
+  alignas(16) uint32_t ahi[128];  // rank keys: fp32 bits, or the high words of fp64 scores
+  uint32_t alo[128];              // low words of the fp64 scores (fp64 path only)
   int chan[128];
   float qpos[128], qneg[128];
   int warp_cnt[8];
 };
 
 // Top-k1 channels of a_i = sum_h |q_h,i| (ties: lower channel), ascending, with the
-// per-channel sums of the positive and negative parts of q over the group.  The
-// channel score is summed in fp64, where a sum of <= 8 bf16 magnitudes is exact, and
-// ranked on its bit pattern (order-preserving for non-negative doubles): the high
-// words decide unless another channel shares this one's high word.
-// Every thread of a block of >= 128 threads calls this after filling qf[G][128].
+// per-channel sums of the positive and negative parts of q over the group.
+// The scores are ranked exactly.  A sum of <= 8 bf16 magnitudes is usually exact in
+// fp32 (each addition is checked: with x >= y >= 0, x + y is exact iff
+// (x + y) - x == y); then the fp32 bit patterns rank like the exact sums.  Otherwise
+// the block sums in fp64 (as the oracle does) and ranks on the fp64 bit patterns,
+// high words first.  Every thread of a block of >= 128 threads calls this after
+// filling qf[G][128].
 __device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int k1) {
   const int tid = threadIdx.x;
   __syncthreads();
-  uint32_t hi = 0, lo = 0;
+  float sf = 0.f;
+  bool exact = true;
   if (tid < 128) {
-    double s = 0.0;
-    for (int h = 0; h < G; ++h) s += fabs((double)qf[h][tid]);
-    const unsigned long long u = (unsigned long long)__double_as_longlong(s);
-    hi = (uint32_t)(u >> 32);
-    lo = (uint32_t)u;
-    cs.ahi[tid] = hi;
-    cs.alo[tid] = lo;
+    for (int h = 0; h < G; ++h) {
+      const float x = fabsf(qf[h][tid]);
+      const float big = fmaxf(sf, x), small = fminf(sf, x);
+      const float sum = big + small;
+      exact &= (sum - big) == small;
+      sf = sum;
+    }
+  }
+  const bool fast = __syncthreads_and(exact);
+  uint32_t key = 0, lo = 0;
+  if (tid < 128) {
+    if (fast) {
+      key = __float_as_uint(sf) + 1u;  // +1: never 0, so key - 1 below cannot wrap
+    } else {
+      double s = 0.0;
+      for (int h = 0; h < G; ++h) s += fabs((double)qf[h][tid]);
+      const unsigned long long u = (unsigned long long)__double_as_longlong(s);
+      key = (uint32_t)(u >> 32);
+      lo = (uint32_t)u;
+      cs.alo[tid] = lo;
+    }
+    cs.ahi[tid] = key;
   }
   __syncthreads();
   bool sel = false;
   unsigned bal = 0;
   if (tid < 128) {
-    // rank = #greater + #equal at a lower channel
     const uint4* h4 = reinterpret_cast<const uint4*>(cs.ahi);
-    int g0 = 0, g1 = 0, e0 = 0, e1 = 0;
+    const int mine = tid >> 2;
+    int rank;
+    if (fast) {
+      // rank = #(j < tid: key_j >= key) + #(j > tid: key_j > key); a group of four
+      // wholly below this channel compares against key - 1
+      int r0 = 0, r1 = 0;
+#pragma unroll
+      for (int j4 = 0; j4 < 32; ++j4) {
+        const uint4 u = h4[j4];
+        const uint32_t t = j4 < mine ? key - 1u : key;
+        r0 += (u.x > t) + (u.y > t);
+        r1 += (u.z > t) + (u.w > t);
+      }
+      rank = r0 + r1;
+      for (int j = 4 * mine; j < tid; ++j) rank += cs.ahi[j] == key;  // equal, lower, same group
+    } else {
+      int g0 = 0, g1 = 0, e0 = 0, e1 = 0;
 #pragma unroll 8
-    for (int j4 = 0; j4 < 32; ++j4) {
-      const uint4 u = h4[j4];
-      g0 += (u.x > hi) + (u.y > hi);
-      g1 += (u.z > hi) + (u.w > hi);
-      e0 += (u.x == hi) + (u.y == hi);
-      e1 += (u.z == hi) + (u.w == hi);
-    }
-    int rank = g0 + g1;
-    if (e0 + e1 > 1) {  // another channel has the same high word: the low words decide
-      for (int j = 0; j < 128; ++j) {
-        if (cs.ahi[j] != hi || j == tid) continue;
-        const uint32_t l = cs.alo[j];
-        rank += (l > lo) | ((l == lo) & (j < tid));
+      for (int j4 = 0; j4 < 32; ++j4) {
+        const uint4 u = h4[j4];
+        g0 += (u.x > key) + (u.y > key);
+        g1 += (u.z > key) + (u.w > key);
+        e0 += (u.x == key) + (u.y == key);
+        e1 += (u.z == key) + (u.w == key);
+      }
+      rank = g0 + g1;
+      if (e0 + e1 > 1) {  // another channel has the same high word: the low words decide
+        const uint4* l4 = reinterpret_cast<const uint4*>(cs.alo);
+        for (int j4 = 0; j4 < 32; ++j4) {
+          const uint4 u = h4[j4], l = l4[j4];
+          const uint32_t hv[4] = {u.x, u.y, u.z, u.w}, lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            if (hv[e] == key && j != tid) rank += (lv[e] > lo) | ((lv[e] == lo) & (j < tid));
+          }
+        }
       }
     }
     sel = rank < k1;
@@ -444,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ChanSmem cs;
   __shared__ AttnSmem<STAGES> as;
-  __shared__ uint64_t sbar, pbar;
+  __shared__ uint64_t pbar;
   __shared__ __align__(16) uint8_t new_kv[512];
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -484,10 +523,12 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   }
   const int n = n0 + (do_append ? 1 : 0);
   const int NP = (n + P - 1) / P;
+  // this CTA's slice [p0, p1) of the pages (8-page aligned)
+  const int per = ((NP + C - 1) / C + 7) & ~7;
+  const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
 
   // 2. barriers; prefetch of the sequence's page-table row (needed after the select)
   if (tid == 0) {
-    mbar_init(&sbar, 1);
     mbar_init(&pbar, 1);
     fence_mbar_init();
   }
@@ -534,30 +575,33 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
 
   // 6. page bounds of this CTA's slice [p0, p1) (8-page aligned).  The k1 Kmax and
   // k1 Kmin row pieces of a tile (the region holds the whole slice whenever it fits)
-  // are bulk-copied at once (one round trip); the appended token is folded into its
+  // are copied at once by every thread in 16-byte cp.async chunks (one round trip);
+  // the appended token is folded into its
   // page's staged summary (a fold that the append may already have done changes
   // nothing: max and min are idempotent); then every thread bounds pages from shared
   // memory, and the scores go to every CTA's key array.
-  const int per = ((NP + C - 1) / C + 7) & ~7;
-  const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
   const int tcap = (p.region_bytes / (4 * k1)) & ~7;
   rkv_bf16* stg = reinterpret_cast<rkv_bf16*>(ring);
   const int pnew = do_append ? n0 / P : -1;
   bool waited = false;
-  for (int t0 = p0, tile = 0; t0 < p1; t0 += tcap, ++tile) {
+  for (int t0 = p0; t0 < p1; t0 += tcap) {
     const int cnt = min(tcap, p1 - t0);
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
-    fence_proxy_async_smem();
     __syncthreads();  // the previous tile (or the query) is consumed
-    if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
-    __syncthreads();
-    for (int i = tid; i < 2 * k1; i += kThreads) {
-      const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
-      const int ch = cs.chan[i < k1 ? i : i - k1];
-      bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0,
-               (uint32_t)cnt8 * 2, &sbar);
+    {
+      // consecutive threads take consecutive 16-byte chunks (8 pages) of the rows
+      const int cpr = cnt8 >> 3;
+      for (int e = tid; e < 2 * k1 * cpr; e += kThreads) {
+        const int i = e / cpr, c = e - i * cpr;
+        const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
+        const int ch = cs.chan[i < k1 ? i : i - k1];
+        cp_async16(ring + (size_t)i * cnt8 * 2 + c * 16, base + ((size_t)unit * 128 + ch) * p.max_pages + t0 + c * 8,
+                   16u);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
     }
-    if (!mbar_wait(&sbar, (uint32_t)(tile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
     if (pnew >= t0 && pnew < t0 + cnt) {
       const int j = pnew - t0;
       const bool first = (n0 % P) == 0;
@@ -619,16 +663,18 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
       flag_error(p.err, RKV_DEVERR_PAGE_ID);
     }
   }
-  // 7. top-k2: every CTA runs the same select over all keys (no exchange needed); the
-  // list is ascending.  Its scratch lives in the region, free between the scoring and
-  // the attention.
+  // 7. top-k2: every CTA runs the same select over all keys (no exchange needed), each
+  // thread holding its keys in registers; the list is ascending.  Its scratch lives in
+  // the region, free between the scoring and the attention.  (The key array is 16-byte
+  // aligned and followed by the list and the page-table row, so the select's reads
+  // past NP stay inside this CTA's shared memory.)
   const int k = min(p.k2[b], NP);
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
   } else {
-    topk_adaptive<kThreads>(NP, k, [&](int i) { return keys[i]; }, *reinterpret_cast<TopkSmem<kThreads>*>(ring),
-                            sel, nullptr);
+    topk_regs_any<kThreads>(keys, NP, k, *reinterpret_cast<TopkSmem<kThreads>*>(ring), sel);
   }
+  if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   __syncthreads();
   if (rank == 0 && p.sel_pages) {  // the caller's copy (CTA 0 only)
     int32_t* user_pages = p.sel_pages + (size_t)unit * p.sel_pages_stride;
@@ -636,7 +682,6 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     if (tid == 0 && k < p.sel_pages_stride) user_pages[k] = -1;
   }
   fence_proxy_async_smem();  // generic writes to the region before the attention's TMA loads
-  if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   if (!mbar_wait(&pbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
   __syncthreads();
 

@@ -126,6 +126,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+
 // Tiled TMA load of one box of a 2-D tensor map into this CTA's shared memory;
 // completion is signalled on `bar` as transaction bytes.  `map` must live in
 // parameter, constant or global memory (a __grid_constant__ kernel parameter).
@@ -213,97 +214,6 @@ __device__ __forceinline__ void flag_error(int32_t* word, int32_t bit) {
   if (word) atomicOr(word, bit);
 }
 
-// ------------------------------------------------------------------ block scan
-// Exclusive prefix sum of one int per thread over a block of NT threads.
-// `scratch` needs NT/32 + 1 ints of shared memory.  Returns the block total in *total.
-template <int NT>
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = (lane < NT / 32) ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < NT / 32) scratch[lane] = w;   // inclusive warp totals
-    if (lane == NT / 32 - 1) scratch[NT / 32] = w;
-  }
-  __syncthreads();
-  const int base = (warp > 0) ? scratch[warp - 1] : 0;
-  *total = scratch[NT / 32];
-  const int r = base + x - v;
-  __syncthreads();   // scratch may be reused right after
-  return r;
-}
-
-// ------------------------------------------------------------------ radix select
-// Block-wide threshold search for the k largest of n uint32 keys (k <= n).
-// Returns T = the k-th largest key and need_eq = how many keys equal to T belong to
-// the top k (the rest of the top k are the keys > T).  Four 8-bit digit passes from
-// the most significant byte; `key(i)` is called for i in [0, n) several times.
-// `hist` needs 256 + 2 uint32 of shared memory.
-template <int NT, class KeyFn>
-__device__ void block_radix_threshold(int n, int k, KeyFn key, uint32_t* hist, uint32_t* T_out,
-                                      int* need_out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += NT) {
-      const uint32_t u = key(i);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      uint32_t c[8];
-      uint32_t s = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[lane * 8 + j];
-        s += c[j];
-      }
-      // suffix sum over lanes: above = sum of lanes > lane
-      uint32_t incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-      }
-      const uint32_t above = incl - s;
-      if (above < (uint32_t)remaining && incl >= (uint32_t)remaining) {
-        uint32_t acc = above;
-        for (int j = 7; j >= 0; --j) {
-          if (acc + c[j] >= (uint32_t)remaining) {
-            hist[256] = (uint32_t)(lane * 8 + j);
-            hist[257] = (uint32_t)remaining - acc;
-            break;
-          }
-          acc += c[j];
-        }
-      }
-    }
-    __syncthreads();
-    const uint32_t bucket = hist[256];
-    remaining = (int)hist[257];
-    prefix |= bucket << shift;
-    mask |= 255u << shift;
-    __syncthreads();
-  }
-  *T_out = prefix;
-  *need_out = remaining;
-}
-
 // ------------------------------------------------------------------ adaptive-bin top-k
 // Top k of n uint32 keys, ordered by (key descending, index ascending), for
 // 1 <= k < n: the ascending indices go to out[0..k) (and out2, when not null).
@@ -316,12 +226,16 @@ __device__ void block_radix_threshold(int n, int k, KeyFn key, uint32_t* hist, u
 // If the interval has shrunk to a single key value with more keys than that, the
 // equal keys are taken by ascending index.  Keys are order-preserving images of
 // floats in practice, so one round usually leaves a handful of candidates.
-// `key(i)` is called several times for each i in [0, n); every thread calls this.
+//
+// Thread t owns the contiguous keys [t seg, t seg + seg), seg odd: strided
+// shared-memory reads then hit distinct banks, a run of equal keys adds to the
+// histogram once, and the compaction is one pass with one block scan.  `key(i)` is
+// called several times for each i in [0, n); every thread of the block calls this.
 constexpr int kTkBins = 1024;
 constexpr int kTkCand = 32;
 template <int NT>
 struct TopkSmem {
-  uint32_t hist[kTkBins];
+  alignas(16) uint32_t hist[kTkBins];
   int cand[kTkCand];
   uint32_t ckey[kTkCand];
   uint32_t wlo[NT / 32], whi[NT / 32];
@@ -336,11 +250,13 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
   constexpr int NW = NT / 32;
   constexpr int BPT = kTkBins / NT;  // bins per thread
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned lt = (1u << lane) - 1u;
+  const int seg = ((n + NT - 1) / NT) | 1;
+  const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
 
   // 1. the key range
   uint32_t lo = 0xffffffffu, hi = 0u;
-  for (int i = tid; i < n; i += NT) {
+#pragma unroll 4
+  for (int i = s0; i < s1; ++i) {
     const uint32_t u = key(i);
     lo = min(lo, u);
     hi = max(hi, u);
@@ -366,18 +282,37 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
     const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;  // (range >> shift) < 1024
     for (int i = tid; i < kTkBins; i += NT) ts.hist[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += NT) {
+    int run_bin = -1, run = 0;
+#pragma unroll 4
+    for (int i = s0; i < s1; ++i) {
       const uint32_t u = key(i);
-      if (u >= lo && u <= hi) atomicAdd(&ts.hist[(u - lo) >> shift], 1u);
+      const int bin = (u >= lo && u <= hi) ? (int)((u - lo) >> shift) : -1;
+      if (bin != run_bin) {
+        if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
+        run_bin = bin;
+        run = 0;
+      }
+      ++run;
     }
+    if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
     __syncthreads();
     uint32_t c[BPT];
+    if constexpr (BPT % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < BPT; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(&ts.hist[tid * BPT + j]);
+        c[j] = v.x;
+        c[j + 1] = v.y;
+        c[j + 2] = v.z;
+        c[j + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) c[j] = ts.hist[tid * BPT + j];
+    }
     int s = 0;
 #pragma unroll
-    for (int j = 0; j < BPT; ++j) {
-      c[j] = ts.hist[tid * BPT + j];
-      s += (int)c[j];
-    }
+    for (int j = 0; j < BPT; ++j) s += (int)c[j];
     int incl = s;  // sum over the lanes >= this one
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -410,20 +345,13 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
     // the next round's first barrier orders these reads before the next writes
   }
 
-  // 3. the boundary pair (T, t) among at most kTkCand candidates (one atomic per warp
-  // and pass gathers them; the ranking reads a contiguous copy of their keys)
+  // 3. the boundary pair (T, t) among at most kTkCand candidates
   const bool by_index = nin > kTkCand;  // then lo == hi
   if (!by_index) {
-    for (int i0 = 0; i0 < n; i0 += NT) {
-      const int i = i0 + tid;
-      uint32_t u = 0;
-      const bool in = i < n && (u = key(i), u >= lo && u <= hi);
-      const unsigned m = __ballot_sync(0xffffffffu, in);
-      int slot0 = 0;
-      if (m && lane == 0) slot0 = atomicAdd(&ts.ncand, __popc(m));
-      slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-      if (in) {
-        const int slot = slot0 + __popc(m & lt);
+    for (int i = s0; i < s1; ++i) {
+      const uint32_t u = key(i);
+      if (u >= lo && u <= hi) {
+        const int slot = atomicAdd(&ts.ncand, 1);
         if (slot < kTkCand) {
           ts.cand[slot] = i;
           ts.ckey[slot] = u;
@@ -462,44 +390,273 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
     return (u > T || (u == T && i <= tI)) ? 1 : 0;
   };
 
-  // 4. ascending compaction: warp w owns a contiguous span of indices
-  const int span = (((n + NW - 1) / NW) + 31) & ~31;
-  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
-  int cnt = 0, bcnt = 0;
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    const int t = i < w1 ? pick(i) : 0;
-    cnt += __popc(__ballot_sync(0xffffffffu, t == 1));
-    bcnt += __popc(__ballot_sync(0xffffffffu, t == 2));
+  // 4. ascending compaction: counts per thread, one block scan, then the writes
+  int c1 = 0, c2 = 0;
+#pragma unroll 4
+  for (int i = s0; i < s1; ++i) {
+    const int t = pick(i);
+    c1 += t == 1;
+    c2 += t == 2;
   }
-  if (lane == 0) {
-    ts.wa[warp] = cnt;
-    ts.wb[warp] = bcnt;
+  int x1 = c1, x2 = c2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y1 = __shfl_up_sync(0xffffffffu, x1, o), y2 = __shfl_up_sync(0xffffffffu, x2, o);
+    if (lane >= o) {
+      x1 += y1;
+      x2 += y2;
+    }
+  }
+  if (lane == 31) {
+    ts.wa[warp] = x1;
+    ts.wb[warp] = x2;
   }
   __syncthreads();
-  int base = 0, bseen = 0;
+  int base = x1 - c1, bseen = x2 - c2;
   for (int w = 0; w < warp; ++w) {
     base += ts.wa[w];
     bseen += ts.wb[w];
   }
   int o = base + min(need, bseen);
-  for (int i0 = w0; i0 < w1; i0 += 32) {
-    const int i = i0 + lane;
-    const int t = i < w1 ? pick(i) : 0;
-    const unsigned m2 = __ballot_sync(0xffffffffu, t == 2);
-    const bool take = t == 1 || (t == 2 && bseen + __popc(m2 & lt) < need);
-    const unsigned mt = __ballot_sync(0xffffffffu, take);
-    if (take) {
-      const int pos = o + __popc(mt & lt);
-      if (pos < k) {
-        out[pos] = i;
-        if (out2) out2[pos] = i;
+  for (int i = s0; i < s1; ++i) {
+    const int t = pick(i);
+    if (t == 1 || (t == 2 && bseen < need)) {
+      if (o < k) {
+        out[o] = i;
+        if (out2) out2[o] = i;
       }
+      ++o;
     }
-    o += __popc(mt);
-    bseen += __popc(m2);
+    bseen += t == 2;
   }
   __syncthreads();  // the scratch may be reused right after
+}
+
+// The same select with every thread's keys held in registers: thread t owns keys
+// [t KPT, t KPT + KPT) of a shared-memory array (read once, by 16-byte loads when KPT
+// is a multiple of 4), so each pass is an unrolled loop over registers instead of a
+// chain of shared-memory loads; the candidates are ranked by warp 0 with shuffles.
+// Needs n <= NT * KPT, `keys` 16-byte aligned and readable up to NT * KPT entries
+// (entries from n on are ignored).  Every thread of the block calls this.
+template <int NT, int KPT>
+__device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
+  static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kTkBins / NT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = tid * KPT;
+  uint32_t kv[KPT];
+  if (i0 < n) {
+    if constexpr (KPT % 4 == 0) {
+#pragma unroll
+      for (int j = 0; j < KPT; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + i0 + j);
+        kv[j] = v.x;
+        kv[j + 1] = v.y;
+        kv[j + 2] = v.z;
+        kv[j + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) kv[j] = keys[i0 + j];
+    }
+  }
+  const int nv = max(0, min(KPT, n - i0));  // valid keys of this thread: kv[0 .. nv)
+  uint4* h4 = reinterpret_cast<uint4*>(ts.hist);
+  for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) ts.ncand = 0;
+
+  // 1. the key range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j)
+    if (j < nv) {
+      lo = min(lo, kv[j]);
+      hi = max(hi, kv[j]);
+    }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+  if (lane == 0) {
+    ts.wlo[warp] = lo;
+    ts.whi[warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, ts.wlo[w]);
+    hi = max(hi, ts.whi[w]);
+  }
+
+  // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
+  int need = k, nin = n;
+  bool cleared = true;
+  while (nin > kTkCand && lo != hi) {
+    if (!cleared) {
+      for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+    }
+    cleared = false;
+    const uint32_t range = hi - lo;
+    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
+    int run_bin = -1, run = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const uint32_t u = kv[j];
+      const int bin = (j < nv && u >= lo && u <= hi) ? (int)((u - lo) >> shift) : -1;
+      if (bin != run_bin) {
+        if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
+        run_bin = bin;
+        run = 0;
+      }
+      ++run;
+    }
+    if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
+    __syncthreads();
+    uint32_t c[BPT];
+#pragma unroll
+    for (int j = 0; j < BPT; j += 4) {
+      const uint4 v = h4[(tid * BPT + j) >> 2];
+      c[j] = v.x;
+      c[j + 1] = v.y;
+      c[j + 2] = v.z;
+      c[j + 3] = v.w;
+    }
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) sum += (int)c[j];
+    int incl = sum;  // over the lanes >= this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(FULL, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) ts.wa[warp] = incl;
+    __syncthreads();
+    int above = incl - sum;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      if (w > warp) above += ts.wa[w];
+    if (above < need && above + sum >= need) {
+      int acc = above;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (acc + (int)c[j] >= need) {
+          ts.bstar = tid * BPT + j;
+          ts.need = need - acc;
+          ts.nb = (int)c[j];
+          break;
+        }
+        acc += (int)c[j];
+      }
+    }
+    __syncthreads();
+    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
+    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
+    lo = nlo;
+    need = ts.need;
+    nin = ts.nb;
+  }
+
+  // 3. the boundary pair (T, t): candidates gathered by one atomic per thread that has
+  // any, ranked by warp 0 (lane l holds candidate l) with shuffles
+  const bool by_index = nin > kTkCand;  // then lo == hi
+  if (!by_index) {
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) cnt += j < nv && kv[j] >= lo && kv[j] <= hi;
+    if (cnt > 0) {
+      int slot = atomicAdd(&ts.ncand, cnt);
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (j < nv && kv[j] >= lo && kv[j] <= hi) {
+          if (slot < kTkCand) {
+            ts.cand[slot] = i0 + j;
+            ts.ckey[slot] = kv[j];
+          }
+          ++slot;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nc = min(ts.ncand, kTkCand);
+      const int ci = lane < nc ? ts.cand[lane] : 0;
+      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
+      int r = 0;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const uint32_t a = __shfl_sync(FULL, cu, m);
+        const int cm = __shfl_sync(FULL, ci, m);
+        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
+      }
+      if (lane < nc && r == need - 1) {
+        ts.tkey = cu;
+        ts.tidx = ci;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t T = by_index ? lo : ts.tkey;
+  const int tI = by_index ? 0 : ts.tidx;
+
+  // 4. ascending compaction: 0 not taken, 1 taken, 2 a boundary key taken by index
+  int pk[KPT];
+  int c1 = 0, c2 = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t u = kv[j];
+    int t = 0;
+    if (j < nv) {
+      if (u > hi) t = 1;
+      else if (u >= lo) t = by_index ? 2 : ((u > T || (u == T && i0 + j <= tI)) ? 1 : 0);
+    }
+    pk[j] = t;
+    c1 += t == 1;
+    c2 += t == 2;
+  }
+  int x1 = c1, x2 = c2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y1 = __shfl_up_sync(FULL, x1, o), y2 = __shfl_up_sync(FULL, x2, o);
+    if (lane >= o) {
+      x1 += y1;
+      x2 += y2;
+    }
+  }
+  if (lane == 31) {
+    ts.wa[warp] = x1;
+    ts.wb[warp] = x2;
+  }
+  __syncthreads();
+  int base = x1 - c1, bseen = x2 - c2;
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    if (w < warp) {
+      base += ts.wa[w];
+      bseen += ts.wb[w];
+    }
+  int o = base + min(need, bseen);
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int t = pk[j];
+    if (t == 1 || (t == 2 && bseen < need)) {
+      if (o < k) out[o] = i0 + j;
+      ++o;
+    }
+    bseen += t == 2;
+  }
+  __syncthreads();  // the scratch may be reused right after
+}
+
+// topk_regs with the smallest keys-per-thread count that covers n (n <= 32 NT).
+template <int NT>
+__device__ void topk_regs_any(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
+  if (n <= NT) topk_regs<NT, 1>(keys, n, k, ts, out);
+  else if (n <= 2 * NT) topk_regs<NT, 2>(keys, n, k, ts, out);
+  else if (n <= 4 * NT) topk_regs<NT, 4>(keys, n, k, ts, out);
+  else if (n <= 8 * NT) topk_regs<NT, 8>(keys, n, k, ts, out);
+  else if (n <= 16 * NT) topk_regs<NT, 16>(keys, n, k, ts, out);
+  else topk_regs<NT, 32>(keys, n, k, ts, out);
 }
 
 }  // namespace rkv

@@ -42,6 +42,7 @@ constexpr int kPoolTile = 2048;
 constexpr int kPoolThreads = 256;
 constexpr int kMaxPool = 255;
 constexpr int kSelectThreads = 1024;
+constexpr int kSelectStagedMax = 48 * 1024;  // prefix tokens whose keys the select stages (192 KB)
 
 struct SnapParams {
   CUtensorMap tmk;        // k as [B*Hkv*Lmax rows][128] bf16, 128-row x 64-channel boxes, 128-B swizzle
@@ -302,10 +303,15 @@ __global__ void __launch_bounds__(kPoolThreads) snap_pool_kernel(const __grid_co
   }
 }
 
-// Top keep1-w pooled prefix positions + the window.  grid B*Hkv, 1024 threads.
+// Top keep1-w pooled prefix positions (value desc, position asc) + the window,
+// ascending.  grid B*Hkv, 1024 threads.  kStaged: the unit's pooled scores are first
+// copied into dynamic shared memory as order-preserving keys (prompts up to
+// kSelectStagedMax prefix tokens); otherwise every pass of the select reads them from
+// global memory (L2).
+template <bool kStaged>
 __global__ void __launch_bounds__(kSelectThreads) snap_select_kernel(const __grid_constant__ SnapParams p) {
-  __shared__ uint32_t hist[258];
-  __shared__ int scan_scratch[kSelectThreads / 32 + 1];
+  extern __shared__ uint32_t skeys[];
+  __shared__ TopkSmem<kSelectThreads> ts;
   const int unit = blockIdx.x, b = unit / p.Hkv, tid = threadIdx.x;
   const int Lp = p.L[b] - p.w;
   const int k = p.keep1[b] - p.w;
@@ -317,37 +323,26 @@ __global__ void __launch_bounds__(kSelectThreads) snap_select_kernel(const __gri
   }
   if (k <= 0) return;
   const float* pooled = p.pooled + (size_t)unit * p.Lmax;
-  uint32_t T;
-  int need;
-  block_radix_threshold<kSelectThreads>(Lp, k, [&](int i) { return float_key(pooled[i]); }, hist, &T, &need);
-
-  const int seg = (Lp + kSelectThreads - 1) / kSelectThreads;
-  const int s0 = min(Lp, tid * seg), s1 = min(Lp, s0 + seg);
-  int ceq = 0;
-  for (int i = s0; i < s1; ++i) ceq += float_key(pooled[i]) == T;
-  int total;
-  const int eq_base = block_exclusive_scan<kSelectThreads>(ceq, scan_scratch, &total);
-  int csel = 0;
-  for (int i = s0, er = eq_base; i < s1; ++i) {
-    const uint32_t u = float_key(pooled[i]);
-    if (u > T) ++csel;
-    else if (u == T) { csel += er < need; ++er; }
-  }
-  const int out_base = block_exclusive_scan<kSelectThreads>(csel, scan_scratch, &total);
-  for (int i = s0, er = eq_base, o = out_base; i < s1; ++i) {
-    const uint32_t u = float_key(pooled[i]);
-    bool take = u > T;
-    if (u == T) { take = er < need; ++er; }
-    if (take && o < k) out[o++] = i;
+  if (kStaged) {
+    for (int i = tid; i < Lp; i += kSelectThreads) skeys[i] = float_key(pooled[i]);
+    __syncthreads();
+    topk_adaptive<kSelectThreads>(Lp, k, [&](int i) { return skeys[i]; }, ts, out, nullptr);
+  } else {
+    topk_adaptive<kSelectThreads>(Lp, k, [&](int i) { return float_key(pooled[i]); }, ts, out, nullptr);
   }
 }
 
 // Survivors' K/V into the cache pages and their summaries.
-// grid (ceil(max keep1 / P), Hkv, B), 128 threads: channel pair = tid % 64, the two
-// halves of the block take alternate tokens of the page.
+// grid (ceil(max keep1 / P), Hkv, B), 128 threads, one page each (P = 8 kRows).  Thread t moves the
+// 16-byte piece t % 16 (channels 8 (t % 16) .. +7) of rows t / 16, t / 16 + 8, ... of
+// the page (K and V): the row indices are loaded first, then every piece, then the
+// stores.  Page summaries: per-thread max / min over its rows, combined across the
+// row groups by a shuffle and a 4-warp shared-memory pass.
+template <int kRows>  // rows per thread: page size / 8
 __global__ void __launch_bounds__(128) snap_compact_kernel(const __grid_constant__ SnapParams p) {
-  __shared__ float red[4][64];
+  __shared__ float red[2][4][128];
   const int b = blockIdx.z, g = blockIdx.y, pg = blockIdx.x, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int unit = b * p.Hkv + g;
   const int n = p.keep1[b];
   if (pg == 0 && g == 0 && tid == 0) p.seq_len[b] = n;
@@ -357,49 +352,71 @@ __global__ void __launch_bounds__(128) snap_compact_kernel(const __grid_constant
     if (tid == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
     return;
   }
-  const int c2 = tid & 63, half = tid >> 6;
-  const int32_t* kept = p.kept + (size_t)unit * p.kept_stride;
-  const size_t src_base = ((size_t)b * p.Hkv + g) * p.Lmax * 128 + 2 * c2;
-  const size_t dst_base = (((size_t)phys * p.Hkv + g) * p.P) * 128 + 2 * c2;
-  float mx0 = -INFINITY, mx1 = -INFINITY, mn0 = INFINITY, mn1 = INFINITY;
-  const int end = min(n, (pg + 1) * p.P);
+  const int piece = tid & 15, rg = tid >> 4;
+  const int cnt = min(p.P, n - pg * p.P);
   const int L = p.L[b];
-  for (int i = pg * p.P + half; i < end; i += 2) {
-    const int t = kept[i];
-    if (t < 0 || t >= L) {   // never expected: the select kernel writes every position
+  const int32_t* kept = p.kept + (size_t)unit * p.kept_stride + pg * p.P;
+  const size_t src0 = ((size_t)b * p.Hkv + g) * p.Lmax * 128 + piece * 8;
+  const size_t dst0 = (((size_t)phys * p.Hkv + g) * p.P) * 128 + piece * 8;
+  int t[kRows];
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const int r = rg + 8 * j;
+    t[j] = r < cnt ? kept[r] : -1;
+  }
+  uint4 kv[kRows], vv[kRows];
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const bool ok = t[j] >= 0 && t[j] < L;
+    kv[j] = ok ? *reinterpret_cast<const uint4*>(p.k + src0 + (size_t)t[j] * 128) : make_uint4(0, 0, 0, 0);
+    vv[j] = ok ? *reinterpret_cast<const uint4*>(p.v + src0 + (size_t)t[j] * 128) : make_uint4(0, 0, 0, 0);
+  }
+  float mx[8], mn[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mx[e] = -INFINITY;
+    mn[e] = INFINITY;
+  }
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const int r = rg + 8 * j;
+    if (r >= cnt) continue;
+    if (t[j] < 0 || t[j] >= L) {  // never expected: the select writes every position
       flag_error(p.err, RKV_DEVERR_CAPACITY);
       continue;
     }
-    const size_t src = src_base + (size_t)t * 128;
-    const uint32_t ku = *reinterpret_cast<const uint32_t*>(p.k + src);
-    const uint32_t vu = *reinterpret_cast<const uint32_t*>(p.v + src);
-    const size_t dst = dst_base + (size_t)(i - pg * p.P) * 128;
-    *reinterpret_cast<uint32_t*>(p.k_pages + dst) = ku;
-    *reinterpret_cast<uint32_t*>(p.v_pages + dst) = vu;
-    const float x0 = bf16_lo(ku), x1 = bf16_hi(ku);
-    mx0 = fmaxf(mx0, x0);
-    mx1 = fmaxf(mx1, x1);
-    mn0 = fminf(mn0, x0);
-    mn1 = fminf(mn1, x1);
+    *reinterpret_cast<uint4*>(p.k_pages + dst0 + (size_t)r * 128) = kv[j];
+    *reinterpret_cast<uint4*>(p.v_pages + dst0 + (size_t)r * 128) = vv[j];
+    const uint32_t w4[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+      mx[2 * e] = fmaxf(mx[2 * e], x0);
+      mx[2 * e + 1] = fmaxf(mx[2 * e + 1], x1);
+      mn[2 * e] = fminf(mn[2 * e], x0);
+      mn[2 * e + 1] = fminf(mn[2 * e + 1], x1);
+    }
   }
-  if (half == 1) {
-    red[0][c2] = mx0;
-    red[1][c2] = mx1;
-    red[2][c2] = mn0;
-    red[3][c2] = mn1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {  // lanes l and l ^ 16 hold the same piece
+    mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+    mn[e] = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], 16));
+  }
+  if (lane < 16) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red[0][warp][piece * 8 + e] = mx[e];
+      red[1][warp][piece * 8 + e] = mn[e];
+    }
   }
   __syncthreads();
-  if (half == 0) {
-    mx0 = fmaxf(mx0, red[0][c2]);
-    mx1 = fmaxf(mx1, red[1][c2]);
-    mn0 = fminf(mn0, red[2][c2]);
-    mn1 = fminf(mn1, red[3][c2]);
-    const size_t row = ((size_t)unit * 128 + 2 * c2) * p.max_pages + pg;
-    p.kmax[row] = (rkv_bf16)(__float_as_uint(mx0) >> 16);
-    p.kmax[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mx1) >> 16);
-    p.kmin[row] = (rkv_bf16)(__float_as_uint(mn0) >> 16);
-    p.kmin[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mn1) >> 16);
-  }
+  const int c = tid;
+  const float M = fmaxf(fmaxf(red[0][0][c], red[0][1][c]), fmaxf(red[0][2][c], red[0][3][c]));
+  const float m = fminf(fminf(red[1][0][c], red[1][1][c]), fminf(red[1][2][c], red[1][3][c]));
+  const size_t row = ((size_t)unit * 128 + c) * p.max_pages + pg;
+  // the values came from bf16 bit patterns, so the top 16 bits are exact
+  p.kmax[row] = (rkv_bf16)(__float_as_uint(M) >> 16);
+  p.kmin[row] = (rkv_bf16)(__float_as_uint(m) >> 16);
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -484,11 +501,28 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   launch_begin(K_SNAP_POOL, s);
   snap_pool_kernel<<<dim3((Lmax_seen + kPoolTile - 1) / kPoolTile, (unsigned)units), kPoolThreads, 0, s>>>(p);
   launch_end(K_SNAP_POOL, s);
+  int Lp_max = 0;
+  for (int b = 0; b < a.B; ++b) Lp_max = a.prompt_len[b] - a.w > Lp_max ? a.prompt_len[b] - a.w : Lp_max;
+  static bool sel_attr = false;
+  if (!sel_attr) {
+    cudaFuncSetAttribute(snap_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kSelectStagedMax * 4);
+    sel_attr = true;
+  }
   launch_begin(K_SNAP_SELECT, s);
-  snap_select_kernel<<<(unsigned)units, kSelectThreads, 0, s>>>(p);
+  if (Lp_max <= kSelectStagedMax)
+    snap_select_kernel<true><<<(unsigned)units, kSelectThreads, (size_t)(Lp_max > 0 ? Lp_max : 1) * 4, s>>>(p);
+  else
+    snap_select_kernel<false><<<(unsigned)units, kSelectThreads, 0, s>>>(p);
   launch_end(K_SNAP_SELECT, s);
   launch_begin(K_SNAP_COMPACT, s);
-  snap_compact_kernel<<<dim3((keep_max + p.P - 1) / p.P, a.Hkv, a.B), 128, 0, s>>>(p);
+  const dim3 cgrid((keep_max + p.P - 1) / p.P, a.Hkv, a.B);
+  if (p.P == 16)
+    snap_compact_kernel<2><<<cgrid, 128, 0, s>>>(p);
+  else if (p.P == 32)
+    snap_compact_kernel<4><<<cgrid, 128, 0, s>>>(p);
+  else
+    snap_compact_kernel<8><<<cgrid, 128, 0, s>>>(p);
   launch_end(K_SNAP_COMPACT, s);
   return cudaGetLastError();
 }
