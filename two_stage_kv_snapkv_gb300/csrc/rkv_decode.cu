@@ -27,6 +27,7 @@
 // rows; fp32 online softmax; P split into bf16 hi + lo so the P.V product keeps
 // ~16 bits of the probabilities.
 #include <climits>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 #include <cuda.h>
@@ -483,7 +484,7 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ChanSmem cs;
   __shared__ AttnSmem<STAGES> as;
-  __shared__ uint64_t pbar;
+  __shared__ uint64_t sbar, pbar;
   __shared__ __align__(16) uint8_t new_kv[512];
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -498,7 +499,9 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   int32_t* ptab = sel + p.max_pages;
   float* inbox = reinterpret_cast<float*>(ptab + p.max_pages);
   const int hpc = (G + C - 1) / C;  // heads finished per CTA
-  float(*qf)[128] = reinterpret_cast<float(*)[128]>(ring);  // until the summaries are staged
+  // the query as floats, in the inbox (idle until the partial states arrive), so the
+  // whole region is free for the summaries from the start
+  float(*qf)[128] = reinterpret_cast<float(*)[128]>(inbox);
 
   // every CTA of the cluster must be running before anyone stores into its shared
   // memory: arrive now, wait just before the first remote store
@@ -523,12 +526,27 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   }
   const int n = n0 + (do_append ? 1 : 0);
   const int NP = (n + P - 1) / P;
-  // this CTA's slice [p0, p1) of the pages (8-page aligned)
+  // this CTA's slice [p0, p1) of the pages (8-page aligned).  When the summaries of
+  // all 128 channels over the slice fit in the region, they are staged right away
+  // (cp.async, 16-byte chunks), while the query arrives and the channels are chosen;
+  // otherwise only the chosen channels' rows are staged, after the select.
   const int per = ((NP + C - 1) / C + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
+  const int slice8 = (p1 - p0 + 7) & ~7;
+  const bool all_ch = p1 > p0 && 2 * 128 * slice8 * 2 <= p.region_bytes;
+  if (all_ch) {
+    const int cpr = slice8 >> 3;
+    for (int e = tid; e < 256 * cpr; e += kThreads) {
+      const int i = e / cpr, c = e - i * cpr;
+      cp_async16(ring + (size_t)i * slice8 * 2 + c * 16,
+                 (i < 128 ? p.kmax : p.kmin) + ((size_t)unit * 128 + (i & 127)) * p.max_pages + p0 + c * 8, 16u);
+    }
+    cp_async_commit();
+  }
 
   // 2. barriers; prefetch of the sequence's page-table row (needed after the select)
   if (tid == 0) {
+    mbar_init(&sbar, 1);
     mbar_init(&pbar, 1);
     fence_mbar_init();
   }
@@ -553,12 +571,18 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
 
   // 4. append (rank 0): the token goes into its slot and its page's Kmax/Kmin are
   // folded.  Within this step every CTA takes the token from new_kv, so nothing waits
-  // for these writes: the loads are issued here, the stores after the scoring.
+  // for these writes.  Their loads are issued after the first summary tile has landed
+  // (a barrier waits for a thread's outstanding loads, and the Kmax/Kmin loads need
+  // the length first: issued here they would hold up the channel select), the stores
+  // after the scoring.
   const bool appender = do_append && rank == 0 && tid < 64;
   uint32_t app_k = 0, app_v = 0, app_mx = 0, app_mn = 0;
   int app_phys = -1;
   size_t app_row = 0;
-  if (appender) {
+  bool app_loaded = false;
+  auto append_loads = [&]() {
+    if (!appender || app_loaded) return;
+    app_loaded = true;
     const int page = n0 / P;
     const size_t src = ((size_t)b * p.Hkv + g) * 128 + 2 * tid;
     app_row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + page;
@@ -567,51 +591,59 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     app_v = *reinterpret_cast<const uint32_t*>(p.v_new + src);
     app_mx = (uint32_t)p.kmax[app_row] | ((uint32_t)p.kmax[app_row + p.max_pages] << 16);
     app_mn = (uint32_t)p.kmin[app_row] | ((uint32_t)p.kmin[app_row + p.max_pages] << 16);
-  }
+  };
 
   // 5. channels (every CTA)
   const int k1 = p.k1[b];
   select_channels(qf, cs, G, k1);
 
-  // 6. page bounds of this CTA's slice [p0, p1) (8-page aligned).  The k1 Kmax and
-  // k1 Kmin row pieces of a tile (the region holds the whole slice whenever it fits)
-  // are copied at once by every thread in 16-byte cp.async chunks (one round trip);
-  // the appended token is folded into its
+  // 6. page bounds of this CTA's slice [p0, p1).  Staged rows: all 128 channels' Kmax
+  // then Kmin (rows ch and 128 + ch), or the k1 chosen channels' (rows kk and k1 + kk,
+  // copied per tile now, the region holding the whole slice whenever it fits).  The
+  // appended token is folded into its
   // page's staged summary (a fold that the append may already have done changes
   // nothing: max and min are idempotent); then every thread bounds pages from shared
   // memory, and the scores go to every CTA's key array.
-  const int tcap = (p.region_bytes / (4 * k1)) & ~7;
+  const int lo_row0 = all_ch ? 128 : k1;  // Kmin row of chosen channel kk: lo_row0 + hi row
+  const int tcap = all_ch ? slice8 : (p.region_bytes / (4 * k1)) & ~7;
   rkv_bf16* stg = reinterpret_cast<rkv_bf16*>(ring);
   const int pnew = do_append ? n0 / P : -1;
   bool waited = false;
+  int stile = 0;  // bulk-staged tiles so far (phase of sbar)
   for (int t0 = p0; t0 < p1; t0 += tcap) {
     const int cnt = min(tcap, p1 - t0);
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
-    __syncthreads();  // the previous tile (or the query) is consumed
-    {
-      // consecutive threads take consecutive 16-byte chunks (8 pages) of the rows
-      const int cpr = cnt8 >> 3;
-      for (int e = tid; e < 2 * k1 * cpr; e += kThreads) {
-        const int i = e / cpr, c = e - i * cpr;
+    __syncthreads();  // the previous tile is consumed
+    if (all_ch) {
+      cp_async_wait<0>();
+    } else {
+      // one bulk copy per row (the rows are long here: the slice did not fit whole)
+      fence_proxy_async_smem();
+      if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
+      __syncthreads();
+      for (int i = tid; i < 2 * k1; i += kThreads) {
         const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
         const int ch = cs.chan[i < k1 ? i : i - k1];
-        cp_async16(ring + (size_t)i * cnt8 * 2 + c * 16, base + ((size_t)unit * 128 + ch) * p.max_pages + t0 + c * 8,
-                   16u);
+        bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0, (uint32_t)cnt8 * 2,
+                 &sbar);
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncthreads();
+      if (!mbar_wait(&sbar, (uint32_t)(stile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
+      ++stile;
     }
+    __syncthreads();
+    append_loads();
     if (pnew >= t0 && pnew < t0 + cnt) {
       const int j = pnew - t0;
       const bool first = (n0 % P) == 0;
       const rkv_bf16* kn = reinterpret_cast<const rkv_bf16*>(new_kv);
-      for (int kk = tid; kk < k1; kk += kThreads) {
-        const float x = bf16_f(kn[cs.chan[kk]]);
-        const float hi = first ? x : fmaxf(bf16_f(stg[kk * cnt8 + j]), x);
-        const float lo = first ? x : fminf(bf16_f(stg[(k1 + kk) * cnt8 + j]), x);
-        stg[kk * cnt8 + j] = (rkv_bf16)(__float_as_uint(hi) >> 16);
-        stg[(k1 + kk) * cnt8 + j] = (rkv_bf16)(__float_as_uint(lo) >> 16);
+      const int nrows = all_ch ? 128 : k1;
+      for (int r = tid; r < nrows; r += kThreads) {
+        const float x = bf16_f(kn[all_ch ? r : cs.chan[r]]);
+        const int rh = r, rl = all_ch ? 128 + r : k1 + r;
+        const float hi = first ? x : fmaxf(bf16_f(stg[rh * cnt8 + j]), x);
+        const float lo = first ? x : fminf(bf16_f(stg[rl * cnt8 + j]), x);
+        stg[rh * cnt8 + j] = (rkv_bf16)(__float_as_uint(hi) >> 16);
+        stg[rl * cnt8 + j] = (rkv_bf16)(__float_as_uint(lo) >> 16);
       }
       __syncthreads();
     }
@@ -619,29 +651,40 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
       cluster_wait();
       waited = true;
     }
-    for (int j = tid; j < cnt; j += kThreads) {
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // independent chains
-      int kk = 0;
-      for (; kk + 1 < k1; kk += 2) {
-        s0 = fmaf(cs.qpos[kk], bf16_f(stg[kk * cnt8 + j]), s0);
-        s1 = fmaf(cs.qneg[kk], bf16_f(stg[(k1 + kk) * cnt8 + j]), s1);
-        s2 = fmaf(cs.qpos[kk + 1], bf16_f(stg[(kk + 1) * cnt8 + j]), s2);
-        s3 = fmaf(cs.qneg[kk + 1], bf16_f(stg[(k1 + kk + 1) * cnt8 + j]), s3);
+    // row of chosen channel kk's Kmax: chan[kk] (all channels staged) or kk; its Kmin
+    // row is lo_row0 further
+    auto score = [&](auto all) {
+      constexpr bool kAll = decltype(all)::value;
+      for (int j = tid; j < cnt; j += kThreads) {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // independent chains
+        int kk = 0;
+        for (; kk + 1 < k1; kk += 2) {
+          const int r0 = kAll ? cs.chan[kk] : kk, r1 = kAll ? cs.chan[kk + 1] : kk + 1;
+          s0 = fmaf(cs.qpos[kk], bf16_f(stg[r0 * cnt8 + j]), s0);
+          s1 = fmaf(cs.qneg[kk], bf16_f(stg[(lo_row0 + r0) * cnt8 + j]), s1);
+          s2 = fmaf(cs.qpos[kk + 1], bf16_f(stg[r1 * cnt8 + j]), s2);
+          s3 = fmaf(cs.qneg[kk + 1], bf16_f(stg[(lo_row0 + r1) * cnt8 + j]), s3);
+        }
+        if (kk < k1) {
+          const int r0 = kAll ? cs.chan[kk] : kk;
+          s0 = fmaf(cs.qpos[kk], bf16_f(stg[r0 * cnt8 + j]), s0);
+          s1 = fmaf(cs.qneg[kk], bf16_f(stg[(lo_row0 + r0) * cnt8 + j]), s1);
+        }
+        const uint32_t key = float_key((s0 + s2) + (s1 + s3));
+        for (int r = 0; r < C; ++r) cluster.map_shared_rank(keys, r)[t0 + j] = key;
       }
-      if (kk < k1) {
-        s0 = fmaf(cs.qpos[kk], bf16_f(stg[kk * cnt8 + j]), s0);
-        s1 = fmaf(cs.qneg[kk], bf16_f(stg[(k1 + kk) * cnt8 + j]), s1);
-      }
-      const uint32_t key = float_key((s0 + s2) + (s1 + s3));
-      for (int r = 0; r < C; ++r) cluster.map_shared_rank(keys, r)[t0 + j] = key;
-    }
+    };
+    if (all_ch)
+      score(std::true_type{});
+    else
+      score(std::false_type{});
   }
   if (!waited) cluster_wait();
   fence_proxy_async_smem();  // generic accesses to the region before the attention's TMA loads
   cluster.sync();            // every CTA holds every page's key
 
-  // the append's stores: their loads completed long ago, and nothing in this step
-  // waits for them
+  // the append's stores: nothing in this step waits for them
+  append_loads();  // (only if this CTA staged no tile)
   if (appender) {
     if (app_phys >= 0 && app_phys < p.num_phys) {
       const int slot = n0 % P;

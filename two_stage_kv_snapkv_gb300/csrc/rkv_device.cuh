@@ -346,8 +346,9 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
   }
 
   // 3. the boundary pair (T, t) among at most kTkCand candidates
-  const bool by_index = nin > kTkCand;  // then lo == hi
-  if (!by_index) {
+  const bool all_in = need == nin;                // every key in [lo, hi] is taken
+  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
+  if (!by_index && !all_in) {
     for (int i = s0; i < s1; ++i) {
       const uint32_t u = key(i);
       if (u >= lo && u <= hi) {
@@ -377,10 +378,10 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
         ts.tidx = ci;
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
-  const uint32_t T = by_index ? lo : ts.tkey;
-  const int tI = by_index ? 0 : ts.tidx;
+  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
+  const int tI = (by_index || all_in) ? n : ts.tidx;  // all_in: every key >= lo is taken
   // 0: not taken, 1: taken, 2: a boundary key, taken by ascending index
   auto pick = [&](int i) -> int {
     const uint32_t u = key(i);
@@ -560,8 +561,9 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
 
   // 3. the boundary pair (T, t): candidates gathered by one atomic per thread that has
   // any, ranked by warp 0 (lane l holds candidate l) with shuffles
-  const bool by_index = nin > kTkCand;  // then lo == hi
-  if (!by_index) {
+  const bool all_in = need == nin;                // every key in [lo, hi] is taken
+  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
+  if (!by_index && !all_in) {
     int cnt = 0;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) cnt += j < nv && kv[j] >= lo && kv[j] <= hi;
@@ -594,10 +596,10 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
         ts.tidx = ci;
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
-  const uint32_t T = by_index ? lo : ts.tkey;
-  const int tI = by_index ? 0 : ts.tidx;
+  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
+  const int tI = (by_index || all_in) ? n : ts.tidx;  // all_in: every key >= lo is taken
 
   // 4. ascending compaction: 0 not taken, 1 taken, 2 a boundary key taken by index
   int pk[KPT];
