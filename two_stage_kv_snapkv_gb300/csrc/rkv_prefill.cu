@@ -30,8 +30,6 @@ namespace rkv {
 namespace {
 
 constexpr int kTcTile = 128;                      // keys per tile (the MMA's M or N)
-constexpr int kTcTilesPerItem = 16;               // tiles per CTA
-constexpr int kTcItemKeys = kTcTile * kTcTilesPerItem;
 constexpr int kTcStages = 2;                      // K tiles in flight per CTA
 constexpr int kTcThreads = 192;                   // warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int kTcOperandBytes = 128 * 256;        // 128 rows x 128 bf16: two 128 x 64 boxes
@@ -50,6 +48,8 @@ struct SnapParams {
   const rkv_bf16* k;
   const rkv_bf16* v;
   int B, Hq, Hkv, G, w, R, Lmax, nsplit;
+  int item_keys;          // keys per scoring CTA (a multiple of 128)
+  int cgroup;             // pages per compaction CTA (1 .. 8)
   float scale_log2;
   float2* part;           // [units][nsplit][128] (m, l)
   float2* rowstat;        // [units][128] (M, 1/l)
@@ -79,7 +79,7 @@ __device__ __forceinline__ uint32_t tc_swz(int row, int piece) {
 
 // ---------------------------------------------------------------------------
 // Both passes.  grid (nsplit, B*Hkv), 192 threads, dynamic smem kTcSmem; CTA
-// `split` scores keys [split * 2048, ...) of its unit (pass 1: all L keys; pass 2:
+// `split` scores keys [split * item_keys, ...) of its unit (pass 1: all L keys; pass 2:
 // the L - w prefix keys).
 //   warp 4 (one lane): TMA loads of the K tiles into a two-stage ring;
 //   warp 5 (one lane): per tile, eight K=16 MMAs into accumulator (tile % 2) of TMEM;
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv, split = blockIdx.x;
   const int L = p.L[b];
   const int col_end = kStats ? L : L - p.w;  // keys scored by this pass
-  const int t_begin = split * kTcItemKeys;
-  const int t_end = min(col_end, t_begin + kTcItemKeys);
+  const int t_begin = split * p.item_keys;
+  const int t_end = min(col_end, t_begin + p.item_keys);
   const int ntiles = t_end > t_begin ? (t_end - t_begin + kTcTile - 1) / kTcTile : 0;
   if (ntiles == 0) {
     if (kStats && tid < 128) p.part[((size_t)unit * p.nsplit + split) * 128 + tid] = make_float2(-1e30f, 0.f);
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kPoolThreads) snap_pool_kernel(const __grid_co
 // ascending.  grid B*Hkv, 1024 threads.  kStaged: the unit's pooled scores are first
 // copied into dynamic shared memory as order-preserving keys (prompts up to
 // kSelectStagedMax prefix tokens); otherwise every pass of the select reads them from
-// global memory (L2).
+// global memory (L2), lane-interleaved so that each warp load is one coalesced line.
 template <bool kStaged>
 __global__ void __launch_bounds__(kSelectThreads) snap_select_kernel(const __grid_constant__ SnapParams p) {
   extern __shared__ uint32_t skeys[];
@@ -324,99 +324,136 @@ __global__ void __launch_bounds__(kSelectThreads) snap_select_kernel(const __gri
   if (k <= 0) return;
   const float* pooled = p.pooled + (size_t)unit * p.Lmax;
   if (kStaged) {
-    for (int i = tid; i < Lp; i += kSelectThreads) skeys[i] = float_key(pooled[i]);
+    // eight loads in flight per thread, then the stores
+    for (int i0 = tid; i0 < Lp; i0 += 8 * kSelectThreads) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j * kSelectThreads;
+        v[j] = i < Lp ? pooled[i] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = i0 + j * kSelectThreads;
+        if (i < Lp) skeys[i] = float_key(v[j]);
+      }
+    }
     __syncthreads();
     topk_adaptive<kSelectThreads>(Lp, k, [&](int i) { return skeys[i]; }, ts, out, nullptr);
   } else {
-    topk_adaptive<kSelectThreads>(Lp, k, [&](int i) { return float_key(pooled[i]); }, ts, out, nullptr);
+    topk_strided<kSelectThreads>(Lp, k, [&](int i) { return float_key(pooled[i]); }, ts, out);
   }
 }
 
 // Survivors' K/V into the cache pages and their summaries.
-// grid (ceil(max keep1 / P), Hkv, B), 128 threads, one page each (P = 8 kRows).  Thread t moves the
-// 16-byte piece t % 16 (channels 8 (t % 16) .. +7) of rows t / 16, t / 16 + 8, ... of
-// the page (K and V): the row indices are loaded first, then every piece, then the
-// stores.  Page summaries: per-thread max / min over its rows, combined across the
-// row groups by a shuffle and a 4-warp shared-memory pass.
+// grid (ceil(max keep1 / (cgroup P)), Hkv, B), 128 threads; a CTA fills a group of
+// cgroup <= 8 consecutive pages of one (sequence, KV head), P = 8 kRows.  The group's kept
+// positions are read into shared memory first.  Per page, thread t moves the 16-byte
+// piece t % 16 (channels 8 (t % 16) .. +7) of rows t / 16, t / 16 + 8, ... (K and V)
+// and keeps their max / min, which a shuffle and a 4-warp shared-memory pass combine
+// into the page's summary column of a [channel][8 pages] tile; with groups of 8, each
+// channel's 8 pages then go out as one 16-byte store (the summaries are channel-major).
 template <int kRows>  // rows per thread: page size / 8
 __global__ void __launch_bounds__(128) snap_compact_kernel(const __grid_constant__ SnapParams p) {
+  constexpr int P = 8 * kRows;
   __shared__ float red[2][4][128];
-  const int b = blockIdx.z, g = blockIdx.y, pg = blockIdx.x, tid = threadIdx.x;
+  __shared__ int32_t idx[8 * P];
+  __shared__ __align__(16) uint16_t tile[2][128][8];
+  const int b = blockIdx.z, g = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int unit = b * p.Hkv + g;
   const int n = p.keep1[b];
-  if (pg == 0 && g == 0 && tid == 0) p.seq_len[b] = n;
-  if (pg * p.P >= n) return;
-  const int phys = p.page_table[(size_t)b * p.max_pages + pg];
-  if (phys < 0 || phys >= p.num_phys) {
-    if (tid == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
-    return;
-  }
+  const int pg0 = blockIdx.x * p.cgroup;
+  if (blockIdx.x == 0 && g == 0 && tid == 0) p.seq_len[b] = n;
+  if (pg0 * P >= n) return;
+  const int npg = min(p.cgroup, (n + P - 1) / P - pg0);
+  const int r_end = min(p.cgroup * P, n - pg0 * P);  // kept rows of this group
+  const int32_t* kept = p.kept + (size_t)unit * p.kept_stride + (size_t)pg0 * P;
+  for (int r = tid; r < r_end; r += 128) idx[r] = kept[r];
+  __syncthreads();
   const int piece = tid & 15, rg = tid >> 4;
-  const int cnt = min(p.P, n - pg * p.P);
   const int L = p.L[b];
-  const int32_t* kept = p.kept + (size_t)unit * p.kept_stride + pg * p.P;
   const size_t src0 = ((size_t)b * p.Hkv + g) * p.Lmax * 128 + piece * 8;
-  const size_t dst0 = (((size_t)phys * p.Hkv + g) * p.P) * 128 + piece * 8;
-  int t[kRows];
+  for (int q = 0; q < npg; ++q) {
+    const int pg = pg0 + q;
+    const int phys = p.page_table[(size_t)b * p.max_pages + pg];
+    const bool page_ok = phys >= 0 && phys < p.num_phys;
+    if (!page_ok && tid == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
+    const int cnt = min(P, n - pg * P);
+    const size_t dst0 = (((size_t)(page_ok ? phys : 0) * p.Hkv + g) * P) * 128 + piece * 8;
+    int t[kRows];
+    uint4 kv[kRows], vv[kRows];
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) {
-    const int r = rg + 8 * j;
-    t[j] = r < cnt ? kept[r] : -1;
-  }
-  uint4 kv[kRows], vv[kRows];
-#pragma unroll
-  for (int j = 0; j < kRows; ++j) {
-    const bool ok = t[j] >= 0 && t[j] < L;
-    kv[j] = ok ? *reinterpret_cast<const uint4*>(p.k + src0 + (size_t)t[j] * 128) : make_uint4(0, 0, 0, 0);
-    vv[j] = ok ? *reinterpret_cast<const uint4*>(p.v + src0 + (size_t)t[j] * 128) : make_uint4(0, 0, 0, 0);
-  }
-  float mx[8], mn[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    mx[e] = -INFINITY;
-    mn[e] = INFINITY;
-  }
-#pragma unroll
-  for (int j = 0; j < kRows; ++j) {
-    const int r = rg + 8 * j;
-    if (r >= cnt) continue;
-    if (t[j] < 0 || t[j] >= L) {  // never expected: the select writes every position
-      flag_error(p.err, RKV_DEVERR_CAPACITY);
-      continue;
+    for (int j = 0; j < kRows; ++j) {
+      const int r = rg + 8 * j;
+      t[j] = r < cnt ? idx[q * P + r] : -1;
+      const bool ok = t[j] >= 0 && t[j] < L;
+      kv[j] = ok ? *reinterpret_cast<const uint4*>(p.k + src0 + (size_t)t[j] * 128) : make_uint4(0, 0, 0, 0);
+      vv[j] = ok ? *reinterpret_cast<const uint4*>(p.v + src0 + (size_t)t[j] * 128) : make_uint4(0, 0, 0, 0);
     }
-    *reinterpret_cast<uint4*>(p.k_pages + dst0 + (size_t)r * 128) = kv[j];
-    *reinterpret_cast<uint4*>(p.v_pages + dst0 + (size_t)r * 128) = vv[j];
-    const uint32_t w4[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
-      mx[2 * e] = fmaxf(mx[2 * e], x0);
-      mx[2 * e + 1] = fmaxf(mx[2 * e + 1], x1);
-      mn[2 * e] = fminf(mn[2 * e], x0);
-      mn[2 * e + 1] = fminf(mn[2 * e + 1], x1);
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {  // lanes l and l ^ 16 hold the same piece
-    mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
-    mn[e] = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], 16));
-  }
-  if (lane < 16) {
+    float mx[8], mn[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      red[0][warp][piece * 8 + e] = mx[e];
-      red[1][warp][piece * 8 + e] = mn[e];
+      mx[e] = -INFINITY;
+      mn[e] = INFINITY;
+    }
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      const int r = rg + 8 * j;
+      if (r >= cnt) continue;
+      if (t[j] < 0 || t[j] >= L) {  // never expected: the select writes every position
+        flag_error(p.err, RKV_DEVERR_CAPACITY);
+        continue;
+      }
+      if (page_ok) {
+        *reinterpret_cast<uint4*>(p.k_pages + dst0 + (size_t)r * 128) = kv[j];
+        *reinterpret_cast<uint4*>(p.v_pages + dst0 + (size_t)r * 128) = vv[j];
+      }
+      const uint32_t w4[4] = {kv[j].x, kv[j].y, kv[j].z, kv[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+        mx[2 * e] = fmaxf(mx[2 * e], x0);
+        mx[2 * e + 1] = fmaxf(mx[2 * e + 1], x1);
+        mn[2 * e] = fminf(mn[2 * e], x0);
+        mn[2 * e + 1] = fminf(mn[2 * e + 1], x1);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {  // lanes l and l ^ 16 hold the same piece
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+      mn[e] = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], 16));
+    }
+    if (lane < 16) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        red[0][warp][piece * 8 + e] = mx[e];
+        red[1][warp][piece * 8 + e] = mn[e];
+      }
+    }
+    __syncthreads();
+    {
+      const int c = tid;
+      const float M = fmaxf(fmaxf(red[0][0][c], red[0][1][c]), fmaxf(red[0][2][c], red[0][3][c]));
+      const float m = fminf(fminf(red[1][0][c], red[1][1][c]), fminf(red[1][2][c], red[1][3][c]));
+      // the values came from bf16 bit patterns, so the top 16 bits are exact
+      tile[0][c][q] = (uint16_t)(__float_as_uint(M) >> 16);
+      tile[1][c][q] = (uint16_t)(__float_as_uint(m) >> 16);
+    }
+    __syncthreads();  // red is reused by the next page
+  }
+  // channel c's summaries of pages pg0 .. pg0 + npg - 1 (one 16-byte store when whole)
+  const int c = tid;
+  const size_t row = ((size_t)unit * 128 + c) * p.max_pages + pg0;  // 16-byte aligned when cgroup == 8
+  if (npg == 8) {
+    *reinterpret_cast<uint4*>(p.kmax + row) = *reinterpret_cast<const uint4*>(&tile[0][c][0]);
+    *reinterpret_cast<uint4*>(p.kmin + row) = *reinterpret_cast<const uint4*>(&tile[1][c][0]);
+  } else {
+    for (int q = 0; q < npg; ++q) {
+      p.kmax[row + q] = tile[0][c][q];
+      p.kmin[row + q] = tile[1][c][q];
     }
   }
-  __syncthreads();
-  const int c = tid;
-  const float M = fmaxf(fmaxf(red[0][0][c], red[0][1][c]), fmaxf(red[0][2][c], red[0][3][c]));
-  const float m = fminf(fminf(red[1][0][c], red[1][1][c]), fminf(red[1][2][c], red[1][3][c]));
-  const size_t row = ((size_t)unit * 128 + c) * p.max_pages + pg;
-  // the values came from bf16 bit patterns, so the top 16 bits are exact
-  p.kmax[row] = (rkv_bf16)(__float_as_uint(M) >> 16);
-  p.kmin[row] = (rkv_bf16)(__float_as_uint(m) >> 16);
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -472,8 +509,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     Lmax_seen = a.prompt_len[b] > Lmax_seen ? a.prompt_len[b] : Lmax_seen;
     keep_max = a.keep1[b] > keep_max ? a.keep1[b] : keep_max;
   }
-  // one CTA per 2048 keys of a unit
-  p.nsplit = (Lmax_seen + kTcItemKeys - 1) / kTcItemKeys;
+  // keys per scoring CTA: 2048 (measured fastest once the grid covers the GPU), halved
+  // down to 512 while there would be fewer CTAs than SMs
+  p.item_keys = 2048;
+  for (;;) {
+    long items = 0;
+    for (int b = 0; b < a.B; ++b) items += (long)a.Hkv * ((a.prompt_len[b] + p.item_keys - 1) / p.item_keys);
+    if (items >= num_sms() || p.item_keys <= 512) break;
+    p.item_keys /= 2;
+  }
+  p.nsplit = (Lmax_seen + p.item_keys - 1) / p.item_keys;
   if (p.nsplit > kMaxSnapSplit) {
     set_last_error("prompt longer than the scoring kernels' split table (524288 tokens)");
     return cudaErrorInvalidValue;
@@ -516,7 +561,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     snap_select_kernel<false><<<(unsigned)units, kSelectThreads, 0, s>>>(p);
   launch_end(K_SNAP_SELECT, s);
   launch_begin(K_SNAP_COMPACT, s);
-  const dim3 cgrid((keep_max + p.P - 1) / p.P, a.Hkv, a.B);
+  // 8 pages per CTA (whole 16-byte summary stores) while that still fills one wave of
+  // resident CTAs (16 per SM), fewer pages per CTA for small caches
+  p.cgroup = 8;
+  while (p.cgroup > 1 && (long)((keep_max + p.cgroup * p.P - 1) / (p.cgroup * p.P)) * a.Hkv * a.B < 16L * num_sms())
+    p.cgroup /= 2;
+  const dim3 cgrid((keep_max + p.cgroup * p.P - 1) / (p.cgroup * p.P), a.Hkv, a.B);
   if (p.P == 16)
     snap_compact_kernel<2><<<cgrid, 128, 0, s>>>(p);
   else if (p.P == 32)
