@@ -650,212 +650,6 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   __syncthreads();  // the scratch may be reused right after
 }
 
-// The same select for keys read from global memory (L2): every pass walks the keys
-// lane-interleaved, so a warp's loads are one coalesced 128-byte line.  Runs of equal
-// bins along consecutive lanes add to the histogram once; candidates are gathered with
-// one atomic per warp; the compaction gives each warp a contiguous span of indices and
-// orders within it by ballots.  Every thread of the block calls this.
-template <int NT, class KeyFn>
-__device__ void topk_strided(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t* out) {
-  static_assert(NT % 32 == 0 && kTkBins % NT == 0, "bins must split evenly over the threads");
-  constexpr unsigned FULL = 0xffffffffu;
-  constexpr int NW = NT / 32;
-  constexpr int BPT = kTkBins / NT;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned lt = (1u << lane) - 1u;
-
-  // every pass reads KB keys per thread before using any (loads in flight together)
-  constexpr int KB = 8;
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for (int i0 = tid; i0 < n; i0 += KB * NT) {
-    uint32_t u[KB];
-#pragma unroll
-    for (int j = 0; j < KB; ++j) u[j] = i0 + j * NT < n ? key(i0 + j * NT) : 0u;
-#pragma unroll
-    for (int j = 0; j < KB; ++j)
-      if (i0 + j * NT < n) {
-        lo = min(lo, u[j]);
-        hi = max(hi, u[j]);
-      }
-  }
-  lo = __reduce_min_sync(FULL, lo);
-  hi = __reduce_max_sync(FULL, hi);
-  if (lane == 0) {
-    ts.wlo[warp] = lo;
-    ts.whi[warp] = hi;
-  }
-  if (tid == 0) ts.ncand = 0;
-  __syncthreads();
-  for (int w = 0; w < NW; ++w) {
-    lo = min(lo, ts.wlo[w]);
-    hi = max(hi, ts.whi[w]);
-  }
-
-  int need = k, nin = n;
-  while (nin > kTkCand && lo != hi) {
-    const uint32_t range = hi - lo;
-    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
-    for (int i = tid; i < kTkBins; i += NT) ts.hist[i] = 0u;
-    __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += KB * NT) {
-      uint32_t u[KB];
-#pragma unroll
-      for (int j = 0; j < KB; ++j) {
-        const int i = i0 + j * NT + tid;
-        u[j] = i < n ? key(i) : 0u;
-      }
-#pragma unroll
-      for (int j = 0; j < KB; ++j) {
-        const int i = i0 + j * NT + tid;
-        const int bin = (i < n && u[j] >= lo && u[j] <= hi) ? (int)((u[j] - lo) >> shift) : -1;
-        const int prev = __shfl_up_sync(FULL, bin, 1);
-        const bool head = lane == 0 || bin != prev;
-        const unsigned heads = __ballot_sync(FULL, head);
-        if (head && bin >= 0) {
-          const unsigned after = heads & ~((2u << lane) - 1u);
-          const int next = after ? __ffs(after) - 1 : 32;
-          atomicAdd(&ts.hist[bin], (uint32_t)(next - lane));
-        }
-      }
-    }
-    __syncthreads();
-    uint32_t c[BPT];
-    int sum = 0;
-#pragma unroll
-    for (int j = 0; j < BPT; ++j) {
-      c[j] = ts.hist[tid * BPT + j];
-      sum += (int)c[j];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_down_sync(FULL, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    if (lane == 0) ts.wa[warp] = incl;
-    __syncthreads();
-    int above = incl - sum;
-    for (int w = warp + 1; w < NW; ++w) above += ts.wa[w];
-    if (above < need && above + sum >= need) {
-      int acc = above;
-#pragma unroll
-      for (int j = BPT - 1; j >= 0; --j) {
-        if (acc + (int)c[j] >= need) {
-          ts.bstar = tid * BPT + j;
-          ts.need = need - acc;
-          ts.nb = (int)c[j];
-          break;
-        }
-        acc += (int)c[j];
-      }
-    }
-    __syncthreads();
-    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
-    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
-    lo = nlo;
-    need = ts.need;
-    nin = ts.nb;
-  }
-
-  const bool all_in = need == nin;
-  const bool by_index = !all_in && nin > kTkCand;
-  if (!by_index && !all_in) {
-    for (int i0 = 0; i0 < n; i0 += NT) {
-      const int i = i0 + tid;
-      uint32_t u = 0;
-      const bool in = i < n && (u = key(i), u >= lo && u <= hi);
-      const unsigned m = __ballot_sync(FULL, in);
-      int slot0 = 0;
-      if (m && lane == 0) slot0 = atomicAdd(&ts.ncand, __popc(m));
-      slot0 = __shfl_sync(FULL, slot0, 0);
-      if (in) {
-        const int slot = slot0 + __popc(m & lt);
-        if (slot < kTkCand) {
-          ts.cand[slot] = i;
-          ts.ckey[slot] = u;
-        }
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int nc = min(ts.ncand, kTkCand);
-      const int ci = lane < nc ? ts.cand[lane] : 0;
-      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
-      int r = 0;
-#pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const uint32_t a = __shfl_sync(FULL, cu, m);
-        const int cm = __shfl_sync(FULL, ci, m);
-        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
-      }
-      if (lane < nc && r == need - 1) {
-        ts.tkey = cu;
-        ts.tidx = ci;
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
-  const int tI = (by_index || all_in) ? n : ts.tidx;
-  auto pick = [&](int i) -> int {
-    const uint32_t u = key(i);
-    if (u > hi) return 1;
-    if (u < lo) return 0;
-    if (by_index) return 2;
-    return (u > T || (u == T && i <= tI)) ? 1 : 0;
-  };
-
-  const int span = (((n + NW - 1) / NW) + 31) & ~31;
-  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
-  int cnt = 0, bcnt = 0;
-  for (int i0 = w0; i0 < w1; i0 += KB * 32) {
-    int t[KB];
-#pragma unroll
-    for (int j = 0; j < KB; ++j) {
-      const int i = i0 + j * 32 + lane;
-      t[j] = (i0 + j * 32 < w1 && i < w1) ? pick(i) : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < KB; ++j) {
-      cnt += __popc(__ballot_sync(FULL, t[j] == 1));
-      bcnt += __popc(__ballot_sync(FULL, t[j] == 2));
-    }
-  }
-  if (lane == 0) {
-    ts.wa[warp] = cnt;
-    ts.wb[warp] = bcnt;
-  }
-  __syncthreads();
-  int base = 0, bseen = 0;
-  for (int w = 0; w < warp; ++w) {
-    base += ts.wa[w];
-    bseen += ts.wb[w];
-  }
-  int o = base + min(need, bseen);
-  for (int i0 = w0; i0 < w1; i0 += KB * 32) {
-    int t[KB];
-#pragma unroll
-    for (int j = 0; j < KB; ++j) {
-      const int i = i0 + j * 32 + lane;
-      t[j] = (i0 + j * 32 < w1 && i < w1) ? pick(i) : 0;
-    }
-#pragma unroll
-    for (int j = 0; j < KB; ++j) {
-      const int i = i0 + j * 32 + lane;
-      const unsigned m2 = __ballot_sync(FULL, t[j] == 2);
-      const bool take = t[j] == 1 || (t[j] == 2 && bseen + __popc(m2 & lt) < need);
-      const unsigned mt = __ballot_sync(FULL, take);
-      if (take) {
-        const int pos = o + __popc(mt & lt);
-        if (pos < k) out[pos] = i;
-      }
-      o += __popc(mt);
-      bseen += __popc(m2);
-    }
-  }
-  __syncthreads();
-}
-
 // topk_regs with the smallest keys-per-thread count that covers n (n <= 32 NT).
 template <int NT>
 __device__ void topk_regs_any(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {

@@ -23,6 +23,8 @@
 // puts the query rows on the TMEM lanes (one row per epilogue thread: the row's
 // running max and sum stay in that thread); pass 2 swaps the operands so the keys
 // are the lanes (one key per thread: its column sum over the rows is a private loop).
+#include <cooperative_groups.h>
+
 #include "rkv_device.cuh"
 #include "rkv_internal.h"
 
@@ -39,8 +41,9 @@ constexpr int kMaxSnapSplit = 256;
 constexpr int kPoolTile = 2048;
 constexpr int kPoolThreads = 256;
 constexpr int kMaxPool = 255;
-constexpr int kSelectThreads = 1024;
-constexpr int kSelectStagedMax = 48 * 1024;  // prefix tokens whose keys the select stages (192 KB)
+constexpr int kSelectThreads = 512;
+constexpr int kSelectMaxCluster = 8;
+constexpr int kSelectSliceMax = 48 * 1024;  // keys a select CTA stages (192 KB of shared memory)
 
 struct SnapParams {
   CUtensorMap tmk;        // k as [B*Hkv*Lmax rows][128] bf16, 128-row x 64-channel boxes, 128-B swizzle
@@ -304,44 +307,263 @@ __global__ void __launch_bounds__(kPoolThreads) snap_pool_kernel(const __grid_co
 }
 
 // Top keep1-w pooled prefix positions (value desc, position asc) + the window,
-// ascending.  grid B*Hkv, 1024 threads.  kStaged: the unit's pooled scores are first
-// copied into dynamic shared memory as order-preserving keys (prompts up to
-// kSelectStagedMax prefix tokens); otherwise every pass of the select reads them from
-// global memory (L2), lane-interleaved so that each warp load is one coalesced line.
-template <bool kStaged>
+// ascending.  One thread-block cluster of C CTAs per unit: grid (C, B*Hkv), cluster
+// (C, 1, 1), 512 threads.  CTA r stages prefix positions [r per, r per + per) as
+// order-preserving keys in shared memory and the select of topk_adaptive runs over
+// the cluster: the key range, each round's 1024-bin histogram, the boundary
+// candidates and the compaction totals are combined through distributed shared
+// memory (every CTA derives the same boundary), and each CTA writes the selected
+// positions of its own slice at its offset in the ascending list.
+struct SelectSmem {
+  uint32_t hist[kTkBins];  // this CTA's histogram (read by every CTA of the cluster)
+  uint32_t lo, hi;         // this CTA's key range
+  int cnt1, cnt2;          // this CTA's taken / boundary-by-index counts
+  int ncand;               // rank 0: candidates gathered from the cluster
+  int cand[kTkCand];
+  uint32_t ckey[kTkCand];
+  uint32_t T;              // the boundary pair, written into every CTA by rank 0
+  int tI;
+  uint32_t wlo[kSelectThreads / 32], whi[kSelectThreads / 32];
+  int wa[kSelectThreads / 32], wb[kSelectThreads / 32];
+  int bstar, need, nb;
+};
+
 __global__ void __launch_bounds__(kSelectThreads) snap_select_kernel(const __grid_constant__ SnapParams p) {
   extern __shared__ uint32_t skeys[];
-  __shared__ TopkSmem<kSelectThreads> ts;
-  const int unit = blockIdx.x, b = unit / p.Hkv, tid = threadIdx.x;
+  __shared__ SelectSmem ss;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int NT = kSelectThreads, NW = NT / 32, BPT = kTkBins / NT;
+  const int C = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  const int unit = blockIdx.y, b = unit / p.Hkv, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Lp = p.L[b] - p.w;
   const int k = p.keep1[b] - p.w;
   int32_t* out = p.kept + (size_t)unit * p.kept_stride;
-  for (int i = tid; i < p.w; i += kSelectThreads) out[k + i] = Lp + i;
-  if (k >= Lp) {
-    for (int i = tid; i < Lp; i += kSelectThreads) out[i] = i;
+  // the same branch in every CTA of the cluster: no cluster barrier is skipped by some
+  if (k >= Lp || k <= 0) {
+    if (rank == 0)
+      for (int i = tid; i < p.w; i += NT) out[k + i] = Lp + i;
+    if (k >= Lp)
+      for (int i = rank * NT + tid; i < Lp; i += C * NT) out[i] = i;
     return;
   }
-  if (k <= 0) return;
-  const float* pooled = p.pooled + (size_t)unit * p.Lmax;
-  if (kStaged) {
-    // eight loads in flight per thread, then the stores
-    for (int i0 = tid; i0 < Lp; i0 += 8 * kSelectThreads) {
-      float v[8];
+  if (rank == 0)
+    for (int i = tid; i < p.w; i += NT) out[k + i] = Lp + i;
+  const int per = (Lp + C - 1) / C;
+  const int s0 = min(Lp, rank * per), s1 = min(Lp, s0 + per), nl = s1 - s0;
+  const float* pooled = p.pooled + (size_t)unit * p.Lmax + s0;
+  // stage this slice's keys (eight loads in flight per thread) and its range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int i0 = tid; i0 < nl; i0 += 8 * NT) {
+    float v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j * kSelectThreads;
-        v[j] = i < Lp ? pooled[i] : 0.f;
+    for (int j = 0; j < 8; ++j) v[j] = i0 + j * NT < nl ? pooled[i0 + j * NT] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (i0 + j * NT < nl) {
+        const uint32_t u = float_key(v[j]);
+        skeys[i0 + j * NT] = u;
+        lo = min(lo, u);
+        hi = max(hi, u);
       }
+  }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+  if (lane == 0) {
+    ss.wlo[warp] = lo;
+    ss.whi[warp] = hi;
+  }
+  if (tid == 0) ss.ncand = 0;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < NW; ++w) {
+      lo = min(lo, ss.wlo[w]);
+      hi = max(hi, ss.whi[w]);
+    }
+    ss.lo = lo;
+    ss.hi = hi;
+  }
+  cluster.sync();
+  {
+    uint32_t rl[kSelectMaxCluster], rh[kSelectMaxCluster];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j * kSelectThreads;
-        if (i < Lp) skeys[i] = float_key(v[j]);
+    for (int r = 0; r < kSelectMaxCluster; ++r) {
+      rl[r] = r < C ? cluster.map_shared_rank(&ss, r)->lo : 0xffffffffu;
+      rh[r] = r < C ? cluster.map_shared_rank(&ss, r)->hi : 0u;
+    }
+    lo = 0xffffffffu;
+    hi = 0u;
+#pragma unroll
+    for (int r = 0; r < kSelectMaxCluster; ++r) {
+      lo = min(lo, rl[r]);
+      hi = max(hi, rh[r]);
+    }
+  }
+  // thread t owns the contiguous local keys [t seg, t seg + seg), seg odd
+  const int seg = ((nl + NT - 1) / NT) | 1;
+  const int t0 = min(nl, tid * seg), t1 = min(nl, t0 + seg);
+
+  int need = k, nin = Lp;
+  while (nin > kTkCand && lo != hi) {
+    const uint32_t range = hi - lo;
+    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
+    for (int i = tid; i < kTkBins; i += NT) ss.hist[i] = 0u;
+    __syncthreads();
+    int run_bin = -1, run = 0;
+    for (int i = t0; i < t1; ++i) {
+      const uint32_t u = skeys[i];
+      const int bin = (u >= lo && u <= hi) ? (int)((u - lo) >> shift) : -1;
+      if (bin != run_bin) {
+        if (run_bin >= 0) atomicAdd(&ss.hist[run_bin], (uint32_t)run);
+        run_bin = bin;
+        run = 0;
+      }
+      ++run;
+    }
+    if (run_bin >= 0) atomicAdd(&ss.hist[run_bin], (uint32_t)run);
+    cluster.sync();  // every CTA's histogram is complete
+    uint32_t c[BPT];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      uint32_t v[kSelectMaxCluster];  // every CTA's count of the bin, loads in flight together
+#pragma unroll
+      for (int r = 0; r < kSelectMaxCluster; ++r) v[r] = r < C ? cluster.map_shared_rank(ss.hist, r)[tid * BPT + j] : 0u;
+      c[j] = 0;
+#pragma unroll
+      for (int r = 0; r < kSelectMaxCluster; ++r) c[j] += v[r];
+      sum += (int)c[j];
+    }
+    int incl = sum;  // over the lanes >= this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(FULL, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) ss.wa[warp] = incl;
+    __syncthreads();
+    int above = incl - sum;
+    for (int w = warp + 1; w < NW; ++w) above += ss.wa[w];
+    if (above < need && above + sum >= need) {
+      int acc = above;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (acc + (int)c[j] >= need) {
+          ss.bstar = tid * BPT + j;
+          ss.need = need - acc;
+          ss.nb = (int)c[j];
+          break;
+        }
+        acc += (int)c[j];
       }
     }
-    __syncthreads();
-    topk_adaptive<kSelectThreads>(Lp, k, [&](int i) { return skeys[i]; }, ts, out, nullptr);
-  } else {
-    topk_strided<kSelectThreads>(Lp, k, [&](int i) { return float_key(pooled[i]); }, ts, out);
+    cluster.sync();  // every CTA has read every histogram (they are cleared next round)
+    const uint32_t nlo = lo + ((uint32_t)ss.bstar << shift);
+    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
+    lo = nlo;
+    need = ss.need;
+    nin = ss.nb;
+  }
+
+  const bool all_in = need == nin;
+  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
+  if (!by_index && !all_in) {
+    // candidates into rank 0's list, ranked there; (T, t) sent to every CTA
+    SelectSmem* r0 = cluster.map_shared_rank(&ss, 0);
+    for (int i = t0; i < t1; ++i) {
+      const uint32_t u = skeys[i];
+      if (u >= lo && u <= hi) {
+        const int slot = atomicAdd(&r0->ncand, 1);
+        if (slot < kTkCand) {
+          r0->cand[slot] = s0 + i;
+          r0->ckey[slot] = u;
+        }
+      }
+    }
+    cluster.sync();
+    if (rank == 0 && warp == 0) {
+      const int nc = min(ss.ncand, kTkCand);
+      const int ci = lane < nc ? ss.cand[lane] : 0;
+      const uint32_t cu = lane < nc ? ss.ckey[lane] : 0u;
+      int r = 0;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const uint32_t a2 = __shfl_sync(FULL, cu, m);
+        const int cm = __shfl_sync(FULL, ci, m);
+        r += (m < nc) & ((a2 > cu) | ((a2 == cu) & (cm < ci)));
+      }
+      if (lane < nc && r == need - 1)
+        for (int q = 0; q < C; ++q) {
+          SelectSmem* o = cluster.map_shared_rank(&ss, q);
+          o->T = cu;
+          o->tI = ci;
+        }
+    }
+    cluster.sync();
+  }
+  const uint32_t T = (by_index || all_in) ? lo : ss.T;
+  const int tI = (by_index || all_in) ? Lp : ss.tI;
+  auto pick = [&](int i) -> int {  // i: local index
+    const uint32_t u = skeys[i];
+    if (u > hi) return 1;
+    if (u < lo) return 0;
+    if (by_index) return 2;
+    return (u > T || (u == T && s0 + i <= tI)) ? 1 : 0;
+  };
+  // compaction: thread counts, block scan, cluster totals, then the writes
+  int c1 = 0, c2 = 0;
+  for (int i = t0; i < t1; ++i) {
+    const int t = pick(i);
+    c1 += t == 1;
+    c2 += t == 2;
+  }
+  int x1 = c1, x2 = c2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y1 = __shfl_up_sync(FULL, x1, o), y2 = __shfl_up_sync(FULL, x2, o);
+    if (lane >= o) {
+      x1 += y1;
+      x2 += y2;
+    }
+  }
+  if (lane == 31) {
+    ss.wa[warp] = x1;
+    ss.wb[warp] = x2;
+  }
+  __syncthreads();
+  int base = x1 - c1, bseen = x2 - c2;
+  for (int w = 0; w < warp; ++w) {
+    base += ss.wa[w];
+    bseen += ss.wb[w];
+  }
+  if (tid == NT - 1) {
+    ss.cnt1 = base + c1;
+    ss.cnt2 = bseen + c2;
+  }
+  cluster.sync();  // every CTA's totals are in place
+  {
+    int a1[kSelectMaxCluster], a2[kSelectMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kSelectMaxCluster; ++r) {
+      a1[r] = r < rank ? cluster.map_shared_rank(&ss, r)->cnt1 : 0;
+      a2[r] = r < rank ? cluster.map_shared_rank(&ss, r)->cnt2 : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kSelectMaxCluster; ++r) {
+      base += a1[r];
+      bseen += a2[r];
+    }
+  }
+  cluster.sync();  // no CTA leaves while another still reads its shared memory
+  int o = base + min(need, bseen);
+  for (int i = t0; i < t1; ++i) {
+    const int t = pick(i);
+    if (t == 1 || (t == 2 && bseen < need)) {
+      if (o < k) out[o] = s0 + i;
+      ++o;
+    }
+    bseen += t == 2;
   }
 }
 
@@ -546,20 +768,46 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   launch_begin(K_SNAP_POOL, s);
   snap_pool_kernel<<<dim3((Lmax_seen + kPoolTile - 1) / kPoolTile, (unsigned)units), kPoolThreads, 0, s>>>(p);
   launch_end(K_SNAP_POOL, s);
-  int Lp_max = 0;
+  // select: clusters of up to 8 CTAs per unit (about 4096 prefix positions per CTA)
+  // while the units alone leave SMs idle; 2 once they cover the SMs (measured: wider
+  // clusters then only add cluster barriers)
+  int Lp_max = 1;
   for (int b = 0; b < a.B; ++b) Lp_max = a.prompt_len[b] - a.w > Lp_max ? a.prompt_len[b] - a.w : Lp_max;
+  int csel = (Lp_max + 4095) / 4096;
+  int by_units = (int)((long)num_sms() / (long)units);
+  by_units = by_units > 2 ? by_units : 2;
+  const int by_smem = (Lp_max + kSelectSliceMax - 1) / kSelectSliceMax;  // the slices must fit
+  csel = csel < by_units ? csel : by_units;
+  csel = csel > by_smem ? csel : by_smem;
+  csel = csel < 1 ? 1 : (csel > kSelectMaxCluster ? kSelectMaxCluster : csel);
+  const int slice = (Lp_max + csel - 1) / csel;
+  if (slice > kSelectSliceMax) {
+    set_last_error("prompt longer than the select's shared-memory staging (393216 tokens)");
+    return cudaErrorInvalidValue;
+  }
   static bool sel_attr = false;
   if (!sel_attr) {
-    cudaFuncSetAttribute(snap_select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSelectStagedMax * 4);
+    cudaFuncSetAttribute(snap_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelectSliceMax * 4);
     sel_attr = true;
   }
-  launch_begin(K_SNAP_SELECT, s);
-  if (Lp_max <= kSelectStagedMax)
-    snap_select_kernel<true><<<(unsigned)units, kSelectThreads, (size_t)(Lp_max > 0 ? Lp_max : 1) * 4, s>>>(p);
-  else
-    snap_select_kernel<false><<<(unsigned)units, kSelectThreads, 0, s>>>(p);
-  launch_end(K_SNAP_SELECT, s);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csel, (unsigned)units, 1);
+    cfg.blockDim = dim3(kSelectThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)slice * 4;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csel;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    launch_begin(K_SNAP_SELECT, s);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, snap_select_kernel, p);
+    launch_end(K_SNAP_SELECT, s);
+    if (e != cudaSuccess) return e;
+  }
   launch_begin(K_SNAP_COMPACT, s);
   // 8 pages per CTA (whole 16-byte summary stores) while that still fills one wave of
   // resident CTAs (16 per SM), fewer pages per CTA for small caches
