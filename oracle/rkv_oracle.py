@@ -35,6 +35,9 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
   page_scores ............ per-token bound (brute force), P=1 closed form
   topk_pages ............. top-k property with planted ties
   sparse_attention ....... k1=d, k2=all pages == torch SDPA (library)
+  exact_token_scores ..... group sum == G, one-head case == scipy softmax (library)
+  exact_topk_recall ...... all pages -> 1, the top-K's own pages -> 1,
+                           K >= n closed form, brute force on tiny inputs
   default_pool_kernel .... PARITY UNPINNED (the pages give no rule)
   derived k1 in split .... PARITY UNPINNED (the pages give no rule)
 """
@@ -58,6 +61,8 @@ __all__ = [
     "page_scores",
     "topk_pages",
     "sparse_attention",
+    "exact_token_scores",
+    "exact_topk_recall",
     "hsa_decode_unit",
 ]
 
@@ -337,3 +342,44 @@ def hsa_decode_unit(q_group: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, n: int,
     use = pages if pages_override is None else np.asarray(pages_override)
     out = sparse_attention(q_group, Kc, Vc, n, use, page_size, scale)
     return dict(channels=chans, channel_score=a, page_score=sig, pages=pages, out=out)
+
+
+def exact_token_scores(q_group: np.ndarray, Kc: np.ndarray, n: int, scale: float | None = None) -> np.ndarray:
+    """Exact attention mass of every cached token, summed over the GQA group.
+
+    e_t = sum over the group's heads h of softmax_t(q_h . k_t * scale) over the n
+    cached tokens.  This is the score behind the Exact-TopK baseline ([summary],
+    "Surprising findings" / "Limitations") and the oracle top-k of [adapted], "Where
+    it sits -- the mechanism gap"; READING: summed over the group like stage 1's
+    GQA-group-level scores.  q_group [G, d]; Kc [>= n, d].  Returns [n].
+    """
+    d = q_group.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    z = (q_group @ Kc[:n].T) * scale               # [G, n]
+    z = z - z.max(axis=1, keepdims=True)
+    e = np.exp(z)
+    p = e / e.sum(axis=1, keepdims=True)
+    return p.sum(axis=0)
+
+
+def exact_topk_recall(q_group: np.ndarray, Kc: np.ndarray, n: int, pages: np.ndarray, page_size: int,
+                      k_tokens: int, scale: float | None = None) -> dict:
+    """How much of the exact top-K selection a page selection covers.
+
+    The exact top-K tokens are the K = min(k_tokens, n) largest e_t (ties: lower
+    index), e_t from exact_token_scores; READING: K is the stage-2 token budget
+    (k2 pages of P tokens).  recall = |top-K tokens inside the selected pages| / K;
+    mass = (their e_t sum) / (the top-K's e_t sum).  This is the selection-overlap
+    comparison of [adapted], "Evidence", against the Exact-TopK baseline.
+    """
+    e = exact_token_scores(q_group, Kc, n, scale)
+    K = min(k_tokens, n)
+    order = np.lexsort((np.arange(n), -e))
+    top = order[:K]
+    inside = np.zeros(n, dtype=bool)
+    for p in np.asarray(pages):
+        inside[p * page_size:min(n, (p + 1) * page_size)] = True
+    hit = inside[top]
+    return dict(scores=e, top=np.sort(top), recall=hit.sum() / K if K else 1.0,
+                mass=e[top][hit].sum() / e[top].sum() if K else 1.0, hits=int(hit.sum()), K=K)

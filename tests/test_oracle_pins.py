@@ -339,3 +339,77 @@ def test_planted_needle_survives_and_is_selected():
     qd = _bf16(rng.standard_normal((Hq, d)) + math.sqrt(d) * u)
     dec = O.hsa_decode_unit(qd, Kc, Vc, 64, kmax, kmin, P, k1=16, k2=1)
     assert int(np.where(kept == needle)[0][0]) // P in dec["pages"].tolist()
+
+
+# ------------------------------------------------------------------ exact top-K recall diagnostic
+def _rand_unit(rng, G=4, n=70, d=128):
+    q = rng.standard_normal((G, d))
+    K = rng.standard_normal((n, d))
+    return q, K
+
+
+def test_exact_scores_sum_to_group_size():
+    """Each head's attention over the cached tokens sums to one: the group sum is G."""
+    rng = np.random.default_rng(11)
+    for G in (1, 2, 4, 8):
+        q, K = _rand_unit(rng, G=G, n=53)
+        e = O.exact_token_scores(q, K, 53)
+        assert e.shape == (53,) and np.all(e >= 0)
+        assert abs(e.sum() - G) < 1e-12
+
+
+def test_exact_scores_one_head_is_softmax():
+    """With one head the score is the softmax of the scaled logits (scipy's softmax)."""
+    import scipy.special
+    rng = np.random.default_rng(12)
+    q, K = _rand_unit(rng, G=1, n=40)
+    e = O.exact_token_scores(q, K, 40)
+    ref = scipy.special.softmax(K @ q[0] / math.sqrt(128))
+    np.testing.assert_allclose(e, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_recall_all_pages_and_own_pages_is_one():
+    rng = np.random.default_rng(13)
+    q, K = _rand_unit(rng, n=70)
+    P, Kt = 16, 24
+    r = O.exact_topk_recall(q, K, 70, np.arange(5), P, Kt)
+    assert r["recall"] == 1.0 and abs(r["mass"] - 1.0) < 1e-15 and r["K"] == Kt
+    own = np.unique(r["top"] // P)
+    r2 = O.exact_topk_recall(q, K, 70, own, P, Kt)
+    assert r2["recall"] == 1.0
+    missing = np.setdiff1d(np.arange(5), own)
+    if missing.size:   # pages holding none of the top-K add nothing
+        r3 = O.exact_topk_recall(q, K, 70, missing, P, Kt)
+        assert r3["recall"] == 0.0 and r3["mass"] == 0.0
+
+
+def test_recall_whole_cache_budget_closed_form():
+    """K >= n: every token is in the top-K, so recall is the covered share of the
+    tokens and the mass is the covered share of the group's total mass G."""
+    rng = np.random.default_rng(14)
+    G, n, P = 4, 61, 16
+    q, K = _rand_unit(rng, G=G, n=n)
+    pages = np.array([0, 2, 3])
+    r = O.exact_topk_recall(q, K, n, pages, P, 10_000)
+    covered = [t for t in range(n) if t // P in set(pages.tolist())]
+    assert r["K"] == n and r["recall"] == len(covered) / n
+    e = O.exact_token_scores(q, K, n)
+    assert abs(r["mass"] - e[covered].sum() / G) < 1e-12
+
+
+def test_recall_brute_force_tiny():
+    """Pure-Python ranking of the scores on tiny inputs, with planted ties."""
+    rng = np.random.default_rng(15)
+    for trial in range(20):
+        n, P, Kt = int(rng.integers(5, 30)), 4, int(rng.integers(1, 12))
+        q, K = _rand_unit(rng, G=2, n=n, d=128)
+        if trial % 4 == 0:
+            K[1] = K[3]            # equal keys: equal scores, the lower index ranks first
+        pages = rng.choice(-(-n // P), size=max(1, -(-n // P) // 2), replace=False)
+        r = O.exact_topk_recall(q, K, n, pages, P, Kt)
+        e = r["scores"]
+        ranked = sorted(range(n), key=lambda t: (-float(e[t]), t))
+        top = ranked[:min(Kt, n)]
+        hits = [t for t in top if t // P in set(int(x) for x in pages)]
+        assert r["top"].tolist() == sorted(top)
+        assert r["hits"] == len(hits) and r["recall"] == len(hits) / len(top)
