@@ -187,6 +187,32 @@ class Setup:
         return dict(snap_stats=kbytes, snap_colsum=kbytes, snap_compact=surv, total=2 * kbytes + surv)
 
 
+def selection_recall(setup: Setup) -> dict:
+    """Exact-TopK recall of HSA's page choice on this workload (outside any timed region):
+    one eager pass, the library's recall diagnostic after the first and the last decode
+    step, over every (sequence, KV head)."""
+    rkv, wl = setup.rkv, setup.wl
+    stride = max(setup.k2) + 1
+    pg = torch.empty((wl.B, wl.Hkv, stride), dtype=torch.int32, device=setup.dev)
+    k_tokens = [k * wl.page_size for k in setup.k2]
+    setup.prefill()
+    rec, mass = [], []
+    for t in range(wl.steps):
+        d = setup.dec[t]
+        rkv.rkv_decode_step(setup.cache, d["q"], d["k_new"], d["v_new"], setup.k1, setup.k2, setup.out[t],
+                            sel_pages=pg, workspace=setup.dws)
+        if t in (0, wl.steps - 1):
+            r, m = rkv.rkv_exact_topk_recall(setup.cache, d["q"], pg, k_tokens)
+            rec.append(r.flatten())
+            mass.append(m.flatten())
+    r, m = torch.cat(rec).double(), torch.cat(mass).double()
+    return dict(token_recall_mean=round(float(r.mean()), 4), token_recall_min=round(float(r.min()), 4),
+                mass_recall_mean=round(float(m.mean()), 4), mass_recall_min=round(float(m.min()), 4),
+                k_tokens=self_or_range(k_tokens), steps=[0, wl.steps - 1],
+                what="share of the exact top-k_tokens tokens (attention summed over the GQA group) and of their "
+                     "attention mass inside the pages HSA selected")
+
+
 def capture(fn, stream) -> torch.cuda.CUDAGraph:
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -379,6 +405,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         roofline=roofline, kernels=kernels, gpu_launches=int(launches_per_pass * args.steps),
         clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]),
     )
+    res["selection"] = selection_recall(setup)
     if rank == 0 and not args.no_e2e:
         res["e2e"] = run_e2e(setup, args, stream, rkv)
     if rank == 0 and not args.no_cpu_baseline:

@@ -247,6 +247,31 @@ rkv_status rkv_decode_hsa_noalloc(const rkv_cache* cache, const rkv_bf16* q, int
                                   int32_t* sel_channels, int32_t* sel_pages,
                                   int32_t sel_pages_stride, void* stream);
 
+/*
+ * Exact-TopK recall of a page selection: a diagnostic, not a step of the method.
+ * The summary page of "RocketKV: Accelerating Long-Context LLM Inference via
+ * Two-Stage KV Cache Compression" measures RocketKV against the Exact-TopK
+ * baseline ("Surprising findings", "Limitations"); "RocketKV-adapted" compares
+ * selections by overlap with an oracle top-k ("Where it sits -- the mechanism gap",
+ * "Evidence").
+ * For every (sequence b, KV head g) of the cache as it stands (n = seq_len[b]
+ * tokens), with the group's query heads q[b][g*G .. g*G+G):
+ *   e_t = sum over the group's heads h of softmax over t < n of (q_h . k_t * scale)
+ *   top = the K = min(k_tokens[b], n) tokens of largest e_t (ties: lower index)
+ *   recall[b*Hkv+g] = |top tokens inside the selected pages| / K      (1 when K = 0)
+ *   mass[b*Hkv+g]   = (e_t summed over those) / (e_t summed over top)  (may be NULL)
+ * sel_pages: device [B][Hkv][sel_pages_stride] page ids as rkv_decode_hsa writes
+ * them (ascending; a -1 ends a shorter list; ids outside [0, NP) are ignored).
+ * k_tokens: HOST [B] (the stage-2 token budget, k2 * page_size).  q: device
+ * [B][Hq][128] bf16; recall, mass: device [B*Hkv] fp32; 16-byte aligned.
+ * Supports n <= 49152 per sequence (RKV_ERR_UNSUPPORTED if the cache could hold
+ * more).  Reads every cached key twice.  Bad page ids set RKV_DEVERR_PAGE_ID.
+ */
+rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
+                                 const int32_t* sel_pages, int32_t sel_pages_stride,
+                                 const int32_t* k_tokens, float scale, float* recall, float* mass,
+                                 void* stream);
+
 /* Synchronise `stream`, read and clear cache->error_word.  RKV_OK when it was 0,
  * RKV_ERR_TIMEOUT when the timeout bit was set, else RKV_ERR_DEVICE_DATA; *bits
  * (if not NULL) receives the raw word. */

@@ -138,3 +138,26 @@ def test_append_rejects_bad_arguments(rkv):
     assert lib.rkv_append_page_summary(ctypes.byref(cache), ctypes.c_void_p(0x1000), None, 1, None) == \
         rkv.RKV_ERR_INVALID_ARG
     assert lib.rkv_append_page_summary(ctypes.byref(cache), None, None, 64 * 16 + 1, None) == rkv.RKV_ERR_INVALID_ARG
+
+
+def test_recall_rejects_bad_arguments_without_launching(rkv):
+    """The recall diagnostic validates on the host: nothing launches on a bad call."""
+    import ctypes
+    c = rkv.RkvCacheStruct()
+    c.B, c.Hkv, c.head_dim, c.page_size, c.max_pages, c.num_phys_pages = 1, 1, 128, 16, 8, 8
+    fake = ctypes.c_void_p(4096)
+    for name in ("k_pages", "v_pages", "page_table", "seq_len", "kmax", "kmin", "error_word", "step_sync"):
+        setattr(c, name, fake)
+    n0 = rkv.rkv_launch_count()
+    kt = (ctypes.c_int32 * 1)(16)
+    # Hq not a multiple of Hkv... group of 3
+    st = rkv.lib().rkv_exact_topk_recall(ctypes.byref(c), fake, 3, fake, 4, kt, 0.088, fake, fake, None)
+    assert st == rkv.RKV_ERR_UNSUPPORTED
+    # NULL recall output
+    st = rkv.lib().rkv_exact_topk_recall(ctypes.byref(c), fake, 4, fake, 4, kt, 0.088, None, None, None)
+    assert st == rkv.RKV_ERR_INVALID_ARG and "NULL" in rkv.rkv_last_error()
+    # negative token budget
+    kt[0] = -1
+    st = rkv.lib().rkv_exact_topk_recall(ctypes.byref(c), fake, 4, fake, 4, kt, 0.088, fake, fake, None)
+    assert st == rkv.RKV_ERR_INVALID_ARG
+    assert rkv.rkv_launch_count() == n0

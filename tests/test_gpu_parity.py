@@ -302,3 +302,46 @@ def test_workload4_batched_ragged(rkv, path):
 
 def test_workload5_one_layer_sampled(rkv):
     assert _sampled_full(rkv, 5, [(0, 0), (7, 7)], {0, 63}) <= ATOL_OUT
+
+
+# ------------------------------------------------------------------ Exact-TopK recall diagnostic
+@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa8_w16", "gqa2_p32", "needles"])
+def test_exact_topk_recall_matches_oracle(rkv, name):
+    """Recall and mass of the GPU's page selection against the oracle's exact top-K,
+    after every decode step.  The top-K may differ only by tokens whose exact score is
+    within 1e-5 relative of the K-th score."""
+    wl = SMALL[name]
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+    P = wl.page_size
+    k_tokens = [k2 * P for k2 in run.k2]
+    for step in range(min(wl.steps, 6)):
+        d, out, ch, pg = run.decode_step(step)
+        rec, mass = rkv.rkv_exact_topk_recall(run.cache, d["q"], pg, k_tokens)
+        rec, mass = rec.cpu().numpy(), mass.cpu().numpy()
+        for u in units:
+            r = u.step(run, d, out, ch, pg)
+            qg = f64(d["q"][u.b, u.g * wl.G:(u.g + 1) * wl.G])
+            ref = O.exact_topk_recall(qg, u.Kc, u.n, r["pages"], P, k_tokens[u.b])
+            e, K = ref["scores"], ref["K"]
+            kth = np.sort(e)[::-1][K - 1] if K else 0.0
+            band = int(np.sum(np.abs(e - kth) <= 1e-5 * abs(kth))) if K < u.n else 0
+            got_hits = rec[u.b, u.g] * K
+            assert abs(got_hits - ref["hits"]) <= band + 1e-3, (name, step, u.b, u.g, got_hits, ref["hits"], band)
+            assert abs(mass[u.b, u.g] - ref["mass"]) <= 1e-4 + band / max(K, 1), (mass[u.b, u.g], ref["mass"])
+    assert run.status()[0] == rkv.RKV_OK
+
+
+def test_exact_topk_recall_full_selection_is_one(rkv):
+    """Every page selected (k2 >= pages): recall and mass are exactly one."""
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[600, 450], budget=64, window=8, page_size=16, steps=1,
+                  pool_kernel=5)
+    run = GpuRun(wl, rkv)
+    run.k2 = [4096, 4096]
+    run.prefill()
+    d, out, ch, pg = run.decode_step(0)
+    rec, mass = rkv.rkv_exact_topk_recall(run.cache, d["q"], pg, [64, 64])
+    assert torch.all(rec == 1.0) and torch.allclose(mass, torch.ones_like(mass))

@@ -114,7 +114,7 @@ const char* kernel_name(int kind) {
   static const char* names[K_NUM_KINDS] = {
       "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
       "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
-      "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step"};
+      "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step",     "recall"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
 }
 
@@ -358,6 +358,35 @@ rkv_status rkv_decode_step(const rkv_cache* cache, const rkv_bf16* q, const rkv_
   if (!k_new || !v_new) return fail(RKV_ERR_INVALID_ARG, "rkv_decode_step needs k_new and v_new");
   return decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, sel_channels, sel_pages, sel_pages_stride,
                        workspace, workspace_bytes, stream, "rkv_decode_step launch");
+}
+
+rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* sel_pages,
+                                 int32_t sel_pages_stride, const int32_t* k_tokens, float scale, float* recall,
+                                 float* mass, void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
+  if (!q || !sel_pages || !k_tokens || !recall) return fail(RKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!al16(q) || !al16(recall) || (mass && !al16(mass)) || !al16(sel_pages))
+    return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if (sel_pages_stride < 1) return fail(RKV_ERR_INVALID_ARG, "sel_pages_stride=%d", sel_pages_stride);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
+  if ((long)cache->max_pages * cache->page_size > rkv::recall_max_tokens())
+    return fail(RKV_ERR_UNSUPPORTED, "the recall diagnostic supports caches of at most %d tokens per sequence",
+                rkv::recall_max_tokens());
+  for (int b = 0; b < cache->B; ++b)
+    if (k_tokens[b] < 0) return fail(RKV_ERR_INVALID_ARG, "k_tokens[%d]=%d", b, k_tokens[b]);
+  rkv::RecallArgs a;
+  a.cache = *cache;
+  a.q = q;
+  a.Hq = Hq;
+  a.sel_pages = sel_pages;
+  a.sel_pages_stride = sel_pages_stride;
+  a.k_tokens = k_tokens;
+  a.scale = scale;
+  a.recall = recall;
+  a.mass = mass;
+  return cuda_status(rkv::launch_recall(a, static_cast<cudaStream_t>(stream)), "rkv_exact_topk_recall launch");
 }
 
 int32_t rkv_decode_path(int32_t path) {

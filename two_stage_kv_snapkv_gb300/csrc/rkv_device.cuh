@@ -244,8 +244,10 @@ struct TopkSmem {
   uint32_t tkey;
 };
 
-template <int NT, class KeyFn>
-__device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t* out, int32_t* out2) {
+// take(pos, i) receives every selected index i with its position pos in the ascending
+// list (each from exactly one thread).
+template <int NT, class KeyFn, class TakeFn>
+__device__ void topk_adaptive_fn(int n, int k, KeyFn key, TopkSmem<NT>& ts, TakeFn take) {
   static_assert(NT % 32 == 0 && kTkBins % NT == 0, "bins must split evenly over the threads");
   constexpr int NW = NT / 32;
   constexpr int BPT = kTkBins / NT;  // bins per thread
@@ -422,15 +424,21 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
   for (int i = s0; i < s1; ++i) {
     const int t = pick(i);
     if (t == 1 || (t == 2 && bseen < need)) {
-      if (o < k) {
-        out[o] = i;
-        if (out2) out2[o] = i;
-      }
+      if (o < k) take(o, i);
       ++o;
     }
     bseen += t == 2;
   }
   __syncthreads();  // the scratch may be reused right after
+}
+
+// topk_adaptive_fn writing the ascending indices to out[0..k) (and out2, when not null).
+template <int NT, class KeyFn>
+__device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t* out, int32_t* out2) {
+  topk_adaptive_fn<NT>(n, k, key, ts, [&](int pos, int i) {
+    out[pos] = i;
+    if (out2) out2[pos] = i;
+  });
 }
 
 // The same select with every thread's keys held in registers: thread t owns keys

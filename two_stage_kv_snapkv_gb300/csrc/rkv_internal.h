@@ -26,6 +26,7 @@ enum KernelKind {
   K_HSA_ATTEND,
   K_HSA_COMBINE,
   K_HSA_STEP,
+  K_RECALL,
   K_NUM_KINDS
 };
 const char* kernel_name(int kind);
@@ -88,5 +89,20 @@ struct DecodeArgs {
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages);
 bool decode_fused_ok(const rkv_cache& c);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// --------------------------------------------------------------- diagnostics
+struct RecallArgs {
+  rkv_cache cache;
+  const rkv_bf16* q;
+  int Hq;
+  const int32_t* sel_pages;
+  int sel_pages_stride;
+  const int32_t* k_tokens;  // host [B]
+  float scale;
+  float* recall;
+  float* mass;  // may be null
+};
+int recall_max_tokens();
+cudaError_t launch_recall(const RecallArgs& a, cudaStream_t s);
 
 }  // namespace rkv

@@ -83,6 +83,9 @@ _lib.rkv_decode_path.restype = _i32
 _lib.rkv_decode_hsa_noalloc.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp,
                                         _vp, _i32, _vp]
 _lib.rkv_decode_hsa_noalloc.restype = _i32
+_lib.rkv_exact_topk_recall.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _vp, _i32, _i32p, _f32, _vp, _vp,
+                                       _vp]
+_lib.rkv_exact_topk_recall.restype = _i32
 _lib.rkv_get_device_status.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32p]
 _lib.rkv_get_device_status.restype = _i32
 _lib.rkv_last_error.argtypes = []
@@ -102,7 +105,7 @@ _lib.rkv_profile_read.restype = ctypes.c_char_p
 
 EXPORTED = ["rkv_split_ratio", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
             "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
-            "rkv_decode_path", "rkv_get_device_status", "rkv_last_error",
+            "rkv_decode_path", "rkv_exact_topk_recall", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
             "rkv_profile_reset", "rkv_profile_read"]
 
@@ -258,6 +261,25 @@ def rkv_decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_n
     _check(_lib.rkv_decode_step(ctypes.byref(cache.struct), _ptr(q), _ptr(k_new), _ptr(v_new), Hq, _host_i32(k1),
                                 _host_i32(k2), scale, _ptr(out), _ptr(sel_channels), _ptr(sel_pages), stride,
                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def rkv_exact_topk_recall(cache: PagedCache, q: torch.Tensor, sel_pages: torch.Tensor, k_tokens: Sequence[int],
+                          recall: Optional[torch.Tensor] = None, mass: Optional[torch.Tensor] = None,
+                          scale: Optional[float] = None, stream=None) -> tuple:
+    """Exact-TopK recall of a page selection, per (sequence, KV head): the share of the
+    exact top-k_tokens[b] tokens (attention summed over the GQA group) and of their
+    attention mass that lies in sel_pages ([B, Hkv, stride] as rkv_decode_hsa writes it).
+    Returns (recall, mass), [B, Hkv] fp32 device tensors."""
+    B, Hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if recall is None:
+        recall = torch.empty((B, cache.Hkv), dtype=torch.float32, device=q.device)
+    if mass is None:
+        mass = torch.empty((B, cache.Hkv), dtype=torch.float32, device=q.device)
+    _check(_lib.rkv_exact_topk_recall(ctypes.byref(cache.struct), _ptr(q), Hq, _ptr(sel_pages), sel_pages.shape[-1],
+                                      _host_i32(k_tokens), scale, _ptr(recall), _ptr(mass), _stream(stream)))
+    return recall, mass
 
 
 def rkv_decode_path(path: int = -1) -> int:
