@@ -26,6 +26,7 @@ reading is marked READING below and listed in the design doc.
 
 Parity status per function (what pins it, in tests/test_oracle_pins.py):
   split_ratio ............ worked example c=64 -> 10.3x / 6.2x, clip ends, c1*c2=c
+  split_ratio_mt ......... c1 = 1, c2 = c, keep1 = L; k1 as split_ratio at r = 0
   window_column_scores ... row-sum invariant, zero-query closed form,
                            causal decomposition, pure-Python brute force
   max_pool ............... scipy.ndimage.maximum_filter1d
@@ -49,6 +50,7 @@ import numpy as np
 
 __all__ = [
     "split_ratio",
+    "split_ratio_mt",
     "default_pool_kernel",
     "window_column_scores",
     "window_scores",
@@ -122,6 +124,27 @@ def split_ratio(prompt_len: int, budget: int, head_dim: int, page_size: int,
 # --------------------------------------------------------------------------
 # a2-a5: stage 1, SnapKV++ eviction at prefill (one sequence)
 # --------------------------------------------------------------------------
+def split_ratio_mt(prompt_len: int, budget: int, head_dim: int, page_size: int, k1_override: int = 0) -> dict:
+    """The split of RocketKV-MT: no stage-1 eviction, stage 2 takes the whole ratio.
+
+    [summary, Approach]: RocketKV-MT retains the evicted tokens for later turns;
+    [adapted, "Should you use this?"]: the variant skips permanent eviction so that
+    earlier tokens survive for later queries.  READING: stage 1 keeps the whole
+    prompt (keep1 = L, c1 = 1) and HSA runs over the full history with c2 = c; k1, k2
+    follow split_ratio's readings with that c2.
+    """
+    c = prompt_len / budget
+    c2 = c
+    if k1_override > 0:
+        k1 = int(k1_override)
+    else:
+        k1 = 16 * int(math.floor(head_dim / (16.0 * math.sqrt(max(c2, 1e-300))) + 0.5))
+        k1 = min(max(k1, 16), head_dim)
+    k2 = max(1, budget // page_size)
+    return dict(c=c, r=0.0, c1=1.0, c2=c2, keep1=int(prompt_len), k1=k1, k2=k2,
+                pool_kernel=default_pool_kernel(prompt_len))
+
+
 def window_column_scores(q_win: np.ndarray, k: np.ndarray, scale: float | None = None) -> np.ndarray:
     """Column sums of the observation window's attention weights, per KV head.
 

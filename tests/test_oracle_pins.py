@@ -413,3 +413,16 @@ def test_recall_brute_force_tiny():
         hits = [t for t in top if t // P in set(int(x) for x in pages)]
         assert r["top"].tolist() == sorted(top)
         assert r["hits"] == len(hits) and r["recall"] == len(hits) / len(top)
+
+
+# ------------------------------------------------------------------ RocketKV-MT split
+def test_split_mt_keeps_the_prompt_and_gives_stage2_the_ratio():
+    for L, budget, P in [(32768, 512, 16), (8192, 2048, 32), (100, 256, 16)]:
+        s = O.split_ratio_mt(L, budget, 128, P)
+        assert s["keep1"] == L and s["c1"] == 1.0 and s["r"] == 0.0
+        assert abs(s["c1"] * s["c2"] - L / budget) < 1e-12
+        assert s["k2"] == max(1, budget // P)
+        # k1 takes the same rule as the two-stage split would at c2 = c
+        k1 = 16 * round(128 / (16 * math.sqrt(L / budget)))
+        assert s["k1"] == min(max(k1, 16), 128)
+    assert O.split_ratio_mt(32768, 512, 128, 16, k1_override=40)["k1"] == 40
