@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, help="1..5 (2: Llama3.1-8B layer, 32K prompt)")
+    ap.add_argument("--workload", type=int, default=2, help="1..6 (2: Llama3.1-8B layer, 32K prompt; 6: workload 4's batch under RocketKV-MT)")
     ap.add_argument("--seed", type=int, default=0x5EED)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -129,7 +129,10 @@ class Setup:
             d["v_new"] = d["v_new"].unsqueeze(2).contiguous()
         self.splits = []
         for L in wl.prompt_lens:
-            s = rkv.rkv_split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0)
+            if wl.mt:
+                s = rkv.rkv_split_ratio_mt(L, wl.budget, wl.d, wl.page_size, wl.k1 or 0)
+            else:
+                s = rkv.rkv_split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0)
             if wl.pool_kernel:
                 s["pool_kernel"] = wl.pool_kernel
             self.splits.append(s)
@@ -182,7 +185,8 @@ class Setup:
 
     def prefill_bytes(self) -> dict:
         wl = self.wl
-        kbytes = sum(wl.Hkv * L * 128 * 2 for L in wl.prompt_lens)
+        # stage-1 scoring reads K once per pass; without eviction (RocketKV-MT) it is skipped
+        kbytes = 0 if wl.mt else sum(wl.Hkv * L * 128 * 2 for L in wl.prompt_lens)
         surv = sum(wl.Hkv * k * 128 * 2 * 2 * 2 for k in self.keep1)   # K+V read and written
         return dict(snap_stats=kbytes, snap_colsum=kbytes, snap_compact=surv, total=2 * kbytes + surv)
 

@@ -119,6 +119,19 @@ rkv_status rkv_split_ratio(int32_t prompt_len, int32_t budget, int32_t head_dim,
                            int32_t page_size, int32_t window, int32_t k1_override,
                            rkv_split* out);
 
+/*
+ * The split of RocketKV-MT ("RocketKV: Accelerating Long-Context LLM Inference via
+ * Two-Stage KV Cache Compression", research-map summary, "Approach": the variant
+ * that retains the tokens stage 1 would evict; "RocketKV-adapted", "Should you use
+ * this?": it skips permanent eviction).  Nothing is evicted (keep1 = prompt_len,
+ * c1 = 1, r = 0) and HSA takes the whole ratio c = prompt_len / budget as c2; k1,
+ * k2 and pool_kernel follow the same rules as rkv_split_ratio with that c2.  Passing
+ * this keep1 to rkv_prefill_evict builds the paged cache and summaries over the whole
+ * prompt and skips the stage-1 scoring.  Host only.
+ */
+rkv_status rkv_split_ratio_mt(int32_t prompt_len, int32_t budget, int32_t head_dim,
+                              int32_t page_size, int32_t k1_override, rkv_split* out);
+
 /* Bytes of workspace rkv_prefill_evict needs for these sizes. */
 size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t window,
                                   int32_t max_prompt_len);
@@ -146,6 +159,9 @@ size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t wi
  *   kept_idx : device [B][Hkv][kept_stride] int32, receives the kept positions.
  *   pooled_scores : device [B][Hkv][max_prompt_len] fp32 receiving S' for
  *            t < L-w, or NULL.
+ * When no sequence evicts anything (keep1[b] == prompt_len[b] for every b, as
+ * rkv_split_ratio_mt gives) the stage-1 scoring is skipped: kept_idx receives every
+ * position and pooled_scores is left untouched.
  */
 rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv_bf16* v,
                              int32_t B, int32_t Hq, int32_t window, int32_t max_prompt_len,

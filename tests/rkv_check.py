@@ -49,7 +49,10 @@ def check_topk(gpu_idx, scores: np.ndarray, k: int, rel: float = REL_TIE, what: 
 def splits_for(wl: W.Workload, rkv) -> list:
     out = []
     for L in wl.prompt_lens:
-        s = rkv.rkv_split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0)
+        if wl.mt:
+            s = rkv.rkv_split_ratio_mt(L, wl.budget, wl.d, wl.page_size, wl.k1 or 0)
+        else:
+            s = rkv.rkv_split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0)
         if wl.pool_kernel:
             s["pool_kernel"] = wl.pool_kernel
         out.append(s)
@@ -132,7 +135,8 @@ class OracleUnit:
         Lp = self.L - wl.window
         gp = run.pooled[b, g, :Lp].double().cpu().numpy()
         ref = self.res["pooled"][0]
-        if Lp > 0:
+        evicts = any(k < L for k, L in zip(run.keep1, wl.prompt_lens))
+        if Lp > 0 and evicts:   # when no sequence evicts, the scoring (and S') is skipped
             scale = max(float(ref.max()), 1e-30)
             err = np.abs(gp - ref)
             assert np.all(err <= 1e-4 * np.abs(ref) + 1e-6 * scale), \

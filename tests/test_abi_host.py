@@ -161,3 +161,14 @@ def test_recall_rejects_bad_arguments_without_launching(rkv):
     st = rkv.lib().rkv_exact_topk_recall(ctypes.byref(c), fake, 4, fake, 4, kt, 0.088, fake, fake, None)
     assert st == rkv.RKV_ERR_INVALID_ARG
     assert rkv.rkv_launch_count() == n0
+
+
+@pytest.mark.parametrize("L,budget,P", [(32768, 512, 16), (8192, 2048, 32), (100, 256, 16), (109000, 256, 16)])
+def test_host_split_mt_matches_oracle(rkv, L, budget, P):
+    from oracle import rkv_oracle as O
+    got = rkv.rkv_split_ratio_mt(L, budget, 128, P)
+    ref = O.split_ratio_mt(L, budget, 128, P)
+    for key in ("keep1", "k1", "k2", "pool_kernel"):
+        assert got[key] == ref[key], key
+    for key in ("c", "r", "c1", "c2"):
+        assert abs(got[key] - ref[key]) <= 1e-12 * max(1.0, abs(ref[key])), key

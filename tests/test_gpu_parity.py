@@ -345,3 +345,29 @@ def test_exact_topk_recall_full_selection_is_one(rkv):
     d, out, ch, pg = run.decode_step(0)
     rec, mass = rkv.rkv_exact_topk_recall(run.cache, d["q"], pg, [64, 64])
     assert torch.all(rec == 1.0) and torch.allclose(mass, torch.ones_like(mass))
+
+
+# ------------------------------------------------------------------ RocketKV-MT
+def test_mt_small_end_to_end(rkv, path):
+    """RocketKV-MT: nothing evicted, HSA over the whole prompt plus the new tokens."""
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=12,
+                  pool_kernel=5, mt=True, name="mt_small")
+    run = GpuRun(wl, rkv)
+    assert run.keep1 == [700, 1000]
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+        np.testing.assert_array_equal(u.kept, np.arange(u.L))
+        u.check_cache(run)
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in units:
+            u.step(run, d, out, ch, pg, check_cache=(step % 4 == 0))
+    assert run.status()[0] == rkv.RKV_OK
+
+
+def test_workload6_mt_batched_sampled(rkv):
+    wl = W.workload(6)
+    longest = int(np.argmax(wl.prompt_lens))
+    assert _sampled_full(rkv, 6, [(longest, 2), (0, 5)], {0, 255}) <= ATOL_OUT

@@ -218,6 +218,30 @@ rkv_status rkv_split_ratio(int32_t prompt_len, int32_t budget, int32_t head_dim,
   return RKV_OK;
 }
 
+rkv_status rkv_split_ratio_mt(int32_t prompt_len, int32_t budget, int32_t head_dim, int32_t page_size,
+                              int32_t k1_override, rkv_split* out) {
+  if (!out) return fail(RKV_ERR_INVALID_ARG, "out is NULL");
+  if (prompt_len < 1 || budget < 1 || head_dim < 1 || page_size < 1 || k1_override < 0)
+    return fail(RKV_ERR_INVALID_ARG, "sizes must be positive");
+  const double c = (double)prompt_len / (double)budget;
+  int k1 = k1_override;
+  if (k1 <= 0) {
+    k1 = 16 * (int)std::floor((double)head_dim / (16.0 * std::sqrt(c)) + 0.5);
+    k1 = k1 < 16 ? 16 : (k1 > head_dim ? head_dim : k1);
+  }
+  int k2 = budget / page_size;
+  k2 = k2 < 1 ? 1 : k2;
+  out->c = c;
+  out->r = 0.0;
+  out->c1 = 1.0;
+  out->c2 = c;
+  out->keep1 = prompt_len;
+  out->k1 = k1;
+  out->k2 = k2;
+  out->pool_kernel = prompt_len <= 8192 ? 7 : (prompt_len <= 49152 ? 31 : 63);
+  return RKV_OK;
+}
+
 size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t window, int32_t max_prompt_len) {
   if (B < 1 || Hkv < 1 || max_prompt_len < 1) return 0;
   return rkv::prefill_ws_bytes(B, Hq, Hkv, window, max_prompt_len);

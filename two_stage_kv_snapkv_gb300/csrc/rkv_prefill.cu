@@ -755,19 +755,25 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     cudaFuncSetAttribute(snap_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     attrs = true;
   }
+  // nothing to evict anywhere (RocketKV-MT's split): the kept set is every position,
+  // so the scoring passes are skipped and the select only writes the identity
+  bool evicts = false;
+  for (int b = 0; b < a.B; ++b) evicts |= a.keep1[b] < a.prompt_len[b];
   const dim3 sgrid(p.nsplit, (unsigned)units);
-  launch_begin(K_SNAP_STATS, s);
-  snap_score_kernel<true><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
-  launch_end(K_SNAP_STATS, s);
-  launch_begin(K_SNAP_STATS_COMBINE, s);
-  snap_stats_combine_kernel<<<(unsigned)units, 128, 0, s>>>(p);
-  launch_end(K_SNAP_STATS_COMBINE, s);
-  launch_begin(K_SNAP_COLSUM, s);
-  snap_score_kernel<false><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
-  launch_end(K_SNAP_COLSUM, s);
-  launch_begin(K_SNAP_POOL, s);
-  snap_pool_kernel<<<dim3((Lmax_seen + kPoolTile - 1) / kPoolTile, (unsigned)units), kPoolThreads, 0, s>>>(p);
-  launch_end(K_SNAP_POOL, s);
+  if (evicts) {
+    launch_begin(K_SNAP_STATS, s);
+    snap_score_kernel<true><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
+    launch_end(K_SNAP_STATS, s);
+    launch_begin(K_SNAP_STATS_COMBINE, s);
+    snap_stats_combine_kernel<<<(unsigned)units, 128, 0, s>>>(p);
+    launch_end(K_SNAP_STATS_COMBINE, s);
+    launch_begin(K_SNAP_COLSUM, s);
+    snap_score_kernel<false><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
+    launch_end(K_SNAP_COLSUM, s);
+    launch_begin(K_SNAP_POOL, s);
+    snap_pool_kernel<<<dim3((Lmax_seen + kPoolTile - 1) / kPoolTile, (unsigned)units), kPoolThreads, 0, s>>>(p);
+    launch_end(K_SNAP_POOL, s);
+  }
   // select: clusters of up to 8 CTAs per unit (about 4096 prefix positions per CTA)
   // while the units alone leave SMs idle; 2 once they cover the SMs (measured: wider
   // clusters then only add cluster barriers)

@@ -63,6 +63,8 @@ _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _lib.rkv_split_ratio.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(RkvSplit)]
 _lib.rkv_split_ratio.restype = _i32
+_lib.rkv_split_ratio_mt.argtypes = [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(RkvSplit)]
+_lib.rkv_split_ratio_mt.restype = _i32
 _lib.rkv_prefill_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.rkv_prefill_workspace_size.restype = _sz
 _lib.rkv_prefill_evict.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32p, _i32p, _i32p, _f32,
@@ -103,7 +105,7 @@ _lib.rkv_profile_release.restype = None
 _lib.rkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
 _lib.rkv_profile_read.restype = ctypes.c_char_p
 
-EXPORTED = ["rkv_split_ratio", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
+EXPORTED = ["rkv_split_ratio", "rkv_split_ratio_mt", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
             "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
             "rkv_decode_path", "rkv_exact_topk_recall", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
@@ -195,6 +197,15 @@ def rkv_split_ratio(prompt_len: int, budget: int, head_dim: int = HEAD_DIM, page
                     k1_override: int = 0) -> dict:
     out = RkvSplit()
     _check(_lib.rkv_split_ratio(prompt_len, budget, head_dim, page_size, window, k1_override, ctypes.byref(out)))
+    return dict(c=out.c, r=out.r, c1=out.c1, c2=out.c2, keep1=out.keep1, k1=out.k1, k2=out.k2,
+                pool_kernel=out.pool_kernel)
+
+
+def rkv_split_ratio_mt(prompt_len: int, budget: int, head_dim: int = HEAD_DIM, page_size: int = 16,
+                       k1_override: int = 0) -> dict:
+    """RocketKV-MT's split: nothing evicted (keep1 = prompt_len), HSA takes the whole ratio."""
+    out = RkvSplit()
+    _check(_lib.rkv_split_ratio_mt(prompt_len, budget, head_dim, page_size, k1_override, ctypes.byref(out)))
     return dict(c=out.c, r=out.r, c1=out.c1, c2=out.c2, keep1=out.keep1, k1=out.k1, k2=out.k2,
                 pool_kernel=out.pool_kernel)
 

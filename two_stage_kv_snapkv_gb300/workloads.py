@@ -72,6 +72,7 @@ class Workload:
     outlier_channels: int = 0            # per KV head, keys scaled x8
     sinks: int = 0                       # first tokens, keys scaled x8
     layers: int = 1
+    mt: bool = False                     # RocketKV-MT: no stage-1 eviction
 
     @property
     def G(self) -> int:
@@ -88,7 +89,8 @@ def _uniform_lengths(B, lo, hi, seed):
 
 
 def workload(n: int, seed: int = 0x5EED) -> Workload:
-    """The five benchmark workloads of this project, by number 1..5."""
+    """The benchmark workloads of this project, by number 1..6 (6: workload 4's batch
+    under RocketKV-MT, HSA over the whole un-evicted prompts)."""
     if n == 1:   # tiny single layer, GQA 4, 4 needles per KV head
         return Workload("tiny_4k_gqa4", 1, 8, 2, 128, [4096], 256, 32, 16, 16,
                         pool_kernel=7, k1=64, needles_per_head=4)
@@ -105,19 +107,23 @@ def workload(n: int, seed: int = 0x5EED) -> Workload:
     if n == 5:   # 32-layer decode, batch 8, 64K prompts
         return Workload("llama8b_32layer_b8_64k", 8, 32, 8, 128, [65536] * 8, 4096, 32, 16, 64,
                         outlier_channels=4, sinks=4, layers=32)
+    if n == 6:   # workload 4's batch with nothing evicted (RocketKV-MT)
+        lens = _uniform_lengths(16, 8192, 32768, seed_for(seed, 4, "lengths"))
+        return Workload("llama8b_batch16_8k_32k_mt", 16, 32, 8, 128, lens, 2048, 32, 32, 256,
+                        outlier_channels=4, sinks=4, mt=True)
     raise ValueError(f"no workload {n}")
 
 
 def custom(B=1, Hq=4, Hkv=2, d=128, prompt_lens=(512,), budget=64, window=8, page_size=16,
            steps=4, pool_kernel=5, k1=None, needles_per_head=0, outlier_channels=0, sinks=0,
-           name="custom") -> Workload:
+           name="custom", mt=False) -> Workload:
     """A small workload for parity tests (sizes the oracle finishes in seconds)."""
     pl = list(prompt_lens)
     if len(pl) == 1 and B > 1:
         pl = pl * B
     return Workload(name, B, Hq, Hkv, d, pl, budget, window, page_size, steps,
                     pool_kernel=pool_kernel, k1=k1, needles_per_head=needles_per_head,
-                    outlier_channels=outlier_channels, sinks=sinks)
+                    outlier_channels=outlier_channels, sinks=sinks, mt=mt)
 
 
 # ---------------------------------------------------------------- structure
