@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0x5EED)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-decode-steps", type=int, default=16)
+    ap.add_argument("--cpu-decode-steps", type=int, default=0, help="decode steps per oracle sample (0: all)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="repeat the oracle sample until this much CPU time")
     ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
     ap.add_argument("--decode-path", choices=["auto", "split", "fused"], default="auto",
                     help="decode implementation: one fused launch per step (auto/fused) or four kernels")
@@ -392,15 +393,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic (seeded; see DESIGN.md input recipe)",
-        config=dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, head_dim=wl.d, prompt_len=wl.prompt_lens[0]
-                    if wl.B == 1 else f"{min(wl.prompt_lens)}..{max(wl.prompt_lens)}", budget=wl.budget,
-                    window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, keep1=self_or_range(setup.keep1),
-                    k1=self_or_range(setup.k1), k2=self_or_range(setup.k2), pool_kernel=self_or_range(setup.kp),
-                    step="one request: split + prefill evict + every decode step (append + HSA)",
-                    l2="flushed (256 MB write) before the prefill and before every decode step; flush not timed",
-                    timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
-                    decode_path=args.decode_path,
-                    parallelism=f"replica x{world}" if world > 1 else "single GPU"),
+        config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world),
         prefill_evict_ms=round(statistics.mean(pre_all), 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),
         decode_achieved_gbs=round(step_total / (dec_mean_ms * 1e-3) / 1e9, 1),
@@ -413,12 +406,34 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     if rank == 0 and not args.no_e2e:
         res["e2e"] = run_e2e(setup, args, stream, rkv)
     if rank == 0 and not args.no_cpu_baseline:
-        o = oracle_sample(setup, args.cpu_decode_steps)
+        steps = args.cpu_decode_steps or wl.steps
+        vals, secs, reps = [], 0.0, 0
+        while secs < args.cpu_seconds and reps < 100:
+            o = oracle_sample(setup, steps)
+            vals.append(o["value"])
+            secs += o["seconds"]
+            reps += 1
+            if secs + o["seconds"] > 3 * args.cpu_seconds:
+                break
+        o = dict(value=statistics.mean(vals), seconds=secs)
         res["cpu_baseline"] = dict(value=round(o["value"], 3), unit=UNIT, cores=host_cores(), kind="oracle",
-                                   sample=f"oracle prefill of all {wl.B * wl.Hkv} units + {args.cpu_decode_steps} "
-                                          f"of {wl.steps} decode steps ({o['seconds']:.1f} s), extrapolated to the "
-                                          f"whole request: steps / (prefill + steps * mean step)")
+                                   sample=f"{reps} x (oracle prefill of all {wl.B * wl.Hkv} units + {steps} of "
+                                          f"{wl.steps} decode steps), {o['seconds']:.1f} s of CPU time in total; "
+                                          f"value = steps / (prefill + steps * mean step), mean over the repetitions")
     return res
+
+
+def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    return dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, head_dim=wl.d, prompt_len=wl.prompt_lens[0]
+                if wl.B == 1 else f"{min(wl.prompt_lens)}..{max(wl.prompt_lens)}", budget=wl.budget,
+                window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, keep1=self_or_range(keep1),
+                k1=self_or_range(k1), k2=self_or_range(k2), pool_kernel=self_or_range(kp),
+                split="RocketKV-MT (nothing evicted)" if wl.mt else "two-stage",
+                step="one request: split + prefill evict + every decode step (append + HSA)",
+                l2="flushed (256 MB write) before the prefill and before every decode step; flush not timed",
+                timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
+                decode_path=decode_path, parallelism=f"replica x{world}" if world > 1 else "single GPU")
 
 
 def whole_job_value(total_ms: float, decode_steps: int, passes: int, world: int, device) -> tuple:
@@ -514,7 +529,10 @@ def run_reference(args, rank: int, world: int) -> dict:
         d["k_new"] = d["k_new"].unsqueeze(2)
         d["v_new"] = d["v_new"].unsqueeze(2)
         setup.dec.append(d)
-    sp = [O.split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0) for L in wl.prompt_lens]
+    if wl.mt:
+        sp = [O.split_ratio_mt(L, wl.budget, wl.d, wl.page_size, wl.k1 or 0) for L in wl.prompt_lens]
+    else:
+        sp = [O.split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0) for L in wl.prompt_lens]
     setup.keep1 = [s["keep1"] for s in sp]
     setup.k1 = [s["k1"] for s in sp]
     setup.k2 = [s["k2"] for s in sp]
@@ -530,7 +548,7 @@ def run_reference(args, rank: int, world: int) -> dict:
     return dict(impl="reference", metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(1e3 / value * wl.steps, 3), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)",
-                config=dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, decode_steps=wl.steps),
+                config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world),
                 cpu_baseline=dict(value=round(value, 3), unit=UNIT, cores=host_cores(), kind="oracle",
                                   sample=f"per step: oracle prefill of all units + {nsteps} decode steps, "
                                          f"extrapolated to the whole request ({secs:.1f} s total)"),
