@@ -139,6 +139,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// 2^x by the special function unit's single instruction (PTX ex2.approx.ftz.f32):
+// relative error of a few ulps, results below 2^-126 flushed to zero.  Used where the
+// exponential is the inner loop's cost (the scoring epilogues).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Dynamic shared memory rounded up to a 1024-byte boundary (the 128-byte swizzle atom).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_u32(p);

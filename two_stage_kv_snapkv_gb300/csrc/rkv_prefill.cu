@@ -227,10 +227,10 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            s0 += exp2f(z[j] - m_new);
-            s1 += exp2f(z[j + 1] - m_new);
+            s0 += ex2_approx(z[j] - m_new);
+            s1 += ex2_approx(z[j + 1] - m_new);
           }
-          l_run = l_run * exp2f(m_run - m_new) + (s0 + s1);
+          l_run = l_run * ex2_approx(m_run - m_new) + (s0 + s1);
           m_run = m_new;
         }
       } else {
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const float2 a0 = rs[c * 32 + j], a1 = rs[c * 32 + j + 1];
-            s0 = fmaf(exp2f(__uint_as_float(v[j]) * sl - a0.x), a0.y, s0);
-            s1 = fmaf(exp2f(__uint_as_float(v[j + 1]) * sl - a1.x), a1.y, s1);
+            s0 = fmaf(ex2_approx(fmaf(__uint_as_float(v[j]), sl, -a0.x)), a0.y, s0);
+            s1 = fmaf(ex2_approx(fmaf(__uint_as_float(v[j + 1]), sl, -a1.x)), a1.y, s1);
           }
         }
         const int t = t0 + tid;
