@@ -9,8 +9,9 @@
 // group times the w window queries, row r = head*w + j at position L-w+j):
 //   snap_score<stats>   pass 1: per-row max and sum of exp of the scaled logits
 //                       over the keys each row may see (causal), per split of L
-//   snap_stats_combine  merge of the splits -> (M_r, 1/l_r)
-//   snap_score<colsum>  pass 2: recompute the logits, S[t] = sum_r exp(z - M_r)/l_r
+//   snap_stats_combine  merge of the splits -> lse_r = M_r + log2(l_r) (base 2)
+//   snap_score<colsum>  pass 2: recompute the logits, S[t] = sum_r 2^(z - lse_r)
+//                       (= sum_r exp(z - M_r) / l_r in base 2)
 //                       for prefix tokens t < L-w (the group sum is the row sum)
 //   snap_pool           centred max-pool of S (out-of-range positions ignored)
 //   snap_select         block radix select of the top keep1-w pooled positions
@@ -55,7 +56,7 @@ struct SnapParams {
   int cgroup;             // pages per compaction CTA (1 .. 8)
   float scale_log2;
   float2* part;           // [units][nsplit][128] (m, l)
-  float2* rowstat;        // [units][128] (M, 1/l)
+  float* rowlse;          // [units][128] base-2 log-sum-exp of each row, +inf for rows without keys
   float* S;               // [units][Lmax]
   float* pooled;          // [units][Lmax]
   int32_t* kept;          // [units][kept_stride]
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
   __shared__ uint64_t full_b[kTcStages], empty_b[kTcStages], tfull_b[2], tempty_b[2];
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
-  __shared__ float2 rs[128];  // pass 2: (M_r, 1/l_r)
+  __shared__ __align__(16) float rs[128];  // pass 2: lse_r = M_r + log2(l_r) (base 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv, split = blockIdx.x;
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
     *reinterpret_cast<uint4*>(qs + tc_swz(r, piece)) = v;
   }
   if (!kStats)
-    for (int r = tid; r < 128; r += kTcThreads) rs[r] = p.rowstat[(size_t)unit * 128 + r];
+    for (int r = tid; r < 128; r += kTcThreads) rs[r] = p.rowlse[(size_t)unit * 128 + r];
   fence_proxy_async_smem();  // the generic writes of Q, before the MMAs read it
   tc_fence_before();
   __syncthreads();
@@ -216,19 +217,31 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
           tc_ld32_wait(lane_addr + d * 128 + c * 32, v);
-          float z[32];
-          float mx = -INFINITY;
+          float s0 = 0.f, s1 = 0.f, m_new;
+          if (c * 32 + 32 <= vis) {  // the row sees the whole chunk: no mask; sl > 0, so max(v)*sl = max(v*sl)
+            float mx = __uint_as_float(v[0]);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            z[j] = (c * 32 + j < vis) ? __uint_as_float(v[j]) * sl : -INFINITY;
-            mx = fmaxf(mx, z[j]);
-          }
-          const float m_new = fmaxf(m_run, mx);
-          float s0 = 0.f, s1 = 0.f;
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+            m_new = fmaxf(m_run, mx * sl);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            s0 += ex2_approx(z[j] - m_new);
-            s1 += ex2_approx(z[j + 1] - m_new);
+            for (int j = 0; j < 32; j += 2) {
+              s0 += ex2_approx(fmaf(__uint_as_float(v[j]), sl, -m_new));
+              s1 += ex2_approx(fmaf(__uint_as_float(v[j + 1]), sl, -m_new));
+            }
+          } else {
+            float z[32];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              z[j] = (c * 32 + j < vis) ? __uint_as_float(v[j]) * sl : -INFINITY;
+              mx = fmaxf(mx, z[j]);
+            }
+            m_new = fmaxf(m_run, mx);
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              s0 += ex2_approx(z[j] - m_new);
+              s1 += ex2_approx(z[j + 1] - m_new);
+            }
           }
           l_run = l_run * ex2_approx(m_run - m_new) + (s0 + s1);
           m_run = m_new;
@@ -240,10 +253,12 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
           uint32_t v[32];
           tc_ld32_wait(lane_addr + d * 128 + c * 32, v);
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 a0 = rs[c * 32 + j], a1 = rs[c * 32 + j + 1];
-            s0 = fmaf(ex2_approx(fmaf(__uint_as_float(v[j]), sl, -a0.x)), a0.y, s0);
-            s1 = fmaf(ex2_approx(fmaf(__uint_as_float(v[j + 1]), sl, -a1.x)), a1.y, s1);
+          for (int j = 0; j < 32; j += 4) {  // p = 2^(z - M_r) / l_r = 2^(z - lse_r)
+            const float4 a = *reinterpret_cast<const float4*>(&rs[c * 32 + j]);
+            s0 += ex2_approx(fmaf(__uint_as_float(v[j]), sl, -a.x));
+            s1 += ex2_approx(fmaf(__uint_as_float(v[j + 1]), sl, -a.y));
+            s0 += ex2_approx(fmaf(__uint_as_float(v[j + 2]), sl, -a.z));
+            s1 += ex2_approx(fmaf(__uint_as_float(v[j + 3]), sl, -a.w));
           }
         }
         const int t = t0 + tid;
@@ -280,8 +295,8 @@ __global__ void __launch_bounds__(128) snap_stats_combine_kernel(const __grid_co
   for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, pp[(size_t)s * 128].x);
   float l = 0.f;
   for (int s = 0; s < p.nsplit; ++s) l += pp[(size_t)s * 128].y * exp2f(pp[(size_t)s * 128].x - M);
-  // rows without keys (r >= R) get a huge M and zero weight so they add nothing
-  p.rowstat[(size_t)unit * 128 + r] = (r < p.R && l > 0.f) ? make_float2(M, 1.f / l) : make_float2(1e30f, 0.f);
+  // rows without keys (r >= R) get +inf, so 2^(z - lse) = 0 and they add nothing
+  p.rowlse[(size_t)unit * 128 + r] = (r < p.R && l > 0.f) ? M + log2f(l) : INFINITY;
 }
 
 // Centred max-pool.  grid (ceil(Lmax / 2048), B*Hkv), 256 threads.
@@ -706,7 +721,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   uint8_t* w = static_cast<uint8_t*>(a.ws);
   p.part = reinterpret_cast<float2*>(w);
   w += align256(units * kMaxSnapSplit * 128 * 8);
-  p.rowstat = reinterpret_cast<float2*>(w);
+  p.rowlse = reinterpret_cast<float*>(w);
   w += align256(units * 128 * 8);
   p.S = reinterpret_cast<float*>(w);
   w += align256(units * a.Lmax * 4);
