@@ -31,6 +31,8 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
                            causal decomposition, pure-Python brute force
   max_pool ............... scipy.ndimage.maximum_filter1d
   select_kept ............ single-query special case == top-k of raw logits
+  prefill_chunked_unit ... one chunk == prefill_evict_unit; under budget == no
+                           eviction; size and window invariants
   page_summaries ......... append == rebuild, membership + bound properties
   channel_select ......... top-k property with planted ties
   page_scores ............ per-token bound (brute force), P=1 closed form
@@ -57,6 +59,7 @@ __all__ = [
     "max_pool",
     "select_kept",
     "prefill_evict_unit",
+    "prefill_chunked_unit",
     "page_summaries",
     "append_summaries",
     "channel_select",
@@ -237,6 +240,37 @@ def prefill_evict_unit(q_win: np.ndarray, k: np.ndarray, keep1: int, pool_kernel
     Sp = max_pool(S, pool_kernel)
     kept = np.stack([select_kept(Sp[g], keep1, L, w) for g in range(Hkv)])
     return dict(scores=S, pooled=Sp, kept=kept)
+
+
+def prefill_chunked_unit(q_wins: list, k_chunks: list, v_chunks: list, keep1: int, pool_kernel: int,
+                         scale: float | None = None) -> dict:
+    """Stage 1 over a prompt that arrives in chunks, re-enforcing the budget per chunk.
+
+    [adapted], "Evidence": stage-1 eviction re-enforces the budget across
+    chunked-prefill calls.  READING: each chunk's tokens join the survivors held so
+    far (in cache order); whenever that exceeds keep1, SnapKV++ runs again over the
+    whole held sequence with the chunk's last w queries as the observation window
+    (prefill_evict_unit with L = the held length) and keeps its survivors.  One KV
+    cache per KV head, as in prefill_evict_unit.
+    q_wins[c] [Hq, w, d]; k_chunks[c], v_chunks[c] [Hkv, m_c, d].  Returns the final
+    held K and V [Hkv, n, d] and, per chunk, the held length and the kept indices
+    (into the held sequence before that chunk's eviction; None when nothing was
+    evicted).
+    """
+    Hkv = k_chunks[0].shape[0]
+    K = np.zeros((Hkv, 0, k_chunks[0].shape[2]))
+    V = np.zeros((Hkv, 0, v_chunks[0].shape[2]))
+    history = []
+    for q_win, kc, vc in zip(q_wins, k_chunks, v_chunks):
+        K = np.concatenate([K, kc], axis=1)
+        V = np.concatenate([V, vc], axis=1)
+        kept = None
+        if K.shape[1] > keep1:
+            kept = prefill_evict_unit(q_win, K, keep1, pool_kernel, scale)["kept"]
+            K = np.stack([K[g, kept[g]] for g in range(Hkv)])
+            V = np.stack([V[g, kept[g]] for g in range(Hkv)])
+        history.append(dict(held=K.shape[1], kept=kept))
+    return dict(K=K, V=V, history=history)
 
 
 # --------------------------------------------------------------------------

@@ -426,3 +426,51 @@ def test_split_mt_keeps_the_prompt_and_gives_stage2_the_ratio():
         k1 = 16 * round(128 / (16 * math.sqrt(L / budget)))
         assert s["k1"] == min(max(k1, 16), 128)
     assert O.split_ratio_mt(32768, 512, 128, 16, k1_override=40)["k1"] == 40
+
+
+# ------------------------------------------------------------------ chunked prefill
+def _chunks(rng, Hq=4, Hkv=2, w=8, lens=(100, 60, 90), d=128):
+    q = [rng.standard_normal((Hq, w, d)) for _ in lens]
+    k = [rng.standard_normal((Hkv, m, d)) for m in lens]
+    v = [rng.standard_normal((Hkv, m, d)) for m in lens]
+    return q, k, v
+
+
+def test_chunked_single_chunk_is_prefill_evict():
+    rng = np.random.default_rng(21)
+    q, k, v = _chunks(rng, lens=(150,))
+    r = O.prefill_chunked_unit(q, k, v, keep1=64, pool_kernel=5)
+    ref = O.prefill_evict_unit(q[0], k[0], 64, 5)["kept"]
+    np.testing.assert_array_equal(r["history"][0]["kept"], ref)
+    for g in range(2):
+        np.testing.assert_array_equal(r["K"][g], k[0][g, ref[g]])
+        np.testing.assert_array_equal(r["V"][g], v[0][g, ref[g]])
+
+
+def test_chunked_under_budget_keeps_everything():
+    rng = np.random.default_rng(22)
+    q, k, v = _chunks(rng, lens=(20, 30, 10))
+    r = O.prefill_chunked_unit(q, k, v, keep1=64, pool_kernel=5)
+    assert all(h["kept"] is None for h in r["history"]) and [h["held"] for h in r["history"]] == [20, 50, 60]
+    np.testing.assert_array_equal(r["K"], np.concatenate(k, axis=1))
+
+
+def test_chunked_invariants():
+    """The held length never exceeds keep1 after an eviction, the chunk's window is
+    always kept, and the kept indices are ascending."""
+    rng = np.random.default_rng(23)
+    w, keep1 = 8, 64
+    q, k, v = _chunks(rng, w=w, lens=(100, 60, 90, 9))
+    r = O.prefill_chunked_unit(q, k, v, keep1=keep1, pool_kernel=5)
+    held = 0
+    for c, h in enumerate(r["history"]):
+        before = held + k[c].shape[1]
+        if h["kept"] is not None:
+            assert h["held"] == keep1
+            for g in range(2):
+                kept = h["kept"][g]
+                assert np.all(np.diff(kept) > 0)
+                np.testing.assert_array_equal(kept[-w:], np.arange(before - w, before))
+        else:
+            assert h["held"] == before <= keep1
+        held = h["held"]
