@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-decode-steps", type=int, default=0, help="decode steps per oracle sample (0: all)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="repeat the oracle sample until this much CPU time")
+    ap.add_argument("--prefill-chunk", type=int, default=8192,
+                    help="also time a chunked prefill of the same prompts with chunks of about this many tokens "
+                         "(0: skip)")
     ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
     ap.add_argument("--decode-path", choices=["auto", "split", "fused"], default="auto",
                     help="decode implementation: one fused launch per step (auto/fused) or four kernels")
@@ -122,7 +125,7 @@ class Setup:
     """Everything one rank needs for K passes of one workload (layer 0)."""
 
     def __init__(self, wl: W.Workload, rkv, seed: int, dev):
-        self.wl, self.rkv, self.dev = wl, rkv, dev
+        self.wl, self.rkv, self.dev, self.seed = wl, rkv, dev, seed
         self.inp = W.prefill_tensors(wl, seed, 0, dev, tail="zero")
         self.dec = [W.decode_tensors(wl, t, seed, 0, dev) for t in range(wl.steps)]
         for d in self.dec:
@@ -216,6 +219,52 @@ def selection_recall(setup: Setup) -> dict:
                 k_tokens=self_or_range(k_tokens), steps=[0, wl.steps - 1],
                 what="share of the exact top-k_tokens tokens (attention summed over the GQA group) and of their "
                      "attention mass inside the pages HSA selected")
+
+
+def chunked_prefill(setup: Setup, stream, chunk_tokens: int, reps: int) -> dict:
+    """The same prompts prefilled in chunks (rkv_prefill_chunk per chunk, the stage-1
+    budget re-enforced at every chunk), outside the main timed region: one CUDA graph
+    per request, L2 flushed before each replay, 3 untimed replays first."""
+    rkv, wl = setup.rkv, setup.wl
+    plan = W.chunk_plan(wl, chunk_tokens)
+    chunks = [W.chunk_tensors(wl, setup.inp, plan, c, setup.seed, 0, setup.dev) for c in range(len(plan))]
+    cache = rkv.PagedCache(wl.B, wl.Hkv, wl.page_size, setup.cache.max_pages, setup.dev,
+                           page_table=setup.cache.page_table)
+    kept = torch.empty_like(setup.kept)
+    held = [[0] * wl.B]
+    for c in range(len(plan)):
+        held.append([min(k, h + m) for k, h, m in zip(setup.keep1, held[c], plan[c])])
+    total = max(h + m for c in range(len(plan)) for h, m in zip(held[c], plan[c]))
+    ws = rkv.prefill_chunk_workspace(wl.B, wl.Hq, wl.Hkv, wl.window, total, setup.dev)
+
+    def run():
+        cache.seq_len.zero_()
+        for c, ch in enumerate(chunks):
+            rkv.rkv_prefill_chunk(ch["q_win"], ch["k"], ch["v"], ch["chunk_len"], held[c], setup.keep1, setup.kp,
+                                  cache, kept, workspace=ws)
+
+    run()
+    torch.cuda.synchronize()
+    st, bits = rkv.rkv_get_device_status(cache, stream)
+    if st != rkv.RKV_OK or cache.seq_len.tolist() != held[-1]:
+        raise RuntimeError(f"chunked prefill: device status {st} bits {bits}")
+    n0 = rkv.rkv_launch_count()
+    g = capture(run, stream)
+    launches = rkv.rkv_launch_count() - n0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for i in range(reps + 3):
+        setup.flush()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        stream.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    return dict(chunk_tokens=chunk_tokens, chunks=len(plan), chunk_len=self_or_range([m for p in plan for m in p]),
+                ms=round(statistics.mean(times), 4), launches=launches, replays=reps,
+                what="whole request: every chunk gathered with the survivors, scored, re-evicted to keep1 and "
+                     "written back to the pages")
 
 
 def capture(fn, stream) -> torch.cuda.CUDAGraph:
@@ -403,6 +452,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]),
     )
     res["selection"] = selection_recall(setup)
+    if args.prefill_chunk > 0:
+        res["chunked_prefill"] = chunked_prefill(setup, stream, args.prefill_chunk, max(args.steps, 3))
     if rank == 0 and not args.no_e2e:
         res["e2e"] = run_e2e(setup, args, stream, rkv)
     if rank == 0 and not args.no_cpu_baseline:

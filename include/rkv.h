@@ -58,6 +58,7 @@ typedef enum {
 #define RKV_DEVERR_PAGE_ID   0x1  /* page_table entry outside [0, num_phys_pages) */
 #define RKV_DEVERR_CAPACITY  0x2  /* seq_len (+ appended tokens) beyond max_pages * page_size */
 #define RKV_DEVERR_TIMEOUT   0x4  /* a bounded wait on an mbarrier ran out */
+#define RKV_DEVERR_SEQ_LEN   0x8  /* device seq_len differs from the held_len the host passed */
 
 #define RKV_HEAD_DIM 128
 #define RKV_MAX_BATCH 256
@@ -170,6 +171,41 @@ rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv
                              const rkv_cache* cache, int32_t* kept_idx, int32_t kept_stride,
                              float* pooled_scores, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/* Bytes of workspace rkv_prefill_chunk needs when held_len[b] + chunk_len[b] <= max_total_len. */
+size_t rkv_prefill_chunk_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t window,
+                                        int32_t max_total_len);
+
+/*
+ * Stage 1 over a prompt that arrives in chunks, the budget re-enforced at every
+ * chunk ([adapted], "Evidence": stage-1 eviction holds its budget across
+ * chunked-prefill calls).  Reading taken: the chunk's tokens join the n_b =
+ * held_len[b] + chunk_len[b] tokens held so far (the cache's tokens first, in
+ * cache order), and SnapKV++ as in rkv_prefill_evict runs over that sequence with
+ * prompt_len = n_b and keep1 = min(keep1[b], n_b), the chunk's last `window` queries
+ * being the observation window.  The survivors are written back to the cache's
+ * pages from position 0, their summaries rebuilt, seq_len[b] = min(keep1[b], n_b).
+ * A sequence with n_b <= keep1[b] keeps everything; when that holds for every b the
+ * scoring is skipped.  Start from an empty cache (seq_len 0) for the first chunk.
+ *   q_win    : device [B][Hq][window][128] bf16, the chunk's last `window` queries.
+ *   k_chunk, v_chunk : device [B][Hkv][chunk_max][128] bf16; rows >= chunk_len[b]
+ *              are never read.
+ *   chunk_len, held_len, keep1, pool_kernel : host [B]; window <= chunk_len[b] <=
+ *              chunk_max; held_len[b] must equal the cache's seq_len[b] (the device
+ *              checks it: a mismatch sets RKV_DEVERR_SEQ_LEN); keep1[b] >= window.
+ *   cache    : read (the held tokens) and rewritten in place; the held tokens are
+ *              copied to the workspace before any page is written.
+ *   kept_idx : device [B][Hkv][kept_stride] int32, receives the kept positions of
+ *              the n_b-token sequence, ascending.
+ *   workspace: rkv_prefill_chunk_workspace_size(B, Hq, Hkv, window, max_b n_b)
+ *              bytes or more.
+ */
+rkv_status rkv_prefill_chunk(const rkv_bf16* q_win, const rkv_bf16* k_chunk, const rkv_bf16* v_chunk,
+                             int32_t B, int32_t Hq, int32_t window, int32_t chunk_max,
+                             const int32_t* chunk_len, const int32_t* held_len,
+                             const int32_t* keep1, const int32_t* pool_kernel, float scale,
+                             const rkv_cache* cache, int32_t* kept_idx, int32_t kept_stride,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Append n_new tokens to every sequence and bring the page summaries up to date

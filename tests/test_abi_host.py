@@ -172,3 +172,35 @@ def test_host_split_mt_matches_oracle(rkv, L, budget, P):
         assert got[key] == ref[key], key
     for key in ("c", "r", "c1", "c2"):
         assert abs(got[key] - ref[key]) <= 1e-12 * max(1.0, abs(ref[key])), key
+
+
+def test_prefill_chunk_rejects_bad_arguments_without_launching(rkv):
+    lib = rkv.lib()
+    cache = _fake_cache(rkv)
+    i32 = ctypes.c_int32 * 2
+
+    def call(m=(300, 100), held=(0, 0), keep=(200, 200), kp=(7, 7), w=32, Hq=8, stride=256, chunk_max=512,
+             ws=None):
+        if ws is None:
+            total = max(h + c for h, c in zip(held, m))
+            ws = lib.rkv_prefill_chunk_workspace_size(2, Hq, 2, w, total)
+        return lib.rkv_prefill_chunk(ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000), ctypes.c_void_p(0x300000),
+                                     2, Hq, w, chunk_max, i32(*m), i32(*held), i32(*keep), i32(*kp),
+                                     ctypes.c_float(0.088), ctypes.byref(cache), ctypes.c_void_p(0x400000), stride,
+                                     ctypes.c_void_p(0x500000), ws, None)
+
+    before = rkv.rkv_launch_count()
+    assert call(m=(20, 100)) == rkv.RKV_ERR_INVALID_ARG             # chunk shorter than the window
+    assert call(m=(513, 100)) == rkv.RKV_ERR_INVALID_ARG            # longer than chunk_max
+    assert call(held=(-1, 0)) == rkv.RKV_ERR_INVALID_ARG            # negative held length
+    assert call(held=(1025, 0)) == rkv.RKV_ERR_INVALID_ARG          # more held than the pages hold
+    assert call(keep=(20, 200)) == rkv.RKV_ERR_INVALID_ARG          # keep1 < window
+    assert call(keep=(2000, 200), held=(1000, 0)) == rkv.RKV_ERR_INVALID_ARG   # survivors beyond capacity
+    assert call(stride=150) == rkv.RKV_ERR_INVALID_ARG              # kept_stride < min(keep1, held + chunk)
+    assert call(kp=(8, 7)) == rkv.RKV_ERR_INVALID_ARG               # even pooling kernel
+    assert call(w=33) == rkv.RKV_ERR_UNSUPPORTED                    # G*w > 128
+    need = lib.rkv_prefill_chunk_workspace_size(2, 8, 2, 32, 300)
+    assert call(ws=need - 16) == rkv.RKV_ERR_WORKSPACE
+    # the chunked workspace adds the gathered K and V to the single-shot one
+    assert lib.rkv_prefill_chunk_workspace_size(2, 8, 2, 32, 300) > lib.rkv_prefill_workspace_size(2, 8, 2, 32, 300)
+    assert rkv.rkv_launch_count() == before

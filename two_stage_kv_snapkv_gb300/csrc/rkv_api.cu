@@ -114,7 +114,8 @@ const char* kernel_name(int kind) {
   static const char* names[K_NUM_KINDS] = {
       "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
       "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
-      "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step",     "recall"};
+      "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step",     "recall",
+      "chunk_gather"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
 }
 
@@ -301,6 +302,68 @@ rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
   return cuda_status(rkv::launch_prefill(a, static_cast<cudaStream_t>(stream)), "rkv_prefill_evict launch");
+}
+
+size_t rkv_prefill_chunk_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t window, int32_t max_total_len) {
+  if (B < 1 || Hkv < 1 || max_total_len < 1) return 0;
+  return rkv::prefill_chunk_ws_bytes(B, Hq, Hkv, window, max_total_len);
+}
+
+rkv_status rkv_prefill_chunk(const rkv_bf16* q_win, const rkv_bf16* k_chunk, const rkv_bf16* v_chunk, int32_t B,
+                             int32_t Hq, int32_t window, int32_t chunk_max, const int32_t* chunk_len,
+                             const int32_t* held_len, const int32_t* keep1, const int32_t* pool_kernel, float scale,
+                             const rkv_cache* cache, int32_t* kept_idx, int32_t kept_stride, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
+  if (B != cache->B) return fail(RKV_ERR_INVALID_ARG, "B=%d differs from cache B=%d", B, cache->B);
+  if (!q_win || !k_chunk || !v_chunk || !kept_idx || !chunk_len || !held_len || !keep1 || !pool_kernel || !workspace)
+    return fail(RKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!al16(q_win) || !al16(k_chunk) || !al16(v_chunk) || !al16(kept_idx) || !al16(workspace))
+    return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  const int G = Hq / cache->Hkv;
+  if (window < 1 || G * window > 128)
+    return fail(RKV_ERR_UNSUPPORTED, "window=%d: need 1 <= G*window <= 128 (G=%d)", window, G);
+  if (chunk_max < 1) return fail(RKV_ERR_INVALID_ARG, "chunk_max=%d", chunk_max);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
+  const long long cap = (long long)cache->max_pages * cache->page_size;
+  long long Lc = 1;
+  for (int b = 0; b < B; ++b) {
+    const int m = chunk_len[b], h = held_len[b], kk = keep1[b], kp = pool_kernel[b];
+    if (m < window || m > chunk_max)
+      return fail(RKV_ERR_INVALID_ARG, "chunk_len[%d]=%d outside [window, chunk_max]", b, m);
+    if (h < 0 || h > cap) return fail(RKV_ERR_INVALID_ARG, "held_len[%d]=%d outside [0, cache capacity]", b, h);
+    if (kk < window) return fail(RKV_ERR_INVALID_ARG, "keep1[%d]=%d below window", b, kk);
+    const long long n = (long long)h + m, keep = kk < n ? kk : n;
+    if (n > INT32_MAX / 2) return fail(RKV_ERR_INVALID_ARG, "held_len[%d] + chunk_len[%d] too large", b, b);
+    if (keep > cap) return fail(RKV_ERR_INVALID_ARG, "keep1[%d]=%d exceeds the cache capacity", b, kk);
+    if (keep > kept_stride) return fail(RKV_ERR_INVALID_ARG, "kept_stride=%d < %lld kept in sequence %d", kept_stride, keep, b);
+    if (kp < 1 || kp > 255 || kp % 2 == 0)
+      return fail(RKV_ERR_INVALID_ARG, "pool_kernel[%d]=%d must be odd in [1, 255]", b, kp);
+    Lc = n > Lc ? n : Lc;
+  }
+  const size_t need = rkv::prefill_chunk_ws_bytes(B, Hq, cache->Hkv, window, (int)Lc);
+  if (workspace_bytes < need)
+    return fail(RKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  rkv::PrefillChunkArgs a;
+  a.q_win = q_win;
+  a.k_chunk = k_chunk;
+  a.v_chunk = v_chunk;
+  a.Hq = Hq;
+  a.w = window;
+  a.chunk_max = chunk_max;
+  a.chunk_len = chunk_len;
+  a.held_len = held_len;
+  a.keep1 = keep1;
+  a.pool_kernel = pool_kernel;
+  a.scale = scale;
+  a.cache = *cache;
+  a.kept_idx = kept_idx;
+  a.kept_stride = kept_stride;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  return cuda_status(rkv::launch_prefill_chunk(a, static_cast<cudaStream_t>(stream)), "rkv_prefill_chunk launch");
 }
 
 rkv_status rkv_append_page_summary(const rkv_cache* cache, const rkv_bf16* k_new, const rkv_bf16* v_new,

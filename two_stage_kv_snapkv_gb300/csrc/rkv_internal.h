@@ -27,6 +27,7 @@ enum KernelKind {
   K_HSA_COMBINE,
   K_HSA_STEP,
   K_RECALL,
+  K_CHUNK_GATHER,
   K_NUM_KINDS
 };
 const char* kernel_name(int kind);
@@ -66,6 +67,26 @@ struct PrefillArgs {
 };
 size_t prefill_ws_bytes(int B, int Hq, int Hkv, int w, int Lmax);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+// Chunked prefill: the held survivors plus one chunk, re-evicted to keep1.
+struct PrefillChunkArgs {
+  const rkv_bf16* q_win;    // [B][Hq][w][128]: the chunk's last w queries
+  const rkv_bf16* k_chunk;  // [B][Hkv][chunk_max][128]
+  const rkv_bf16* v_chunk;
+  int Hq, w, chunk_max;
+  const int32_t* chunk_len;   // host [B]
+  const int32_t* held_len;    // host [B]
+  const int32_t* keep1;       // host [B]
+  const int32_t* pool_kernel; // host [B]
+  float scale;
+  rkv_cache cache;
+  int32_t* kept_idx;
+  int kept_stride;
+  void* ws;
+  size_t ws_bytes;
+};
+size_t prefill_chunk_ws_bytes(int B, int Hq, int Hkv, int w, int Lc);
+cudaError_t launch_prefill_chunk(const PrefillChunkArgs& a, cudaStream_t s);
 
 // --------------------------------------------------------------- decode
 enum DecodePath { DECODE_AUTO = 0, DECODE_SPLIT = 1, DECODE_FUSED = 2 };

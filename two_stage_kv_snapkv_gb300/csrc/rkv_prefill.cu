@@ -846,4 +846,113 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// --------------------------------------------------------------------------
+// Chunked prefill: the held survivors (read through the page table) and the new
+// chunk, back to back into contiguous [B][Hkv][Lc][128] K and V in the workspace, so
+// the stage-1 pipeline above can run over them.  grid (ceil(Lc / 16), Hkv, B), 256
+// threads: 16 rows x 16 pieces of 16 bytes per pass.
+struct GatherParams {
+  const rkv_bf16* k_pages;
+  const rkv_bf16* v_pages;
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  int32_t* err;
+  const rkv_bf16* k_chunk;
+  const rkv_bf16* v_chunk;
+  rkv_bf16* k_out;
+  rkv_bf16* v_out;
+  int Hkv, P, max_pages, num_phys, chunk_max, Lc;
+  int32_t held[RKV_MAX_BATCH];
+  int32_t chunk[RKV_MAX_BATCH];
+};
+
+__global__ void __launch_bounds__(256) chunk_gather_kernel(const __grid_constant__ GatherParams p) {
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int held = p.held[b], n = held + p.chunk[b];
+  if (blockIdx.x == 0 && g == 0 && threadIdx.x == 0 && p.seq_len[b] != held) flag_error(p.err, RKV_DEVERR_SEQ_LEN);
+  const int t = blockIdx.x * 16 + (threadIdx.x >> 4), piece = threadIdx.x & 15;
+  if (t >= n) return;
+  const rkv_bf16 *ks, *vs;
+  if (t < held) {
+    const int phys = p.page_table[(size_t)b * p.max_pages + t / p.P];
+    if (phys < 0 || phys >= p.num_phys) {
+      if (piece == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
+      return;
+    }
+    const size_t row = (((size_t)phys * p.Hkv + g) * p.P + t % p.P) * 128;
+    ks = p.k_pages + row;
+    vs = p.v_pages + row;
+  } else {
+    const size_t row = (((size_t)b * p.Hkv + g) * p.chunk_max + (t - held)) * 128;
+    ks = p.k_chunk + row;
+    vs = p.v_chunk + row;
+  }
+  const size_t dst = (((size_t)b * p.Hkv + g) * p.Lc + t) * 128 + piece * 8;
+  *reinterpret_cast<uint4*>(p.k_out + dst) = reinterpret_cast<const uint4*>(ks)[piece];
+  *reinterpret_cast<uint4*>(p.v_out + dst) = reinterpret_cast<const uint4*>(vs)[piece];
+}
+
+size_t prefill_chunk_ws_bytes(int B, int Hq, int Hkv, int w, int Lc) {
+  return 2 * align256((size_t)B * Hkv * Lc * 128 * 2) + prefill_ws_bytes(B, Hq, Hkv, w, Lc);
+}
+
+cudaError_t launch_prefill_chunk(const PrefillChunkArgs& a, cudaStream_t s) {
+  const rkv_cache& c = a.cache;
+  int Lc = 1;
+  int32_t n[RKV_MAX_BATCH], keep[RKV_MAX_BATCH];
+  for (int b = 0; b < c.B; ++b) {
+    n[b] = a.held_len[b] + a.chunk_len[b];
+    keep[b] = a.keep1[b] < n[b] ? a.keep1[b] : n[b];
+    Lc = n[b] > Lc ? n[b] : Lc;
+  }
+  uint8_t* w = static_cast<uint8_t*>(a.ws);
+  const size_t kv_bytes = align256((size_t)c.B * c.Hkv * Lc * 128 * 2);
+  GatherParams gp;
+  gp.k_pages = c.k_pages;
+  gp.v_pages = c.v_pages;
+  gp.page_table = c.page_table;
+  gp.seq_len = c.seq_len;
+  gp.err = c.error_word;
+  gp.k_chunk = a.k_chunk;
+  gp.v_chunk = a.v_chunk;
+  gp.k_out = reinterpret_cast<rkv_bf16*>(w);
+  gp.v_out = reinterpret_cast<rkv_bf16*>(w + kv_bytes);
+  gp.Hkv = c.Hkv;
+  gp.P = c.page_size;
+  gp.max_pages = c.max_pages;
+  gp.num_phys = c.num_phys_pages;
+  gp.chunk_max = a.chunk_max;
+  gp.Lc = Lc;
+  for (int b = 0; b < c.B; ++b) {
+    gp.held[b] = a.held_len[b];
+    gp.chunk[b] = a.chunk_len[b];
+  }
+  launch_begin(K_CHUNK_GATHER, s);
+  chunk_gather_kernel<<<dim3((Lc + 15) / 16, c.Hkv, c.B), 256, 0, s>>>(gp);
+  launch_end(K_CHUNK_GATHER, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  PrefillArgs pa;
+  pa.q_win = a.q_win;
+  pa.k = gp.k_out;
+  pa.v = gp.v_out;
+  pa.B = c.B;
+  pa.Hq = a.Hq;
+  pa.Hkv = c.Hkv;
+  pa.G = a.Hq / c.Hkv;
+  pa.w = a.w;
+  pa.Lmax = Lc;
+  pa.prompt_len = n;
+  pa.keep1 = keep;
+  pa.pool_kernel = a.pool_kernel;
+  pa.scale = a.scale;
+  pa.cache = c;
+  pa.kept_idx = a.kept_idx;
+  pa.kept_stride = a.kept_stride;
+  pa.pooled_out = nullptr;
+  pa.ws = w + 2 * kv_bytes;
+  pa.ws_bytes = a.ws_bytes - 2 * kv_bytes;
+  return launch_prefill(pa, s);
+}
+
 }  // namespace rkv

@@ -25,6 +25,7 @@ RKV_ERR_TIMEOUT = 6
 DEVERR_PAGE_ID = 0x1
 DEVERR_CAPACITY = 0x2
 DEVERR_TIMEOUT = 0x4
+DEVERR_SEQ_LEN = 0x8
 HEAD_DIM = 128
 MAX_BATCH = 256
 
@@ -70,6 +71,11 @@ _lib.rkv_prefill_workspace_size.restype = _sz
 _lib.rkv_prefill_evict.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32p, _i32p, _i32p, _f32,
                                    ctypes.POINTER(RkvCacheStruct), _vp, _i32, _vp, _vp, _sz, _vp]
 _lib.rkv_prefill_evict.restype = _i32
+_lib.rkv_prefill_chunk_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.rkv_prefill_chunk_workspace_size.restype = _sz
+_lib.rkv_prefill_chunk.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32p, _i32p, _i32p, _i32p, _f32,
+                                   ctypes.POINTER(RkvCacheStruct), _vp, _i32, _vp, _sz, _vp]
+_lib.rkv_prefill_chunk.restype = _i32
 _lib.rkv_append_page_summary.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _vp, _i32, _vp]
 _lib.rkv_append_page_summary.restype = _i32
 _lib.rkv_decode_workspace_size.argtypes = [_i32, _i32, _i32, _i32]
@@ -105,7 +111,8 @@ _lib.rkv_profile_release.restype = None
 _lib.rkv_profile_read.argtypes = [_i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)]
 _lib.rkv_profile_read.restype = ctypes.c_char_p
 
-EXPORTED = ["rkv_split_ratio", "rkv_split_ratio_mt", "rkv_prefill_workspace_size", "rkv_prefill_evict", "rkv_append_page_summary",
+EXPORTED = ["rkv_split_ratio", "rkv_split_ratio_mt", "rkv_prefill_workspace_size", "rkv_prefill_evict",
+            "rkv_prefill_chunk_workspace_size", "rkv_prefill_chunk", "rkv_append_page_summary",
             "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
             "rkv_decode_path", "rkv_exact_topk_recall", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
@@ -234,6 +241,30 @@ def rkv_prefill_evict(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pro
                                   _host_i32(keep1), _host_i32(pool_kernel), scale, ctypes.byref(cache.struct),
                                   _ptr(kept_idx), kept_idx.shape[-1], _ptr(pooled_scores), _ptr(workspace),
                                   workspace.numel(), _stream(stream)))
+
+
+def prefill_chunk_workspace(B: int, Hq: int, Hkv: int, window: int, max_total_len: int,
+                            device="cuda") -> torch.Tensor:
+    n = _lib.rkv_prefill_chunk_workspace_size(B, Hq, Hkv, window, max_total_len)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def rkv_prefill_chunk(q_win: torch.Tensor, k_chunk: torch.Tensor, v_chunk: torch.Tensor, chunk_len: Sequence[int],
+                      held_len: Sequence[int], keep1: Sequence[int], pool_kernel: Sequence[int], cache: PagedCache,
+                      kept_idx: torch.Tensor, scale: Optional[float] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """One chunk of a chunked prefill; held_len is the cache's seq_len before the call."""
+    B, Hq, w, d = q_win.shape
+    chunk_max = k_chunk.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        total = max(int(h) + int(m) for h, m in zip(held_len, chunk_len))
+        workspace = prefill_chunk_workspace(B, Hq, cache.Hkv, w, total, q_win.device)
+    _check(_lib.rkv_prefill_chunk(_ptr(q_win), _ptr(k_chunk), _ptr(v_chunk), B, Hq, w, chunk_max,
+                                  _host_i32(chunk_len), _host_i32(held_len), _host_i32(keep1),
+                                  _host_i32(pool_kernel), scale, ctypes.byref(cache.struct), _ptr(kept_idx),
+                                  kept_idx.shape[-1], _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def rkv_append_page_summary(cache: PagedCache, k_new: Optional[torch.Tensor] = None,

@@ -200,6 +200,40 @@ def prefill_tensors(wl: Workload, seed: int = 0x5EED, layer: int = 0, device="cp
                 prompt_len=list(wl.prompt_lens))
 
 
+def chunk_plan(wl: Workload, chunk_tokens: int) -> list:
+    """Chunk lengths for a chunked prefill of the workload's prompts: [chunk][b].
+
+    Every prompt is cut into the same number of near-equal chunks, ceil(Lmax /
+    chunk_tokens) of them, fewer where a chunk would be shorter than the window.
+    """
+    nc = max(1, -(-wl.Lmax // chunk_tokens))
+    while nc > 1 and min(wl.prompt_lens) // nc < wl.window:
+        nc -= 1
+    bounds = [[(L * i) // nc for i in range(nc + 1)] for L in wl.prompt_lens]
+    return [[bb[c + 1] - bb[c] for bb in bounds] for c in range(nc)]
+
+
+def chunk_tensors(wl: Workload, prompt: dict, plan: list, c: int, seed: int = 0x5EED, layer: int = 0,
+                  device="cpu") -> dict:
+    """Chunk c of a chunked prefill: its keys and values cut from the prompt's
+    ([B,Hkv,max chunk,d], zero-padded), and its observation window -- the prompt's
+    own for the last chunk, fresh seeded queries for the others."""
+    B, Hkv, d = wl.B, wl.Hkv, wl.d
+    cmax = max(plan[c])
+    k = torch.zeros((B, Hkv, cmax, d), dtype=torch.bfloat16, device=device)
+    v = torch.zeros_like(k)
+    for b in range(B):
+        s = sum(plan[i][b] for i in range(c))
+        m = plan[c][b]
+        k[b, :, :m] = prompt["k"][b, :, s:s + m]
+        v[b, :, :m] = prompt["v"][b, :, s:s + m]
+    if c == len(plan) - 1:
+        q = prompt["q_win"]
+    else:
+        q = normal((B, wl.Hq, wl.window, d), seed_for(seed, layer, "q_win_chunk", c), device)
+    return dict(q_win=q, k=k, v=v, chunk_len=list(plan[c]))
+
+
 def decode_tensors(wl: Workload, step: int, seed: int = 0x5EED, layer: int = 0, device="cpu") -> dict:
     """One decode step's inputs: q [B,Hq,d], k_new / v_new [B,Hkv,d] (bf16)."""
     B, Hq, Hkv, d = wl.B, wl.Hq, wl.Hkv, wl.d
