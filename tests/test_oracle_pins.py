@@ -474,3 +474,33 @@ def test_chunked_invariants():
         else:
             assert h["held"] == before <= keep1
         held = h["held"]
+
+
+def test_chunked_with_no_early_eviction_is_single_shot():
+    """When no chunk but the last one overflows keep1, chunking changes nothing: the
+    result equals one stage-1 eviction over the whole prompt with the last chunk's
+    window."""
+    rng = np.random.default_rng(24)
+    q, k, v = _chunks(rng, lens=(30, 25, 90))
+    r = O.prefill_chunked_unit(q, k, v, keep1=64, pool_kernel=5)
+    assert [h["kept"] is None for h in r["history"]] == [True, True, False]
+    K, V = np.concatenate(k, axis=1), np.concatenate(v, axis=1)
+    ref = O.prefill_evict_unit(q[-1], K, 64, 5)["kept"]
+    for g in range(2):
+        np.testing.assert_array_equal(r["K"][g], K[g, ref[g]])
+        np.testing.assert_array_equal(r["V"][g], V[g, ref[g]])
+
+
+def test_chunked_survivors_keep_prompt_order():
+    """Every held row is a row of the prompt, each at most once, in prompt order; an
+    evicted token never returns."""
+    rng = np.random.default_rng(25)
+    q, k, v = _chunks(rng, lens=(120, 70, 45, 80))
+    r = O.prefill_chunked_unit(q, k, v, keep1=64, pool_kernel=3)
+    K = np.concatenate(k, axis=1)
+    for g in range(2):
+        pos = [int(np.flatnonzero((K[g] == row).all(axis=1))[0]) for row in r["K"][g]]
+        assert np.all(np.diff(pos) > 0)
+        # positions evicted by the first chunk's eviction are gone for good
+        first = set(O.prefill_evict_unit(q[0], k[0], 64, 3)["kept"][g].tolist())
+        assert all(p >= 120 or p in first for p in pos)
