@@ -667,6 +667,75 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   __syncthreads();  // the scratch may be reused right after
 }
 
+// Top-k by counting, for up to a few hundred keys.  Key i's rank is the number of keys that
+// beat it (larger, or equal at a lower index); i is taken iff its rank is below k, so
+// exactly k are taken, ties going to the lower index.  Thread t owns indices t + NT m
+// (m < KPT) and compares them with all n keys, read by broadcast 16-byte loads:
+// n KPT compares per thread and two barriers, against the several barrier-separated
+// passes of the histogram select.  Needs n <= NT KPT and `keys` 16-byte aligned; reads
+// keys[0, n) only.  The ascending list goes to out[0..k).  Every thread calls this.
+template <int NT, int KPT>
+__device__ void topk_rank(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
+  constexpr int NW = NT / 32;
+  static_assert(NT % 32 == 0 && KPT * NW <= kTkBins, "counts must fit the histogram scratch");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* cnt = reinterpret_cast<int*>(ts.hist);
+  const int n4 = n >> 2;
+  uint32_t kv[KPT], km[KPT];
+  int rk[KPT], g4[KPT];
+#pragma unroll
+  for (int m = 0; m < KPT; ++m) {
+    const int i = tid + NT * m;
+    kv[m] = i < n ? keys[i] : 0u;
+    km[m] = kv[m] - 1u;  // j < i beats i iff key_j >= key_i, i.e. key_j > key_i - 1
+    rk[m] = 0;
+    g4[m] = i >> 2;
+  }
+  // whole groups of four: groups below i's own compare against key_i - 1
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+#pragma unroll 4
+  for (int j4 = 0; j4 < n4; ++j4) {
+    const uint4 u = k4[j4];
+#pragma unroll
+    for (int m = 0; m < KPT; ++m) {
+      const uint32_t t = j4 < g4[m] ? km[m] : kv[m];
+      rk[m] += ((u.x > t) + (u.y > t)) + ((u.z > t) + (u.w > t));
+    }
+  }
+  bool taken[KPT];
+#pragma unroll
+  for (int m = 0; m < KPT; ++m) {
+    const int i = tid + NT * m;
+    taken[m] = false;
+    if (i >= n) continue;
+    // key_i = 0: key_i - 1 wrapped, so the groups below i's counted nothing; all beat i
+    if (kv[m] == 0u) rk[m] += 4 * min(g4[m], n4);
+    // i's own group was compared as if it lay above i: add the equal members below i
+    if (g4[m] < n4)
+      for (int j = 4 * g4[m]; j < i; ++j) rk[m] += keys[j] == kv[m];
+    // the last n % 4 keys, one by one
+    for (int j = 4 * n4; j < n; ++j) rk[m] += keys[j] > kv[m] || (keys[j] == kv[m] && j < i);
+    taken[m] = rk[m] < k;
+  }
+  // ascending compaction: index order is (m, warp, lane)
+  unsigned bal[KPT];
+#pragma unroll
+  for (int m = 0; m < KPT; ++m) {
+    bal[m] = __ballot_sync(0xffffffffu, taken[m]);
+    if (lane == 0) cnt[m * NW + warp] = __popc(bal[m]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < KPT; ++m) {
+    if (taken[m]) {
+      int pos = __popc(bal[m] & ((1u << lane) - 1u));
+      for (int q = 0; q < m * NW + warp; ++q) pos += cnt[q];
+      out[pos] = tid + NT * m;
+    }
+  }
+  __syncthreads();  // the list is complete and the scratch may be reused
+}
+
 // topk_regs with the smallest keys-per-thread count that covers n (n <= 32 NT).
 template <int NT>
 __device__ void topk_regs_any(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
