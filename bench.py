@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--prefill-chunk", type=int, default=8192,
                     help="also time a chunked prefill of the same prompts with chunks of about this many tokens "
                          "(0: skip)")
+    ap.add_argument("--one-layer", action="store_true", help="run only layer 0 of a multi-layer workload")
     ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
     ap.add_argument("--decode-path", choices=["auto", "split", "fused"], default="auto",
                     help="decode implementation: one fused launch per step (auto/fused) or four kernels")
@@ -124,10 +125,10 @@ class ClockSampler:
 class Setup:
     """Everything one rank needs for K passes of one workload (layer 0)."""
 
-    def __init__(self, wl: W.Workload, rkv, seed: int, dev):
-        self.wl, self.rkv, self.dev, self.seed = wl, rkv, dev, seed
-        self.inp = W.prefill_tensors(wl, seed, 0, dev, tail="zero")
-        self.dec = [W.decode_tensors(wl, t, seed, 0, dev) for t in range(wl.steps)]
+    def __init__(self, wl: W.Workload, rkv, seed: int, dev, layer: int = 0, share: "Setup | None" = None):
+        self.wl, self.rkv, self.dev, self.seed, self.layer = wl, rkv, dev, seed, layer
+        self.inp = W.prefill_tensors(wl, seed, layer, dev, tail="zero")
+        self.dec = [W.decode_tensors(wl, t, seed, layer, dev) for t in range(wl.steps)]
         for d in self.dec:
             d["k_new"] = d["k_new"].unsqueeze(2).contiguous()
             d["v_new"] = d["v_new"].unsqueeze(2).contiguous()
@@ -150,10 +151,11 @@ class Setup:
         pt = W.page_table(wl.B, max_pages, seed, dev)
         self.cache = rkv.PagedCache(wl.B, wl.Hkv, P, max_pages, dev, page_table=pt)
         self.kept = torch.empty((wl.B, wl.Hkv, max(self.keep1)), dtype=torch.int32, device=dev)
-        self.pws = rkv.prefill_workspace(wl.B, wl.Hq, wl.Hkv, wl.window, wl.Lmax, dev)
-        self.dws = rkv.decode_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, dev)
+        # layers run one after another on one stream, so they can share the scratch
+        self.pws = share.pws if share else rkv.prefill_workspace(wl.B, wl.Hq, wl.Hkv, wl.window, wl.Lmax, dev)
+        self.dws = share.dws if share else rkv.decode_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, dev)
         self.out = torch.empty((wl.steps, wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
-        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.flush_buf = share.flush_buf if share else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     # one call each, on the current stream
     def prefill(self):
@@ -330,18 +332,33 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
 
     wl = W.workload(args.workload, args.seed)
     rkv.rkv_decode_path({"auto": 0, "split": 1, "fused": 2}[args.decode_path])
-    setup = Setup(wl, rkv, rank_seed(args.seed, rank), dev)
+    seed = rank_seed(args.seed, rank)
+    nl = 1 if args.one_layer else wl.layers
+    setup = Setup(wl, rkv, seed, dev)
+    # a multi-layer workload keeps every layer resident: stage 1 for all of them, then
+    # each decode step runs HSA for every layer in turn, as a model's decode step does
+    layers = [setup] + [Setup(wl, rkv, seed, dev, layer=l, share=setup) for l in range(1, nl)]
+    multi = nl > 1
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
 
+    def prefill_all():
+        for s in layers:
+            s.prefill()
+
+    def decode_all(t: int):
+        for s in layers:
+            s.decode(t)
+
     # eager warm-up (sets kernel attributes, checks the path runs)
-    setup.prefill()
+    prefill_all()
     for t in range(wl.steps):
-        setup.decode(t)
+        decode_all(t)
     torch.cuda.synchronize()
-    st, bits = rkv.rkv_get_device_status(setup.cache, stream)
-    if st != rkv.RKV_OK:
-        raise RuntimeError(f"device status {st} bits {bits}")
+    for s in layers:
+        st, bits = rkv.rkv_get_device_status(s.cache, stream)
+        if st != rkv.RKV_OK:
+            raise RuntimeError(f"layer {s.layer}: device status {st} bits {bits}")
 
     if args.ncu:
         setup.prefill()
@@ -350,15 +367,17 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         torch.cuda.synchronize()
         return {}
 
-    # graphs: one for the prefill, one per decode step
+    # graphs: one for the prefill (every layer), one per decode step (every layer)
     n0 = rkv.rkv_launch_count()
-    g_pre = capture(setup.prefill, stream)
-    g_dec = [capture(lambda t=t: setup.decode(t), stream) for t in range(wl.steps)]
+    g_pre = capture(prefill_all, stream)
+    n1 = rkv.rkv_launch_count()
+    g_dec = [capture(lambda t=t: decode_all(t), stream) for t in range(wl.steps)]
     launches_per_pass = rkv.rkv_launch_count() - n0
+    launches_per_step = (rkv.rkv_launch_count() - n1) / wl.steps
     # instrumented copies: library events around every kernel launch
     rkv.profile_enable(True)
-    gi_pre = capture(setup.prefill, stream)
-    gi_dec = [capture(lambda t=t: setup.decode(t), stream) for t in range(wl.steps)]
+    gi_pre = capture(prefill_all, stream)
+    gi_dec = [capture(lambda t=t: decode_all(t), stream) for t in range(wl.steps)]
     rkv.profile_enable(False)
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (wl.steps + 1))]
@@ -369,7 +388,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         pre.replay()
         ev[1].record(stream)
         for t in range(wl.steps):
-            setup.flush()
+            if not multi:   # one layer: every step starts cold; several: the other layers evict it
+                setup.flush()
             ev[2 + 2 * t].record(stream)
             dec[t].replay()
             ev[3 + 2 * t].record(stream)
@@ -394,7 +414,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         torch.distributed.barrier()
     clocks = clk.summary()
     pass_ms = [p + sum(d) for p, d in zip(pre_all, dec_all)]
-    total_ms, value = whole_job_value(sum(pass_ms), wl.steps, args.steps, world, dev)
+    total_ms, value = whole_job_value(sum(pass_ms), wl.steps * nl, args.steps, world, dev)
 
     # per-kernel durations from the instrumented graphs (same work, same flushes)
     rkv.profile_reset()
@@ -403,7 +423,6 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         rkv.profile_accumulate()
     prof = {k: v for k, v in rkv.profile_read().items() if v[0] > 0}
     rkv.profile_release()
-    dominant = max(prof, key=lambda k: prof[k][1])
 
     peaks = measured_peaks()
     step_bytes = [setup.decode_bytes(t) for t in range(wl.steps)]
@@ -422,6 +441,17 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         ab = algo_bytes(k)
         kernels[k] = dict(launches=n, avg_us=round(avg_ms * 1e3, 3), share=round(ms / sum(v[1] for v in prof.values()), 4),
                           algo_bytes=ab, achieved_gbs=(round(ab / (avg_ms * 1e-3) / 1e9, 1) if ab else None))
+    dec_mean_ms = statistics.mean(x for d in dec_all for x in d) / nl   # one layer's decode step
+    if multi and launches_per_step == nl and "hsa_step" in kernels:
+        # the decode graphs hold only hsa_step launches, back to back: their event time
+        # divided by the launches is the kernel's own average duration, which the event
+        # nodes of the instrumented copy (one per launch) would serialise and inflate
+        hk = kernels["hsa_step"]
+        hk["avg_us_instrumented"] = hk["avg_us"]
+        hk["avg_us"] = round(dec_mean_ms * 1e3, 3)
+        hk["achieved_gbs"] = round(hk["algo_bytes"] / (dec_mean_ms * 1e-3) / 1e9, 1)
+        hk["duration_from"] = "uninstrumented decode graphs: event time / hsa_step launches"
+    dominant = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches"])
     dk = kernels[dominant]
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -436,26 +466,33 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
                     traffic=traffic, peak_source=peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
                     if peaks["source"] == "measured" else "fallback 6.8 TB/s")
 
-    dec_mean_ms = statistics.mean(x for d in dec_all for x in d)
     step_total = statistics.mean(sb["step_total"] for sb in step_bytes)
+    pre_layer_ms = statistics.mean(pre_all) / nl
     res = dict(
         metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic (seeded; see DESIGN.md input recipe)",
-        config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world),
-        prefill_evict_ms=round(statistics.mean(pre_all), 4),
+        config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world, nl),
+        prefill_evict_ms=round(pre_layer_ms, 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),
         decode_achieved_gbs=round(step_total / (dec_mean_ms * 1e-3) / 1e9, 1),
         decode_compulsory_mb_per_step=round(step_total / 1e6, 3),
-        prefill_achieved_gbs=round(pb["total"] / (statistics.mean(pre_all) * 1e-3) / 1e9, 1),
+        prefill_achieved_gbs=round(pb["total"] / (pre_layer_ms * 1e-3) / 1e9, 1),
         roofline=roofline, kernels=kernels, gpu_launches=int(launches_per_pass * args.steps),
         clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]),
     )
+    if multi:
+        res["prefill_all_layers_ms"] = round(statistics.mean(pre_all), 4)
+        res["decode_all_layers_us_per_step"] = round(dec_mean_ms * nl * 1e3, 3)
+        res["memory_gb"] = dict(prompt_kv=round(nl * 2 * wl.Hkv * sum(wl.prompt_lens) * 256 / 1e9, 2),
+                                cache_pages=round(sum(s.cache.nbytes() for s in layers) / 1e9, 2))
     res["selection"] = selection_recall(setup)
     if args.prefill_chunk > 0:
         res["chunked_prefill"] = chunked_prefill(setup, stream, args.prefill_chunk, max(args.steps, 3))
     if rank == 0 and not args.no_e2e:
         res["e2e"] = run_e2e(setup, args, stream, rkv)
+        if multi:
+            res["e2e"]["layers"] = 1   # layer 0 alone, through the host buffers
     if rank == 0 and not args.no_cpu_baseline:
         steps = args.cpu_decode_steps or wl.steps
         vals, secs, reps = [], 0.0, 0
@@ -474,16 +511,22 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     return res
 
 
-def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int) -> dict:
+def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int, layers: int = 1) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
+    if layers > 1:
+        step = (f"one request over {layers} layers: split + prefill evict of every layer + every decode step "
+                f"(append + HSA for each layer in turn); value counts layer-steps")
+        l2 = ("flushed (256 MB write) before the prefill; not between decode steps: each step streams "
+              f"{layers} layers' caches, far more than L2, so every layer starts cold; flush not timed")
+    else:
+        step = "one request: split + prefill evict + every decode step (append + HSA)"
+        l2 = "flushed (256 MB write) before the prefill and before every decode step; flush not timed"
     return dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, head_dim=wl.d, prompt_len=wl.prompt_lens[0]
                 if wl.B == 1 else f"{min(wl.prompt_lens)}..{max(wl.prompt_lens)}", budget=wl.budget,
-                window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, keep1=self_or_range(keep1),
-                k1=self_or_range(k1), k2=self_or_range(k2), pool_kernel=self_or_range(kp),
-                split="RocketKV-MT (nothing evicted)" if wl.mt else "two-stage",
-                step="one request: split + prefill evict + every decode step (append + HSA)",
-                l2="flushed (256 MB write) before the prefill and before every decode step; flush not timed",
-                timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
+                window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, layers=layers,
+                keep1=self_or_range(keep1), k1=self_or_range(k1), k2=self_or_range(k2),
+                pool_kernel=self_or_range(kp), split="RocketKV-MT (nothing evicted)" if wl.mt else "two-stage",
+                step=step, l2=l2, timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
                 decode_path=decode_path, parallelism=f"replica x{world}" if world > 1 else "single GPU")
 
 
@@ -599,9 +642,11 @@ def run_reference(args, rank: int, world: int) -> dict:
     return dict(impl="reference", metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(1e3 / value * wl.steps, 3), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)",
-                config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world),
+                config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world,
+                                       wl.layers),
                 cpu_baseline=dict(value=round(value, 3), unit=UNIT, cores=host_cores(), kind="oracle",
-                                  sample=f"per step: oracle prefill of all units + {nsteps} decode steps, "
+                                  sample=f"per step: oracle prefill of all units + {nsteps} decode steps"
+                                         f"{' of layer 0' if wl.layers > 1 else ''}, "
                                          f"extrapolated to the whole request ({secs:.1f} s total)"),
                 e2e=dict(value=round(value, 3), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
