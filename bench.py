@@ -57,6 +57,8 @@ def parse():
                     help="also time a chunked prefill of the same prompts with chunks of about this many tokens "
                          "(0: skip)")
     ap.add_argument("--one-layer", action="store_true", help="run only layer 0 of a multi-layer workload")
+    ap.add_argument("--ncu-every-kernel", action="store_true",
+                    help="one eager launch of every library kernel, no warm-up (for an ncu launch list)")
     ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
     ap.add_argument("--decode-path", choices=["auto", "split", "fused"], default="auto",
                     help="decode implementation: one fused launch per step (auto/fused) or four kernels")
@@ -269,6 +271,40 @@ def chunked_prefill(setup: Setup, stream, chunk_tokens: int, reps: int) -> dict:
                      "written back to the pages")
 
 
+def ncu_every_kernel(setup: Setup) -> None:
+    """One launch of every kernel of the library on this workload, eagerly and with no
+    warm-up, for an ncu launch list with DRAM counters (`--ncu-every-kernel`)."""
+    rkv, wl = setup.rkv, setup.wl
+    setup.prefill()                       # the six stage-1 kernels
+    rkv.rkv_decode_path(2)
+    setup.decode(0)                       # the fused step
+    rkv.rkv_decode_path(1)
+    setup.decode(1)                       # append_small + the four-kernel decode
+    n_new = 2 * wl.page_size
+    kn = W.normal((wl.B, wl.Hkv, n_new, wl.d), W.seed_for(setup.seed, "ncu_append"), setup.dev)
+    rkv.rkv_append_page_summary(setup.cache, kn, kn, n_new)   # append_pages + append_advance
+    stride = max(setup.k2) + 1
+    pg = torch.empty((wl.B, wl.Hkv, stride), dtype=torch.int32, device=setup.dev)
+    d = setup.dec[2]
+    rkv.rkv_decode_hsa(setup.cache, d["q"], setup.k1, setup.k2, setup.out[2], sel_pages=pg, workspace=setup.dws)
+    rkv.rkv_exact_topk_recall(setup.cache, d["q"], pg, [k * wl.page_size for k in setup.k2])
+    rkv.rkv_decode_path(0)
+    plan = W.chunk_plan(wl, 8192)
+    cache = rkv.PagedCache(wl.B, wl.Hkv, wl.page_size, setup.cache.max_pages, setup.dev,
+                           page_table=setup.cache.page_table)
+    held = [0] * wl.B
+    for c in range(min(2, len(plan))):    # chunk_gather + the stage-1 kernels
+        ch = W.chunk_tensors(wl, setup.inp, plan, c, setup.seed, 0, setup.dev)
+        rkv.rkv_prefill_chunk(ch["q_win"], ch["k"], ch["v"], ch["chunk_len"], held, setup.keep1, setup.kp, cache,
+                              setup.kept)
+        held = [min(k, h + m) for k, h, m in zip(setup.keep1, held, plan[c])]
+    torch.cuda.synchronize()
+    for cch in (setup.cache, cache):
+        st, bits = rkv.rkv_get_device_status(cch)
+        if st != rkv.RKV_OK:
+            raise RuntimeError(f"device status {st} bits {bits}")
+
+
 def capture(fn, stream) -> torch.cuda.CUDAGraph:
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -341,6 +377,10 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     multi = nl > 1
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
+
+    if args.ncu_every_kernel:
+        ncu_every_kernel(setup)
+        return {}
 
     def prefill_all():
         for s in layers:

@@ -170,3 +170,60 @@ def test_chunked_prefill_flags_a_stale_held_len(rkv):
     cache = _run_chunks(rkv, case, held_len_offset=16)
     st, bits = rkv.rkv_get_device_status(cache)
     assert st == rkv.RKV_ERR_DEVICE_DATA and bits & rkv.DEVERR_SEQ_LEN
+
+
+def _chunked_full(rkv, n: int, units, chunk_tokens: int = 8192, seed: int = 0x5EED):
+    """A bench workload prefilled in chunks as the bench times it (the same plan, the
+    same launches), with sampled (sequence, KV head) units checked after every chunk."""
+    from rkv_check import splits_for
+    dev = torch.device("cuda")
+    wl = W.workload(n)
+    s = splits_for(wl, rkv)
+    keep1, kp = [x["keep1"] for x in s], [x["pool_kernel"] for x in s]
+    P, G, w = wl.page_size, wl.G, wl.window
+    prompt = W.prefill_tensors(wl, seed, 0, dev, tail="zero")
+    plan = W.chunk_plan(wl, chunk_tokens)
+    max_pages = (max(keep1) + P - 1) // P + 8
+    cache = rkv.PagedCache(wl.B, wl.Hkv, P, max_pages, dev, page_table=W.page_table(wl.B, (max_pages + 7) // 8 * 8,
+                                                                                       seed, dev))
+    kept = torch.full((wl.B, wl.Hkv, max(keep1)), -7, dtype=torch.int32, device=dev)
+    held_len = [0] * wl.B
+    held = {u: (np.zeros((0, 128)), np.zeros((0, 128))) for u in units}
+    for c in range(len(plan)):
+        ch = W.chunk_tensors(wl, prompt, plan, c, seed, 0, dev)
+        rkv.rkv_prefill_chunk(ch["q_win"], ch["k"], ch["v"], ch["chunk_len"], held_len, keep1, kp, cache, kept)
+        for (b, g) in units:
+            m = plan[c][b]
+            K = np.concatenate([held[(b, g)][0], f64(ch["k"][b, g, :m])])
+            V = np.concatenate([held[(b, g)][1], f64(ch["v"][b, g, :m])])
+            nn = K.shape[0]
+            keep = min(keep1[b], nn)
+            got = kept[b, g, :keep].cpu().numpy().astype(np.int64)
+            assert np.all(np.diff(got) > 0)
+            if nn > keep1[b]:
+                ref = O.prefill_evict_unit(f64(ch["q_win"][b, g * G:(g + 1) * G]), K[None], keep1[b], kp[b])
+                np.testing.assert_array_equal(got[keep - w:], np.arange(nn - w, nn))
+                check_topk(got[: keep - w], ref["pooled"][0], keep - w, what=f"chunk {c} unit {(b, g)}")
+            else:
+                np.testing.assert_array_equal(got, np.arange(nn))
+            held[(b, g)] = (K[got], V[got])
+            Kg, Vg = cache.token_kv(b, keep)
+            np.testing.assert_array_equal(f64(Kg[g]), K[got])
+            np.testing.assert_array_equal(f64(Vg[g]), V[got])
+            kmax, kmin = O.page_summaries(K[got], keep, P)
+            NP = kmax.shape[1]
+            np.testing.assert_array_equal(f64(cache.kmax[b, g, :, :NP]), kmax)
+            np.testing.assert_array_equal(f64(cache.kmin[b, g, :, :NP]), kmin)
+        held_len = [min(k, h + m) for k, h, m in zip(keep1, held_len, plan[c])]
+        assert cache.seq_len.tolist() == held_len
+    st, bits = rkv.rkv_get_device_status(cache)
+    assert st == rkv.RKV_OK, bits
+
+
+def test_chunked_workload2_llama_layer_32k(rkv):
+    _chunked_full(rkv, 2, [(0, 0), (0, 5)])
+
+
+def test_chunked_workload4_batched_ragged(rkv):
+    wl = W.workload(4)
+    _chunked_full(rkv, 4, [(int(np.argmax(wl.prompt_lens)), 2), (int(np.argmin(wl.prompt_lens)), 7)])

@@ -526,15 +526,27 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   }
   const int n = n0 + (do_append ? 1 : 0);
   const int NP = (n + P - 1) / P;
+  // 2. barriers (before the length arrives)
+  if (tid == 0) {
+    mbar_init(&sbar, 1);
+    mbar_init(&pbar, 1);
+    fence_mbar_init();
+  }
   // this CTA's slice [p0, p1) of the pages (8-page aligned).  When the summaries of
   // all 128 channels over the slice fit in the region, they are staged right away
-  // (cp.async, 16-byte chunks), while the query arrives and the channels are chosen;
-  // otherwise only the chosen channels' rows are staged, after the select.
+  // (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and the channels are
+  // chosen: rows of 64 pages or more by one bulk copy each (every row starts on a
+  // 16-byte boundary since max_pages and p0 are multiples of 8), shorter ones in
+  // 16-byte cp.async pieces (on GB300 the bulk copies cost 0.6 us more to issue at 32
+  // pages a row and saved about 1 us at 160).  Otherwise only the chosen channels' rows
+  // are staged, after the select.  The page-table row (needed after the select) comes
+  // by bulk copy.
   const int per = ((NP + C - 1) / C + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
   const int slice8 = (p1 - p0 + 7) & ~7;
   const bool all_ch = p1 > p0 && 2 * 128 * slice8 * 2 <= p.region_bytes;
-  if (all_ch) {
+  const bool bulk_rows = all_ch && slice8 >= 64;
+  if (all_ch && !bulk_rows) {
     const int cpr = slice8 >> 3;
     for (int e = tid; e < 256 * cpr; e += kThreads) {
       const int i = e / cpr, c = e - i * cpr;
@@ -543,22 +555,22 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     }
     cp_async_commit();
   }
-
-  // 2. barriers; prefetch of the sequence's page-table row (needed after the select)
-  if (tid == 0) {
-    mbar_init(&sbar, 1);
-    mbar_init(&pbar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
   const int np4 = ((NP + 3) & ~3);  // whole 16-byte groups; within the row (max_pages % 8 == 0)
   if (tid == 0) {
+    if (bulk_rows) mbar_arrive_expect_tx(&sbar, (uint32_t)(256 * slice8 * 2));
     if (np4 > 0) {
       mbar_arrive_expect_tx(&pbar, (uint32_t)np4 * 4);
       bulk_g2s(ptab, p.page_table + (size_t)b * p.max_pages, (uint32_t)np4 * 4, &pbar);
     } else {
       mbar_arrive_expect_tx(&pbar, 0);
     }
+  }
+  __syncthreads();
+  if (bulk_rows) {
+    for (int i = tid; i < 256; i += kThreads)
+      bulk_g2s(ring + (size_t)i * slice8 * 2,
+               (i < 128 ? p.kmax : p.kmin) + ((size_t)unit * 128 + (i & 127)) * p.max_pages + p0,
+               (uint32_t)slice8 * 2, &sbar);
   }
 
   // 3. query of the group and the new token's rows into shared memory
@@ -614,8 +626,9 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     const int cnt = min(tcap, p1 - t0);
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
     __syncthreads();  // the previous tile is consumed
-    if (all_ch) {
-      cp_async_wait<0>();
+    if (all_ch) {  // the one tile, staged at the start
+      if (!bulk_rows) cp_async_wait<0>();
+      else if (!mbar_wait(&sbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
     } else {
       // one bulk copy per row (the rows are long here: the slice did not fit whole)
       fence_proxy_async_smem();
@@ -682,6 +695,12 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   if (!waited) cluster_wait();
   fence_proxy_async_smem();  // generic accesses to the region before the attention's TMA loads
   cluster.sync();            // every CTA holds every page's key
+
+  // the arrival count of sequence b's clusters: every CTA of this cluster has read the
+  // length by now (before its second barrier), so the last cluster of b to count here
+  // may advance seq_len (step 11).  Only the result waits, until the end.
+  int arrivals = -1;
+  if (do_append && rank == 0 && tid == 0) arrivals = atomicAdd(&p.sync[b], 1);
 
   // the append's stores: nothing in this step waits for them
   append_loads();  // (only if this CTA staged no tile)
@@ -767,14 +786,12 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     p.out[((size_t)b * p.Hq + (size_t)g * G + h) * 128 + tid] = L > 0.f ? O / L : 0.f;
   }
 
-  // 11. the last cluster of sequence b to get here advances seq_len (every CTA of every
-  // cluster of b read it at the start, before its cluster's first barrier)
-  if (do_append && rank == 0 && tid == 0) {
-    __threadfence();
-    if (atomicAdd(&p.sync[b], 1) == p.Hkv - 1) {
-      p.sync[b] = 0;
-      p.seq_len[b] = n;
-    }
+  // 11. the last cluster of sequence b to count advances seq_len (every CTA of every
+  // cluster of b read it before that cluster counted); nothing in this launch reads it
+  // again, and the next launch sees it
+  if (arrivals == p.Hkv - 1) {
+    p.sync[b] = 0;
+    p.seq_len[b] = n;
   }
 }
 
