@@ -273,7 +273,9 @@ def chunked_prefill(setup: Setup, stream, chunk_tokens: int, reps: int) -> dict:
 
 def ncu_every_kernel(setup: Setup) -> None:
     """One launch of every kernel of the library on this workload, eagerly and with no
-    warm-up, for an ncu launch list with DRAM counters (`--ncu-every-kernel`)."""
+    warm-up, for an ncu launch list with DRAM counters (`--ncu-every-kernel`): stage 1,
+    the fused and the four-kernel decode steps, a multi-token append, the recall
+    diagnostic, the SparQ-only step and two chunks of a chunked prefill."""
     rkv, wl = setup.rkv, setup.wl
     setup.prefill()                       # the six stage-1 kernels
     rkv.rkv_decode_path(2)
@@ -288,6 +290,8 @@ def ncu_every_kernel(setup: Setup) -> None:
     d = setup.dec[2]
     rkv.rkv_decode_hsa(setup.cache, d["q"], setup.k1, setup.k2, setup.out[2], sel_pages=pg, workspace=setup.dws)
     rkv.rkv_exact_topk_recall(setup.cache, d["q"], pg, [k * wl.page_size for k in setup.k2])
+    if setup.cache.max_pages * wl.page_size <= 32768:   # the token path's limit
+        rkv.rkv_decode_sparq(setup.cache, d["q"], setup.k1, [k * wl.page_size for k in setup.k2], setup.out[2])
     rkv.rkv_decode_path(0)
     plan = W.chunk_plan(wl, 8192)
     cache = rkv.PagedCache(wl.B, wl.Hkv, wl.page_size, setup.cache.max_pages, setup.dev,
@@ -511,7 +515,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     res = dict(
         metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
-        dtype="bf16", data="synthetic (seeded; see DESIGN.md input recipe)",
+        dtype="bf16", data="synthetic (seeded normal bf16 with the workload's shapes, outlier channels, sinks and needles)",
         config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world, nl),
         prefill_evict_ms=round(pre_layer_ms, 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),

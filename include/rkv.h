@@ -299,6 +299,33 @@ rkv_status rkv_decode_hsa_noalloc(const rkv_cache* cache, const rkv_bf16* q, int
                                   int32_t* sel_channels, int32_t* sel_pages,
                                   int32_t sel_pages_stride, void* stream);
 
+/* Bytes of workspace rkv_decode_sparq needs. */
+size_t rkv_sparq_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_pages,
+                                int32_t page_size);
+
+/*
+ * SparQ-only selection: HSA with one-token pages (RocketKV summary, ablation of the
+ * two halves of HSA: SparQ's channel selection alone; "RocketKV-adapted", "Where it
+ * sits -- the mechanism gap": SparQ-style top-magnitude channels along the head
+ * dimension).  Reading taken: with a page of one token, Kmax = Kmin = the key, so the
+ * page bound of rkv_decode_hsa becomes the key's partial dot product over the chosen
+ * channels.  Per sequence b and KV head g, with n = seq_len[b]:
+ *   1. channels S = top-k1[b] of sum over the group's heads of |q_h,i| (ties: lower);
+ *   2. s_t = sum_h sum_{i in S} q_h,i k_t,i for every cached token t < n, read from
+ *      the cache's key rows (any page_size);
+ *   3. tokens = top-min(k_tokens[b], n) by (s_t desc, t asc);
+ *   4. out_h = softmax(q_h . k_t * scale) . v_t over all 128 channels of those tokens.
+ * Arguments as rkv_decode_hsa, with k_tokens (host [B], >= 1) in place of k2 and
+ * sel_tokens (device [B][Hkv][sel_tokens_stride] int32, ascending, then -1 when there
+ * is room; may be NULL) in place of sel_pages.  No append: call
+ * rkv_append_page_summary first.  Caches of more than 32768 tokens per sequence
+ * (max_pages * page_size) return RKV_ERR_UNSUPPORTED.
+ */
+rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
+                            const int32_t* k1, const int32_t* k_tokens, float scale, float* out,
+                            int32_t* sel_channels, int32_t* sel_tokens, int32_t sel_tokens_stride,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * Exact-TopK recall of a page selection: a diagnostic, not a step of the method.
  * The summary page of "RocketKV: Accelerating Long-Context LLM Inference via

@@ -22,7 +22,7 @@ Sources (cited by short name below):
   rocketkv_compression_ratio", "Adaptation notes", "Evidence".
 
 Where the pages leave a step open the plainest reading is taken; each such
-reading is marked READING below and listed in the design doc.
+reading is marked READING below.
 
 Parity status per function (what pins it, in tests/test_oracle_pins.py):
   split_ratio ............ worked example c=64 -> 10.3x / 6.2x, clip ends, c1*c2=c
@@ -38,6 +38,8 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
   page_scores ............ per-token bound (brute force), P=1 closed form
   topk_pages ............. top-k property with planted ties
   sparse_attention ....... k1=d, k2=all pages == torch SDPA (library)
+  sparq_decode_unit ...... token scores == brute-force partial dot products; all
+                           tokens == SDPA; k1=d ranks by the full dot product
   exact_token_scores ..... group sum == G, one-head case == scipy softmax (library)
   exact_topk_recall ...... all pages -> 1, the top-K's own pages -> 1,
                            K >= n closed form, brute force on tiny inputs
@@ -69,6 +71,7 @@ __all__ = [
     "exact_token_scores",
     "exact_topk_recall",
     "hsa_decode_unit",
+    "sparq_decode_unit",
 ]
 
 
@@ -399,6 +402,20 @@ def hsa_decode_unit(q_group: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, n: int,
     use = pages if pages_override is None else np.asarray(pages_override)
     out = sparse_attention(q_group, Kc, Vc, n, use, page_size, scale)
     return dict(channels=chans, channel_score=a, page_score=sig, pages=pages, out=out)
+
+
+def sparq_decode_unit(q_group: np.ndarray, Kc: np.ndarray, Vc: np.ndarray, n: int, k1: int, k_tokens: int,
+                      scale: float | None = None, tokens_override: np.ndarray | None = None) -> dict:
+    """SparQ-only selection: the HSA step with pages of one token.
+
+    [summary] (ablation of HSA's two halves) and [adapted, "Where it sits"]: SparQ
+    picks tokens by the query's top-magnitude channels alone.  READING: HSA with
+    page_size 1, where each page's Kmax and Kmin are its one key, so the bound is the
+    key's partial dot product over the chosen channels; k_tokens whole one-token pages
+    are attended.  Returns the hsa_decode_unit dict, pages being token indices.
+    """
+    kmax, kmin = page_summaries(Kc, n, 1)
+    return hsa_decode_unit(q_group, Kc, Vc, n, kmax, kmin, 1, k1, k_tokens, scale, tokens_override)
 
 
 def exact_token_scores(q_group: np.ndarray, Kc: np.ndarray, n: int, scale: float | None = None) -> np.ndarray:

@@ -204,3 +204,26 @@ def test_prefill_chunk_rejects_bad_arguments_without_launching(rkv):
     # the chunked workspace adds the gathered K and V to the single-shot one
     assert lib.rkv_prefill_chunk_workspace_size(2, 8, 2, 32, 300) > lib.rkv_prefill_workspace_size(2, 8, 2, 32, 300)
     assert rkv.rkv_launch_count() == before
+
+
+def test_sparq_rejects_bad_arguments_without_launching(rkv):
+    lib = rkv.lib()
+    i32 = ctypes.c_int32 * 2
+
+    def call(cache=None, k1=(32, 32), kt=(64, 64), stride=0, ws=None, sel=None):
+        cache = cache or _fake_cache(rkv)
+        if ws is None:
+            ws = lib.rkv_sparq_workspace_size(2, 8, 2, cache.max_pages, cache.page_size)
+        return lib.rkv_decode_sparq(ctypes.byref(cache), ctypes.c_void_p(0x80000), 8, i32(*k1), i32(*kt),
+                                    ctypes.c_float(0.088), ctypes.c_void_p(0x90000), None, sel, stride,
+                                    ctypes.c_void_p(0xA0000), ws, None)
+
+    before = rkv.rkv_launch_count()
+    assert call(k1=(0, 32)) == rkv.RKV_ERR_INVALID_ARG
+    assert call(k1=(129, 32)) == rkv.RKV_ERR_INVALID_ARG
+    assert call(kt=(0, 64)) == rkv.RKV_ERR_INVALID_ARG
+    assert call(sel=ctypes.c_void_p(0xB0000), stride=63) == rkv.RKV_ERR_INVALID_ARG
+    assert call(ws=16) == rkv.RKV_ERR_WORKSPACE
+    assert call(cache=_fake_cache(rkv, max_pages=4096, num_phys_pages=8192)) == rkv.RKV_ERR_UNSUPPORTED  # 64K tokens
+    assert call(cache=_fake_cache(rkv, page_size=8)) == rkv.RKV_ERR_UNSUPPORTED
+    assert rkv.rkv_launch_count() == before

@@ -320,6 +320,48 @@ def test_sparse_attention_on_selected_pages_equals_sdpa():
     np.testing.assert_allclose(out, _sdpa(q, Kc[tok], Vc[tok], 0.3), rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- SparQ-only (one-token pages)
+def test_sparq_scores_are_partial_dot_products():
+    """The token score is the group's partial dot product over the chosen channels,
+    computed here token by token in pure Python."""
+    G, d, n = 3, 16, 23
+    q = _rand((G, d), 30, scale=1.3)
+    Kc = _rand((n, d), 31)
+    Vc = _rand((n, d), 32)
+    k1 = 5
+    res = O.sparq_decode_unit(q, Kc, Vc, n, k1, k_tokens=7)
+    chans = res["channels"]
+    assert len(chans) == k1
+    for t in range(n):
+        s = 0.0
+        for h in range(G):
+            for i in chans:
+                s += float(q[h, i]) * float(Kc[t, i])
+        assert abs(res["page_score"][t] - s) <= 1e-12 * (1 + abs(s))
+    order = sorted(range(n), key=lambda t: (-res["page_score"][t], t))[:7]
+    np.testing.assert_array_equal(res["pages"], sorted(order))
+
+
+def test_sparq_all_tokens_equals_sdpa():
+    G, d, n = 4, 32, 37
+    q = _rand((G, d), 33)
+    Kc = _rand((n, d), 34)
+    Vc = _rand((n, d), 35)
+    res = O.sparq_decode_unit(q, Kc, Vc, n, k1=8, k_tokens=n + 5)
+    np.testing.assert_array_equal(res["pages"], np.arange(n))
+    np.testing.assert_allclose(res["out"], _sdpa(q, Kc, Vc, 1.0 / math.sqrt(d)), rtol=1e-12, atol=1e-13)
+
+
+def test_sparq_with_every_channel_ranks_by_the_full_dot_product():
+    G, d, n = 2, 16, 30
+    q = _rand((G, d), 36)
+    Kc = _rand((n, d), 37)
+    res = O.sparq_decode_unit(q, Kc, Kc, n, k1=d, k_tokens=6)
+    full = (q.sum(axis=0) @ Kc.T)
+    np.testing.assert_allclose(res["page_score"], full, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(res["pages"], np.sort(np.argsort(-full, kind="stable")[:6]))
+
+
 # ---------------------------------------------------------------- end to end (qualitative)
 def test_planted_needle_survives_and_is_selected():
     Hq, Hkv, w, L, d, P = 4, 1, 8, 512, 64, 16

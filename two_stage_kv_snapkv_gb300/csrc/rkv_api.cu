@@ -115,7 +115,7 @@ const char* kernel_name(int kind) {
       "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
       "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
       "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step",     "recall",
-      "chunk_gather"};
+      "chunk_gather", "sparq_score",  "sparq_topk",     "sparq_attend"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
 }
 
@@ -445,6 +445,59 @@ rkv_status rkv_decode_step(const rkv_cache* cache, const rkv_bf16* q, const rkv_
   if (!k_new || !v_new) return fail(RKV_ERR_INVALID_ARG, "rkv_decode_step needs k_new and v_new");
   return decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, sel_channels, sel_pages, sel_pages_stride,
                        workspace, workspace_bytes, stream, "rkv_decode_step launch");
+}
+
+size_t rkv_sparq_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_pages, int32_t page_size) {
+  if (B < 1 || Hkv < 1 || max_pages < 1 || page_size < 1) return 0;
+  return rkv::sparq_ws_bytes(B, Hq, Hkv, max_pages, page_size);
+}
+
+rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* k1,
+                            const int32_t* k_tokens, float scale, float* out, int32_t* sel_channels,
+                            int32_t* sel_tokens, int32_t sel_tokens_stride, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
+  if (!q || !k1 || !k_tokens || !out || !workspace) return fail(RKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!al16(q) || !al16(out) || !al16(workspace) || (sel_channels && !al16(sel_channels)) ||
+      (sel_tokens && !al16(sel_tokens)))
+    return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
+  const long cap = (long)cache->max_pages * cache->page_size;
+  if (cap > rkv::sparq_max_tokens())
+    return fail(RKV_ERR_UNSUPPORTED, "the token path supports caches of at most %d tokens per sequence",
+                rkv::sparq_max_tokens());
+  for (int b = 0; b < cache->B; ++b) {
+    if (k1[b] < 1 || k1[b] > RKV_HEAD_DIM) return fail(RKV_ERR_INVALID_ARG, "k1[%d]=%d outside [1, 128]", b, k1[b]);
+    if (k_tokens[b] < 1) return fail(RKV_ERR_INVALID_ARG, "k_tokens[%d]=%d", b, k_tokens[b]);
+    if (sel_tokens) {
+      const long kk = k_tokens[b] < cap ? k_tokens[b] : cap;
+      if (sel_tokens_stride < kk)
+        return fail(RKV_ERR_INVALID_ARG, "sel_tokens_stride=%d < %ld", sel_tokens_stride, kk);
+    }
+  }
+  const size_t need = rkv::sparq_ws_bytes(cache->B, Hq, cache->Hkv, cache->max_pages, cache->page_size);
+  if (workspace_bytes < need)
+    return fail(RKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  rkv::DecodeArgs a;
+  a.cache = *cache;
+  a.q = q;
+  a.k_new = nullptr;
+  a.v_new = nullptr;
+  a.mode = 0;
+  a.Hq = Hq;
+  a.G = Hq / cache->Hkv;
+  a.k1 = k1;
+  a.k2 = k_tokens;
+  a.scale = scale;
+  a.out = out;
+  a.sel_channels = sel_channels;
+  a.sel_pages = sel_tokens;
+  a.sel_pages_stride = sel_tokens_stride;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  return cuda_status(rkv::launch_sparq(a, static_cast<cudaStream_t>(stream)), "rkv_decode_sparq launch");
 }
 
 rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* sel_pages,

@@ -86,6 +86,7 @@ struct HsaParams {
   int32_t* sel_pages;
   int sel_pages_stride;
   int B, Hkv, Hq, G, P, max_pages, num_phys, nsplit, cluster, region_bytes;
+  int tok_stride;          // row stride of sigma / selp on the token path (max_pages * P)
   float scale_log2;
   int32_t k1[RKV_MAX_BATCH];
   int32_t k2[RKV_MAX_BATCH];
@@ -268,7 +269,10 @@ static_assert((int)sizeof(TopkSmem<kThreads>) <= ring_bytes(kFusedStages), "ring
 // which may still be being written.  Leaves the CTA's merged state in the returned
 // CtaPart (inside `ring`, ring_bytes(STAGES) of 1024-aligned shared memory) and sets
 // *timed_out when a bounded wait ran out.
-template <int STAGES>
+// kTok (token selection): `sel` lists n selected tokens, ascending; item i is tokens
+// sel[16 i .. 16 i + 15], gathered row by row with 16-byte cp.async into the same
+// swizzled stage layout the tiled TMA loads produce (rows past n are zero-filled).
+template <int STAGES, bool kTok = false>
 __device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int32_t* ptab, int b, int g, int n,
                                int it0, int it1, uint8_t* ring, AttnSmem<STAGES>& a, int new_pos,
                                const uint8_t* new_kv, int* timed_out_out) {
@@ -299,6 +303,32 @@ __device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int
   auto issue = [&](int j) {
     const int s = j % STAGES;
     const int it = it0 + warp + j * kAtWarps;
+    if constexpr (kTok) {
+      // lanes 0-15: the 16 pieces of each token's K row; lanes 16-31: its V row
+      const int base = it * kChunkTok, nv = min(kChunkTok, n - base);
+      const int which = lane >> 4, piece = lane & 15;
+      const rkv_bf16* pool = which ? p.v_pages : p.k_pages;
+      uint8_t* half = wbuf + s * kStageBytes + which * 2 * kHalfBytes + (piece >> 3) * kHalfBytes;
+#pragma unroll 4
+      for (int r = 0; r < kChunkTok; ++r) {
+        bool ok = r < nv;
+        size_t row = 0;
+        if (ok) {
+          const int t = sel[base + r];
+          const int page = t / P;
+          const int phys = (t >= 0 && page < p.max_pages) ? ptab[page] : -1;
+          ok = phys >= 0 && phys < p.num_phys;
+          if (!ok && lane == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
+          row = ((size_t)phys * p.Hkv + g) * P + (t - page * P);
+        }
+        cp_async16(half + r * 128 + (((piece & 7) ^ (r & 7)) << 4), ok ? pool + row * 128 + piece * 8 : pool,
+                   ok ? 16u : 0u);
+      }
+      cp_async_commit();
+      if (lane == 0) a.tstart[warp][s] = n - nv;  // so that n - tstart counts the chunk's tokens
+      __syncwarp();
+      return;
+    }
     int page = sel[it / cpp];
     const int chunk = it % cpp;
     const bool page_ok = page >= 0 && page < NP;  // always true for the select's output
@@ -330,11 +360,16 @@ __device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int
 
   const int pre = min(nj, STAGES);
   for (int j = 0; j < pre; ++j) issue(j);
+  if constexpr (kTok)  // one cp.async group per ring slot, empty or not, so waits count evenly
+    for (int j = pre; j < STAGES; ++j) cp_async_commit();
   int issued = pre, consumed = 0, timed_out = 0;
   const float sl = p.scale_log2;
   for (int j = 0; j < nj; ++j) {
     const int s = j % STAGES;
-    if (!mbar_wait(&a.bars[warp][s], (uint32_t)((j / STAGES) & 1))) {
+    if constexpr (kTok) {
+      cp_async_wait<STAGES - 1>();  // this lane's pieces of chunk j have landed
+      __syncwarp();                 // and so have the other lanes'
+    } else if (!mbar_wait(&a.bars[warp][s], (uint32_t)((j / STAGES) & 1))) {
       flag_error(p.err, RKV_DEVERR_TIMEOUT);
       timed_out = 1;
       break;
@@ -417,8 +452,11 @@ __device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int
     if (j + STAGES < nj) {
       issue(j + STAGES);
       issued = j + STAGES + 1;
+    } else if constexpr (kTok) {
+      cp_async_commit();
     }
   }
+  if constexpr (kTok) cp_async_wait<0>();
   if (timed_out) {
     // wait (bounded) for this warp's copies still in flight before the ring is reused
     for (int j = consumed; j < issued; ++j) mbar_wait(&a.bars[warp][j % STAGES], (uint32_t)((j / STAGES) & 1));
@@ -895,6 +933,117 @@ __global__ void __launch_bounds__(128) hsa_combine_kernel(const __grid_constant_
   p.out[bh * 128 + c] = L > 0.f ? O / L : 0.f;
 }
 
+// ---------------------------------------------------------------------------
+// Token path (SparQ-only: HSA with one-token pages).  With P = 1 a page's Kmax and
+// Kmin are its one key, so the bound is the key's partial dot product over the chosen
+// channels: s_t = sum_h sum_{i in S} q_h,i k_t,i = sum_{i in S} (sum_h q_h,i) k_t,i,
+// read from the paged cache's key rows; the top-k2 tokens are attended.
+// Step 1: channels and token scores.  grid (ceil(max tokens / 512), B*Hkv), 256
+// threads; a half-warp scores a token (16 bytes of its row per lane).
+// ---------------------------------------------------------------------------
+constexpr int kTokScore = 512;  // tokens scored per CTA
+__global__ void __launch_bounds__(kScoreThreads) sparq_score_kernel(const __grid_constant__ HsaParams p) {
+  __shared__ ChanSmem cs;
+  __shared__ float qf[8][128];
+  __shared__ __align__(16) float qsel[128];
+  const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv;
+  const int tid = threadIdx.x;
+  const int n = seq_length(p, b);
+  const int t0 = blockIdx.x * kTokScore;
+  const bool write_ch = (blockIdx.x == 0) && (p.sel_channels != nullptr);
+  if (t0 >= n && !write_ch) return;
+  const int G = p.G, P = p.P;
+  const rkv_bf16* qg = p.q + ((size_t)b * p.Hq + (size_t)g * G) * 128;
+  for (int i = tid; i < G * 128; i += kScoreThreads) qf[i >> 7][i & 127] = bf16_f(qg[i]);
+  const int k1 = p.k1[b];
+  select_channels(qf, cs, G, k1);
+  if (write_ch && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
+  if (tid < 128) qsel[tid] = 0.f;
+  __syncthreads();
+  if (tid < k1) qsel[cs.chan[tid]] = cs.qpos[tid] + cs.qneg[tid];  // sum over the group's heads
+  __syncthreads();
+  const int piece = tid & 15;
+  const float4 qa = reinterpret_cast<const float4*>(qsel)[2 * piece];
+  const float4 qb = reinterpret_cast<const float4*>(qsel)[2 * piece + 1];
+  const int32_t* prow = p.page_table + (size_t)b * p.max_pages;
+  float* sg = p.sigma + (size_t)unit * p.tok_stride;
+  const int t1 = min(n, t0 + kTokScore);
+  for (int tb = t0; tb < t1; tb += kScoreThreads / 16) {  // the same trip count for every lane
+    const int t = tb + (tid >> 4);
+    const bool in = t < t1;
+    const int page = t / P;
+    const int phys = in ? prow[page] : -1;
+    float acc = 0.f;
+    const bool ok = phys >= 0 && phys < p.num_phys;
+    if (ok) {
+      const uint4 u = reinterpret_cast<const uint4*>(p.k_pages + (((size_t)phys * p.Hkv + g) * P + (t - page * P)) *
+                                                                     128)[piece];
+      acc = fmaf(qa.x, bf16_lo(u.x), qa.y * bf16_hi(u.x));
+      acc = fmaf(qa.z, bf16_lo(u.y), fmaf(qa.w, bf16_hi(u.y), acc));
+      acc = fmaf(qb.x, bf16_lo(u.z), fmaf(qb.y, bf16_hi(u.z), acc));
+      acc = fmaf(qb.z, bf16_lo(u.w), fmaf(qb.w, bf16_hi(u.w), acc));
+    } else if (in && piece == 0) {
+      flag_error(p.err, RKV_DEVERR_PAGE_ID);
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (in && piece == 0) sg[t] = ok ? acc : -INFINITY;
+  }
+}
+
+// Token path, step 2: top-k2 tokens, ascending.  grid B*Hkv, 1024 threads, dynamic
+// shared memory = the sequence's token count of keys (at most kTokMax).
+constexpr int kTokMax = 32768;
+__global__ void __launch_bounds__(kTopkThreads) sparq_topk_kernel(const __grid_constant__ HsaParams p) {
+  extern __shared__ uint32_t keys[];
+  __shared__ TopkSmem<kTopkThreads> ts;
+  const int unit = blockIdx.x, b = unit / p.Hkv;
+  const int tid = threadIdx.x;
+  const int n = min(seq_length(p, b), kTokMax);
+  const int k = min(p.k2[b], n);
+  int32_t* out = p.selp + (size_t)unit * p.tok_stride;
+  int32_t* user = p.sel_pages ? p.sel_pages + (size_t)unit * p.sel_pages_stride : nullptr;
+  if (user && tid == 0 && k < p.sel_pages_stride) user[k] = -1;
+  if (k >= n) {
+    for (int i = tid; i < n; i += kTopkThreads) {
+      out[i] = i;
+      if (user) user[i] = i;
+    }
+    return;
+  }
+  const float* sg = p.sigma + (size_t)unit * p.tok_stride;
+  for (int i = tid; i < n; i += kTopkThreads) keys[i] = float_key(sg[i]);
+  __syncthreads();
+  topk_adaptive<kTopkThreads>(n, k, [&](int i) { return keys[i]; }, ts, out, user);
+}
+
+// Token path, step 3: attention over a range of the selected tokens' 16-token chunks.
+// grid (nsplit, B*Hkv), 128 threads.
+__global__ void __launch_bounds__(kThreads) sparq_attend_kernel(const __grid_constant__ HsaParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ AttnSmem<kSplitStages> as;
+  const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv, split = blockIdx.x;
+  const int n = min(seq_length(p, b), kTokMax);
+  const int k = min(p.k2[b], n);
+  const int items = (k + kChunkTok - 1) / kChunkTok;
+  const int ips = (items + p.nsplit - 1) / p.nsplit;
+  const int it0 = min(items, split * ips), it1 = min(items, it0 + ips);
+  int to = 0;
+  const CtaPart* part = attend_cta<kSplitStages, true>(p, p.selp + (size_t)unit * p.tok_stride,
+                                                       p.page_table + (size_t)b * p.max_pages, b, g, k, it0, it1,
+                                                       align1024(smem), as, -1, nullptr, &to);
+  const int c = threadIdx.x;
+  for (int h = 0; h < p.G; ++h) {
+    const size_t bh = (size_t)b * p.Hq + (size_t)g * p.G + h;
+    if (p.nsplit == 1) {
+      p.out[bh * 128 + c] = part->L[h] > 0.f ? part->O[h][c] / part->L[h] : 0.f;
+    } else {
+      p.part_o[(bh * p.nsplit + split) * 128 + c] = part->O[h][c];
+      if (c == 0) p.part_ml[bh * p.nsplit + split] = make_float2(part->M[h], part->L[h]);
+    }
+  }
+}
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // A [rows][128] bf16 page pool as a 2-D tensor map with 16-row x 64-channel boxes.
@@ -943,6 +1092,7 @@ HsaParams make_params(const DecodeArgs& a, bool* ok) {
   }
   p.nsplit = 1;
   p.cluster = 1;
+  p.tok_stride = c.max_pages * c.page_size;
   return p;
 }
 
@@ -1093,6 +1243,60 @@ size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages) {
   const size_t units = (size_t)B * Hkv;
   return align256(units * max_pages * 4) * 2 + align256((size_t)B * Hq * kMaxSplit * 128 * 4) +
          align256((size_t)B * Hq * kMaxSplit * 8);
+}
+
+size_t sparq_ws_bytes(int B, int Hq, int Hkv, int max_pages, int page_size) {
+  const size_t units = (size_t)B * Hkv;
+  const size_t tok = (size_t)max_pages * page_size;
+  return align256(units * tok * 4) * 2 + align256((size_t)B * Hq * kMaxSplit * 128 * 4) +
+         align256((size_t)B * Hq * kMaxSplit * 8);
+}
+
+int sparq_max_tokens() { return kTokMax; }
+
+cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s) {
+  bool ok = false;
+  HsaParams p = make_params(a, &ok);  // the tensor maps are not used on this path
+  const rkv_cache& c = a.cache;
+  const size_t units = (size_t)c.B * c.Hkv;
+  uint8_t* w = static_cast<uint8_t*>(a.ws);
+  const size_t sg = align256(units * (size_t)p.tok_stride * 4);
+  p.sigma = reinterpret_cast<float*>(w);
+  p.selp = reinterpret_cast<int32_t*>(w + sg);
+  p.part_o = reinterpret_cast<float*>(w + 2 * sg);
+  p.part_ml = reinterpret_cast<float2*>(w + 2 * sg + align256((size_t)c.B * a.Hq * kMaxSplit * 128 * 4));
+  int kmax = 1;
+  for (int b = 0; b < c.B; ++b) kmax = a.k2[b] > kmax ? a.k2[b] : kmax;
+  kmax = kmax < p.tok_stride ? kmax : p.tok_stride;
+  const int items = (kmax + kChunkTok - 1) / kChunkTok;
+  int nsplit = (4 * num_sms() + (int)units - 1) / (int)units;
+  const int by_items = (items + kAtWarps - 1) / kAtWarps;
+  nsplit = nsplit < by_items ? nsplit : by_items;
+  nsplit = nsplit < 1 ? 1 : (nsplit > kMaxSplit ? kMaxSplit : nsplit);
+  p.nsplit = nsplit;
+  static bool attrs = false;
+  if (!attrs) {
+    cudaFuncSetAttribute(sparq_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+    cudaFuncSetAttribute(sparq_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokMax * 4);
+    attrs = true;
+  }
+  const int ntok = p.tok_stride < kTokMax ? p.tok_stride : kTokMax;
+  launch_begin(K_SPARQ_SCORE, s);
+  sparq_score_kernel<<<dim3((ntok + kTokScore - 1) / kTokScore, (unsigned)units), kScoreThreads, 0, s>>>(p);
+  launch_end(K_SPARQ_SCORE, s);
+  launch_begin(K_SPARQ_TOPK, s);
+  sparq_topk_kernel<<<(unsigned)units, kTopkThreads, (size_t)ntok * 4, s>>>(p);
+  launch_end(K_SPARQ_TOPK, s);
+  launch_begin(K_SPARQ_ATTEND, s);
+  sparq_attend_kernel<<<dim3(nsplit, (unsigned)units), kThreads, kSplitSmem, s>>>(p);
+  launch_end(K_SPARQ_ATTEND, s);
+  if (nsplit > 1) {
+    launch_begin(K_HSA_COMBINE, s);
+    hsa_combine_kernel<<<(unsigned)(c.B * a.Hq), 128, 0, s>>>(p);
+    launch_end(K_HSA_COMBINE, s);
+  }
+  (void)ok;
+  return cudaGetLastError();
 }
 
 bool decode_fused_ok(const rkv_cache& c) { return c.max_pages <= kFusedMaxPages; }

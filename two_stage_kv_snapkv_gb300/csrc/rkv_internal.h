@@ -28,6 +28,9 @@ enum KernelKind {
   K_HSA_STEP,
   K_RECALL,
   K_CHUNK_GATHER,
+  K_SPARQ_SCORE,
+  K_SPARQ_TOPK,
+  K_SPARQ_ATTEND,
   K_NUM_KINDS
 };
 const char* kernel_name(int kind);
@@ -108,6 +111,10 @@ struct DecodeArgs {
   size_t ws_bytes;
 };
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages);
+// Token path (SparQ-only): k2 counts tokens; k_new must be null.
+size_t sparq_ws_bytes(int B, int Hq, int Hkv, int max_pages, int page_size);
+int sparq_max_tokens();
+cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s);
 bool decode_fused_ok(const rkv_cache& c);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
