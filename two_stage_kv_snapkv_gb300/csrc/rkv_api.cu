@@ -465,6 +465,8 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
     return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
   const long cap = (long)cache->max_pages * cache->page_size;
+  if ((long long)cache->num_phys_pages * cache->Hkv * cache->page_size >= (1LL << 31))
+    return fail(RKV_ERR_UNSUPPORTED, "the token path indexes pool rows with 32-bit integers");
   if (cap > rkv::sparq_max_tokens())
     return fail(RKV_ERR_UNSUPPORTED, "the token path supports caches of at most %d tokens per sequence",
                 rkv::sparq_max_tokens());

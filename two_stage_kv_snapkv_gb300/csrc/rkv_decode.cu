@@ -269,9 +269,10 @@ static_assert((int)sizeof(TopkSmem<kThreads>) <= ring_bytes(kFusedStages), "ring
 // which may still be being written.  Leaves the CTA's merged state in the returned
 // CtaPart (inside `ring`, ring_bytes(STAGES) of 1024-aligned shared memory) and sets
 // *timed_out when a bounded wait ran out.
-// kTok (token selection): `sel` lists n selected tokens, ascending; item i is tokens
-// sel[16 i .. 16 i + 15], gathered row by row with 16-byte cp.async into the same
-// swizzled stage layout the tiled TMA loads produce (rows past n are zero-filled).
+// kTok (token selection): n selected tokens, item i being tokens 16 i .. 16 i + 15;
+// sel[j] is token j's row in the K/V pools (-1: zero-filled and masked), gathered row
+// by row with 16-byte cp.async into the same swizzled stage layout the tiled TMA
+// loads produce (rows past n are zero-filled too).
 template <int STAGES, bool kTok = false>
 __device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int32_t* ptab, int b, int g, int n,
                                int it0, int it1, uint8_t* ring, AttnSmem<STAGES>& a, int new_pos,
@@ -311,18 +312,9 @@ __device__ CtaPart* attend_cta(const HsaParams& p, const int32_t* sel, const int
       uint8_t* half = wbuf + s * kStageBytes + which * 2 * kHalfBytes + (piece >> 3) * kHalfBytes;
 #pragma unroll 4
       for (int r = 0; r < kChunkTok; ++r) {
-        bool ok = r < nv;
-        size_t row = 0;
-        if (ok) {
-          const int t = sel[base + r];
-          const int page = t / P;
-          const int phys = (t >= 0 && page < p.max_pages) ? ptab[page] : -1;
-          ok = phys >= 0 && phys < p.num_phys;
-          if (!ok && lane == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
-          row = ((size_t)phys * p.Hkv + g) * P + (t - page * P);
-        }
-        cp_async16(half + r * 128 + (((piece & 7) ^ (r & 7)) << 4), ok ? pool + row * 128 + piece * 8 : pool,
-                   ok ? 16u : 0u);
+        const int row = r < nv ? sel[base + r] : -1;
+        cp_async16(half + r * 128 + (((piece & 7) ^ (r & 7)) << 4),
+                   row >= 0 ? pool + (size_t)row * 128 + piece * 8 : pool, row >= 0 ? 16u : 0u);
       }
       cp_async_commit();
       if (lane == 0) a.tstart[warp][s] = n - nv;  // so that n - tstart counts the chunk's tokens
@@ -939,13 +931,15 @@ __global__ void __launch_bounds__(128) hsa_combine_kernel(const __grid_constant_
 // channels: s_t = sum_h sum_{i in S} q_h,i k_t,i = sum_{i in S} (sum_h q_h,i) k_t,i,
 // read from the paged cache's key rows; the top-k2 tokens are attended.
 // Step 1: channels and token scores.  grid (ceil(max tokens / 512), B*Hkv), 256
-// threads; a half-warp scores a token (16 bytes of its row per lane).
+// threads; a half-warp scores a token (16 bytes of its row per lane), eight tokens
+// rows in flight at a time.
 // ---------------------------------------------------------------------------
 constexpr int kTokScore = 512;  // tokens scored per CTA
 __global__ void __launch_bounds__(kScoreThreads) sparq_score_kernel(const __grid_constant__ HsaParams p) {
   __shared__ ChanSmem cs;
   __shared__ float qf[8][128];
   __shared__ __align__(16) float qsel[128];
+  __shared__ int sphys[kTokScore / 16];
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv;
   const int tid = threadIdx.x;
   const int n = seq_length(p, b);
@@ -965,29 +959,40 @@ __global__ void __launch_bounds__(kScoreThreads) sparq_score_kernel(const __grid
   const int piece = tid & 15;
   const float4 qa = reinterpret_cast<const float4*>(qsel)[2 * piece];
   const float4 qb = reinterpret_cast<const float4*>(qsel)[2 * piece + 1];
-  const int32_t* prow = p.page_table + (size_t)b * p.max_pages;
-  float* sg = p.sigma + (size_t)unit * p.tok_stride;
   const int t1 = min(n, t0 + kTokScore);
-  for (int tb = t0; tb < t1; tb += kScoreThreads / 16) {  // the same trip count for every lane
-    const int t = tb + (tid >> 4);
-    const bool in = t < t1;
-    const int page = t / P;
-    const int phys = in ? prow[page] : -1;
-    float acc = 0.f;
-    const bool ok = phys >= 0 && phys < p.num_phys;
-    if (ok) {
-      const uint4 u = reinterpret_cast<const uint4*>(p.k_pages + (((size_t)phys * p.Hkv + g) * P + (t - page * P)) *
-                                                                     128)[piece];
-      acc = fmaf(qa.x, bf16_lo(u.x), qa.y * bf16_hi(u.x));
-      acc = fmaf(qa.z, bf16_lo(u.y), fmaf(qa.w, bf16_hi(u.y), acc));
-      acc = fmaf(qb.x, bf16_lo(u.z), fmaf(qb.y, bf16_hi(u.z), acc));
-      acc = fmaf(qb.z, bf16_lo(u.w), fmaf(qb.w, bf16_hi(u.w), acc));
-    } else if (in && piece == 0) {
-      flag_error(p.err, RKV_DEVERR_PAGE_ID);
+  // the physical pages of this CTA's tokens (t0 is page-aligned: P divides 512)
+  const int npg = (t1 - t0 + P - 1) / P;
+  for (int i = tid; i < npg; i += kScoreThreads) sphys[i] = p.page_table[(size_t)b * p.max_pages + t0 / P + i];
+  __syncthreads();
+  float* sg = p.sigma + (size_t)unit * p.tok_stride;
+  constexpr int kU = 8;  // tokens per half-warp per pass: their rows are loaded back to back
+  for (int tb = t0; tb < t1; tb += 16 * kU) {  // the same trip count for every lane
+    uint4 u[kU];
+    bool ok[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int t = tb + (tid >> 4) + 16 * j;
+      const int lp = (t - t0) / P;
+      const int phys = t < t1 ? sphys[lp] : -1;
+      ok[j] = phys >= 0 && phys < p.num_phys;
+      if (ok[j])
+        u[j] = reinterpret_cast<const uint4*>(
+            p.k_pages + (((size_t)phys * p.Hkv + g) * P + (t - t0 - lp * P)) * 128)[piece];
+      else
+        u[j] = make_uint4(0, 0, 0, 0);
+      if (t < t1 && !ok[j] && piece == 0) flag_error(p.err, RKV_DEVERR_PAGE_ID);
     }
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (in && piece == 0) sg[t] = ok ? acc : -INFINITY;
+    for (int j = 0; j < kU; ++j) {
+      float acc = fmaf(qa.x, bf16_lo(u[j].x), qa.y * bf16_hi(u[j].x));
+      acc = fmaf(qa.z, bf16_lo(u[j].y), fmaf(qa.w, bf16_hi(u[j].y), acc));
+      acc = fmaf(qb.x, bf16_lo(u[j].z), fmaf(qb.y, bf16_hi(u[j].z), acc));
+      acc = fmaf(qb.z, bf16_lo(u[j].w), fmaf(qb.w, bf16_hi(u[j].w), acc));
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      const int t = tb + (tid >> 4) + 16 * j;
+      if (t < t1 && piece == 0) sg[t] = ok[j] ? acc : -INFINITY;
+    }
   }
 }
 
@@ -1018,7 +1023,11 @@ __global__ void __launch_bounds__(kTopkThreads) sparq_topk_kernel(const __grid_c
 }
 
 // Token path, step 3: attention over a range of the selected tokens' 16-token chunks.
-// grid (nsplit, B*Hkv), 128 threads.
+// grid (nsplit, B*Hkv), 128 threads.  Dynamic shared memory: the ring (1024-aligned),
+// then the CTA's token rows (at most kTokRowItems chunks of 16).
+constexpr int kTokRowItems = 512;
+constexpr int kTokAttendSmem = 1024 + ring_bytes(kSplitStages) + 1024 + kTokRowItems * kChunkTok * 4;
+static_assert(ring_bytes(kSplitStages) >= kWarpCombineBytes, "the ring doubles as the warp-combine buffer");
 __global__ void __launch_bounds__(kThreads) sparq_attend_kernel(const __grid_constant__ HsaParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ AttnSmem<kSplitStages> as;
@@ -1028,10 +1037,23 @@ __global__ void __launch_bounds__(kThreads) sparq_attend_kernel(const __grid_con
   const int items = (k + kChunkTok - 1) / kChunkTok;
   const int ips = (items + p.nsplit - 1) / p.nsplit;
   const int it0 = min(items, split * ips), it1 = min(items, it0 + ips);
+  // this CTA's tokens as rows of the K/V pools, resolved once (the chunk loop then
+  // issues its copies without waiting on the list or the page table)
+  int32_t* rows = reinterpret_cast<int32_t*>(align1024(smem) + ring_bytes(kSplitStages) + 1024);
+  const int r0 = it0 * kChunkTok, r1 = min(k, it1 * kChunkTok);
+  const int32_t* list = p.selp + (size_t)unit * p.tok_stride;
+  const int32_t* prow = p.page_table + (size_t)b * p.max_pages;
+  for (int i = r0 + (int)threadIdx.x; i < r1; i += kThreads) {
+    const int t = list[i], page = t / p.P;
+    const int phys = (t >= 0 && page < p.max_pages) ? prow[page] : -1;
+    const bool ok = phys >= 0 && phys < p.num_phys;
+    if (!ok) flag_error(p.err, RKV_DEVERR_PAGE_ID);
+    rows[i - r0] = ok ? (phys * p.Hkv + g) * p.P + (t - page * p.P) : -1;
+  }
+  __syncthreads();
   int to = 0;
-  const CtaPart* part = attend_cta<kSplitStages, true>(p, p.selp + (size_t)unit * p.tok_stride,
-                                                       p.page_table + (size_t)b * p.max_pages, b, g, k, it0, it1,
-                                                       align1024(smem), as, -1, nullptr, &to);
+  const CtaPart* part = attend_cta<kSplitStages, true>(p, rows - r0, nullptr, b, g, k, it0, it1, align1024(smem), as,
+                                                       -1, nullptr, &to);
   const int c = threadIdx.x;
   for (int h = 0; h < p.G; ++h) {
     const size_t bh = (size_t)b * p.Hq + (size_t)g * p.G + h;
@@ -1272,11 +1294,13 @@ cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s) {
   int nsplit = (4 * num_sms() + (int)units - 1) / (int)units;
   const int by_items = (items + kAtWarps - 1) / kAtWarps;
   nsplit = nsplit < by_items ? nsplit : by_items;
+  const int by_rows = (items + kTokRowItems - 1) / kTokRowItems;  // a CTA resolves at most 512 items' rows
+  nsplit = nsplit > by_rows ? nsplit : by_rows;
   nsplit = nsplit < 1 ? 1 : (nsplit > kMaxSplit ? kMaxSplit : nsplit);
   p.nsplit = nsplit;
   static bool attrs = false;
   if (!attrs) {
-    cudaFuncSetAttribute(sparq_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+    cudaFuncSetAttribute(sparq_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokAttendSmem);
     cudaFuncSetAttribute(sparq_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokMax * 4);
     attrs = true;
   }
@@ -1288,7 +1312,7 @@ cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s) {
   sparq_topk_kernel<<<(unsigned)units, kTopkThreads, (size_t)ntok * 4, s>>>(p);
   launch_end(K_SPARQ_TOPK, s);
   launch_begin(K_SPARQ_ATTEND, s);
-  sparq_attend_kernel<<<dim3(nsplit, (unsigned)units), kThreads, kSplitSmem, s>>>(p);
+  sparq_attend_kernel<<<dim3(nsplit, (unsigned)units), kThreads, kTokAttendSmem, s>>>(p);
   launch_end(K_SPARQ_ATTEND, s);
   if (nsplit > 1) {
     launch_begin(K_HSA_COMBINE, s);
