@@ -57,6 +57,8 @@ def parse():
                     help="also time a chunked prefill of the same prompts with chunks of about this many tokens "
                          "(0: skip)")
     ap.add_argument("--one-layer", action="store_true", help="run only layer 0 of a multi-layer workload")
+    ap.add_argument("--mode", choices=["hsa", "quest", "sparq"], default="hsa",
+                    help="decode selection: HSA (default), Quest-only (every channel), SparQ-only (one-token pages)")
     ap.add_argument("--ncu-every-kernel", action="store_true",
                     help="one eager launch of every library kernel, no warm-up (for an ncu launch list)")
     ap.add_argument("--ncu", action="store_true", help="one plain pass, no graphs (for an ncu launch list)")
@@ -127,8 +129,9 @@ class ClockSampler:
 class Setup:
     """Everything one rank needs for K passes of one workload (layer 0)."""
 
-    def __init__(self, wl: W.Workload, rkv, seed: int, dev, layer: int = 0, share: "Setup | None" = None):
-        self.wl, self.rkv, self.dev, self.seed, self.layer = wl, rkv, dev, seed, layer
+    def __init__(self, wl: W.Workload, rkv, seed: int, dev, layer: int = 0, share: "Setup | None" = None,
+                 mode: str = "hsa"):
+        self.wl, self.rkv, self.dev, self.seed, self.layer, self.mode = wl, rkv, dev, seed, layer, mode
         self.inp = W.prefill_tensors(wl, seed, layer, dev, tail="zero")
         self.dec = [W.decode_tensors(wl, t, seed, layer, dev) for t in range(wl.steps)]
         for d in self.dec:
@@ -144,8 +147,10 @@ class Setup:
                 s["pool_kernel"] = wl.pool_kernel
             self.splits.append(s)
         self.keep1 = [s["keep1"] for s in self.splits]
-        self.k1 = [s["k1"] for s in self.splits]
+        # Quest-only: HSA with every channel; SparQ-only: one-token pages, the same token budget
+        self.k1 = [s["k1"] if mode != "quest" else wl.d for s in self.splits]
         self.k2 = [s["k2"] for s in self.splits]
+        self.k_tokens = [k * wl.page_size for k in self.k2]
         self.kp = [s["pool_kernel"] for s in self.splits]
         P = wl.page_size
         max_pages = (max(self.keep1) + wl.steps + P - 1) // P
@@ -156,6 +161,9 @@ class Setup:
         # layers run one after another on one stream, so they can share the scratch
         self.pws = share.pws if share else rkv.prefill_workspace(wl.B, wl.Hq, wl.Hkv, wl.window, wl.Lmax, dev)
         self.dws = share.dws if share else rkv.decode_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, dev)
+        self.sws = None
+        if mode == "sparq":
+            self.sws = share.sws if share else rkv.sparq_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, P, dev)
         self.out = torch.empty((wl.steps, wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
         self.flush_buf = share.flush_buf if share else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -167,8 +175,15 @@ class Setup:
 
     def decode(self, t: int):
         d = self.dec[t]
-        self.rkv.rkv_decode_step(self.cache, d["q"], d["k_new"], d["v_new"], self.k1, self.k2, self.out[t],
-                                 workspace=self.dws)
+        self.step(d["q"], d["k_new"], d["v_new"], self.out[t])
+
+    def step(self, q, k_new, v_new, out):
+        """One decode step of this mode: append the token, then select and attend."""
+        if self.mode == "sparq":
+            self.rkv.rkv_append_page_summary(self.cache, k_new, v_new, 1)
+            self.rkv.rkv_decode_sparq(self.cache, q, self.k1, self.k_tokens, out, workspace=self.sws)
+        else:
+            self.rkv.rkv_decode_step(self.cache, q, k_new, v_new, self.k1, self.k2, out, workspace=self.dws)
 
     def flush(self):
         self.flush_buf.zero_()
@@ -182,14 +197,18 @@ class Setup:
         for b in range(wl.B):
             n = self.keep1[b] + t + 1
             NP = -(-n // P)
-            summ += wl.Hkv * 2 * self.k1[b] * NP * 2
-            kv += wl.Hkv * min(self.k2[b], NP) * P * 128 * 2 * 2
+            if self.mode == "sparq":   # every key row to score, the chosen tokens' K and V rows
+                summ += wl.Hkv * n * 128 * 2
+                kv += wl.Hkv * min(self.k_tokens[b], n) * 128 * 2 * 2
+            else:
+                summ += wl.Hkv * 2 * self.k1[b] * NP * 2
+                kv += wl.Hkv * min(self.k2[b], NP) * P * 128 * 2 * 2
         q = wl.B * wl.Hq * 128 * 2
         out = wl.B * wl.Hq * 128 * 4
         append = wl.B * wl.Hkv * (128 * 2 * 2 * 2 + 128 * 2 * 2 * 2)   # new k,v read+write, summaries
         total = summ + kv + q + out + append
         return dict(hsa_score=summ + q, hsa_attend=kv + q + out, append_small=append, hsa_step=total,
-                    step_total=total)
+                    sparq_score=summ + q, sparq_attend=kv + q + out, step_total=total)
 
     def prefill_bytes(self) -> dict:
         wl = self.wl
@@ -350,8 +369,11 @@ def oracle_sample(setup: Setup, decode_steps: int) -> dict:
             Kc = np.concatenate([Kc, kn[b, g][None]])
             Vc = np.concatenate([Vc, vn[b, g][None]])
             kmax, kmin = O.append_summaries(kmax, kmin, Kc, n_old, 1, wl.page_size)
-            O.hsa_decode_unit(q[b, g * G:(g + 1) * G], Kc, Vc, n_old + 1, kmax, kmin, wl.page_size,
-                              setup.k1[b], setup.k2[b])
+            if setup.mode == "sparq":
+                O.sparq_decode_unit(q[b, g * G:(g + 1) * G], Kc, Vc, n_old + 1, setup.k1[b], setup.k_tokens[b])
+            else:
+                O.hsa_decode_unit(q[b, g * G:(g + 1) * G], Kc, Vc, n_old + 1, kmax, kmin, wl.page_size,
+                                  setup.k1[b], setup.k2[b])
             u[2], u[3], u[4] = Kc, Vc, (kmax, kmin)
     t_dec = (time.perf_counter() - t1) / max(1, decode_steps)
     whole = t_prefill + wl.steps * t_dec
@@ -374,10 +396,10 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     rkv.rkv_decode_path({"auto": 0, "split": 1, "fused": 2}[args.decode_path])
     seed = rank_seed(args.seed, rank)
     nl = 1 if args.one_layer else wl.layers
-    setup = Setup(wl, rkv, seed, dev)
+    setup = Setup(wl, rkv, seed, dev, mode=args.mode)
     # a multi-layer workload keeps every layer resident: stage 1 for all of them, then
     # each decode step runs HSA for every layer in turn, as a model's decode step does
-    layers = [setup] + [Setup(wl, rkv, seed, dev, layer=l, share=setup) for l in range(1, nl)]
+    layers = [setup] + [Setup(wl, rkv, seed, dev, layer=l, share=setup, mode=args.mode) for l in range(1, nl)]
     multi = nl > 1
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
@@ -473,7 +495,7 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     pb = setup.prefill_bytes()
 
     def algo_bytes(kind):
-        if kind in ("hsa_score", "hsa_attend", "append_small", "hsa_step"):
+        if kind in ("hsa_score", "hsa_attend", "append_small", "hsa_step", "sparq_score", "sparq_attend"):
             return statistics.mean(sb[kind] for sb in step_bytes)
         if kind in pb:
             return pb[kind]
@@ -516,7 +538,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic (seeded normal bf16 with the workload's shapes, outlier channels, sinks and needles)",
-        config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world, nl),
+        config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world, nl,
+                               args.mode),
         prefill_evict_ms=round(pre_layer_ms, 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),
         decode_achieved_gbs=round(step_total / (dec_mean_ms * 1e-3) / 1e9, 1),
@@ -530,7 +553,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         res["decode_all_layers_us_per_step"] = round(dec_mean_ms * nl * 1e3, 3)
         res["memory_gb"] = dict(prompt_kv=round(nl * 2 * wl.Hkv * sum(wl.prompt_lens) * 256 / 1e9, 2),
                                 cache_pages=round(sum(s.cache.nbytes() for s in layers) / 1e9, 2))
-    res["selection"] = selection_recall(setup)
+    res["selection"] = selection_recall(setup) if args.mode != "sparq" else dict(
+        skipped="the recall diagnostic takes a page selection; SparQ-only selects tokens")
     if args.prefill_chunk > 0:
         res["chunked_prefill"] = chunked_prefill(setup, stream, args.prefill_chunk, max(args.steps, 3))
     if rank == 0 and not args.no_e2e:
@@ -555,7 +579,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
     return res
 
 
-def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int, layers: int = 1) -> dict:
+def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int, layers: int = 1,
+                    mode: str = "hsa") -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
     if layers > 1:
         step = (f"one request over {layers} layers: split + prefill evict of every layer + every decode step "
@@ -571,7 +596,9 @@ def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: 
                 keep1=self_or_range(keep1), k1=self_or_range(k1), k2=self_or_range(k2),
                 pool_kernel=self_or_range(kp), split="RocketKV-MT (nothing evicted)" if wl.mt else "two-stage",
                 step=step, l2=l2, timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
-                decode_path=decode_path, parallelism=f"replica x{world}" if world > 1 else "single GPU")
+                decode_path=decode_path, parallelism=f"replica x{world}" if world > 1 else "single GPU",
+                mode={"hsa": "HSA", "quest": "Quest-only (HSA, k1 = every channel)",
+                      "sparq": "SparQ-only (one-token pages, k2 x P tokens)"}[mode])
 
 
 def whole_job_value(total_ms: float, decode_steps: int, passes: int, world: int, device) -> tuple:
@@ -625,8 +652,7 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         for t in range(wl.steps):
             for k in dd:
                 dd[k].copy_(hdec[t][k], non_blocking=True)
-            rkv.rkv_decode_step(setup.cache, dd["q"], dd["k_new"], dd["v_new"], setup.k1, setup.k2, setup.out[t],
-                                workspace=setup.dws)
+            setup.step(dd["q"], dd["k_new"], dd["v_new"], setup.out[t])
             hout[t].copy_(setup.out[t], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -672,8 +698,10 @@ def run_reference(args, rank: int, world: int) -> dict:
     else:
         sp = [O.split_ratio(L, wl.budget, wl.d, wl.page_size, wl.window, wl.k1 or 0) for L in wl.prompt_lens]
     setup.keep1 = [s["keep1"] for s in sp]
-    setup.k1 = [s["k1"] for s in sp]
+    setup.mode = args.mode
+    setup.k1 = [s["k1"] if args.mode != "quest" else wl.d for s in sp]
     setup.k2 = [s["k2"] for s in sp]
+    setup.k_tokens = [k * wl.page_size for k in setup.k2]
     setup.kp = [wl.pool_kernel or s["pool_kernel"] for s in sp]
     for _ in range(args.warmup):
         oracle_sample(setup, 1)
@@ -687,7 +715,7 @@ def run_reference(args, rank: int, world: int) -> dict:
                 warmup=args.warmup, ms_per_step=round(1e3 / value * wl.steps, 3), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)",
                 config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world,
-                                       wl.layers),
+                                       wl.layers, args.mode),
                 cpu_baseline=dict(value=round(value, 3), unit=UNIT, cores=host_cores(), kind="oracle",
                                   sample=f"per step: oracle prefill of all units + {nsteps} decode steps"
                                          f"{' of layer 0' if wl.layers > 1 else ''}, "
