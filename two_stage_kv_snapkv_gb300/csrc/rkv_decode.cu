@@ -588,7 +588,8 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   const int nbox = (slice8 + 63) >> 6;
   const bool box_rows = all_ch && slice8 >= 64 && nbox * kSumBlock <= p.region_bytes;
   const bool bulk_rows = all_ch && slice8 >= 64 && !box_rows;
-  if (all_ch && !bulk_rows) {
+  const bool piece_rows = all_ch && slice8 < 64;  // exactly one of the three staging forms
+  if (piece_rows) {
     const int cpr = slice8 >> 3;
     for (int e = tid; e < 256 * cpr; e += kThreads) {
       const int i = e / cpr, c = e - i * cpr;
@@ -676,7 +677,7 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
     __syncthreads();  // the previous tile is consumed
     if (all_ch) {  // the one tile, staged at the start
-      if (!bulk_rows && !box_rows) cp_async_wait<0>();
+      if (piece_rows) cp_async_wait<0>();
       else if (!mbar_wait(&sbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
     } else {
       // one bulk copy per row (the rows are long here: the slice did not fit whole)
