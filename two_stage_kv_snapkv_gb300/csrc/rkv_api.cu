@@ -163,8 +163,8 @@ int num_sms() {
 }
 
 
-// cuTensorMapEncodeTiled from the driver, looked up once per process.
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  // cuTensorMapEncodeTiled from the driver, looked up once per process
   static std::once_flag once;
   static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   std::call_once(once, [] {
@@ -174,11 +174,6 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
         q == cudaDriverEntryPointSuccess)
       enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
-  return enc;
-}
-
-bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-  const auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {128, rows};
   cuuint64_t strides[1] = {256};
@@ -186,18 +181,6 @@ bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool encode_summary_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
-  const auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -54,12 +54,6 @@ constexpr int kHalfBytes = kChunkTok * 128;   // one 16-token x 64-channel box (
 constexpr int kStageBytes = 4 * kHalfBytes;   // K lo, K hi, V lo, V hi
 constexpr int kWarpCombineBytes = kAtWarps * 8 * (2 + 128) * 4;
 constexpr int kFusedMaxPages = 4096;
-constexpr int kSumBlock = 2 * 128 * 64 * 2;  // one staged box pair: Kmax and Kmin, 128 channels x 64 pages
-
-// Element (row, page j) of summaries staged in boxes: rows 0-127 Kmax, 128-255 Kmin.
-__device__ __forceinline__ int box_index(int row, int j) {
-  return (j >> 6) * (kSumBlock / 2) + (row >> 7) * (kSumBlock / 4) + (row & 127) * 64 + (j & 63);
-}
 constexpr int kMaxCluster = 8;
 
 constexpr int ring_bytes(int stages) { return kAtWarps * stages * kStageBytes; }
@@ -72,8 +66,6 @@ static_assert(ring_bytes(kFusedStages) >= 2 * 128 * 8 * 2, "staging tile too sma
 struct HsaParams {
   CUtensorMap tmk;         // k_pages as [num_phys*Hkv*P rows][128] bf16, 16x64 boxes, 128-B swizzle
   CUtensorMap tmv;         // v_pages, same
-  CUtensorMap tsmax;       // kmax as [B*Hkv*128 rows][max_pages] bf16, 64-page x 128-channel boxes
-  CUtensorMap tsmin;       // kmin, same
   rkv_bf16* k_pages;
   rkv_bf16* v_pages;
   const int32_t* page_table;
@@ -573,23 +565,18 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   // this CTA's slice [p0, p1) of the pages (8-page aligned).  When the summaries of
   // all 128 channels over the slice fit in the region, they are staged right away
   // (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and the channels are
-  // chosen.  Slices of 64 pages or more come as TMA boxes of 64 pages x 128 channels
-  // (one Kmax and one Kmin box per 64 pages: a block of 32 KB, [Kmax | Kmin][channel]
-  // [64 pages]; x = p0 + 64 c is 16-byte aligned since p0 is a multiple of 8), or one
-  // bulk copy per row when those blocks would not fit; shorter slices in 16-byte
-  // cp.async pieces, row-major [row][slice8] (on GB300 the bulk copies cost 0.6 us more
-  // to issue at 32 pages a row and saved about 1 us at 160).  Otherwise only the chosen
-  // channels' rows are staged, after the select.  The page-table row (needed after the
-  // select) comes by bulk copy.
+  // chosen: rows of 64 pages or more by one bulk copy each (every row starts on a
+  // 16-byte boundary since max_pages and p0 are multiples of 8), shorter ones in
+  // 16-byte cp.async pieces (on GB300 the bulk copies cost 0.6 us more to issue at 32
+  // pages a row and saved about 1 us at 160).  Otherwise only the chosen channels' rows
+  // are staged, after the select.  The page-table row (needed after the select) comes
+  // by bulk copy.
   const int per = ((NP + C - 1) / C + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
   const int slice8 = (p1 - p0 + 7) & ~7;
   const bool all_ch = p1 > p0 && 2 * 128 * slice8 * 2 <= p.region_bytes;
-  const int nbox = (slice8 + 63) >> 6;
-  const bool box_rows = all_ch && slice8 >= 64 && nbox * kSumBlock <= p.region_bytes;
-  const bool bulk_rows = all_ch && slice8 >= 64 && !box_rows;
-  const bool piece_rows = all_ch && slice8 < 64;  // exactly one of the three staging forms
-  if (piece_rows) {
+  const bool bulk_rows = all_ch && slice8 >= 64;
+  if (all_ch && !bulk_rows) {
     const int cpr = slice8 >> 3;
     for (int e = tid; e < 256 * cpr; e += kThreads) {
       const int i = e / cpr, c = e - i * cpr;
@@ -600,13 +587,6 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   }
   const int np4 = ((NP + 3) & ~3);  // whole 16-byte groups; within the row (max_pages % 8 == 0)
   if (tid == 0) {
-    if (box_rows) {
-      mbar_arrive_expect_tx(&sbar, (uint32_t)(nbox * kSumBlock));
-      for (int c = 0; c < nbox; ++c) {
-        tma_load_2d(ring + (size_t)c * kSumBlock, &p.tsmax, p0 + 64 * c, unit * 128, &sbar);
-        tma_load_2d(ring + (size_t)c * kSumBlock + kSumBlock / 2, &p.tsmin, p0 + 64 * c, unit * 128, &sbar);
-      }
-    }
     if (bulk_rows) mbar_arrive_expect_tx(&sbar, (uint32_t)(256 * slice8 * 2));
     if (np4 > 0) {
       mbar_arrive_expect_tx(&pbar, (uint32_t)np4 * 4);
@@ -677,7 +657,7 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
     __syncthreads();  // the previous tile is consumed
     if (all_ch) {  // the one tile, staged at the start
-      if (piece_rows) cp_async_wait<0>();
+      if (!bulk_rows) cp_async_wait<0>();
       else if (!mbar_wait(&sbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
     } else {
       // one bulk copy per row (the rows are long here: the slice did not fit whole)
@@ -702,13 +682,11 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
       const int nrows = all_ch ? 128 : k1;
       for (int r = tid; r < nrows; r += kThreads) {
         const float x = bf16_f(kn[all_ch ? r : cs.chan[r]]);
-        const int rl = all_ch ? 128 + r : k1 + r;
-        rkv_bf16& sh = box_rows ? stg[box_index(r, j)] : stg[r * cnt8 + j];
-        rkv_bf16& sl = box_rows ? stg[box_index(rl, j)] : stg[rl * cnt8 + j];
-        const float hi = first ? x : fmaxf(bf16_f(sh), x);
-        const float lo = first ? x : fminf(bf16_f(sl), x);
-        sh = (rkv_bf16)(__float_as_uint(hi) >> 16);
-        sl = (rkv_bf16)(__float_as_uint(lo) >> 16);
+        const int rh = r, rl = all_ch ? 128 + r : k1 + r;
+        const float hi = first ? x : fmaxf(bf16_f(stg[rh * cnt8 + j]), x);
+        const float lo = first ? x : fminf(bf16_f(stg[rl * cnt8 + j]), x);
+        stg[rh * cnt8 + j] = (rkv_bf16)(__float_as_uint(hi) >> 16);
+        stg[rl * cnt8 + j] = (rkv_bf16)(__float_as_uint(lo) >> 16);
       }
       __syncthreads();
     }
@@ -718,38 +696,31 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     }
     // row of chosen channel kk's Kmax: chan[kk] (all channels staged) or kk; its Kmin
     // row is lo_row0 further
-    // layout 0: the chosen channels' rows; 1: all rows, row-major; 2: all rows in boxes
-    auto score = [&](auto layout) {
-      constexpr int kL = decltype(layout)::value;
+    auto score = [&](auto all) {
+      constexpr bool kAll = decltype(all)::value;
       for (int j = tid; j < cnt; j += kThreads) {
-        // element (row, page j) of the staged tile; the Kmin row is lo_row0 further
-        const rkv_bf16* col = kL == 2 ? stg + (j >> 6) * (kSumBlock / 2) + (j & 63) : stg + j;
-        const int rs = kL == 2 ? 64 : cnt8;  // row stride
-        const int lo_off = kL == 2 ? kSumBlock / 4 : lo_row0 * cnt8;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // independent chains
         int kk = 0;
         for (; kk + 1 < k1; kk += 2) {
-          const int r0 = kL ? cs.chan[kk] : kk, r1 = kL ? cs.chan[kk + 1] : kk + 1;
-          s0 = fmaf(cs.qpos[kk], bf16_f(col[r0 * rs]), s0);
-          s1 = fmaf(cs.qneg[kk], bf16_f(col[lo_off + r0 * rs]), s1);
-          s2 = fmaf(cs.qpos[kk + 1], bf16_f(col[r1 * rs]), s2);
-          s3 = fmaf(cs.qneg[kk + 1], bf16_f(col[lo_off + r1 * rs]), s3);
+          const int r0 = kAll ? cs.chan[kk] : kk, r1 = kAll ? cs.chan[kk + 1] : kk + 1;
+          s0 = fmaf(cs.qpos[kk], bf16_f(stg[r0 * cnt8 + j]), s0);
+          s1 = fmaf(cs.qneg[kk], bf16_f(stg[(lo_row0 + r0) * cnt8 + j]), s1);
+          s2 = fmaf(cs.qpos[kk + 1], bf16_f(stg[r1 * cnt8 + j]), s2);
+          s3 = fmaf(cs.qneg[kk + 1], bf16_f(stg[(lo_row0 + r1) * cnt8 + j]), s3);
         }
         if (kk < k1) {
-          const int r0 = kL ? cs.chan[kk] : kk;
-          s0 = fmaf(cs.qpos[kk], bf16_f(col[r0 * rs]), s0);
-          s1 = fmaf(cs.qneg[kk], bf16_f(col[lo_off + r0 * rs]), s1);
+          const int r0 = kAll ? cs.chan[kk] : kk;
+          s0 = fmaf(cs.qpos[kk], bf16_f(stg[r0 * cnt8 + j]), s0);
+          s1 = fmaf(cs.qneg[kk], bf16_f(stg[(lo_row0 + r0) * cnt8 + j]), s1);
         }
         const uint32_t key = float_key((s0 + s2) + (s1 + s3));
         for (int r = 0; r < C; ++r) cluster.map_shared_rank(keys, r)[t0 + j] = key;
       }
     };
-    if (box_rows)
-      score(std::integral_constant<int, 2>{});
-    else if (all_ch)
-      score(std::integral_constant<int, 1>{});
+    if (all_ch)
+      score(std::true_type{});
     else
-      score(std::integral_constant<int, 0>{});
+      score(std::false_type{});
   }
   if (!waited) cluster_wait();
   fence_proxy_async_smem();  // generic accesses to the region before the attention's TMA loads
@@ -1107,9 +1078,6 @@ HsaParams make_params(const DecodeArgs& a, bool* ok) {
   HsaParams p;
   const uint64_t rows = (uint64_t)c.num_phys_pages * c.Hkv * c.page_size;
   *ok = encode_pool_map(&p.tmk, c.k_pages, rows) && encode_pool_map(&p.tmv, c.v_pages, rows);
-  const uint64_t srows = (uint64_t)c.B * c.Hkv * 128;
-  *ok = *ok && encode_summary_map(&p.tsmax, c.kmax, c.max_pages, srows) &&
-        encode_summary_map(&p.tsmin, c.kmin, c.max_pages, srows);
   p.k_pages = c.k_pages;
   p.v_pages = c.v_pages;
   p.page_table = c.page_table;

@@ -46,9 +46,6 @@ void set_last_error(const char* msg);
 // 128-byte swizzle (a box row is 128 B; its 16-byte pieces are XOR-ed with row % 8).
 // False when the driver's encoder is unavailable or rejects the map.
 bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
-// A channel-major summary array [rows][cols] bf16 (cols = max_pages, a multiple of 8)
-// as a 2-D tensor map with 64-page x 128-channel boxes, no swizzle.
-bool encode_summary_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows);
 
 // --------------------------------------------------------------- cache append
 cudaError_t launch_append(const rkv_cache& c, const rkv_bf16* k_new, const rkv_bf16* v_new,
