@@ -746,14 +746,29 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     Lmax_seen = a.prompt_len[b] > Lmax_seen ? a.prompt_len[b] : Lmax_seen;
     keep_max = a.keep1[b] > keep_max ? a.keep1[b] : keep_max;
   }
-  // keys per scoring CTA: 2048 (measured fastest once the grid covers the GPU), halved
-  // down to 512 while there would be fewer CTAs than SMs
-  p.item_keys = 2048;
-  for (;;) {
-    long items = 0;
-    for (int b = 0; b < a.B; ++b) items += (long)a.Hkv * ((a.prompt_len[b] + p.item_keys - 1) / p.item_keys);
-    if (items >= num_sms() || p.item_keys <= 512) break;
-    p.item_keys /= 2;
+  // keys per scoring CTA: a whole number of 128-key tiles T, chosen so that the waves
+  // of resident CTAs (two per SM) times the tiles each CTA scores, plus one tile of
+  // set-up per CTA, is least: the grid then ends in as few partial waves as the
+  // ragged lengths allow (at least 4 tiles a CTA, and within the split table)
+  {
+    const long slots = 2L * num_sms();
+    long best_cost = -1;
+    int best_t = 16;
+    const int t_min = (Lmax_seen + kMaxSnapSplit * kTcTile - 1) / (kMaxSnapSplit * kTcTile);
+    for (int t = t_min > 4 ? t_min : 4; t <= 512; ++t) {
+      long items = 0;
+      for (int b = 0; b < a.B; ++b) {
+        const int tiles = (a.prompt_len[b] + kTcTile - 1) / kTcTile;
+        items += (long)a.Hkv * ((tiles + t - 1) / t);
+      }
+      const long cost = ((items + slots - 1) / slots) * (t + 1);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_t = t;
+      }
+      if (items <= slots) break;  // one wave: larger items only lengthen it
+    }
+    p.item_keys = best_t * kTcTile;
   }
   p.nsplit = (Lmax_seen + p.item_keys - 1) / p.item_keys;
   if (p.nsplit > kMaxSnapSplit) {
