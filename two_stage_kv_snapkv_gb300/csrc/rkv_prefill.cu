@@ -14,8 +14,9 @@
 //                       (= sum_r exp(z - M_r) / l_r in base 2)
 //                       for prefix tokens t < L-w (the group sum is the row sum)
 //   snap_pool           centred max-pool of S (out-of-range positions ignored)
-//   snap_select         block radix select of the top keep1-w pooled positions
-//                       (value desc, position asc) + the window, ascending
+//   snap_select         adaptive-bin select on a thread-block cluster of the top
+//                       keep1-w pooled positions (value desc, position asc) + the
+//                       window, ascending
 //   snap_compact        gather of the survivors' K/V into the cache pages, their
 //                       Kmax/Kmin summaries, seq_len = keep1
 // The logits are tcgen05 MMAs (5th-generation tensor cores, bf16 in, fp32 out in
@@ -24,6 +25,8 @@
 // puts the query rows on the TMEM lanes (one row per epilogue thread: the row's
 // running max and sum stay in that thread); pass 2 swaps the operands so the keys
 // are the lanes (one key per thread: its column sum over the rows is a private loop).
+#include <cmath>
+
 #include <cooperative_groups.h>
 
 #include "rkv_device.cuh"
@@ -746,13 +749,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     Lmax_seen = a.prompt_len[b] > Lmax_seen ? a.prompt_len[b] : Lmax_seen;
     keep_max = a.keep1[b] > keep_max ? a.keep1[b] : keep_max;
   }
-  // keys per scoring CTA: a whole number of 128-key tiles T, chosen so that the waves
-  // of resident CTAs (two per SM) times the tiles each CTA scores, plus one tile of
-  // set-up per CTA, is least: the grid then ends in as few partial waves as the
-  // ragged lengths allow (at least 4 tiles a CTA, and within the split table)
+  // keys per scoring CTA: a whole number of 128-key tiles T.  Cost model, fitted to
+  // GB300 timings of 11, 16 and 23 tiles: a CTA costs T + 2.4 tiles (its set-up is
+  // worth 2.4); with three waves of resident CTAs (two per SM) or more, ragged CTAs
+  // balance out and the cost is the CTAs' total over the slots; with fewer, each wave
+  // costs a whole CTA.  The least-cost T from 4 tiles up (and within the split table).
   {
     const long slots = 2L * num_sms();
-    long best_cost = -1;
+    double best_cost = -1.0;
     int best_t = 16;
     const int t_min = (Lmax_seen + kMaxSnapSplit * kTcTile - 1) / (kMaxSnapSplit * kTcTile);
     for (int t = t_min > 4 ? t_min : 4; t <= 512; ++t) {
@@ -761,12 +765,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
         const int tiles = (a.prompt_len[b] + kTcTile - 1) / kTcTile;
         items += (long)a.Hkv * ((tiles + t - 1) / t);
       }
-      const long cost = ((items + slots - 1) / slots) * (t + 1);
-      if (best_cost < 0 || cost < best_cost) {
+      const double waves = (double)items / (double)slots;
+      const double eff = waves >= 3.0 ? waves : std::ceil(waves);
+      const double cost = eff * (t + 2.4);
+      if (best_cost < 0.0 || cost < best_cost) {
         best_cost = cost;
         best_t = t;
       }
-      if (items <= slots) break;  // one wave: larger items only lengthen it
+      if (items <= slots) break;  // one wave: larger CTAs only lengthen it
     }
     p.item_keys = best_t * kTcTile;
   }
