@@ -25,8 +25,6 @@
 // puts the query rows on the TMEM lanes (one row per epilogue thread: the row's
 // running max and sum stay in that thread); pass 2 swaps the operands so the keys
 // are the lanes (one key per thread: its column sum over the rows is a private loop).
-#include <cmath>
-
 #include <cooperative_groups.h>
 
 #include "rkv_device.cuh"
@@ -749,11 +747,11 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     Lmax_seen = a.prompt_len[b] > Lmax_seen ? a.prompt_len[b] : Lmax_seen;
     keep_max = a.keep1[b] > keep_max ? a.keep1[b] : keep_max;
   }
-  // keys per scoring CTA: a whole number of 128-key tiles T.  Cost model, fitted to
-  // GB300 timings of 11, 16 and 23 tiles: a CTA costs T + 2.4 tiles (its set-up is
-  // worth 2.4); with three waves of resident CTAs (two per SM) or more, ragged CTAs
-  // balance out and the cost is the CTAs' total over the slots; with fewer, each wave
-  // costs a whole CTA.  The least-cost T from 4 tiles up (and within the split table).
+  // keys per scoring CTA: a whole number of 128-key tiles T, the one of least cost
+  // (waves of resident CTAs, two per SM, rounded up) x (T + 2.4): a CTA's set-up is
+  // worth 2.4 tiles, and a partial last wave costs as much as a full one.  The model
+  // ranks 16, 23/24, 27, 32 and 35 tiles as GB300 timings did at 32K-109K prompts and
+  // batches 1-16 (from 4 tiles up, within the split table).
   {
     const long slots = 2L * num_sms();
     double best_cost = -1.0;
@@ -765,9 +763,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
         const int tiles = (a.prompt_len[b] + kTcTile - 1) / kTcTile;
         items += (long)a.Hkv * ((tiles + t - 1) / t);
       }
-      const double waves = (double)items / (double)slots;
-      const double eff = waves >= 3.0 ? waves : std::ceil(waves);
-      const double cost = eff * (t + 2.4);
+      const double cost = (double)((items + slots - 1) / slots) * (t + 2.4);
       if (best_cost < 0.0 || cost < best_cost) {
         best_cost = cost;
         best_t = t;
