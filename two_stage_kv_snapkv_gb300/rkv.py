@@ -7,6 +7,7 @@ torch tensors provide device memory and streams.  Importing this module loads
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 from typing import Optional, Sequence
@@ -147,9 +148,15 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+@functools.lru_cache(maxsize=256)
+def _host_i32_cached(values: tuple):
+    return (ctypes.c_int32 * len(values))(*values)
+
+
 def _host_i32(values: Sequence[int]):
-    arr = (ctypes.c_int32 * len(values))(*[int(v) for v in values])
-    return arr
+    """Host int32 array for the C call; the library only reads it during the call, so
+    arrays of the same values are built once and shared."""
+    return _host_i32_cached(tuple(int(v) for v in values))
 
 
 # ------------------------------------------------------------------ cache
