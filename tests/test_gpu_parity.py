@@ -260,9 +260,9 @@ def test_capacity_overflow_is_flagged(rkv, path):
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sampled_full(rkv, n, units, steps_checked, gen_device="cuda"):
+def _sampled_full(rkv, n, units, steps_checked, gen_device="cuda", layer=0):
     wl = W.workload(n)
-    run = GpuRun(wl, rkv, gen_device=gen_device, tail="zero")
+    run = GpuRun(wl, rkv, gen_device=gen_device, tail="zero", layer=layer)
     run.prefill()
     checks = [OracleUnit(run, b, g) for b, g in units]
     for u in checks:
@@ -302,6 +302,11 @@ def test_workload4_batched_ragged(rkv, path):
 
 def test_workload5_one_layer_sampled(rkv):
     assert _sampled_full(rkv, 5, [(0, 0), (7, 7)], {0, 63}) <= ATOL_OUT
+
+
+def test_workload5_last_layer_sampled(rkv):
+    """Layer 31 of the 32-layer workload: its own seeded keys, outlier channels and sinks."""
+    assert _sampled_full(rkv, 5, [(3, 2)], {0, 63}, layer=31) <= ATOL_OUT
 
 
 # ------------------------------------------------------------------ Exact-TopK recall diagnostic
