@@ -160,7 +160,7 @@ __device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int
       // rank = #(j < tid: key_j >= key) + #(j > tid: key_j > key); a group of four
       // wholly below this channel compares against key - 1
       int r0 = 0, r1 = 0;
-#pragma unroll
+#pragma unroll 4  // runs once per CTA: a short body fetches fewer cold instructions
       for (int j4 = 0; j4 < 32; ++j4) {
         const uint4 u = h4[j4];
         const uint32_t t = j4 < mine ? key - 1u : key;

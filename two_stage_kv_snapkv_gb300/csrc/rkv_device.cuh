@@ -602,7 +602,7 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
       const int ci = lane < nc ? ts.cand[lane] : 0;
       const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
       int r = 0;
-#pragma unroll
+#pragma unroll 4  // runs once per select: a short body fetches fewer cold instructions
       for (int m = 0; m < 32; ++m) {
         const uint32_t a = __shfl_sync(FULL, cu, m);
         const int cm = __shfl_sync(FULL, ci, m);
