@@ -11,7 +11,8 @@
 // * hsa_step_kernel (fused, one launch): one thread-block cluster per (sequence, KV
 //   head).  Optionally appends the new token first.  Every CTA selects the
 //   channels; each CTA stages the summaries of its slice of pages into shared
-//   memory (cp.async, one round trip) and bounds those pages; the page
+//   memory (all channels early for short slices, the chosen ones after the select
+//   for long slices) and bounds those pages; the page
 //   scores are shared through distributed shared memory; every CTA runs the same
 //   top-k2 select, attends over its share of the selected pages, and the CTAs'
 //   partial softmax states are merged through distributed shared memory.  Used
@@ -562,21 +563,18 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     mbar_init(&pbar, 1);
     fence_mbar_init();
   }
-  // this CTA's slice [p0, p1) of the pages (8-page aligned).  When the summaries of
-  // all 128 channels over the slice fit in the region, they are staged right away
-  // (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and the channels are
-  // chosen: rows of 64 pages or more by one bulk copy each (every row starts on a
-  // 16-byte boundary since max_pages and p0 are multiples of 8), shorter ones in
-  // 16-byte cp.async pieces (on GB300 the bulk copies cost 0.6 us more to issue at 32
-  // pages a row and saved about 1 us at 160).  Otherwise only the chosen channels' rows
-  // are staged, after the select.  The page-table row (needed after the select) comes
-  // by bulk copy.
+  // this CTA's slice [p0, p1) of the pages (8-page aligned).  Short slices (under 64
+  // pages) have the summaries of all 128 channels staged right away, in 16-byte
+  // cp.async pieces (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and
+  // the channels are chosen; longer ones stage only the chosen channels' rows, after
+  // the select (on GB300: early all-channel staging saved 0.5 us a step at 26 pages a
+  // slice; at 150-300 pages, waiting for the chosen half saved 0.5-2.9 us).  The
+  // page-table row (needed after the select) comes by bulk copy.
   const int per = ((NP + C - 1) / C + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
   const int slice8 = (p1 - p0 + 7) & ~7;
-  const bool all_ch = p1 > p0 && 2 * 128 * slice8 * 2 <= p.region_bytes;
-  const bool bulk_rows = all_ch && slice8 >= 64;
-  if (all_ch && !bulk_rows) {
+  const bool all_ch = p1 > p0 && slice8 < 64 && 2 * 128 * slice8 * 2 <= p.region_bytes;
+  if (all_ch) {
     const int cpr = slice8 >> 3;
     for (int e = tid; e < 256 * cpr; e += kThreads) {
       const int i = e / cpr, c = e - i * cpr;
@@ -587,7 +585,6 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
   }
   const int np4 = ((NP + 3) & ~3);  // whole 16-byte groups; within the row (max_pages % 8 == 0)
   if (tid == 0) {
-    if (bulk_rows) mbar_arrive_expect_tx(&sbar, (uint32_t)(256 * slice8 * 2));
     if (np4 > 0) {
       mbar_arrive_expect_tx(&pbar, (uint32_t)np4 * 4);
       bulk_g2s(ptab, p.page_table + (size_t)b * p.max_pages, (uint32_t)np4 * 4, &pbar);
@@ -596,12 +593,6 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     }
   }
   __syncthreads();
-  if (bulk_rows) {
-    for (int i = tid; i < 256; i += kThreads)
-      bulk_g2s(ring + (size_t)i * slice8 * 2,
-               (i < 128 ? p.kmax : p.kmin) + ((size_t)unit * 128 + (i & 127)) * p.max_pages + p0,
-               (uint32_t)slice8 * 2, &sbar);
-  }
 
   // 3. query of the group and the new token's rows into shared memory
   if (tid < G * 16) {  // 8 channels per thread
@@ -657,8 +648,7 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
     __syncthreads();  // the previous tile is consumed
     if (all_ch) {  // the one tile, staged at the start
-      if (!bulk_rows) cp_async_wait<0>();
-      else if (!mbar_wait(&sbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
+      cp_async_wait<0>();
     } else {
       // one bulk copy per row (the rows are long here: the slice did not fit whole)
       fence_proxy_async_smem();
