@@ -650,18 +650,33 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     if (all_ch) {  // the one tile, staged at the start
       cp_async_wait<0>();
     } else {
-      // one bulk copy per row (the rows are long here: the slice did not fit whole)
-      fence_proxy_async_smem();
-      if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
-      __syncthreads();
-      for (int i = tid; i < 2 * k1; i += kThreads) {
-        const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
-        const int ch = cs.chan[i < k1 ? i : i - k1];
-        bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0, (uint32_t)cnt8 * 2,
-                 &sbar);
+      if (cnt8 <= 256) {
+        // the chosen channels' rows in 16-byte pieces (one warp instruction moves 512
+        // B; on GB300 0.3-0.6 us a step faster than a bulk copy per row at 150-160 pages)
+        const int cpr = cnt8 >> 3;
+        for (int e = tid; e < 2 * k1 * cpr; e += kThreads) {
+          const int i = e / cpr, c = e - i * cpr;
+          const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
+          const int ch = cs.chan[i < k1 ? i : i - k1];
+          cp_async16(ring + (size_t)i * cnt8 * 2 + c * 16,
+                     base + ((size_t)unit * 128 + ch) * p.max_pages + t0 + c * 8, 16u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+      } else {
+        // one bulk copy per row (long rows: 0.2 us faster than pieces at 384 pages)
+        fence_proxy_async_smem();
+        if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
+        __syncthreads();
+        for (int i = tid; i < 2 * k1; i += kThreads) {
+          const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
+          const int ch = cs.chan[i < k1 ? i : i - k1];
+          bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0,
+                   (uint32_t)cnt8 * 2, &sbar);
+        }
+        if (!mbar_wait(&sbar, (uint32_t)(stile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
+        ++stile;
       }
-      if (!mbar_wait(&sbar, (uint32_t)(stile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
-      ++stile;
     }
     __syncthreads();
     append_loads();
