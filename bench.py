@@ -653,6 +653,8 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
     dq = {k: torch.empty_like(setup.inp[k]) for k in ("q_win", "k", "v")}
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + wl.steps * sum(sizes)
     d2h = hout.numel() * 4
+    host_step = setup.mode != "sparq"
+    staging = rkv.step_host_staging(wl.B, wl.Hq, wl.Hkv, setup.dev)
 
     def one():
         for k in host:
@@ -660,9 +662,13 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         rkv.rkv_prefill_evict(dq["q_win"], dq["k"], dq["v"], wl.prompt_lens, setup.keep1, setup.kp, setup.cache,
                               setup.kept, workspace=setup.pws)
         for t in range(wl.steps):
-            ddev.copy_(hdec[t], non_blocking=True)
-            setup.step(dd["q"], dd["k_new"], dd["v_new"], setup.out[t])
-            hout[t].copy_(setup.out[t], non_blocking=True)
+            if host_step:   # one call: input copy, the fused step, output copy
+                rkv.rkv_decode_step_host(setup.cache, hdec[t], hout[t], wl.Hq, setup.k1, setup.k2, staging,
+                                         setup.dws)
+            else:
+                ddev.copy_(hdec[t], non_blocking=True)
+                setup.step(dd["q"], dd["k_new"], dd["v_new"], setup.out[t])
+                hout[t].copy_(setup.out[t], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         one()
@@ -678,7 +684,9 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         times.append(e0.elapsed_time(e1))
     return dict(value=round(wl.steps * len(times) / (sum(times) / 1e3), 2), unit=UNIT, h2d_bytes_per_step=int(h2d),
                 d2h_bytes_per_step=int(d2h), ms_per_step=round(statistics.mean(times), 4),
-                path="python binding -> C ABI, eager launches, pinned host buffers (one input copy per step)")
+                path=("python binding -> C ABI rkv_decode_step_host (per call: the packed inputs copied in, the "
+                      "step, the output copied out), eager, pinned host buffers") if host_step else
+                     "python binding -> C ABI, eager launches, pinned host buffers (one input copy per step)")
 
 
 def run_reference(args, rank: int, world: int) -> dict:

@@ -266,6 +266,25 @@ rkv_status rkv_decode_step(const rkv_cache* cache, const rkv_bf16* q, const rkv_
                            int32_t sel_pages_stride, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* Bytes of device staging rkv_decode_step_host needs: the packed inputs, then out. */
+size_t rkv_step_host_staging_size(int32_t B, int32_t Hq, int32_t Hkv);
+
+/*
+ * rkv_decode_step with the step's inputs and output in host memory, for a caller
+ * whose tensors live on the host (pinned memory keeps the copies asynchronous).
+ *   host_in  : host, packed bf16: q [B][Hq][128], then k_new [B][Hkv][128], then
+ *              v_new [B][Hkv][128], contiguous.
+ *   host_out : host [B][Hq][128] fp32, written when the stream reaches the copy back.
+ *   staging  : device, rkv_step_host_staging_size(B, Hq, Hkv) bytes or more, 16-byte
+ *              aligned; receives the inputs (one host-to-device copy) and out.
+ * Enqueues on `stream`: the input copy, the decode step, the output copy (one
+ * device-to-host copy).  Other arguments as for rkv_decode_step.
+ */
+rkv_status rkv_decode_step_host(const rkv_cache* cache, const void* host_in, float* host_out,
+                                int32_t Hq, const int32_t* k1, const int32_t* k2, float scale,
+                                void* staging, size_t staging_bytes, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /*
  * Which implementation rkv_decode_hsa / rkv_decode_step use, process-wide:
  * 0 = automatic (the fused one-launch kernel whenever max_pages <= 4096),

@@ -227,3 +227,24 @@ def test_sparq_rejects_bad_arguments_without_launching(rkv):
     assert call(cache=_fake_cache(rkv, max_pages=4096, num_phys_pages=8192)) == rkv.RKV_ERR_UNSUPPORTED  # 64K tokens
     assert call(cache=_fake_cache(rkv, page_size=8)) == rkv.RKV_ERR_UNSUPPORTED
     assert rkv.rkv_launch_count() == before
+
+
+def test_decode_step_host_rejects_bad_arguments_without_launching(rkv):
+    lib = rkv.lib()
+    cache = _fake_cache(rkv, step_sync=0x78000)
+    i32 = ctypes.c_int32 * 2
+    need = lib.rkv_step_host_staging_size(2, 8, 2)
+    ws = lib.rkv_decode_workspace_size(2, 8, 2, cache.max_pages)
+
+    def call(staging=0xC0000, nbytes=need, host_in=0xD0000, k1=(32, 32)):
+        return lib.rkv_decode_step_host(ctypes.byref(cache), ctypes.c_void_p(host_in), ctypes.c_void_p(0xE0000), 8,
+                                        i32(*k1), i32(4, 4), ctypes.c_float(0.088), ctypes.c_void_p(staging), nbytes,
+                                        ctypes.c_void_p(0xA0000), ws, None)
+
+    before = rkv.rkv_launch_count()
+    assert need == 2 * (8 + 4) * 128 * 2 + 2 * 8 * 128 * 4   # the packed inputs (256-aligned), then out
+    assert call(nbytes=need - 1) == rkv.RKV_ERR_WORKSPACE
+    assert call(staging=0xC0008) == rkv.RKV_ERR_INVALID_ARG
+    assert call(host_in=0) == rkv.RKV_ERR_INVALID_ARG
+    assert call(k1=(0, 32)) == rkv.RKV_ERR_INVALID_ARG
+    assert rkv.rkv_launch_count() == before

@@ -376,3 +376,25 @@ def test_workload6_mt_batched_sampled(rkv):
     wl = W.workload(6)
     longest = int(np.argmax(wl.prompt_lens))
     assert _sampled_full(rkv, 6, [(longest, 2), (0, 5)], {0, 255}) <= ATOL_OUT
+
+
+def test_decode_step_from_host_buffers_matches(rkv):
+    """rkv_decode_step_host (host inputs and output) computes what rkv_decode_step does."""
+    wl = SMALL["gqa4_ragged"]
+    runs = [GpuRun(wl, rkv), GpuRun(wl, rkv)]
+    for r in runs:
+        r.prefill()
+    staging = rkv.step_host_staging(wl.B, wl.Hq, wl.Hkv)
+    for step in range(5):
+        d = W.decode_tensors(wl, step, runs[0].seed, 0, runs[0].dev)   # the same draws as decode_step's
+        host_in = torch.cat([d[k].contiguous().view(-1) for k in ("q", "k_new", "v_new")]).cpu().view(torch.uint8)
+        host_in = host_in.pin_memory()
+        host_out = torch.full((wl.B, wl.Hq, 128), float("nan")).pin_memory()
+        rkv.rkv_decode_step_host(runs[1].cache, host_in, host_out, wl.Hq, runs[1].k1, runs[1].k2, staging,
+                                 runs[1].dws)
+        _, out, _, _ = runs[0].decode_step(step)
+        torch.cuda.synchronize()
+        assert torch.equal(host_out, out.cpu())
+    assert torch.equal(runs[0].cache.seq_len, runs[1].cache.seq_len)
+    for r in runs:
+        assert r.status()[0] == rkv.RKV_OK

@@ -386,7 +386,8 @@ size_t rkv_decode_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max
 static rkv_status decode_common(const rkv_cache* cache, const rkv_bf16* q, const rkv_bf16* k_new,
                                 const rkv_bf16* v_new, int32_t Hq, const int32_t* k1, const int32_t* k2, float scale,
                                 float* out, int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
-                                void* workspace, size_t workspace_bytes, void* stream, const char* who) {
+                                void* workspace, size_t workspace_bytes, void* stream, const char* who,
+                                bool validate_only = false) {
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -411,6 +412,7 @@ static rkv_status decode_common(const rkv_cache* cache, const rkv_bf16* q, const
   const size_t need = rkv::decode_ws_bytes(cache->B, Hq, cache->Hkv, cache->max_pages);
   if (workspace_bytes < need)
     return fail(RKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (validate_only) return RKV_OK;
   rkv::DecodeArgs a;
   a.cache = *cache;
   a.q = q;
@@ -500,6 +502,43 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
   return cuda_status(rkv::launch_sparq(a, static_cast<cudaStream_t>(stream)), "rkv_decode_sparq launch");
+}
+
+size_t rkv_step_host_staging_size(int32_t B, int32_t Hq, int32_t Hkv) {
+  if (B < 1 || Hq < 1 || Hkv < 1) return 0;
+  const size_t in = (size_t)B * (Hq + 2 * Hkv) * RKV_HEAD_DIM * 2;
+  return ((in + 255) & ~size_t(255)) + (size_t)B * Hq * RKV_HEAD_DIM * 4;
+}
+
+rkv_status rkv_decode_step_host(const rkv_cache* cache, const void* host_in, float* host_out, int32_t Hq,
+                                const int32_t* k1, const int32_t* k2, float scale, void* staging,
+                                size_t staging_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+  rkv_status st = check_cache(cache);
+  if (st != RKV_OK) return st;
+  if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
+  if (!host_in || !host_out || !staging) return fail(RKV_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!al16(staging)) return fail(RKV_ERR_INVALID_ARG, "staging must be 16-byte aligned");
+  const size_t need = rkv_step_host_staging_size(cache->B, Hq, cache->Hkv);
+  if (staging_bytes < need) return fail(RKV_ERR_WORKSPACE, "staging %zu bytes < %zu needed", staging_bytes, need);
+  const size_t nq = (size_t)cache->B * Hq * RKV_HEAD_DIM, nkv = (size_t)cache->B * cache->Hkv * RKV_HEAD_DIM;
+  const size_t in_bytes = (nq + 2 * nkv) * 2;
+  uint8_t* dev = static_cast<uint8_t*>(staging);
+  const rkv_bf16* q = reinterpret_cast<const rkv_bf16*>(dev);
+  const rkv_bf16* k_new = q + nq;
+  const rkv_bf16* v_new = k_new + nkv;
+  float* out = reinterpret_cast<float*>(dev + ((in_bytes + 255) & ~size_t(255)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the step validates everything else before anything is enqueued
+  st = decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, nullptr, nullptr, 0, workspace, workspace_bytes,
+                     stream, "rkv_decode_step_host", true);
+  if (st != RKV_OK) return st;
+  cudaError_t e = cudaMemcpyAsync(dev, host_in, in_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_status(e, "rkv_decode_step_host input copy");
+  st = decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, nullptr, nullptr, 0, workspace, workspace_bytes,
+                     stream, "rkv_decode_step_host launch", false);
+  if (st != RKV_OK) return st;
+  e = cudaMemcpyAsync(host_out, out, (size_t)cache->B * Hq * RKV_HEAD_DIM * 4, cudaMemcpyDeviceToHost, s);
+  return cuda_status(e, "rkv_decode_step_host output copy");
 }
 
 rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* sel_pages,

@@ -92,6 +92,11 @@ _lib.rkv_decode_path.restype = _i32
 _lib.rkv_decode_hsa_noalloc.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp,
                                         _vp, _i32, _vp]
 _lib.rkv_decode_hsa_noalloc.restype = _i32
+_lib.rkv_step_host_staging_size.argtypes = [_i32, _i32, _i32]
+_lib.rkv_step_host_staging_size.restype = _sz
+_lib.rkv_decode_step_host.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _vp, _i32, _i32p, _i32p, _f32, _vp, _sz,
+                                      _vp, _sz, _vp]
+_lib.rkv_decode_step_host.restype = _i32
 _lib.rkv_sparq_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.rkv_sparq_workspace_size.restype = _sz
 _lib.rkv_decode_sparq.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp, _vp, _i32,
@@ -120,7 +125,7 @@ _lib.rkv_profile_read.restype = ctypes.c_char_p
 EXPORTED = ["rkv_split_ratio", "rkv_split_ratio_mt", "rkv_prefill_workspace_size", "rkv_prefill_evict",
             "rkv_prefill_chunk_workspace_size", "rkv_prefill_chunk", "rkv_append_page_summary",
             "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
-            "rkv_decode_path", "rkv_sparq_workspace_size", "rkv_decode_sparq", "rkv_exact_topk_recall", "rkv_get_device_status", "rkv_last_error",
+            "rkv_decode_path", "rkv_step_host_staging_size", "rkv_decode_step_host", "rkv_sparq_workspace_size", "rkv_decode_sparq", "rkv_exact_topk_recall", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
             "rkv_profile_reset", "rkv_profile_read"]
 
@@ -315,6 +320,26 @@ def rkv_decode_step(cache: PagedCache, q: torch.Tensor, k_new: torch.Tensor, v_n
     _check(_lib.rkv_decode_step(ctypes.byref(cache.struct), _ptr(q), _ptr(k_new), _ptr(v_new), Hq, _host_i32(k1),
                                 _host_i32(k2), scale, _ptr(out), _ptr(sel_channels), _ptr(sel_pages), stride,
                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def step_host_staging(B: int, Hq: int, Hkv: int, device="cuda") -> torch.Tensor:
+    n = _lib.rkv_step_host_staging_size(B, Hq, Hkv)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def rkv_decode_step_host(cache: PagedCache, host_in: torch.Tensor, host_out: torch.Tensor, Hq: int,
+                         k1: Sequence[int], k2: Sequence[int], staging: torch.Tensor, workspace: torch.Tensor,
+                         scale: Optional[float] = None, stream=None):
+    """rkv_decode_step from host buffers: host_in packs q, k_new, v_new (bf16, in that
+    order); host_out [B, Hq, 128] fp32 receives the output.  Pinned host tensors keep
+    the two copies asynchronous."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(HEAD_DIM)
+    if host_in.is_cuda or host_out.is_cuda:
+        raise ValueError("host_in and host_out are host tensors")
+    _check(_lib.rkv_decode_step_host(ctypes.byref(cache.struct), _ptr(host_in), _ptr(host_out), Hq, _host_i32(k1),
+                                     _host_i32(k2), scale, _ptr(staging), staging.numel(), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)))
 
 
 def sparq_workspace(B: int, Hq: int, Hkv: int, max_pages: int, page_size: int, device="cuda") -> torch.Tensor:
