@@ -92,7 +92,8 @@ typedef struct {
  *   step_sync        : [B] int32, zero when the cache is created; rkv_decode_step
  *                      uses it to advance seq_len exactly once per sequence and
  *                      leaves it at zero.  May be NULL if rkv_decode_step is not used.
- * max_pages must be a multiple of 8 and at most 16384 (RKV_ERR_UNSUPPORTED above).
+ * max_pages must be a multiple of 8 and at most 16384, and num_phys_pages * Hkv *
+ * page_size below 2^31 (RKV_ERR_UNSUPPORTED otherwise).
  */
 typedef struct {
   rkv_bf16* k_pages;

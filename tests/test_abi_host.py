@@ -248,3 +248,8 @@ def test_decode_step_host_rejects_bad_arguments_without_launching(rkv):
     assert call(host_in=0) == rkv.RKV_ERR_INVALID_ARG
     assert call(k1=(0, 32)) == rkv.RKV_ERR_INVALID_ARG
     assert rkv.rkv_launch_count() == before
+
+
+def test_page_pools_too_large_for_32_bit_rows_are_rejected(rkv):
+    cache = _fake_cache(rkv, num_phys_pages=1 << 22, Hkv=8, page_size=64)   # 2^31 rows
+    assert _decode_call(rkv, cache) == rkv.RKV_ERR_UNSUPPORTED

@@ -43,6 +43,8 @@ rkv_status check_cache(const rkv_cache* c) {
     return fail(RKV_ERR_INVALID_ARG, "max_pages=%d must be a positive multiple of 8", c->max_pages);
   if (c->max_pages > 16384) return fail(RKV_ERR_UNSUPPORTED, "max_pages=%d above 16384", c->max_pages);
   if (c->num_phys_pages < 1) return fail(RKV_ERR_INVALID_ARG, "num_phys_pages=%d", c->num_phys_pages);
+  if ((long long)c->num_phys_pages * c->Hkv * c->page_size >= (1LL << 31))
+    return fail(RKV_ERR_UNSUPPORTED, "the page pools' rows are indexed with 32-bit integers (TMA coordinates)");
   if (!c->k_pages || !c->v_pages || !c->page_table || !c->seq_len || !c->kmax || !c->kmin || !c->error_word)
     return fail(RKV_ERR_INVALID_ARG, "a cache pointer is NULL");
   if (!al16(c->k_pages) || !al16(c->v_pages) || !al16(c->page_table) || !al16(c->kmax) || !al16(c->kmin))
@@ -467,8 +469,6 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
     return fail(RKV_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(RKV_ERR_INVALID_ARG, "scale must be positive");
   const long cap = (long)cache->max_pages * cache->page_size;
-  if ((long long)cache->num_phys_pages * cache->Hkv * cache->page_size >= (1LL << 31))
-    return fail(RKV_ERR_UNSUPPORTED, "the token path indexes pool rows with 32-bit integers");
   if (cap > rkv::sparq_max_tokens())
     return fail(RKV_ERR_UNSUPPORTED, "the token path supports caches of at most %d tokens per sequence",
                 rkv::sparq_max_tokens());
