@@ -278,8 +278,11 @@ size_t rkv_step_host_staging_size(int32_t B, int32_t Hq, int32_t Hkv);
  *   host_out : host [B][Hq][128] fp32, written when the stream reaches the copy back.
  *   staging  : device, rkv_step_host_staging_size(B, Hq, Hkv) bytes or more, 16-byte
  *              aligned; receives the inputs (one host-to-device copy) and out.
- * Enqueues on `stream`: the input copy, the decode step, the output copy (one
- * device-to-host copy).  Other arguments as for rkv_decode_step.
+ * When both host buffers are pinned memory mapped into the device's address space
+ * (cudaHostAlloc / torch pin_memory, with unified addressing) and 16-byte aligned, the
+ * step's kernel reads the inputs and writes out through that mapping and nothing is
+ * copied; otherwise it enqueues on `stream` the input copy, the decode step and the
+ * output copy (one device-to-host copy).  Other arguments as for rkv_decode_step.
  */
 rkv_status rkv_decode_step_host(const rkv_cache* cache, const void* host_in, float* host_out,
                                 int32_t Hq, const int32_t* k1, const int32_t* k2, float scale,

@@ -504,6 +504,16 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
   return cuda_status(rkv::launch_sparq(a, static_cast<cudaStream_t>(stream)), "rkv_decode_sparq launch");
 }
 
+// Device address of pinned host memory mapped into the device's address space, else null.
+static const void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // unregistered memory: clear the sticky query error
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 size_t rkv_step_host_staging_size(int32_t B, int32_t Hq, int32_t Hkv) {
   if (B < 1 || Hq < 1 || Hkv < 1) return 0;
   const size_t in = (size_t)B * (Hq + 2 * Hkv) * RKV_HEAD_DIM * 2;
@@ -528,6 +538,15 @@ rkv_status rkv_decode_step_host(const rkv_cache* cache, const void* host_in, flo
   const rkv_bf16* v_new = k_new + nkv;
   float* out = reinterpret_cast<float*>(dev + ((in_bytes + 255) & ~size_t(255)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // pinned host buffers mapped into the device's address space (all pinned memory is,
+  // with unified addressing) are read and written by the kernel itself: no copies
+  const void* din = mapped_host(host_in);
+  void* dout = const_cast<void*>(mapped_host(host_out));
+  if (din && dout && al16(din) && al16(dout)) {
+    const rkv_bf16* hq = static_cast<const rkv_bf16*>(din);
+    return decode_common(cache, hq, hq + nq, hq + nq + nkv, Hq, k1, k2, scale, static_cast<float*>(dout), nullptr,
+                         nullptr, 0, workspace, workspace_bytes, stream, "rkv_decode_step_host launch");
+  }
   // the step validates everything else before anything is enqueued
   st = decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, nullptr, nullptr, 0, workspace, workspace_bytes,
                      stream, "rkv_decode_step_host", true);
