@@ -632,8 +632,9 @@ def _source_sha(rel: str) -> str:
 
 
 def run_e2e(setup: Setup, args, stream, rkv) -> dict:
-    """The same request through the public API from pinned host buffers: prompt and
-    per-step inputs copied in, every step's output copied out, inside the timed region."""
+    """The same request through the public API from pinned host buffers, inside the timed
+    region: the prompt copied in, then every step's inputs taken from and its output
+    returned to host memory."""
     wl = setup.wl
     host = {k: setup.inp[k].cpu().pin_memory() for k in ("q_win", "k", "v")}
     # a step's three inputs packed into one pinned buffer (q | k_new | v_new), so each
@@ -662,7 +663,7 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         rkv.rkv_prefill_evict(dq["q_win"], dq["k"], dq["v"], wl.prompt_lens, setup.keep1, setup.kp, setup.cache,
                               setup.kept, workspace=setup.pws)
         for t in range(wl.steps):
-            if host_step:   # one call: input copy, the fused step, output copy
+            if host_step:   # one call: the fused step on the host buffers
                 rkv.rkv_decode_step_host(setup.cache, hdec[t], hout[t], wl.Hq, setup.k1, setup.k2, staging,
                                          setup.dws)
             else:
@@ -684,8 +685,9 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         times.append(e0.elapsed_time(e1))
     return dict(value=round(wl.steps * len(times) / (sum(times) / 1e3), 2), unit=UNIT, h2d_bytes_per_step=int(h2d),
                 d2h_bytes_per_step=int(d2h), ms_per_step=round(statistics.mean(times), 4),
-                path=("python binding -> C ABI rkv_decode_step_host (per call: the packed inputs copied in, the "
-                      "step, the output copied out), eager, pinned host buffers") if host_step else
+                path=("python binding -> C ABI rkv_decode_step_host, eager, pinned host buffers (per call the "
+                      "fused step reads the packed inputs and writes the output through the buffers' device "
+                      "mapping; copy in, step, copy out where they are not mapped)") if host_step else
                      "python binding -> C ABI, eager launches, pinned host buffers (one input copy per step)")
 
 
