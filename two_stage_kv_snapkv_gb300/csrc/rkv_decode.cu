@@ -770,20 +770,29 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     }
   }
   // 7. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
-  // 128 pages by counting each key's rank, beyond that the histogram select with each
-  // thread's keys in registers (on GB300 the counting select was 0.3 us faster at ~90
-  // pages and 1-2 us slower at 200-300); the list is ascending.  The scratch lives in the
-  // region, free between the scoring and the attention.  (The key array is 16-byte
-  // aligned and followed by the list and the page-table row, so the histogram select's
-  // reads past NP stay inside this CTA's shared memory.)
+  // 128 pages by counting each key's rank, up to 1024 the histogram select with each
+  // thread's keys in registers, beyond that the same select looping over the keys in
+  // shared memory.  On GB300 the counting select was 0.3 us faster at ~90 pages and 1-2
+  // us slower at 200-300; at 1212 pages the looping select was 2.9 us faster than 16
+  // register keys a thread, at up to 1032 pages 0.3 us slower than 8.  The list is
+  // ascending.  The scratch lives in the region, free between the scoring and the
+  // attention.  (The key array is 16-byte aligned and followed by the list and the
+  // page-table row, so the register select's reads past NP stay inside this CTA's
+  // shared memory.)
   const int k = min(p.k2[b], NP);
   TopkSmem<kThreads>& tks = *reinterpret_cast<TopkSmem<kThreads>*>(ring);
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
   } else if (NP <= kThreads) {
     topk_rank<kThreads, 1>(keys, NP, k, tks, sel);
+  } else if (NP <= 2 * kThreads) {
+    topk_regs<kThreads, 2>(keys, NP, k, tks, sel);
+  } else if (NP <= 4 * kThreads) {
+    topk_regs<kThreads, 4>(keys, NP, k, tks, sel);
+  } else if (NP <= 8 * kThreads) {
+    topk_regs<kThreads, 8>(keys, NP, k, tks, sel);
   } else {
-    topk_regs_any<kThreads>(keys, NP, k, tks, sel);
+    topk_loop<kThreads>(keys, NP, k, tks, sel);
   }
   if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   __syncthreads();

@@ -736,15 +736,245 @@ __device__ void topk_rank(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   __syncthreads();  // the list is complete and the scratch may be reused
 }
 
-// topk_regs with the smallest keys-per-thread count that covers n (n <= 32 NT).
+// The select of topk_regs with the keys left in shared memory, for n beyond a few keys
+// per thread: thread t owns the 4 G consecutive keys from 4 G t (G = ceil(n / 4 NT)
+// groups of four, each read by one 16-byte load), and every pass is a short loop over
+// its groups.  A block runs the select once, so each of its instructions is fetched
+// cold; past four keys a thread, the unrolled passes of topk_regs cost more in
+// instruction fetches than their register-resident keys save.  Needs `keys` 16-byte
+// aligned; reads keys[0, n rounded up to a multiple of 4) only (entries from n on are
+// ignored).  Every thread of the block calls this.
 template <int NT>
-__device__ void topk_regs_any(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
-  if (n <= NT) topk_regs<NT, 1>(keys, n, k, ts, out);
-  else if (n <= 2 * NT) topk_regs<NT, 2>(keys, n, k, ts, out);
-  else if (n <= 4 * NT) topk_regs<NT, 4>(keys, n, k, ts, out);
-  else if (n <= 8 * NT) topk_regs<NT, 8>(keys, n, k, ts, out);
-  else if (n <= 16 * NT) topk_regs<NT, 16>(keys, n, k, ts, out);
-  else topk_regs<NT, 32>(keys, n, k, ts, out);
+__device__ void topk_loop(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
+  static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kTkBins / NT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = (n + 4 * NT - 1) / (4 * NT);
+  const int i0 = tid * 4 * G;
+  const int nv = max(0, min(4 * G, n - i0));  // valid keys of this thread: i0 .. i0 + nv - 1
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys + i0);
+  // Each pass below walks this thread's valid keys in ascending order: group q (one
+  // 16-byte load), then its members e = 0..3, key offset j = 4 q + e from i0.
+  uint4* h4 = reinterpret_cast<uint4*>(ts.hist);
+  for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) ts.ncand = 0;
+
+  // 1. the key range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll 1
+  for (int q = 0; 4 * q < nv; ++q) {
+    const uint4 v = k4[q];
+    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * q + e < nv) {
+        lo = min(lo, u4[e]);
+        hi = max(hi, u4[e]);
+      }
+  }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+  if (lane == 0) {
+    ts.wlo[warp] = lo;
+    ts.whi[warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, ts.wlo[w]);
+    hi = max(hi, ts.whi[w]);
+  }
+
+  // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
+  int need = k, nin = n;
+  bool cleared = true;
+  while (nin > kTkCand && lo != hi) {
+    if (!cleared) {
+      for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+    }
+    cleared = false;
+    const uint32_t range = hi - lo;
+    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
+    int run_bin = -1, run = 0;  // a run of keys in one bin adds to it once
+#pragma unroll 1
+    for (int q = 0; 4 * q < nv; ++q) {
+      const uint4 v = k4[q];
+      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t u = u4[e];
+        const int bin = (4 * q + e < nv && u >= lo && u <= hi) ? (int)((u - lo) >> shift) : -1;
+        if (bin != run_bin) {
+          if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
+          run_bin = bin;
+          run = 0;
+        }
+        ++run;
+      }
+    }
+    if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
+    __syncthreads();
+    uint32_t c[BPT];
+#pragma unroll
+    for (int j = 0; j < BPT; j += 4) {
+      const uint4 v = h4[(tid * BPT + j) >> 2];
+      c[j] = v.x;
+      c[j + 1] = v.y;
+      c[j + 2] = v.z;
+      c[j + 3] = v.w;
+    }
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) sum += (int)c[j];
+    int incl = sum;  // over the lanes >= this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(FULL, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    if (lane == 0) ts.wa[warp] = incl;
+    __syncthreads();
+    int above = incl - sum;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      if (w > warp) above += ts.wa[w];
+    if (above < need && above + sum >= need) {
+      int acc = above;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        if (acc + (int)c[j] >= need) {
+          ts.bstar = tid * BPT + j;
+          ts.need = need - acc;
+          ts.nb = (int)c[j];
+          break;
+        }
+        acc += (int)c[j];
+      }
+    }
+    __syncthreads();
+    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
+    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
+    lo = nlo;
+    need = ts.need;
+    nin = ts.nb;
+  }
+
+  // 3. the boundary pair (T, t), as in topk_regs
+  const bool all_in = need == nin;                // every key in [lo, hi] is taken
+  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
+  if (!by_index && !all_in) {
+    int cnt = 0;
+#pragma unroll 1
+    for (int q = 0; 4 * q < nv; ++q) {
+      const uint4 v = k4[q];
+      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cnt += 4 * q + e < nv && u4[e] >= lo && u4[e] <= hi;
+    }
+    if (cnt > 0) {
+      int slot = atomicAdd(&ts.ncand, cnt);
+#pragma unroll 1
+      for (int q = 0; 4 * q < nv; ++q) {
+        const uint4 v = k4[q];
+        const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * q + e < nv && u4[e] >= lo && u4[e] <= hi) {
+            if (slot < kTkCand) {
+              ts.cand[slot] = i0 + 4 * q + e;
+              ts.ckey[slot] = u4[e];
+            }
+            ++slot;
+          }
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nc = min(ts.ncand, kTkCand);
+      const int ci = lane < nc ? ts.cand[lane] : 0;
+      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
+      int r = 0;
+#pragma unroll 4
+      for (int m = 0; m < 32; ++m) {
+        const uint32_t a = __shfl_sync(FULL, cu, m);
+        const int cm = __shfl_sync(FULL, ci, m);
+        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
+      }
+      if (lane < nc && r == need - 1) {
+        ts.tkey = cu;
+        ts.tidx = ci;
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
+  const int tI = (by_index || all_in) ? n : ts.tidx;  // all_in: every key >= lo is taken
+
+  // 4. ascending compaction: 0 not taken, 1 taken, 2 a boundary key taken by index
+  int c1 = 0, c2 = 0;
+#pragma unroll 1
+  for (int q = 0; 4 * q < nv; ++q) {
+    const uint4 v = k4[q];
+    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t u = u4[e];
+      const int i = i0 + 4 * q + e;
+      const int t = 4 * q + e >= nv ? 0
+                    : u > hi        ? 1
+                    : u < lo        ? 0
+                    : by_index      ? 2
+                                    : ((u > T || (u == T && i <= tI)) ? 1 : 0);
+      c1 += t == 1;
+      c2 += t == 2;
+    }
+  }
+  int x1 = c1, x2 = c2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y1 = __shfl_up_sync(FULL, x1, o), y2 = __shfl_up_sync(FULL, x2, o);
+    if (lane >= o) {
+      x1 += y1;
+      x2 += y2;
+    }
+  }
+  if (lane == 31) {
+    ts.wa[warp] = x1;
+    ts.wb[warp] = x2;
+  }
+  __syncthreads();
+  int base = x1 - c1, bseen = x2 - c2;
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    if (w < warp) {
+      base += ts.wa[w];
+      bseen += ts.wb[w];
+    }
+  int o = base + min(need, bseen);
+#pragma unroll 1
+  for (int q = 0; 4 * q < nv; ++q) {
+    const uint4 v = k4[q];
+    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t u = u4[e];
+      const int i = i0 + 4 * q + e;
+      const int t = 4 * q + e >= nv ? 0
+                    : u > hi        ? 1
+                    : u < lo        ? 0
+                    : by_index      ? 2
+                                    : ((u > T || (u == T && i <= tI)) ? 1 : 0);
+      if (t == 1 || (t == 2 && bseen < need)) {
+        if (o < k) out[o] = i;
+        ++o;
+      }
+      bseen += t == 2;
+    }
+  }
+  __syncthreads();  // the scratch may be reused right after
 }
 
 }  // namespace rkv
