@@ -770,11 +770,11 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     }
   }
   // 7. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
-  // 128 pages by counting each key's rank, up to 1024 the histogram select with each
+  // 128 pages by counting each key's rank, up to 512 the histogram select with each
   // thread's keys in registers, beyond that the same select looping over the keys in
   // shared memory.  On GB300 the counting select was 0.3 us faster at ~90 pages and 1-2
   // us slower at 200-300; at 1212 pages the looping select was 2.9 us faster than 16
-  // register keys a thread, at up to 1032 pages 0.3 us slower than 8.  The list is
+  // register keys a thread, at 557-966 pages within 0.3 us of 8.  The list is
   // ascending.  The scratch lives in the region, free between the scoring and the
   // attention.  (The key array is 16-byte aligned and followed by the list and the
   // page-table row, so the register select's reads past NP stay inside this CTA's
@@ -789,8 +789,6 @@ __global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constan
     topk_regs<kThreads, 2>(keys, NP, k, tks, sel);
   } else if (NP <= 4 * kThreads) {
     topk_regs<kThreads, 4>(keys, NP, k, tks, sel);
-  } else if (NP <= 8 * kThreads) {
-    topk_regs<kThreads, 8>(keys, NP, k, tks, sel);
   } else {
     topk_loop<kThreads>(keys, NP, k, tks, sel);
   }
