@@ -167,14 +167,14 @@ def test_prefill_select_with_large_tie_groups(rkv, L):
     assert run.status()[0] == rkv.RKV_OK
 
 
-@pytest.mark.parametrize("L,budget", [(1500, 256), (6000, 4096), (12000, 8192), (20000, 16384)])
+@pytest.mark.parametrize("L,budget", [(1500, 256), (3000, 2048), (6000, 4096), (12000, 8192), (20000, 16384)])
 def test_decode_select_with_tied_page_scores(rkv, path, L, budget):
     """Every prompt key is the same vector, so every page of the compressed cache but the
     one taking the new tokens has the same Kmax/Kmin and the same bound.  The top-k2
-    boundary then falls inside a group of equal scores (about 50, 340, 690 or 1200 pages:
-    every kind of select the fused step has, from the counting ranks to the looping
-    histogram select) and the tied pages must go to the lowest page indices, as in the
-    oracle."""
+    boundary then falls inside a group of equal scores (about 50, 170, 340, 690 or 1200
+    pages: every kind of select the fused step has, from the counting ranks to the
+    looping histogram select) and the tied pages must go to the lowest page indices, as
+    in the oracle."""
     wl = W.custom(B=1, Hq=8, Hkv=2, prompt_lens=[L], budget=budget, window=16, page_size=16, steps=2,
                   pool_kernel=3)
     run = GpuRun(wl, rkv)
