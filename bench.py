@@ -623,12 +623,23 @@ def self_or_range(xs):
     return xs[0] if len(set(xs)) == 1 else f"{min(xs)}..{max(xs)}"
 
 
+# the headers every kernel source includes: part of each kernel's code
+KERNEL_HEADERS = ("two_stage_kv_snapkv_gb300/csrc/rkv_device.cuh", "two_stage_kv_snapkv_gb300/csrc/rkv_internal.h",
+                  "include/rkv.h")
+
+
 def _source_sha(rel: str) -> str:
+    """sha256 (first 16 hex digits) of a kernel source file followed by KERNEL_HEADERS;
+    a kernel's recorded DRAM counters stay valid while this is unchanged."""
     import hashlib
-    path = os.path.join(ROOT, rel)
-    if not rel or not os.path.exists(path):
-        return ""
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in (rel, *KERNEL_HEADERS) if rel else ():
+        path = os.path.join(ROOT, f)
+        if not os.path.exists(path):
+            return ""
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16] if rel else ""
 
 
 def run_e2e(setup: Setup, args, stream, rkv) -> dict:
