@@ -10,11 +10,21 @@
 #include <atomic>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "rkv.h"
 #include "rkv_internal.h"
 
 namespace {
+
+// An NVTX range over one library call, named after it: the calls show up on an Nsight
+// timeline around their kernels.  Without a tool attached a push or pop is a no-op.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 thread_local std::string g_err;
 std::atomic<long long> g_launches{0};
@@ -255,6 +265,7 @@ rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv
                              const int32_t* pool_kernel, float scale, const rkv_cache* cache, int32_t* kept_idx,
                              int32_t kept_stride, float* pooled_scores, void* workspace, size_t workspace_bytes,
                              void* stream) {
+  const NvtxRange nvtx_range("rkv_prefill_evict");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -316,6 +327,7 @@ rkv_status rkv_prefill_chunk(const rkv_bf16* q_win, const rkv_bf16* k_chunk, con
                              const int32_t* held_len, const int32_t* keep1, const int32_t* pool_kernel, float scale,
                              const rkv_cache* cache, int32_t* kept_idx, int32_t kept_stride, void* workspace,
                              size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("rkv_prefill_chunk");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -370,6 +382,7 @@ rkv_status rkv_prefill_chunk(const rkv_bf16* q_win, const rkv_bf16* k_chunk, con
 
 rkv_status rkv_append_page_summary(const rkv_cache* cache, const rkv_bf16* k_new, const rkv_bf16* v_new,
                                    int32_t n_new, void* stream) {
+  const NvtxRange nvtx_range("rkv_append_page_summary");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if (n_new < 1) return fail(RKV_ERR_INVALID_ARG, "n_new=%d", n_new);
@@ -438,6 +451,7 @@ static rkv_status decode_common(const rkv_cache* cache, const rkv_bf16* q, const
 rkv_status rkv_decode_hsa(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* k1, const int32_t* k2,
                           float scale, float* out, int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride,
                           void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("rkv_decode_hsa");
   return decode_common(cache, q, nullptr, nullptr, Hq, k1, k2, scale, out, sel_channels, sel_pages, sel_pages_stride,
                        workspace, workspace_bytes, stream, "rkv_decode_hsa launch");
 }
@@ -446,6 +460,7 @@ rkv_status rkv_decode_step(const rkv_cache* cache, const rkv_bf16* q, const rkv_
                            int32_t Hq, const int32_t* k1, const int32_t* k2, float scale, float* out,
                            int32_t* sel_channels, int32_t* sel_pages, int32_t sel_pages_stride, void* workspace,
                            size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("rkv_decode_step");
   if (!k_new || !v_new) return fail(RKV_ERR_INVALID_ARG, "rkv_decode_step needs k_new and v_new");
   return decode_common(cache, q, k_new, v_new, Hq, k1, k2, scale, out, sel_channels, sel_pages, sel_pages_stride,
                        workspace, workspace_bytes, stream, "rkv_decode_step launch");
@@ -460,6 +475,7 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
                             const int32_t* k_tokens, float scale, float* out, int32_t* sel_channels,
                             int32_t* sel_tokens, int32_t sel_tokens_stride, void* workspace, size_t workspace_bytes,
                             void* stream) {
+  const NvtxRange nvtx_range("rkv_decode_sparq");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -523,6 +539,7 @@ size_t rkv_step_host_staging_size(int32_t B, int32_t Hq, int32_t Hkv) {
 rkv_status rkv_decode_step_host(const rkv_cache* cache, const void* host_in, float* host_out, int32_t Hq,
                                 const int32_t* k1, const int32_t* k2, float scale, void* staging,
                                 size_t staging_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("rkv_decode_step_host");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -563,6 +580,7 @@ rkv_status rkv_decode_step_host(const rkv_cache* cache, const void* host_in, flo
 rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* sel_pages,
                                  int32_t sel_pages_stride, const int32_t* k_tokens, float scale, float* recall,
                                  float* mass, void* stream) {
+  const NvtxRange nvtx_range("rkv_exact_topk_recall");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
   if ((st = check_heads(Hq, cache->Hkv)) != RKV_OK) return st;
@@ -595,6 +613,7 @@ int32_t rkv_decode_path(int32_t path) {
 }
 
 rkv_status rkv_get_device_status(const rkv_cache* cache, void* stream, int32_t* bits) {
+  const NvtxRange nvtx_range("rkv_get_device_status");
   if (!cache || !cache->error_word) return fail(RKV_ERR_INVALID_ARG, "cache or error_word is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t word = 0;
