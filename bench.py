@@ -87,6 +87,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
+        self.skip = 0
         self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
 
     def __enter__(self):
@@ -96,6 +97,15 @@ class ClockSampler:
                  "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        # start timing only once the sampler is writing (nvidia-smi takes a moment to
+        # start), so that a short timed region still gets its samples; at most 3 s
+        t0 = time.time()
+        while self.proc is not None and self.proc.poll() is None and time.time() - t0 < 3.0:
+            if os.path.getsize(self.tmp.name) > 0:
+                break
+            time.sleep(0.01)
+        with open(self.tmp.name) as f:   # samples taken before the timed region
+            self.skip = sum(1 for line in f if line.endswith("\n"))
         return self
 
     def __exit__(self, *a):
@@ -115,6 +125,8 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.tmp.name)
+        if len(rows) > self.skip:   # keep only the samples taken during the timed region
+            rows = rows[self.skip:]
         if not rows:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], samples=0)
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -546,7 +558,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         decode_compulsory_mb_per_step=round(step_total / 1e6, 3),
         prefill_achieved_gbs=round(pb["total"] / (pre_layer_ms * 1e-3) / 1e9, 1),
         roofline=roofline, kernels=kernels, gpu_launches=int(launches_per_pass * args.steps),
-        clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"]),
+        clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"],
+                    samples=clocks["samples"]),
     )
     if multi:
         res["prefill_all_layers_ms"] = round(statistics.mean(pre_all), 4)
