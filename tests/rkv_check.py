@@ -11,7 +11,6 @@ Comparison rules (the tolerances the hot path is held to):
 """
 from __future__ import annotations
 
-import math
 
 import numpy as np
 import torch

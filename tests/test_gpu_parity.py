@@ -4,7 +4,6 @@ Small cases run the whole path (prefill, every decode step) unit by unit; the
 full-size workloads run in the launch configuration the bench uses and are
 checked on sampled (sequence, KV head) units.
 """
-import math
 
 import numpy as np
 import pytest
@@ -13,7 +12,7 @@ import torch
 from oracle import rkv_oracle as O
 from two_stage_kv_snapkv_gb300 import workloads as W
 
-from rkv_check import ATOL_OUT, GpuRun, OracleUnit, check_topk, f64
+from rkv_check import ATOL_OUT, GpuRun, OracleUnit, f64
 
 pytestmark = pytest.mark.gpu
 
