@@ -43,8 +43,11 @@ Parity status per function (what pins it, in tests/test_oracle_pins.py):
   exact_token_scores ..... group sum == G, one-head case == scipy softmax (library)
   exact_topk_recall ...... all pages -> 1, the top-K's own pages -> 1,
                            K >= n closed form, brute force on tiny inputs
-  default_pool_kernel .... PARITY UNPINNED (the pages give no rule)
-  derived k1 in split .... PARITY UNPINNED (the pages give no rule)
+  default_pool_kernel .... pinned only at the three prompt lengths the benchmark
+                           workloads fix (4K -> 7, 32K -> 31, 109K -> 63); the pages
+                           give no rule, so between them it is a reading
+  derived k1 in split .... pinned only at the tiny workload's given k1 = 64 (4K,
+                           budget 256); elsewhere a reading (the pages give no rule)
 """
 from __future__ import annotations
 
@@ -84,8 +87,9 @@ def default_pool_kernel(prompt_len: int) -> int:
     [abstract] says SnapKV++ uses an "adaptive pooling size"; [summary, Approach]
     says "large pooling kernel".  Neither gives the rule.  READING: the kernel
     grows with prompt length, 7 up to 8K tokens, 31 up to 48K, 63 beyond.  This
-    reproduces the three sizes the workloads fix (4K->7, 32K->31, 109K->63).
-    PARITY UNPINNED.
+    reproduces the three sizes the workloads fix (4K->7, 32K->31, 109K->63),
+    which tests/golden/pool_kernel_workloads.json pins; between those points the
+    thresholds (8K, 48K) are a reading nothing on the pages can pin.
     """
     if prompt_len <= 8192:
         return 7
@@ -107,7 +111,8 @@ def split_ratio(prompt_len: int, budget: int, head_dim: int, page_size: int,
               including the observation window);
       k2    = budget // page_size (pages attended per step, so k2*P = budget);
       k1    = 16*round(d / (16*sqrt(c2))) clamped to [16, d]: stage 2's ratio is split
-              evenly between the head and sequence dimensions (PARITY UNPINNED);
+              evenly between the head and sequence dimensions (pinned only where a
+              workload fixes k1: 64 at 4K / budget 256);
               k1_override replaces it ([adapted] exposes rocketkv_head_topk1).
     """
     c = prompt_len / budget

@@ -55,6 +55,17 @@ def test_host_split_matches_oracle(rkv, L, budget, P, k1o):
         assert a[key] == pytest.approx(b[key], rel=1e-12), key
 
 
+def test_host_split_pool_kernel_matches_the_workloads(rkv):
+    # the C ABI's default pooling kernel reproduces the sizes the benchmark workloads fix
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "pool_kernel_workloads.json")))
+    for c in g["cases"]:
+        s = rkv.rkv_split_ratio(c["prompt_len"], c["budget"], 128, c["page_size"], 32, 0)
+        assert s["pool_kernel"] == c["pool_kernel"], c["workload"]
+        if "k1" in c:
+            assert s["k1"] == c["k1"], c["workload"]
+
+
 def test_split_rejects_bad_sizes(rkv):
     with pytest.raises(rkv.RkvError) as e:
         rkv.rkv_split_ratio(0, 256)

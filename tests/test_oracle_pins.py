@@ -68,6 +68,24 @@ def test_split_niah_ratio():
     assert 0.72 < s["r"] < 0.8           # not clipped: log2(425.8) < 10
 
 
+def test_default_pool_kernel_matches_the_workloads():
+    # the only sizes anything fixes: the three benchmark workloads that state a pooling
+    # kernel (4K -> 7, 32K -> 31, 109K -> 63); the rule must reproduce each of them, and
+    # the tiny workload's k1 = 64 must come out of the derived split without an override
+    g = json.load(open(os.path.join(GOLD, "pool_kernel_workloads.json")))
+    for c in g["cases"]:
+        assert O.default_pool_kernel(c["prompt_len"]) == c["pool_kernel"], c["workload"]
+        s = O.split_ratio(c["prompt_len"], c["budget"], 128, c["page_size"], 32)
+        assert s["pool_kernel"] == c["pool_kernel"], c["workload"]
+        if "k1" in c:
+            assert s["k1"] == c["k1"], c["workload"]
+    # the kernel is keyed by prompt length, not by the ratio: the same prompt at another
+    # budget pools alike, and the 4K and 109K prompts at equal c differ
+    assert O.split_ratio(32768, 2048, 128, 32, 32)["pool_kernel"] == 31
+    assert O.split_ratio(4096, 16, 128, 16, 32)["pool_kernel"] == 7
+    assert O.split_ratio(109000, 6812, 128, 16, 32)["pool_kernel"] == 63
+
+
 def test_split_derived_sizes():
     # readings (keep1 = round(L/c1), k2 = budget/P, k1 from sqrt(c2)) on the workloads
     cases = [  # L, budget, P, k1_override -> keep1, k1, k2
