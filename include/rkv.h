@@ -374,6 +374,18 @@ rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int3
                                  const int32_t* k_tokens, float scale, float* recall, float* mass,
                                  void* stream);
 
+/*
+ * Self-test of the device failure path (not a step of the method; the pages describe
+ * no GPU code).  Every wait of the library's kernels on an mbarrier (a TMA or bulk
+ * copy landing, another warp's hand-off) gives up after 1 s, sets RKV_DEVERR_TIMEOUT
+ * in cache->error_word, drains what it issued and returns, so a stall never hangs the
+ * GPU.  This call launches one CTA that waits, for at most limit_ns nanoseconds
+ * (1 <= limit_ns <= 1e9), on an mbarrier nothing arrives on and no copy targets; the
+ * wait runs out and the bit is set exactly as a stalled kernel would set it, so that
+ * rkv_get_device_status then returns RKV_ERR_TIMEOUT.  Only error_word is touched.
+ */
+rkv_status rkv_selftest_bounded_wait(const rkv_cache* cache, int64_t limit_ns, void* stream);
+
 /* Synchronise `stream`, read and clear cache->error_word.  RKV_OK when it was 0,
  * RKV_ERR_TIMEOUT when the timeout bit was set, else RKV_ERR_DEVICE_DATA; *bits
  * (if not NULL) receives the raw word. */

@@ -260,10 +260,63 @@ def test_capacity_overflow_is_flagged(rkv, path):
     assert int(run.cache.seq_len[0].item()) == cap
 
 
+def test_bounded_wait_runs_out_and_reports_timeout(rkv):
+    """The failure path of every bounded device wait: a wait on an mbarrier that nothing
+    arrives on runs out, sets the timeout bit, and the host reads RKV_ERR_TIMEOUT; the
+    context stays usable and the next decode step is clean and correct."""
+    wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    unit = OracleUnit(run, 0, 0)
+    unit.check_prefill(run)
+    assert run.status() == (rkv.RKV_OK, 0)
+    for limit_ns in (2_000, 200_000):
+        rkv.rkv_selftest_bounded_wait(run.cache, limit_ns)
+        st, bits = run.status()
+        assert st == rkv.RKV_ERR_TIMEOUT and bits == rkv.DEVERR_TIMEOUT, (st, bits)
+        assert run.status() == (rkv.RKV_OK, 0)   # the word was cleared
+    with pytest.raises(rkv.RkvError):
+        rkv.rkv_selftest_bounded_wait(run.cache, 0)
+    d, out, ch, pg = run.decode_step(0)
+    assert unit.step(run, d, out, ch, pg, check_cache=True)["err"] <= ATOL_OUT
+    assert run.status() == (rkv.RKV_OK, 0)
+
+
+@pytest.mark.parametrize("name", ["gqa4_ragged", "gqa2_p32", "p64_outliers"])
+def test_quest_only_small(rkv, path, name):
+    """Quest-only (the summary page's ablation of HSA's halves): every channel bounds
+    the pages (k1 = 128) while only k2 < NP pages are attended.  Channel and page sets
+    and the output against the oracle's HSA at k1 = d."""
+    wl = SMALL[name]
+    run = GpuRun(wl, rkv)
+    run.k1 = [128] * wl.B
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in units:
+            res = u.step(run, d, out, ch, pg, check_cache=(step % 4 == 0))
+            assert len(res["pages"]) < res["sig"].shape[0], "every page selected: not a Quest-only case"
+            assert np.array_equal(np.sort(ch[u.b, u.g].cpu().numpy()), np.arange(128))
+    assert run.status() == (rkv.RKV_OK, 0)
+
+
+def test_quest_only_workload4_sampled(rkv, path):
+    """Quest-only at full size: workload 4's batch with k1 = 128, sampled units."""
+    wl = W.workload(4)
+    longest = int(np.argmax(wl.prompt_lens))
+    shortest = int(np.argmin(wl.prompt_lens))
+    assert _sampled_full(rkv, 4, [(longest, 3), (shortest, 0)], {0, 255}, k1=128) <= ATOL_OUT
+
+
 # ------------------------------------------------------------------ full-size workloads
-def _sampled_full(rkv, n, units, steps_checked, gen_device="cuda", layer=0):
+def _sampled_full(rkv, n, units, steps_checked, gen_device="cuda", layer=0, k1=None):
     wl = W.workload(n)
     run = GpuRun(wl, rkv, gen_device=gen_device, tail="zero", layer=layer)
+    if k1 is not None:
+        run.k1 = [k1] * wl.B
     run.prefill()
     checks = [OracleUnit(run, b, g) for b, g in units]
     for u in checks:

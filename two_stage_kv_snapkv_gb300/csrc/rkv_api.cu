@@ -127,7 +127,7 @@ const char* kernel_name(int kind) {
       "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
       "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
       "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step",     "recall",
-      "chunk_gather", "sparq_score",  "sparq_topk",     "sparq_attend"};
+      "chunk_gather", "sparq_score",  "sparq_topk",     "sparq_attend", "wait_selftest"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
 }
 
@@ -605,6 +605,17 @@ rkv_status rkv_exact_topk_recall(const rkv_cache* cache, const rkv_bf16* q, int3
   a.recall = recall;
   a.mass = mass;
   return cuda_status(rkv::launch_recall(a, static_cast<cudaStream_t>(stream)), "rkv_exact_topk_recall launch");
+}
+
+rkv_status rkv_selftest_bounded_wait(const rkv_cache* cache, int64_t limit_ns, void* stream) {
+  const NvtxRange nvtx_range("rkv_selftest_bounded_wait");
+  if (!cache || !cache->error_word) return fail(RKV_ERR_INVALID_ARG, "cache or error_word is NULL");
+  if (reinterpret_cast<uintptr_t>(cache->error_word) & 3u)
+    return fail(RKV_ERR_INVALID_ARG, "error_word must be 4-byte aligned");
+  if (limit_ns < 1 || limit_ns > 1000000000LL)
+    return fail(RKV_ERR_INVALID_ARG, "limit_ns=%lld must be in [1, 1e9]", (long long)limit_ns);
+  return cuda_status(rkv::launch_wait_selftest(cache->error_word, (uint64_t)limit_ns, static_cast<cudaStream_t>(stream)),
+                     "rkv_selftest_bounded_wait launch");
 }
 
 int32_t rkv_decode_path(int32_t path) {

@@ -106,13 +106,17 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for phase `parity` of `bar` for at most ~1 s; false when the time ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Time limit of every wait on an mbarrier in the library's kernels: far beyond any
+// copy's latency, short enough that a wait nothing will end returns control.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Wait for phase `parity` of `bar` for at most limit_ns; false when the time ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u && global_ns() - t0 > 1000000000ull) return false;
+    if ((it & 63u) == 63u && global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -237,4 +237,27 @@ cudaError_t launch_recall(const RecallArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Self-test of the failure path every kernel shares: one thread waits on an mbarrier
+// that nothing arrives on and no copy completes, so the bounded wait must run out; it
+// then flags RKV_DEVERR_TIMEOUT exactly as a stalled ring would.  Nothing is in
+// flight on the barrier, so the CTA may exit at once.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, limit_ns)) flag_error(err, RKV_DEVERR_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(int32_t* err, uint64_t limit_ns, cudaStream_t s) {
+  launch_begin(K_WAIT_SELFTEST, s);
+  wait_selftest_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  launch_end(K_WAIT_SELFTEST, s);
+  return cudaGetLastError();
+}
+
 }  // namespace rkv

@@ -31,6 +31,7 @@ enum KernelKind {
   K_SPARQ_SCORE,
   K_SPARQ_TOPK,
   K_SPARQ_ATTEND,
+  K_WAIT_SELFTEST,
   K_NUM_KINDS
 };
 const char* kernel_name(int kind);
@@ -132,5 +133,9 @@ struct RecallArgs {
 };
 int recall_max_tokens();
 cudaError_t launch_recall(const RecallArgs& a, cudaStream_t s);
+
+// One CTA that waits, for at most limit_ns, on an mbarrier nothing arrives on, and
+// flags RKV_DEVERR_TIMEOUT in err when the wait runs out (the failure path's test).
+cudaError_t launch_wait_selftest(int32_t* err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace rkv

@@ -105,6 +105,8 @@ _lib.rkv_decode_sparq.restype = _i32
 _lib.rkv_exact_topk_recall.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _vp, _i32, _i32p, _f32, _vp, _vp,
                                        _vp]
 _lib.rkv_exact_topk_recall.restype = _i32
+_lib.rkv_selftest_bounded_wait.argtypes = [ctypes.POINTER(RkvCacheStruct), ctypes.c_int64, _vp]
+_lib.rkv_selftest_bounded_wait.restype = _i32
 _lib.rkv_get_device_status.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32p]
 _lib.rkv_get_device_status.restype = _i32
 _lib.rkv_last_error.argtypes = []
@@ -125,7 +127,7 @@ _lib.rkv_profile_read.restype = ctypes.c_char_p
 EXPORTED = ["rkv_split_ratio", "rkv_split_ratio_mt", "rkv_prefill_workspace_size", "rkv_prefill_evict",
             "rkv_prefill_chunk_workspace_size", "rkv_prefill_chunk", "rkv_append_page_summary",
             "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
-            "rkv_decode_path", "rkv_step_host_staging_size", "rkv_decode_step_host", "rkv_sparq_workspace_size", "rkv_decode_sparq", "rkv_exact_topk_recall", "rkv_get_device_status", "rkv_last_error",
+            "rkv_decode_path", "rkv_step_host_staging_size", "rkv_decode_step_host", "rkv_sparq_workspace_size", "rkv_decode_sparq", "rkv_exact_topk_recall", "rkv_selftest_bounded_wait", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
             "rkv_profile_reset", "rkv_profile_read"]
 
@@ -386,6 +388,10 @@ def rkv_exact_topk_recall(cache: PagedCache, q: torch.Tensor, sel_pages: torch.T
 def rkv_decode_path(path: int = -1) -> int:
     """0 auto (fused when it fits), 1 four-kernel path, 2 fused; -1 only reads the setting."""
     return int(_lib.rkv_decode_path(path))
+
+
+def rkv_selftest_bounded_wait(cache: PagedCache, limit_ns: int, stream=None) -> None:
+    _check(_lib.rkv_selftest_bounded_wait(ctypes.byref(cache.struct), int(limit_ns), _stream(stream)))
 
 
 def rkv_get_device_status(cache: PagedCache, stream=None) -> tuple:
