@@ -82,13 +82,24 @@ def _compare_two_calls(rkv):
 
 
 def test_noalloc_rejects_caches_beyond_its_scratch(rkv):
-    # 256 sequences x 8 query heads need 2048 x 64 split partials of 512 B: > 32 MiB
-    c = rkv.RkvCacheStruct(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000, 0x78000,
-                           256, 1, 128, 16, 64, 256 * 64)
-    k = (ctypes.c_int32 * 256)(*([32] * 256))
+    # 256 sequences x 8 query heads need 2048 x 64 split partials of 512 B: > 32 MiB.
+    # The cache, query and output are real (small) device allocations, so even if the
+    # size check ever let this call through, no kernel would touch unmapped memory.
+    lib = rkv.lib()
+    B, Hq, Hkv, max_pages = 256, 8, 1, 64
+    need = lib.rkv_decode_workspace_size(B, Hq, Hkv, max_pages)
+    if need <= 32 << 20:
+        pytest.fail(f"this case no longer exceeds the 32 MiB scratch ({need} bytes); pick a larger one")
+    dev = torch.device("cuda")
+    cache = rkv.PagedCache(B, Hkv, 16, max_pages, dev, fill=0.0)
+    q = torch.zeros((B, Hq, 128), dtype=torch.bfloat16, device=dev)
+    out = torch.zeros((B, Hq, 128), dtype=torch.float32, device=dev)
+    k = (ctypes.c_int32 * B)(*([32] * B))
+    torch.cuda.synchronize()
     before = rkv.rkv_launch_count()
-    st = rkv.lib().rkv_decode_hsa_noalloc(ctypes.byref(c), ctypes.c_void_p(0x80000), 8, k, k,
-                                          ctypes.c_float(0.088), ctypes.c_void_p(0x90000), None, None, 0, None)
+    st = lib.rkv_decode_hsa_noalloc(ctypes.byref(cache.struct), ctypes.c_void_p(q.data_ptr()), Hq, k, k,
+                                    ctypes.c_float(0.088), ctypes.c_void_p(out.data_ptr()), None, None, 0,
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == rkv.RKV_ERR_WORKSPACE
     assert "32 MiB" in rkv.rkv_last_error()
     assert rkv.rkv_launch_count() == before

@@ -13,6 +13,9 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "rkv.h"
 #include "rkv_internal.h"
 
@@ -26,22 +29,51 @@ constexpr int kMaxDevices = 128;
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices];
+// The looked-up address per device, with the context it was looked up in: after a
+// cudaDeviceReset the device gets a new primary context, the old address is stale,
+// and the next call looks it up again.
+struct Slot {
+  CUcontext ctx;
+  void* ptr;
+};
+Slot g_scratch[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per device.
+// The current context of the calling thread (cuCtxGetCurrent, taken from the driver
+// through the runtime so the library needs no link against libcuda).
+cudaError_t current_context(CUcontext* out) {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 get = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  if (!get) return cudaErrorNotSupported;
+  return get(out) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch on the current device: looked up on the first call in
+// each (device, context), then reused.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CUcontext ctx = nullptr;
+  if (current_context(&ctx) != cudaSuccess) ctx = nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  Slot& sl = g_scratch[dev];
+  if (!sl.ptr || !ctx || sl.ctx != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // makes the primary context current if none was
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    if (current_context(&ctx) != cudaSuccess) ctx = nullptr;
+    sl.ptr = p;
+    sl.ctx = ctx;
   }
-  *out = g_scratch_ptr[dev];
+  *out = sl.ptr;
   return cudaSuccess;
 }
 
