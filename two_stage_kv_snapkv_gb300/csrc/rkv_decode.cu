@@ -401,22 +401,49 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
       fence_proxy_async_smem();
       __syncwarp();
     }
+    // The chunk's K and V fragments move to registers first, so its stage can be
+    // refilled (the next chunk's copies issued) before the arithmetic: each warp then
+    // keeps STAGES chunks in flight while it computes.
+    const uint32_t kb32 = smem_u32(kb), vb32 = smem_u32(vb);
+    uint32_t kf[4][2][4], vf[8][4];
+#pragma unroll
+    for (int kk2 = 0; kk2 < 4; ++kk2)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        ldsm_x4(kf[kk2][nt][0], kf[kk2][nt][1], kf[kk2][nt][2], kf[kk2][nt][3],
+                swz(kb32, nt * 8 + (lane & 7), kk2 * 4 + (lane >> 3)));
+#pragma unroll
+    for (int nt2 = 0; nt2 < 8; ++nt2)
+      ldsm_x4_t(vf[nt2][0], vf[nt2][1], vf[nt2][2], vf[nt2][3],
+                swz(vb32, (lane & 7) + ((lane >> 3) & 1) * 8, nt2 * 2 + (lane >> 4)));
     // q.K^T for 16 tokens; two accumulators per n-tile shorten the MMA chains
     float sacc[2][2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) sacc[nt][e][0] = sacc[nt][e][1] = sacc[nt][e][2] = sacc[nt][e][3] = 0.f;
-    const uint32_t kb32 = smem_u32(kb), vb32 = smem_u32(vb);
 #pragma unroll
     for (int kk2 = 0; kk2 < 4; ++kk2) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3, swz(kb32, nt * 8 + (lane & 7), kk2 * 4 + (lane >> 3)));
-        mma_16816(sacc[nt][0], qa0[2 * kk2], 0u, qa2[2 * kk2], 0u, b0, b1);
-        mma_16816(sacc[nt][1], qa0[2 * kk2 + 1], 0u, qa2[2 * kk2 + 1], 0u, b2, b3);
+        mma_16816(sacc[nt][0], qa0[2 * kk2], 0u, qa2[2 * kk2], 0u, kf[kk2][nt][0], kf[kk2][nt][1]);
+        mma_16816(sacc[nt][1], qa0[2 * kk2 + 1], 0u, qa2[2 * kk2 + 1], 0u, kf[kk2][nt][2], kf[kk2][nt][3]);
       }
+    }
+    // every lane's V loads have returned (the XOR reads each fragment register) and
+    // the K loads fed the MMAs above: the stage is free for the next chunk
+    uint32_t vtouch = 0;
+#pragma unroll
+    for (int nt2 = 0; nt2 < 8; ++nt2) vtouch ^= vf[nt2][0] ^ vf[nt2][1] ^ vf[nt2][2] ^ vf[nt2][3];
+    asm volatile("" ::"r"(vtouch));
+    __syncwarp();
+    if (j + STAGES < nj) {
+      if constexpr (!kTok)
+        if (lane == 0) fence_proxy_async_smem();  // the generic reads of the stage before the TMA rewrite
+      issue(j + STAGES);
+      issued = j + STAGES + 1;
+    } else if constexpr (kTok) {
+      cp_async_commit();
     }
     const int c0 = 2 * q4;
     const float z0 = (c0 < nvalid) ? (sacc[0][0][0] + sacc[0][1][0]) * sl : -INFINITY;
@@ -442,21 +469,12 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
     const uint32_t pl2 = pack_bf16x2(p2 - bf16_lo(ph2), p3 - bf16_hi(ph2));
 #pragma unroll
     for (int nt2 = 0; nt2 < 8; ++nt2) {
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(v0, v1, v2, v3, swz(vb32, (lane & 7) + ((lane >> 3) & 1) * 8, nt2 * 2 + (lane >> 4)));
-      mma_16816(o[2 * nt2], ph0, 0u, ph2, 0u, v0, v1);
-      mma_16816(o[2 * nt2 + 1], ph0, 0u, ph2, 0u, v2, v3);
-      mma_16816(o[2 * nt2], pl0, 0u, pl2, 0u, v0, v1);
-      mma_16816(o[2 * nt2 + 1], pl0, 0u, pl2, 0u, v2, v3);
+      mma_16816(o[2 * nt2], ph0, 0u, ph2, 0u, vf[nt2][0], vf[nt2][1]);
+      mma_16816(o[2 * nt2 + 1], ph0, 0u, ph2, 0u, vf[nt2][2], vf[nt2][3]);
+      mma_16816(o[2 * nt2], pl0, 0u, pl2, 0u, vf[nt2][0], vf[nt2][1]);
+      mma_16816(o[2 * nt2 + 1], pl0, 0u, pl2, 0u, vf[nt2][2], vf[nt2][3]);
     }
-    __syncwarp();
     consumed = j + 1;
-    if (j + STAGES < nj) {
-      issue(j + STAGES);
-      issued = j + STAGES + 1;
-    } else if constexpr (kTok) {
-      cp_async_commit();
-    }
   }
   if constexpr (kTok) cp_async_wait<0>();
   if (timed_out) {
@@ -520,7 +538,7 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
 
 template <int STAGES, class Params>
-__global__ void __launch_bounds__(kThreads) hsa_step_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ChanSmem cs;
   __shared__ AttnSmem<STAGES> as;

@@ -246,9 +246,9 @@ __device__ __forceinline__ void flag_error(int32_t* word, int32_t bit) {
 // called several times for each i in [0, n); every thread of the block calls this.
 constexpr int kTkBins = 1024;
 constexpr int kTkCand = 32;
-template <int NT>
+template <int NT, int NBINS = kTkBins>
 struct TopkSmem {
-  alignas(16) uint32_t hist[kTkBins];
+  alignas(16) uint32_t hist[NBINS];
   int cand[kTkCand];
   uint32_t ckey[kTkCand];
   uint32_t wlo[NT / 32], whi[NT / 32];
@@ -460,12 +460,14 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
 // chain of shared-memory loads; the candidates are ranked by warp 0 with shuffles.
 // Needs n <= NT * KPT, `keys` 16-byte aligned and readable up to NT * KPT entries
 // (entries from n on are ignored).  Every thread of the block calls this.
-template <int NT, int KPT>
-__device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
-  static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
+template <int NT, int KPT, int NBINS = kTkBins>
+__device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT, NBINS>& ts, int32_t* out) {
+  static_assert(NT % 32 == 0 && NBINS % NT == 0 && (NBINS / NT) % 4 == 0, "bins must split into uint4s");
+  static_assert((NBINS & (NBINS - 1)) == 0 && NBINS >= 1024, "a power of two of at least 1024 bins");
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int NW = NT / 32;
-  constexpr int BPT = kTkBins / NT;
+  constexpr int BPT = NBINS / NT;
+  constexpr int LOG_BINS = NBINS == 1024 ? 10 : (NBINS == 2048 ? 11 : (NBINS == 4096 ? 12 : 13));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i0 = tid * KPT;
   uint32_t kv[KPT];
@@ -486,7 +488,7 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   }
   const int nv = max(0, min(KPT, n - i0));  // valid keys of this thread: kv[0 .. nv)
   uint4* h4 = reinterpret_cast<uint4*>(ts.hist);
-  for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+  for (int j = tid; j < NBINS / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
   if (tid == 0) ts.ncand = 0;
 
   // 1. the key range
@@ -515,12 +517,12 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   bool cleared = true;
   while (nin > kTkCand && lo != hi) {
     if (!cleared) {
-      for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+      for (int j = tid; j < NBINS / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
       __syncthreads();
     }
     cleared = false;
     const uint32_t range = hi - lo;
-    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
+    const int shift = range < (uint32_t)NBINS ? 0 : (32 - __clz(range)) - LOG_BINS;
     int run_bin = -1, run = 0;
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {

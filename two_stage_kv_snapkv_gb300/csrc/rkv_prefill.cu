@@ -301,25 +301,38 @@ __global__ void __launch_bounds__(128) snap_stats_combine_kernel(const __grid_co
 }
 
 // Centred max-pool.  grid (ceil(Lmax / 2048), B*Hkv), 256 threads.
+// The tile and its halo are staged once; window maxima of doubling length are built
+// in place by ping-pong passes (after pass j, M[i] = max of x[i .. i + 2^j)), so a
+// window of kp positions is the max of two overlapping windows of 2^j <= kp: two
+// reads per output after log2(kp) passes, instead of kp reads.  Max is exact, so the
+// result equals the direct definition bit for bit.
 __global__ void __launch_bounds__(kPoolThreads) snap_pool_kernel(const __grid_constant__ SnapParams p) {
-  __shared__ float tile[kPoolTile + kMaxPool];
+  __shared__ float buf[2][kPoolTile + kMaxPool];
   const int unit = blockIdx.y, b = unit / p.Hkv;
   const int Lp = p.L[b] - p.w;
-  const int half = p.kp[b] / 2;
+  const int kp = p.kp[b], half = kp / 2;
   const int t0 = blockIdx.x * kPoolTile;
   if (t0 >= Lp) return;
   const float* S = p.S + (size_t)unit * p.Lmax;
-  for (int i = threadIdx.x; i < kPoolTile + 2 * half; i += kPoolThreads) {
+  const int n = kPoolTile + 2 * half;  // x[i] = S[t0 - half + i], -inf outside the prefix
+  for (int i = threadIdx.x; i < n; i += kPoolThreads) {
     const int t = t0 - half + i;
-    tile[i] = (t >= 0 && t < Lp) ? S[t] : -INFINITY;
+    buf[0][i] = (t >= 0 && t < Lp) ? S[t] : -INFINITY;
+  }
+  int cur = 0, w = 1;
+  while (2 * w <= kp) {  // windows of w -> 2w (only the entries a later read needs)
+    __syncthreads();
+    const float* a = buf[cur];
+    float* o = buf[cur ^ 1];
+    for (int i = threadIdx.x; i + 2 * w <= n; i += kPoolThreads) o[i] = fmaxf(a[i], a[i + w]);
+    cur ^= 1;
+    w *= 2;
   }
   __syncthreads();
+  const float* M = buf[cur];
   float* out = p.pooled + (size_t)unit * p.Lmax;
-  for (int o = threadIdx.x; o < kPoolTile && t0 + o < Lp; o += kPoolThreads) {
-    float m = tile[o];
-    for (int j = 1; j <= 2 * half; ++j) m = fmaxf(m, tile[o + j]);
-    out[t0 + o] = m;
-  }
+  for (int o = threadIdx.x; o < kPoolTile && t0 + o < Lp; o += kPoolThreads)
+    out[t0 + o] = fmaxf(M[o], M[o + kp - w]);  // [o, o + w) and [o + kp - w, o + kp)
 }
 
 // Top keep1-w pooled prefix positions (value desc, position asc) + the window,
