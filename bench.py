@@ -46,12 +46,19 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, help="1..6 (2: Llama3.1-8B layer, 32K prompt; 6: workload 4's batch under RocketKV-MT)")
+    ap.add_argument("--workload", type=int, default=5,
+                    help="1..6 (5, the default: 32 Llama3.1-8B-shaped layers, batch 8, 64K prompts; 2: one layer, 32K "
+                         "prompt; 4: batch 16, 8K-32K prompts; 6: workload 4's batch under RocketKV-MT)")
     ap.add_argument("--seed", type=int, default=0x5EED)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-decode-steps", type=int, default=0, help="decode steps per oracle sample (0: all)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="repeat the oracle sample until this much CPU time")
+    ap.add_argument("--flush", choices=["clean", "write"], default="clean",
+                    help="L2 flush before timed intervals: write 256 MB then read another 256 MB (clean, default), "
+                         "or only the write (leaves dirty lines for the timed kernel to write back)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the batch-16 (workload 4) decode measurement added to the default workload's line")
     ap.add_argument("--prefill-chunk", type=int, default=8192,
                     help="also time a chunked prefill of the same prompts with chunks of about this many tokens "
                          "(0: skip)")
@@ -177,6 +184,10 @@ class Setup:
             self.sws = share.sws if share else rkv.sparq_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, P, dev)
         self.out = torch.empty((wl.steps, wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
         self.flush_buf = share.flush_buf if share else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        # read after the write, so the flush leaves L2 holding clean lines of this buffer
+        # instead of 129 MB of dirty ones that the timed kernel would have to write back
+        self.flush_read = share.flush_read if share else torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+        self.flush_mode = share.flush_mode if share else "clean"
 
     # one call each, on the current stream
     def prefill(self):
@@ -197,7 +208,12 @@ class Setup:
             self.rkv.rkv_decode_step(self.cache, q, k_new, v_new, self.k1, self.k2, out, workspace=self.dws)
 
     def flush(self):
+        """Evict L2 before a timed interval: write a 256 MB buffer (twice L2), then, in
+        the default "clean" mode, read another 256 MB buffer so the write's dirty lines
+        are written back here rather than inside the timed kernel."""
         self.flush_buf.zero_()
+        if self.flush_mode == "clean":
+            self.flush_read.view(torch.int64).max()
 
     # ------------------------------------------------------------ byte accounting
     def decode_bytes(self, t: int) -> dict:
@@ -222,11 +238,16 @@ class Setup:
                     sparq_score=summ + q, sparq_attend=kv + q + out, step_total=total)
 
     def prefill_bytes(self) -> dict:
+        """Stage-1 bytes per layer: `compulsory` reads the prompt's keys once and reads
+        and writes the survivors' K and V (what the method must move); `moved` is what
+        the two scoring passes (row statistics, then column sums) actually stream, the
+        keys twice."""
         wl = self.wl
         # stage-1 scoring reads K once per pass; without eviction (RocketKV-MT) it is skipped
         kbytes = 0 if wl.mt else sum(wl.Hkv * L * 128 * 2 for L in wl.prompt_lens)
         surv = sum(wl.Hkv * k * 128 * 2 * 2 * 2 for k in self.keep1)   # K+V read and written
-        return dict(snap_stats=kbytes, snap_colsum=kbytes, snap_compact=surv, total=2 * kbytes + surv)
+        return dict(snap_stats=kbytes, snap_colsum=kbytes, snap_compact=surv, compulsory=kbytes + surv,
+                    moved=2 * kbytes + surv)
 
 
 def selection_recall(setup: Setup) -> dict:
@@ -347,34 +368,52 @@ def capture(fn, stream) -> torch.cuda.CUDAGraph:
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
-def oracle_sample(setup: Setup, decode_steps: int) -> dict:
-    """Time the oracle on this host: the whole prefill of every unit + `decode_steps` steps."""
+def sample_units(wl: W.Workload, max_units: int = 4) -> list:
+    """The (sequence, KV head) units an oracle sample runs: every unit of a small
+    workload, else `max_units` of them spread over the batch and the heads."""
+    units = [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    if len(units) <= 8:
+        return units
+    step = len(units) / max_units
+    return [units[int(i * step + step / 2) % len(units)] for i in range(max_units)]
+
+
+def oracle_sample(setup, decode_steps: int, units=None) -> dict:
+    """Time the oracle on this host over `units` ((b, g) pairs of layer 0; default all):
+    each unit's stage-1 prefill (with its summary build), then `decode_steps` decode
+    steps of those units (append + HSA).  Returns the measured seconds and the
+    per-unit times, and the whole layer's decode steps/s extrapolated from them:
+    steps / (units of the layer x (prefill + steps x decode step)), every unit of a
+    layer being the same work."""
     import numpy as np
 
     from oracle import rkv_oracle as O
 
     wl = setup.wl
-    f = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
-    q_win = f(setup.inp["q_win"])
-    k = f(setup.inp["k"])
-    v = f(setup.inp["v"])
-    t0 = time.perf_counter()
-    units = []
-    for b in range(wl.B):
-        L = wl.prompt_lens[b]
-        res = O.prefill_evict_unit(q_win[b], k[b, :, :L], setup.keep1[b], setup.kp[b])
-        for g in range(wl.Hkv):
-            kept = res["kept"][g]
-            Kc, Vc = k[b, g, kept], v[b, g, kept]
-            units.append([b, g, Kc, Vc, O.page_summaries(Kc, len(kept), wl.page_size)])
-    t_prefill = time.perf_counter() - t0
+    units = list(units) if units is not None else [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     G = wl.G
-    t1 = time.perf_counter()
+    f = lambda t: t.detach().cpu().double().numpy()  # noqa: E731
+    # the sampled units' inputs, widened before timing
+    ins = []
+    for b, g in units:
+        L = wl.prompt_lens[b]
+        ins.append((b, g, f(setup.inp["q_win"][b, g * G:(g + 1) * G]), f(setup.inp["k"][b, g:g + 1, :L]),
+                    f(setup.inp["v"][b, g, :L])))
+    steps_in = []
     for t in range(decode_steps):
         d = setup.dec[t]
-        q = f(d["q"])
-        kn, vn = f(d["k_new"][:, :, 0]), f(d["v_new"][:, :, 0])
-        for u in units:
+        steps_in.append((f(d["q"]), f(d["k_new"][:, :, 0]), f(d["v_new"][:, :, 0])))
+    t0 = time.perf_counter()
+    state = []
+    for b, g, q_win, k, v in ins:
+        res = O.prefill_evict_unit(q_win, k, setup.keep1[b], setup.kp[b])
+        kept = res["kept"][0]
+        Kc, Vc = k[0, kept], v[kept]
+        state.append([b, g, Kc, Vc, O.page_summaries(Kc, len(kept), wl.page_size)])
+    t_prefill = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    for q, kn, vn in steps_in:
+        for u in state:
             b, g, Kc, Vc, (kmax, kmin) = u
             n_old = len(Kc)
             Kc = np.concatenate([Kc, kn[b, g][None]])
@@ -386,10 +425,20 @@ def oracle_sample(setup: Setup, decode_steps: int) -> dict:
                 O.hsa_decode_unit(q[b, g * G:(g + 1) * G], Kc, Vc, n_old + 1, kmax, kmin, wl.page_size,
                                   setup.k1[b], setup.k2[b])
             u[2], u[3], u[4] = Kc, Vc, (kmax, kmin)
-    t_dec = (time.perf_counter() - t1) / max(1, decode_steps)
-    whole = t_prefill + wl.steps * t_dec
-    return dict(value=wl.steps / whole, t_prefill_s=t_prefill, t_decode_step_s=t_dec, seconds=t_prefill + t_dec *
-                decode_steps)
+    t_dec = time.perf_counter() - t1
+    nu = len(units)
+    pre_u = t_prefill / nu
+    dec_u = t_dec / (nu * max(1, decode_steps))
+    layer_s = wl.B * wl.Hkv * (pre_u + wl.steps * dec_u)
+    return dict(value=wl.steps / layer_s, seconds=t_prefill + t_dec, units=nu, decode_steps=decode_steps,
+                prefill_s_per_unit=pre_u, decode_s_per_unit_step=dec_u)
+
+
+def oracle_sample_text(wl: W.Workload, o: dict, reps: int, seconds: float) -> str:
+    return (f"{reps} x (oracle prefill + {o['decode_steps']} of {wl.steps} decode steps of {o['units']} of the "
+            f"{wl.B * wl.Hkv} (sequence, KV head) units of layer 0), {seconds:.1f} s measured in total; value "
+            f"extrapolated to the whole layer as steps / ({wl.B * wl.Hkv} units x (prefill + {wl.steps} x decode "
+            f"step) per unit), every unit and every layer being the same work")
 
 
 def host_cores() -> int:
@@ -400,14 +449,18 @@ def host_cores() -> int:
 
 
 # --------------------------------------------------------------------------- main arms
-def run_ours(args, rank: int, world: int, dev) -> dict:
+def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool = True) -> dict:
+    """The bench line of one workload (args.workload unless `workload` is given).
+    With extras off only the timed passes and the per-kernel figures are taken (no
+    recall diagnostic, chunked prefill, end-to-end run or CPU oracle)."""
     from two_stage_kv_snapkv_gb300 import rkv
 
-    wl = W.workload(args.workload, args.seed)
+    wl = W.workload(workload or args.workload, args.seed)
     rkv.rkv_decode_path({"auto": 0, "split": 1, "fused": 2}[args.decode_path])
     seed = rank_seed(args.seed, rank)
     nl = 1 if args.one_layer else wl.layers
     setup = Setup(wl, rkv, seed, dev, mode=args.mode)
+    setup.flush_mode = args.flush
     # a multi-layer workload keeps every layer resident: stage 1 for all of them, then
     # each decode step runs HSA for every layer in turn, as a model's decode step does
     layers = [setup] + [Setup(wl, rkv, seed, dev, layer=l, share=setup, mode=args.mode) for l in range(1, nl)]
@@ -550,12 +603,14 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic (seeded normal bf16 with the workload's shapes, outlier channels, sinks and needles)",
         config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world, nl,
-                               args.mode),
+                               args.mode, args.flush),
         prefill_evict_ms=round(pre_layer_ms, 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),
         decode_achieved_gbs=round(step_total / (dec_mean_ms * 1e-3) / 1e9, 1),
         decode_compulsory_mb_per_step=round(step_total / 1e6, 3),
-        prefill_achieved_gbs=round(pb["total"] / (pre_layer_ms * 1e-3) / 1e9, 1),
+        prefill_achieved_gbs=round(pb["compulsory"] / (pre_layer_ms * 1e-3) / 1e9, 1),
+        prefill_compulsory_mb=round(pb["compulsory"] / 1e6, 2),
+        prefill_traffic_ratio=round(pb["moved"] / pb["compulsory"], 3),
         roofline=roofline, kernels=kernels, gpu_launches=int(launches_per_pass * args.steps),
         clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"],
                     samples=clocks["samples"]),
@@ -565,6 +620,8 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
         res["decode_all_layers_us_per_step"] = round(dec_mean_ms * nl * 1e3, 3)
         res["memory_gb"] = dict(prompt_kv=round(nl * 2 * wl.Hkv * sum(wl.prompt_lens) * 256 / 1e9, 2),
                                 cache_pages=round(sum(s.cache.nbytes() for s in layers) / 1e9, 2))
+    if not extras:
+        return res
     res["selection"] = selection_recall(setup) if args.mode != "sparq" else dict(
         skipped="the recall diagnostic takes a page selection; SparQ-only selects tokens")
     if args.prefill_chunk > 0:
@@ -575,33 +632,33 @@ def run_ours(args, rank: int, world: int, dev) -> dict:
             res["e2e"]["layers"] = 1   # layer 0 alone, through the host buffers
     if rank == 0 and not args.no_cpu_baseline:
         steps = args.cpu_decode_steps or wl.steps
+        units = sample_units(wl)
         vals, secs, reps = [], 0.0, 0
         while secs < args.cpu_seconds and reps < 100:
-            o = oracle_sample(setup, steps)
+            o = oracle_sample(setup, steps, units)
             vals.append(o["value"])
             secs += o["seconds"]
             reps += 1
             if secs + o["seconds"] > 3 * args.cpu_seconds:
                 break
-        o = dict(value=statistics.mean(vals), seconds=secs)
-        res["cpu_baseline"] = dict(value=round(o["value"], 3), unit=UNIT, cores=host_cores(), kind="oracle",
-                                   sample=f"{reps} x (oracle prefill of all {wl.B * wl.Hkv} units + {steps} of "
-                                          f"{wl.steps} decode steps), {o['seconds']:.1f} s of CPU time in total; "
-                                          f"value = steps / (prefill + steps * mean step), mean over the repetitions")
+        res["cpu_baseline"] = dict(value=round(statistics.mean(vals), 3), unit=UNIT, cores=host_cores(),
+                                   kind="oracle", sample=oracle_sample_text(wl, o, reps, secs))
     return res
 
 
 def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int, layers: int = 1,
-                    mode: str = "hsa") -> dict:
+                    mode: str = "hsa", flush: str = "clean") -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
+    how = ("256 MB write, then a 256 MB read of another buffer, so no dirty line is left for the timed work "
+           "to write back" if flush == "clean" else "256 MB write")
     if layers > 1:
         step = (f"one request over {layers} layers: split + prefill evict of every layer + every decode step "
                 f"(append + HSA for each layer in turn); value counts layer-steps")
-        l2 = ("flushed (256 MB write) before the prefill; not between decode steps: each step streams "
+        l2 = (f"flushed ({how}) before the prefill; not between decode steps: each step streams "
               f"{layers} layers' caches, far more than L2, so every layer starts cold; flush not timed")
     else:
         step = "one request: split + prefill evict + every decode step (append + HSA)"
-        l2 = "flushed (256 MB write) before the prefill and before every decode step; flush not timed"
+        l2 = f"flushed ({how}) before the prefill and before every decode step; flush not timed"
     return dict(workload=wl.name, B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, head_dim=wl.d, prompt_len=wl.prompt_lens[0]
                 if wl.B == 1 else f"{min(wl.prompt_lens)}..{max(wl.prompt_lens)}", budget=wl.budget,
                 window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, layers=layers,
@@ -707,7 +764,12 @@ def run_e2e(setup: Setup, args, stream, rkv) -> dict:
         stream.synchronize()
         times.append(e0.elapsed_time(e1))
     return dict(value=round(wl.steps * len(times) / (sum(times) / 1e3), 2), unit=UNIT, h2d_bytes_per_step=int(h2d),
-                d2h_bytes_per_step=int(d2h), ms_per_step=round(statistics.mean(times), 4),
+                d2h_bytes_per_step=int(d2h), ms_per_request=round(statistics.mean(times), 4),
+                step=(f"one bench step is one request: the prompt copied in, the prefill, then {wl.steps} decode steps, "
+                      "each taking its inputs from and returning its output to host memory; the byte counts are per "
+                      "request"),
+                h2d_prompt_bytes=int(h2d - wl.steps * sum(sizes)), h2d_bytes_per_decode_step=int(sum(sizes)),
+                d2h_bytes_per_decode_step=int(d2h // wl.steps),
                 path=("python binding -> C ABI rkv_decode_step_host, eager, pinned host buffers (per call the "
                       "fused step reads the packed inputs and writes the output through the buffers' device "
                       "mapping; copy in, step, copy out where they are not mapped)") if host_step else
@@ -728,9 +790,8 @@ def run_reference(args, rank: int, world: int) -> dict:
     setup = _Split()
     setup.wl = wl
     setup.inp = W.prefill_tensors(wl, args.seed, 0, "cpu", tail="zero")
-    nsteps = min(wl.steps, 4)
     setup.dec = []
-    for t in range(nsteps):
+    for t in range(wl.steps):
         d = W.decode_tensors(wl, t, args.seed, 0, "cpu")
         d["k_new"] = d["k_new"].unsqueeze(2)
         d["v_new"] = d["v_new"].unsqueeze(2)
@@ -745,23 +806,25 @@ def run_reference(args, rank: int, world: int) -> dict:
     setup.k2 = [s["k2"] for s in sp]
     setup.k_tokens = [k * wl.page_size for k in setup.k2]
     setup.kp = [wl.pool_kernel or s["pool_kernel"] for s in sp]
+    units = sample_units(wl)
+    # one bench step = one bounded sample: the sampled units' prefill and every decode step
     for _ in range(args.warmup):
-        oracle_sample(setup, 1)
-    vals, secs = [], 0.0
+        oracle_sample(setup, 1, units[:1])
+    vals, secs = [], []
     for _ in range(args.steps):
-        o = oracle_sample(setup, nsteps)
+        o = oracle_sample(setup, wl.steps, units)
         vals.append(o["value"])
-        secs += o["seconds"]
+        secs.append(o["seconds"])
     value = statistics.mean(vals)
     return dict(impl="reference", metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=world, steps=args.steps,
-                warmup=args.warmup, ms_per_step=round(1e3 / value * wl.steps, 3), higher_is_better=True,
+                warmup=args.warmup, ms_per_step=round(1e3 * statistics.mean(secs), 3), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)",
                 config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world,
-                                       wl.layers, args.mode),
+                                       wl.layers, args.mode, args.flush),
+                step=("one bounded sample of the request (ms_per_step is its measured wall time; value is the "
+                      "whole layer's rate extrapolated from it, see cpu_baseline.sample)"),
                 cpu_baseline=dict(value=round(value, 3), unit=UNIT, cores=host_cores(), kind="oracle",
-                                  sample=f"per step: oracle prefill of all units + {nsteps} decode steps"
-                                         f"{' of layer 0' if wl.layers > 1 else ''}, "
-                                         f"extrapolated to the whole request ({secs:.1f} s total)"),
+                                  sample=oracle_sample_text(wl, o, args.steps, sum(secs))),
                 e2e=dict(value=round(value, 3), unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
@@ -782,6 +845,17 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
     res = run_ours(args, rank, world, dev)
+    if res and args.workload == 5 and not args.no_extra and not args.one_layer and args.mode == "hsa":
+        # the batch-16 serving workload (8K-32K prompts), measured in the same run: its
+        # decode step, and the fused step's roofline there
+        torch.cuda.empty_cache()
+        w4 = run_ours(args, rank, world, dev, workload=4, extras=False)
+        if w4:
+            res["workload4"] = dict(workload=w4["config"]["workload"], value=w4["value"], unit=UNIT,
+                                    ms_per_step=w4["ms_per_step"], decode_us_per_step=w4["decode_us_per_step"],
+                                    prefill_evict_ms=w4["prefill_evict_ms"],
+                                    decode_achieved_gbs=w4["decode_achieved_gbs"], roofline=w4["roofline"],
+                                    clocks=w4["clocks"], gpu_launches=w4["gpu_launches"])
     if rank == 0 and res:
         print(json.dumps(res))
     if world > 1:
