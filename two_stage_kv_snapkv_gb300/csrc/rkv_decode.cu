@@ -118,7 +118,8 @@ struct ChanSmem {
   alignas(16) uint32_t ahi[128];  // rank keys: fp32 bits, or the high words of fp64 scores
   uint32_t alo[128];              // low words of the fp64 scores (fp64 path only)
   int chan[128];
-  float qpos[128], qneg[128];
+  alignas(16) float qpos[128];
+  alignas(16) float qneg[128];
   int warp_cnt[8];
 };
 
@@ -177,8 +178,11 @@ __device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int
         r0 += (u.x > t) + (u.y > t);
         r1 += (u.z > t) + (u.w > t);
       }
-      rank = r0 + r1;
-      for (int j = 4 * mine; j < tid; ++j) rank += cs.ahi[j] == key;  // equal, lower, same group
+      // equal keys below this channel in its own group of four (no divergent loop)
+      const uint4 own = h4[mine];
+      const int q = tid & 3;
+      rank = r0 + r1 + (int)((q > 0) & (own.x == key)) + (int)((q > 1) & (own.y == key)) +
+             (int)((q > 2) & (own.z == key));
     } else {
       int g0 = 0, g1 = 0, e0 = 0, e1 = 0;
 #pragma unroll 8
@@ -208,18 +212,25 @@ __device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int
     if ((tid & 31) == 0) cs.warp_cnt[tid >> 5] = __popc(bal);
   }
   __syncthreads();
-  if (tid < 128 && sel) {
+  if (tid < 128) {  // every thread computes; only the chosen channels store (predicated)
+    const int w = tid >> 5;
     int pos = __popc(bal & ((1u << (tid & 31)) - 1u));
-    for (int w = 0; w < (tid >> 5); ++w) pos += cs.warp_cnt[w];
-    cs.chan[pos] = tid;
+    pos += (w > 0 ? cs.warp_cnt[0] : 0) + (w > 1 ? cs.warp_cnt[1] : 0) + (w > 2 ? cs.warp_cnt[2] : 0);
     float sp = 0.f, sn = 0.f;
     for (int h = 0; h < G; ++h) {
       const float x = qf[h][tid];
       sp += fmaxf(x, 0.f);
       sn += fminf(x, 0.f);
     }
-    cs.qpos[pos] = sp;
-    cs.qneg[pos] = sn;
+    if (sel) {
+      cs.chan[pos] = tid;
+      cs.qpos[pos] = sp;
+      cs.qneg[pos] = sn;
+    }
+    if (tid >= k1) {  // zero past the chosen channels, so four sums load as one float4
+      cs.qpos[tid] = 0.f;
+      cs.qneg[tid] = 0.f;
+    }
   }
   __syncthreads();
 }
@@ -564,6 +575,17 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // every CTA of the cluster must be running before anyone stores into its shared
   // memory: arrive now, wait just before the first remote store
   cluster_arrive_relaxed();
+  // barriers of this CTA (shared memory only)
+  if (tid == 0) {
+    mbar_init(&sbar, 1);
+    mbar_init(&pbar, 1);
+    fence_mbar_init();
+  }
+  // The launch may overlap the end of the previous kernel on the stream (programmatic
+  // dependent launch): everything above touches only this CTA's shared memory; wait
+  // here until that kernel has completed and its writes are visible, before the first
+  // global access.  Without such a launch this returns at once.
+  grid_dependency_wait();
 
   // 1. loads that depend on nothing: the group's query (16 bytes per thread), the new
   // token's K and V rows, the sequence length (one round trip for all of them)
@@ -584,12 +606,6 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   }
   const int n = n0 + (do_append ? 1 : 0);
   const int NP = (n + P - 1) / P;
-  // 2. barriers (before the length arrives)
-  if (tid == 0) {
-    mbar_init(&sbar, 1);
-    mbar_init(&pbar, 1);
-    fence_mbar_init();
-  }
   // this CTA's slice [p0, p1) of the pages (8-page aligned).  Short slices (under 64
   // pages) have the summaries of all 128 channels staged right away, in 16-byte
   // cp.async pieces (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and
@@ -749,10 +765,48 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
         for (int r = 0; r < C; ++r) cluster.map_shared_rank(keys, r)[t0 + j] = key;
       }
     };
+    // chosen-channel rows (long slices): a thread bounds two adjacent pages, reading
+    // each row's two bf16 values as one 4-byte load (a warp reads 128 contiguous bytes
+    // of a row) and four channels' q sums as one broadcast 16-byte load.  Measured on
+    // GB300 in isolation (304 pages x 64 channels, 128 threads): 4,650 cycles against
+    // 6,400 for one page per thread and 6,700 for four pages x a quarter of the
+    // channels per lane; the loop is bound by instruction issue of its loads and FMAs.
+    auto score_pairs = [&]() {
+      const uint32_t* st2 = reinterpret_cast<const uint32_t*>(stg);
+      const int rs2 = cnt8 >> 1;  // row stride in page pairs
+      const int npairs = (cnt + 1) >> 1;
+      const float4* qp4 = reinterpret_cast<const float4*>(cs.qpos);
+      const float4* qn4 = reinterpret_cast<const float4*>(cs.qneg);
+      const int k1r = (k1 + 3) & ~3;  // q sums are zero past k1; rows past k1 are clamped
+      for (int jp = tid; jp < npairs; jp += kThreads) {
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+#pragma unroll 2
+        for (int kk = 0; kk < k1r; kk += 4) {
+          const float4 qp = qp4[kk >> 2], qn = qn4[kk >> 2];
+          const float qpa[4] = {qp.x, qp.y, qp.z, qp.w}, qna[4] = {qn.x, qn.y, qn.z, qn.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = min(kk + e, k1 - 1);
+            const uint32_t mx = st2[r * rs2 + jp], mn = st2[(k1 + r) * rs2 + jp];
+            a0 = fmaf(qpa[e], bf16_lo(mx), a0);
+            a1 = fmaf(qpa[e], bf16_hi(mx), a1);
+            b0 = fmaf(qna[e], bf16_lo(mn), b0);
+            b1 = fmaf(qna[e], bf16_hi(mn), b1);
+          }
+        }
+        const int j = 2 * jp;
+        const uint32_t key0 = float_key(a0 + b0), key1 = float_key(a1 + b1);
+        for (int r = 0; r < C; ++r) {
+          uint32_t* kr = cluster.map_shared_rank(keys, r);
+          kr[t0 + j] = key0;
+          if (j + 1 < cnt) kr[t0 + j + 1] = key1;
+        }
+      }
+    };
     if (all_ch)
       score(std::true_type{});
     else
-      score(std::false_type{});
+      score_pairs();
   }
   if (!waited) cluster_wait();
   fence_proxy_async_smem();  // generic accesses to the region before the attention's TMA loads
@@ -788,27 +842,21 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     }
   }
   // 7. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
-  // 128 pages by counting each key's rank, up to 512 the histogram select with each
-  // thread's keys in registers, beyond that the same select looping over the keys in
-  // shared memory.  On GB300 the counting select was 0.3 us faster at ~90 pages and 1-2
-  // us slower at 200-300; at 1212 pages the looping select was 2.9 us faster than 16
-  // register keys a thread, at 557-966 pages within 0.3 us of 8.  The list is
-  // ascending.  The scratch lives in the region, free between the scoring and the
-  // attention.  (The key array is 16-byte aligned and followed by the list and the
-  // page-table row, so the register select's reads past NP stay inside this CTA's
-  // shared memory.)
+  // 128 pages by counting each key's rank, beyond that the histogram select written
+  // without divergent per-key branches (on GB300 it took 2.6 us over 1212 keys where
+  // the branchy looping form took 4.3 us, both with warm instruction caches).  The list
+  // is ascending.  The scratch lives in the region, free between the scoring and the
+  // attention.  (The key array is 16-byte aligned and followed by the list, the
+  // page-table row and the inbox, so the select's reads up to 512 entries past NP stay
+  // inside this CTA's shared memory.)
   const int k = min(p.k2[b], NP);
   TopkSmem<kThreads>& tks = *reinterpret_cast<TopkSmem<kThreads>*>(ring);
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
   } else if (NP <= kThreads) {
     topk_rank<kThreads, 1>(keys, NP, k, tks, sel);
-  } else if (NP <= 2 * kThreads) {
-    topk_regs<kThreads, 2>(keys, NP, k, tks, sel);
-  } else if (NP <= 4 * kThreads) {
-    topk_regs<kThreads, 4>(keys, NP, k, tks, sel);
   } else {
-    topk_loop<kThreads>(keys, NP, k, tks, sel);
+    topk_flat<kThreads>(keys, NP, k, tks, sel);
   }
   if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   __syncthreads();
@@ -821,6 +869,9 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   if (!mbar_wait(&pbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
   __syncthreads();
 
+  // the next kernel on the stream may start launching its CTAs into the slots this one
+  // frees (it waits for this grid's completion before touching memory)
+  grid_launch_dependents();
   // 8. attention over this CTA's share of the selected chunks
   const int items = k * (P / kChunkTok);
   const int ips = (items + C - 1) / C;
@@ -1265,13 +1316,17 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = best_smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = best_C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the step's CTAs may be scheduled while the previous
+  // kernel on the stream finishes (the kernel waits for it before any global access)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e;
   launch_begin(K_HSA_STEP, s);
   if (a.cache.B <= 16) {

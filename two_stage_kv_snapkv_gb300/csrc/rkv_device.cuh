@@ -152,6 +152,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Programmatic dependent launch (PTX griddepcontrol): wait until the prerequisite grid
+// on the stream has completed and its memory writes are visible (a no-op when the
+// kernel was not launched as a dependent), and allow the dependent grid to be
+// scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // Dynamic shared memory rounded up to a 1024-byte boundary (the 128-byte swizzle atom).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_u32(p);
@@ -671,6 +680,410 @@ __device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT, NBINS
     bseen += t == 2;
   }
   __syncthreads();  // the scratch may be reused right after
+}
+
+// The same selection computed by every warp on its own, with warp primitives only:
+// lane l reads keys l, l + 32, l + 64, ... (one coalesced 128-byte row per round), so a
+// warp sweeps all n keys per pass with no block barrier between the passes.  Each
+// warp finds the key range, builds its private 1024-bin histogram over it (refining
+// while the boundary bin holds more than kTkCand keys), ranks the boundary bin's keys
+// and derives the same boundary (T, t); the ascending list is written by ballots in
+// index order, warp w storing the rounds r with r % NW == w.  One block barrier at
+// the end publishes the list.  For 1 <= k < n; every thread of the block calls this.
+struct TopkWarpSmem {
+  alignas(16) uint32_t hist[kTkBins];
+  uint32_t ckey[kTkCand];
+  int cidx[kTkCand];
+};
+
+template <int NT>
+__device__ void topk_warp(const uint32_t* keys, int n, int k, TopkWarpSmem* wsm, int32_t* out) {
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  TopkWarpSmem& ws = wsm[warp];
+  const int R = (n + 31) >> 5;  // rounds of 32 keys
+  auto key_at = [&](int r) -> uint32_t {
+    const int i = r * 32 + lane;
+    return i < n ? keys[i] : 0u;
+  };
+
+  // 1. key range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll 4
+  for (int r = 0; r < R; ++r) {
+    if (r * 32 + lane < n) {
+      const uint32_t u = keys[r * 32 + lane];
+      lo = min(lo, u);
+      hi = max(hi, u);
+    }
+  }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+
+  // 2. shrink [lo, hi] to the bin holding the k-th key; `need` of its `nin` keys are taken
+  int need = k, nin = n;
+  while (nin > kTkCand && lo != hi) {
+    const uint32_t range = hi - lo;
+    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
+    uint4* h4 = reinterpret_cast<uint4*>(ws.hist);
+#pragma unroll
+    for (int j = 0; j < kTkBins / 128; ++j) h4[lane + 32 * j] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+#pragma unroll 4
+    for (int r = 0; r < R; ++r) {
+      const uint32_t u = key_at(r);
+      if (r * 32 + lane < n && u >= lo && u <= hi) atomicAdd(&ws.hist[(u - lo) >> shift], 1u);
+    }
+    __syncwarp();
+    // lane l holds bins [32 l, 32 l + 32)
+    uint32_t c[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = h4[lane * 8 + j];
+      c[4 * j] = v.x;
+      c[4 * j + 1] = v.y;
+      c[4 * j + 2] = v.z;
+      c[4 * j + 3] = v.w;
+    }
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) sum += (int)c[j];
+    int incl = sum;  // keys in this lane's bins and every higher lane's
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(FULL, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    const int above = incl - sum;
+    int bstar = 0, nneed = 0, nb = 0;
+    const bool mine = above < need && above + sum >= need;
+    if (mine) {
+      int acc = above;
+#pragma unroll
+      for (int j = 31; j >= 0; --j) {
+        if (acc + (int)c[j] >= need && nb == 0) {
+          bstar = lane * 32 + j;
+          nneed = need - acc;
+          nb = (int)c[j];
+        }
+        acc += (int)c[j];
+      }
+    }
+    const int src = __ffs(__ballot_sync(FULL, mine)) - 1;
+    bstar = __shfl_sync(FULL, bstar, src);
+    nneed = __shfl_sync(FULL, nneed, src);
+    nb = __shfl_sync(FULL, nb, src);
+    const uint32_t nlo = lo + ((uint32_t)bstar << shift);
+    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
+    lo = nlo;
+    need = nneed;
+    nin = nb;
+    __syncwarp();  // the histogram is read before the next round clears it
+  }
+
+  // 3. boundary pair (T, t) among at most kTkCand keys of [lo, hi]
+  const bool all_in = need == nin;                // every key in [lo, hi] is taken
+  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi: the first `need` by index
+  uint32_t T = lo;
+  int tI = n;
+  if (!all_in && !by_index) {
+    int cnt = 0;
+#pragma unroll 4
+    for (int r = 0; r < R; ++r) {
+      const uint32_t u = key_at(r);
+      const bool f = r * 32 + lane < n && u >= lo && u <= hi;
+      const unsigned m = __ballot_sync(FULL, f);
+      if (f) {
+        const int slot = cnt + __popc(m & lt);
+        ws.ckey[slot] = u;
+        ws.cidx[slot] = r * 32 + lane;
+      }
+      cnt += __popc(m);
+    }
+    __syncwarp();
+    const uint32_t cu = lane < nin ? ws.ckey[lane] : 0u;
+    const int ci = lane < nin ? ws.cidx[lane] : 0;
+    int rank = 0;
+#pragma unroll 8
+    for (int m = 0; m < kTkCand; ++m) {
+      if (m < nin) {
+        const uint32_t a = ws.ckey[m];
+        const int am = ws.cidx[m];
+        rank += (a > cu) | ((a == cu) & (am < ci));
+      }
+    }
+    const bool is_t = lane < nin && rank == need - 1;
+    const int tl = __ffs(__ballot_sync(FULL, is_t)) - 1;
+    T = __shfl_sync(FULL, cu, tl);
+    tI = __shfl_sync(FULL, ci, tl);
+  }
+
+  // 4. ascending list: rounds in index order, a ballot per round
+  int base = 0, eq_seen = 0;
+#pragma unroll 2
+  for (int r = 0; r < R; ++r) {
+    const int i = r * 32 + lane;
+    const uint32_t u = key_at(r);
+    bool f = false, eq = false;
+    if (i < n) {
+      if (u > hi) f = true;
+      else if (u >= lo) {
+        if (by_index) eq = true;
+        else f = u > T || (u == T && i <= tI);
+      }
+    }
+    if (by_index) {  // the first `need` keys equal to lo, by index
+      const unsigned me = __ballot_sync(FULL, eq);
+      f = f || (eq && eq_seen + __popc(me & lt) < need);
+      eq_seen += __popc(me);
+    }
+    const unsigned m = __ballot_sync(FULL, f);
+    if (f && (r % NW) == warp) {
+      const int pos = base + __popc(m & lt);
+      if (pos < k) out[pos] = i;
+    }
+    base += __popc(m);
+  }
+  __syncthreads();  // the list is complete and every warp's scratch is free
+}
+
+// The same selection written without divergent branches in its per-key work: on this
+// GPU a data-dependent branch inside an unrolled per-key loop costs on the order of
+// a hundred cycles (measured: the compaction's two passes took 4,800 cycles with
+// branches and 1,700 with the decisions as bit arithmetic and predicated stores).
+// Thread t owns the contiguous keys [t S, t S + S), S a multiple of 4 (16-byte loads,
+// index-ordered compaction by one block scan); every thread runs the same trip counts.
+// Boundary candidates are gathered by a block scan instead of shared atomics.  Needs
+// n <= NT * S with `keys` 16-byte aligned and readable up to NT * S entries (entries
+// from n on are ignored).  For 1 <= k < n; every thread of the block calls this.
+template <int NT>
+__device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
+  static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
+  constexpr unsigned FULL = 0xffffffffu;
+  constexpr int NW = NT / 32;
+  constexpr int BPT = kTkBins / NT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = ((n + NT - 1) / NT + 3) & ~3;  // keys per thread
+  const int Q = S >> 2;                         // 16-byte groups per thread
+  const int i0 = tid * S;
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys + i0);
+  uint4* h4 = reinterpret_cast<uint4*>(ts.hist);
+  for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+
+  // block-wide exclusive prefix of one int per thread (and the total), by shuffles
+  // and one barrier; `slot` picks one of two scratch rows so back-to-back calls do not
+  // race
+  auto block_scan = [&](int x, int slot, int& total) -> int {
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, incl, o);
+      incl += lane >= o ? y : 0;
+    }
+    int* wsum = slot ? ts.wb : ts.wa;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = incl - x;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const int v = wsum[w];
+      before += w < warp ? v : 0;
+      total += v;
+    }
+    return before;
+  };
+
+  // 1. the key range
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll 1
+  for (int q = 0; q < Q; ++q) {
+    const uint4 v = k4[q];
+    const int j = i0 + 4 * q;
+    lo = min(lo, j < n ? v.x : 0xffffffffu);
+    hi = max(hi, j < n ? v.x : 0u);
+    lo = min(lo, j + 1 < n ? v.y : 0xffffffffu);
+    hi = max(hi, j + 1 < n ? v.y : 0u);
+    lo = min(lo, j + 2 < n ? v.z : 0xffffffffu);
+    hi = max(hi, j + 2 < n ? v.z : 0u);
+    lo = min(lo, j + 3 < n ? v.w : 0xffffffffu);
+    hi = max(hi, j + 3 < n ? v.w : 0u);
+  }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+  if (lane == 0) {
+    ts.wlo[warp] = lo;
+    ts.whi[warp] = hi;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    lo = min(lo, ts.wlo[w]);
+    hi = max(hi, ts.whi[w]);
+  }
+
+  // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
+  int need = k, nin = n;
+  bool cleared = true;
+  while (nin > kTkCand && lo != hi) {
+    if (!cleared) {
+      for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
+      __syncthreads();
+    }
+    cleared = false;
+    const uint32_t range = hi - lo;
+    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
+#pragma unroll 1
+    for (int q = 0; q < Q; ++q) {
+      const uint4 v = k4[q];
+      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t u = u4[e];
+        if ((i0 + 4 * q + e < n) & (u >= lo) & (u <= hi)) atomicAdd(&ts.hist[(u - lo) >> shift], 1u);
+      }
+    }
+    __syncthreads();
+    uint32_t c[BPT];
+#pragma unroll
+    for (int j = 0; j < BPT; j += 4) {
+      const uint4 v = h4[(tid * BPT + j) >> 2];
+      c[j] = v.x;
+      c[j + 1] = v.y;
+      c[j + 2] = v.z;
+      c[j + 3] = v.w;
+    }
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) sum += (int)c[j];
+    int incl = sum;  // over the lanes >= this one
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(FULL, incl, o);
+      incl += lane + o < 32 ? y : 0;
+    }
+    if (lane == 0) ts.wa[warp] = incl;
+    __syncthreads();
+    int above = incl - sum;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) above += w > warp ? ts.wa[w] : 0;
+    if (above < need && above + sum >= need) {  // exactly one thread
+      int acc = above, bstar = 0, nn = 0, nb = 0;
+#pragma unroll
+      for (int j = BPT - 1; j >= 0; --j) {
+        const bool hit = nb == 0 && acc + (int)c[j] >= need;
+        bstar = hit ? tid * BPT + j : bstar;
+        nn = hit ? need - acc : nn;
+        nb = hit ? (int)c[j] : nb;
+        acc += (int)c[j];
+      }
+      ts.bstar = bstar;
+      ts.need = nn;
+      ts.nb = nb;
+    }
+    __syncthreads();
+    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
+    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
+    lo = nlo;
+    need = ts.need;
+    nin = ts.nb;
+    // the next round's first barrier orders these reads before the next writes
+  }
+
+  // 3. the boundary pair (T, t) among at most kTkCand candidates, gathered in index
+  // order by a block scan and ranked by warp 0
+  const bool all_in = need == nin;                // every key in [lo, hi] is taken
+  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
+  if (!by_index && !all_in) {
+    int cnt = 0;
+#pragma unroll 1
+    for (int q = 0; q < Q; ++q) {
+      const uint4 v = k4[q];
+      const int j = i0 + 4 * q;
+      cnt += (j < n) & (v.x >= lo) & (v.x <= hi);
+      cnt += (j + 1 < n) & (v.y >= lo) & (v.y <= hi);
+      cnt += (j + 2 < n) & (v.z >= lo) & (v.z <= hi);
+      cnt += (j + 3 < n) & (v.w >= lo) & (v.w <= hi);
+    }
+    int total;
+    int slot = block_scan(cnt, 0, total);
+#pragma unroll 1
+    for (int q = 0; q < Q; ++q) {
+      const uint4 v = k4[q];
+      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t u = u4[e];
+        const bool f = (i0 + 4 * q + e < n) & (u >= lo) & (u <= hi);
+        if (f & (slot < kTkCand)) {
+          ts.cand[slot] = i0 + 4 * q + e;
+          ts.ckey[slot] = u;
+        }
+        slot += f;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nc = min(nin, kTkCand);
+      const int ci = lane < nc ? ts.cand[lane] : 0;
+      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
+      int r = 0;
+#pragma unroll 8
+      for (int m = 0; m < kTkCand; ++m) {
+        const uint32_t a = ts.ckey[m];
+        const int cm = ts.cand[m];
+        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
+      }
+      if ((lane < nc) & (r == need - 1)) {
+        ts.tkey = cu;
+        ts.tidx = ci;
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
+  const int tI = (by_index || all_in) ? n : ts.tidx;  // all_in: every key >= lo is taken
+  const unsigned bi = by_index ? 1u : 0u;
+
+  // 4. ascending compaction.  Class bit 0: taken; bit 1: a boundary key taken by index
+  // (the first `need` of them in index order).
+  auto cls = [&](uint32_t u, int i) -> unsigned {
+    const unsigned valid = (unsigned)(i < n);
+    const unsigned above = (unsigned)(u > hi);
+    const unsigned inr = (unsigned)(u >= lo) & (above ^ 1u);
+    const unsigned tk = above | (inr & (bi ^ 1u) & ((unsigned)(u > T) | ((unsigned)(u == T) & (unsigned)(i <= tI))));
+    return (0u - valid) & (tk | ((inr & bi) << 1));  // all bits of the class, or none
+  };
+  int c1 = 0, c2 = 0;
+#pragma unroll 1
+  for (int q = 0; q < Q; ++q) {
+    const uint4 v = k4[q];
+    const int j = i0 + 4 * q;
+    const unsigned a = cls(v.x, j), b = cls(v.y, j + 1), c = cls(v.z, j + 2), d = cls(v.w, j + 3);
+    c1 += (int)((a & 1u) + (b & 1u) + (c & 1u) + (d & 1u));
+    c2 += (int)((a >> 1) + (b >> 1) + (c >> 1) + (d >> 1));
+  }
+  int tot1, tot2;
+  const int base = block_scan(c1, 1, tot1);
+  int bseen = block_scan(c2, 0, tot2);
+  int o = base + min(need, bseen);
+#pragma unroll 1
+  for (int q = 0; q < Q; ++q) {
+    const uint4 v = k4[q];
+    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = i0 + 4 * q + e;
+      const unsigned t = cls(u4[e], i);
+      const bool take = (t & 1u) | ((t >> 1) & (unsigned)(bseen < need));
+      if (take & (o < k)) out[o] = i;
+      o += take;
+      bseen += (int)(t >> 1);
+    }
+  }
+  __syncthreads();  // the list is complete and the scratch may be reused
 }
 
 // Top-k by counting, for up to a few hundred keys.  Key i's rank is the number of keys that
