@@ -54,9 +54,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-decode-steps", type=int, default=0, help="decode steps per oracle sample (0: all)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="repeat the oracle sample until this much CPU time")
-    ap.add_argument("--flush", choices=["clean", "write"], default="clean",
-                    help="L2 flush before timed intervals: write 256 MB then read another 256 MB (clean, default), "
-                         "or only the write (leaves dirty lines for the timed kernel to write back)")
+    ap.add_argument("--flush", choices=["write", "clean"], default="write",
+                    help="L2 flush before timed intervals: write a 256 MB buffer (default), or write it and then read "
+                         "another 256 MB buffer so no dirty line is left for the timed kernel to write back (clean)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the batch-16 (workload 4) decode measurement added to the default workload's line")
     ap.add_argument("--prefill-chunk", type=int, default=8192,
@@ -187,7 +187,7 @@ class Setup:
         # read after the write, so the flush leaves L2 holding clean lines of this buffer
         # instead of 129 MB of dirty ones that the timed kernel would have to write back
         self.flush_read = share.flush_read if share else torch.ones(256 << 20, dtype=torch.uint8, device=dev)
-        self.flush_mode = share.flush_mode if share else "clean"
+        self.flush_mode = share.flush_mode if share else "write"
 
     # one call each, on the current stream
     def prefill(self):
@@ -208,9 +208,9 @@ class Setup:
             self.rkv.rkv_decode_step(self.cache, q, k_new, v_new, self.k1, self.k2, out, workspace=self.dws)
 
     def flush(self):
-        """Evict L2 before a timed interval: write a 256 MB buffer (twice L2), then, in
-        the default "clean" mode, read another 256 MB buffer so the write's dirty lines
-        are written back here rather than inside the timed kernel."""
+        """Evict L2 before a timed interval: write a 256 MB buffer (twice L2); in the
+        "clean" mode, then read another 256 MB buffer so the write's dirty lines are
+        written back here rather than inside the timed kernel."""
         self.flush_buf.zero_()
         if self.flush_mode == "clean":
             self.flush_read.view(torch.int64).max()
@@ -647,7 +647,7 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
 
 
 def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int, layers: int = 1,
-                    mode: str = "hsa", flush: str = "clean") -> dict:
+                    mode: str = "hsa", flush: str = "write") -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
     how = ("256 MB write, then a 256 MB read of another buffer, so no dirty line is left for the timed work "
            "to write back" if flush == "clean" else "256 MB write")
