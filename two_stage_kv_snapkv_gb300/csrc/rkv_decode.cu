@@ -548,6 +548,23 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
 
+// Folds bf16 key x into one page's summaries in memory: *mx = max(*mx, x), *mn =
+// min(*mn, x), as reductions (no load; nothing waits for them).  The reductions act
+// on the 4-byte pair holding the entry; the other entry of the pair gets the identity
+// of the operation (-inf for the max, +inf for the min) and keeps its value.
+__device__ __forceinline__ void summary_fold(rkv_bf16* mx, rkv_bf16* mn, rkv_bf16 x) {
+  const bool hi = (reinterpret_cast<uintptr_t>(mx) & 2u) != 0;  // mx and mn have the same offset in their rows
+  const uint16_t ninf = 0xff80u, pinf = 0x7f80u;
+  rkv_bf16* mx2 = reinterpret_cast<rkv_bf16*>(reinterpret_cast<uintptr_t>(mx) & ~(uintptr_t)3);
+  rkv_bf16* mn2 = reinterpret_cast<rkv_bf16*>(reinterpret_cast<uintptr_t>(mn) & ~(uintptr_t)3);
+  asm volatile("red.relaxed.gpu.global.max.noftz.v2.bf16 [%0], {%1, %2};\n" ::"l"(mx2), "h"(hi ? ninf : x),
+               "h"(hi ? x : ninf)
+               : "memory");
+  asm volatile("red.relaxed.gpu.global.min.noftz.v2.bf16 [%0], {%1, %2};\n" ::"l"(mn2), "h"(hi ? pinf : x),
+               "h"(hi ? x : pinf)
+               : "memory");
+}
+
 template <int STAGES, class Params>
 __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -606,6 +623,17 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   }
   const int n = n0 + (do_append ? 1 : 0);
   const int NP = (n + P - 1) / P;
+  // 2. the append (rank 0, threads 0-63: channels 2t and 2t + 1) writes the token into
+  // its slot and folds its key into its page's Kmax/Kmin.  Within this step every CTA
+  // takes the token from new_kv, so nothing waits for these writes, and they need no
+  // load: the fold is a max / min reduction in memory (the first token of a page
+  // stores its key instead).  (On GB300 a barrier, even a warp's, waits for the loads
+  // a thread has in flight, asynchronous copies included: loading the page's
+  // summaries during the selection held rank 0, and with it the cluster, up by about
+  // a microsecond.)
+  const bool appender = do_append && rank == 0 && tid < 64;
+  const int app_page = n0 / P;
+  const size_t app_row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + app_page;
   // this CTA's slice [p0, p1) of the pages (8-page aligned).  Short slices (under 64
   // pages) have the summaries of all 128 channels staged right away, in 16-byte
   // cp.async pieces (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and
@@ -644,30 +672,6 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     dst[4] = bf16_lo(qv.z); dst[5] = bf16_hi(qv.z); dst[6] = bf16_lo(qv.w); dst[7] = bf16_hi(qv.w);
   }
   if (do_append && tid < 32) *reinterpret_cast<uint4*>(new_kv + tid * 16) = nkv;
-
-  // 4. append (rank 0): the token goes into its slot and its page's Kmax/Kmin are
-  // folded.  Within this step every CTA takes the token from new_kv, so nothing waits
-  // for these writes.  Their loads are issued after the first summary tile has landed
-  // (a barrier waits for a thread's outstanding loads, and the Kmax/Kmin loads need
-  // the length first: issued here they would hold up the channel select), the stores
-  // after the scoring.
-  const bool appender = do_append && rank == 0 && tid < 64;
-  uint32_t app_k = 0, app_v = 0, app_mx = 0, app_mn = 0;
-  int app_phys = -1;
-  size_t app_row = 0;
-  bool app_loaded = false;
-  auto append_loads = [&]() {
-    if (!appender || app_loaded) return;
-    app_loaded = true;
-    const int page = n0 / P;
-    const size_t src = ((size_t)b * p.Hkv + g) * 128 + 2 * tid;
-    app_row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + page;
-    app_phys = p.page_table[(size_t)b * p.max_pages + page];
-    app_k = *reinterpret_cast<const uint32_t*>(p.k_new + src);
-    app_v = *reinterpret_cast<const uint32_t*>(p.v_new + src);
-    app_mx = (uint32_t)p.kmax[app_row] | ((uint32_t)p.kmax[app_row + p.max_pages] << 16);
-    app_mn = (uint32_t)p.kmin[app_row] | ((uint32_t)p.kmin[app_row + p.max_pages] << 16);
-  };
 
   // 5. channels (every CTA)
   const int k1 = p.k1[b];
@@ -722,7 +726,6 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
       }
     }
     __syncthreads();
-    append_loads();
     if (pnew >= t0 && pnew < t0 + cnt) {
       const int j = pnew - t0;
       const bool first = (n0 % P) == 0;
@@ -814,33 +817,10 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
 
   // the arrival count of sequence b's clusters: every CTA of this cluster has read the
   // length by now (before its second barrier), so the last cluster of b to count here
-  // may advance seq_len (step 11).  Only the result waits, until the end.
+  // may advance seq_len (step 12).  Only the result waits, until the end.
   int arrivals = -1;
   if (do_append && rank == 0 && tid == 0) arrivals = atomicAdd(&p.sync[b], 1);
 
-  // the append's stores: nothing in this step waits for them
-  append_loads();  // (only if this CTA staged no tile)
-  if (appender) {
-    if (app_phys >= 0 && app_phys < p.num_phys) {
-      const int slot = n0 % P;
-      const size_t dst = (((size_t)app_phys * p.Hkv + g) * P + slot) * 128 + 2 * tid;
-      *reinterpret_cast<uint32_t*>(p.k_pages + dst) = app_k;
-      *reinterpret_cast<uint32_t*>(p.v_pages + dst) = app_v;
-      float mx0 = bf16_lo(app_k), mx1 = bf16_hi(app_k), mn0 = mx0, mn1 = mx1;
-      if (slot > 0) {
-        mx0 = fmaxf(bf16_lo(app_mx), mx0);
-        mx1 = fmaxf(bf16_hi(app_mx), mx1);
-        mn0 = fminf(bf16_lo(app_mn), mn0);
-        mn1 = fminf(bf16_hi(app_mn), mn1);
-      }
-      p.kmax[app_row] = (rkv_bf16)(__float_as_uint(mx0) >> 16);
-      p.kmax[app_row + p.max_pages] = (rkv_bf16)(__float_as_uint(mx1) >> 16);
-      p.kmin[app_row] = (rkv_bf16)(__float_as_uint(mn0) >> 16);
-      p.kmin[app_row + p.max_pages] = (rkv_bf16)(__float_as_uint(mn1) >> 16);
-    } else {
-      flag_error(p.err, RKV_DEVERR_PAGE_ID);
-    }
-  }
   // 7. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
   // 128 pages by counting each key's rank, beyond that the histogram select written
   // without divergent per-key branches (on GB300 it took 2.6 us over 1212 keys where
@@ -906,7 +886,32 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     p.out[((size_t)b * p.Hq + (size_t)g * G + h) * 128 + tid] = L > 0.f ? O / L : 0.f;
   }
 
-  // 11. the last cluster of sequence b to count advances seq_len (every CTA of every
+  // 11. the append's stores: the token's K and V into its slot (its physical page from
+  // the page-table row), its key into the page's Kmax/Kmin
+  if (appender) {
+    const int app_phys = ptab[app_page];
+    const uint32_t app_k = reinterpret_cast<const uint32_t*>(new_kv)[tid];
+    const uint32_t app_v = reinterpret_cast<const uint32_t*>(new_kv)[64 + tid];
+    if (app_phys >= 0 && app_phys < p.num_phys) {
+      const int slot = n0 % P;
+      const size_t dst = (((size_t)app_phys * p.Hkv + g) * P + slot) * 128 + 2 * tid;
+      *reinterpret_cast<uint32_t*>(p.k_pages + dst) = app_k;
+      *reinterpret_cast<uint32_t*>(p.v_pages + dst) = app_v;
+      const rkv_bf16 k0 = (rkv_bf16)(app_k & 0xffffu), k1v = (rkv_bf16)(app_k >> 16);
+      if (slot == 0) {  // a new page: its summaries are this key
+        p.kmax[app_row] = k0;
+        p.kmax[app_row + p.max_pages] = k1v;
+        p.kmin[app_row] = k0;
+        p.kmin[app_row + p.max_pages] = k1v;
+      } else {
+        summary_fold(p.kmax + app_row, p.kmin + app_row, k0);
+        summary_fold(p.kmax + app_row + p.max_pages, p.kmin + app_row + p.max_pages, k1v);
+      }
+    } else {
+      flag_error(p.err, RKV_DEVERR_PAGE_ID);
+    }
+  }
+  // 12. the last cluster of sequence b to count advances seq_len (every CTA of every
   // cluster of b read it before that cluster counted); nothing in this launch reads it
   // again, and the next launch sees it
   if (arrivals == p.Hkv - 1) {
