@@ -179,9 +179,11 @@ class Setup:
         # layers run one after another on one stream, so they can share the scratch
         self.pws = share.pws if share else rkv.prefill_workspace(wl.B, wl.Hq, wl.Hkv, wl.window, wl.Lmax, dev)
         self.dws = share.dws if share else rkv.decode_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, dev)
-        self.sws = None
+        self.sws = self.skt = None
         if mode == "sparq":
             self.sws = share.sws if share else rkv.sparq_workspace(wl.B, wl.Hq, wl.Hkv, self.cache.max_pages, P, dev)
+            # the channel-major key copy SparQ scores from (per layer: it holds the keys)
+            self.skt = rkv.sparq_keys(self.cache, dev)
         self.out = torch.empty((wl.steps, wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
         self.flush_buf = share.flush_buf if share else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         # read after the write, so the flush leaves L2 holding clean lines of this buffer
@@ -194,6 +196,8 @@ class Setup:
         i = self.inp
         self.rkv.rkv_prefill_evict(i["q_win"], i["k"], i["v"], i["prompt_len"], self.keep1, self.kp, self.cache,
                                    self.kept, workspace=self.pws)
+        if self.skt is not None:   # the cache was rewritten: the key copy starts empty
+            self.skt[:self.wl.B * self.wl.Hkv * 4].zero_()
 
     def decode(self, t: int):
         d = self.dec[t]
@@ -203,7 +207,8 @@ class Setup:
         """One decode step of this mode: append the token, then select and attend."""
         if self.mode == "sparq":
             self.rkv.rkv_append_page_summary(self.cache, k_new, v_new, 1)
-            self.rkv.rkv_decode_sparq(self.cache, q, self.k1, self.k_tokens, out, workspace=self.sws)
+            self.rkv.rkv_decode_sparq(self.cache, q, self.k1, self.k_tokens, out, workspace=self.sws,
+                                      keys_t=self.skt)
         else:
             self.rkv.rkv_decode_step(self.cache, q, k_new, v_new, self.k1, self.k2, out, workspace=self.dws)
 
@@ -220,13 +225,17 @@ class Setup:
         """Compulsory HBM bytes of decode step t, by kernel (the method must move these)."""
         wl = self.wl
         P = wl.page_size
-        summ = kv = 0
+        summ = kv = sync = 0
         for b in range(wl.B):
             n = self.keep1[b] + t + 1
             NP = -(-n // P)
-            if self.mode == "sparq":   # every key row to score, the chosen tokens' K and V rows
-                summ += wl.Hkv * n * 128 * 2
+            if self.mode == "sparq":
+                # the chosen channels of every key from the channel-major copy, the chosen
+                # tokens' K and V rows; the copy takes the step's new key (at the first
+                # step every key: its build), read as a row and written along the channels
+                summ += wl.Hkv * n * self.k1[b] * 2
                 kv += wl.Hkv * min(self.k_tokens[b], n) * 128 * 2 * 2
+                sync += wl.Hkv * (n if t == 0 else 1) * 128 * 2 * 2
             else:
                 summ += wl.Hkv * 2 * self.k1[b] * NP * 2
                 kv += wl.Hkv * min(self.k2[b], NP) * P * 128 * 2 * 2
@@ -234,8 +243,9 @@ class Setup:
         out = wl.B * wl.Hq * 128 * 4
         append = wl.B * wl.Hkv * (128 * 2 * 2 * 2 + 128 * 2 * 2 * 2)   # new k,v read+write, summaries
         total = summ + kv + q + out + append
+        total += sync
         return dict(hsa_score=summ + q, hsa_attend=kv + q + out, append_small=append, hsa_step=total,
-                    sparq_score=summ + q, sparq_attend=kv + q + out, step_total=total)
+                    sparq_score=summ + q, sparq_attend=kv + q + out, sparq_keys_sync=sync, step_total=total)
 
     def prefill_bytes(self) -> dict:
         """Stage-1 bytes per layer: `compulsory` reads the prompt's keys once and reads
@@ -343,6 +353,9 @@ def ncu_every_kernel(setup: Setup) -> None:
     rkv.rkv_exact_topk_recall(setup.cache, d["q"], pg, [k * wl.page_size for k in setup.k2])
     if setup.cache.max_pages * wl.page_size <= 32768:   # the token path's limit
         rkv.rkv_decode_sparq(setup.cache, d["q"], setup.k1, [k * wl.page_size for k in setup.k2], setup.out[2])
+        # with the channel-major key copy: sparq_keys_sync + the copy's scoring
+        rkv.rkv_decode_sparq(setup.cache, d["q"], setup.k1, [k * wl.page_size for k in setup.k2], setup.out[2],
+                             keys_t=rkv.sparq_keys(setup.cache, setup.dev))
     rkv.rkv_decode_path(0)
     plan = W.chunk_plan(wl, 8192)
     cache = rkv.PagedCache(wl.B, wl.Hkv, wl.page_size, setup.cache.max_pages, setup.dev,
@@ -559,7 +572,8 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
     pb = setup.prefill_bytes()
 
     def algo_bytes(kind):
-        if kind in ("hsa_score", "hsa_attend", "append_small", "hsa_step", "sparq_score", "sparq_attend"):
+        if kind in ("hsa_score", "hsa_attend", "append_small", "hsa_step", "sparq_score", "sparq_attend",
+                    "sparq_keys_sync"):
             return statistics.mean(sb[kind] for sb in step_bytes)
         if kind in pb:
             return pb[kind]

@@ -214,8 +214,9 @@ rkv_status rkv_prefill_chunk(const rkv_bf16* q_win, const rkv_bf16* k_chunk, con
  * For each b the tokens go to positions [seq_len[b], seq_len[b] + n_new): when
  * k_new is not NULL they are first copied from k_new / v_new (device
  * [B][Hkv][n_new][128] bf16) into their page slots, otherwise they must already
- * be there.  Every touched page's Kmax/Kmin is recomputed from its valid tokens,
- * then seq_len[b] += n_new.  With seq_len = 0 and n_new = n this is a full
+ * be there.  Every touched page's Kmax/Kmin is brought up to date: with k_new, a
+ * page's stored summary (of its earlier tokens) is folded with the new keys; without,
+ * the page is recomputed from its valid tokens.  Then seq_len[b] += n_new.  With seq_len = 0 and n_new = n this is a full
  * rebuild.  A sequence that would outgrow its pages is left unchanged and flags
  * RKV_DEVERR_CAPACITY.
  */
@@ -343,11 +344,27 @@ size_t rkv_sparq_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_
  * is room; may be NULL) in place of sel_pages.  No append: call
  * rkv_append_page_summary first.  Caches of more than 32768 tokens per sequence
  * (max_pages * page_size) return RKV_ERR_UNSUPPORTED.
+ * keys_t (may be NULL): a channel-major copy of the cached keys, the layout SparQ
+ * scores from (each chosen channel's values of every position contiguous, so step 2
+ * reads k1 of the 128 channels): device, 16-byte aligned, keys_t_bytes >=
+ * rkv_sparq_keys_size(B, Hkv, max_pages, page_size) (else RKV_ERR_WORKSPACE).  It is
+ * owned by the caller and kept between calls: it starts zero-filled (empty), and each
+ * call first copies into it the positions the cache gained since the previous call
+ * (all of them the first time), then scores from it.  Zero it again whenever the
+ * cache's positions are rewritten rather than appended (a new prefill).  The
+ * selections and the output are those of the call without it, up to the fp32 order
+ * of the partial dot products.  With NULL, step 2 reads the cache's key rows.
  */
 rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq,
                             const int32_t* k1, const int32_t* k_tokens, float scale, float* out,
                             int32_t* sel_channels, int32_t* sel_tokens, int32_t sel_tokens_stride,
-                            void* workspace, size_t workspace_bytes, void* stream);
+                            void* keys_t, size_t keys_t_bytes, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Bytes of the channel-major key copy rkv_decode_sparq can keep and score from:
+ * a [B*Hkv] int32 record of the positions copied (256-byte padded), then per (b, g)
+ * a [128][max_pages * page_size] bf16 block. */
+size_t rkv_sparq_keys_size(int32_t B, int32_t Hkv, int32_t max_pages, int32_t page_size);
 
 /*
  * Exact-TopK recall of a page selection: a diagnostic, not a step of the method.

@@ -221,13 +221,13 @@ def test_sparq_rejects_bad_arguments_without_launching(rkv):
     lib = rkv.lib()
     i32 = ctypes.c_int32 * 2
 
-    def call(cache=None, k1=(32, 32), kt=(64, 64), stride=0, ws=None, sel=None):
+    def call(cache=None, k1=(32, 32), kt=(64, 64), stride=0, ws=None, sel=None, keys=None, keys_bytes=0):
         cache = cache or _fake_cache(rkv)
         if ws is None:
             ws = lib.rkv_sparq_workspace_size(2, 8, 2, cache.max_pages, cache.page_size)
         return lib.rkv_decode_sparq(ctypes.byref(cache), ctypes.c_void_p(0x80000), 8, i32(*k1), i32(*kt),
                                     ctypes.c_float(0.088), ctypes.c_void_p(0x90000), None, sel, stride,
-                                    ctypes.c_void_p(0xA0000), ws, None)
+                                    keys, keys_bytes, ctypes.c_void_p(0xA0000), ws, None)
 
     before = rkv.rkv_launch_count()
     assert call(k1=(0, 32)) == rkv.RKV_ERR_INVALID_ARG
@@ -237,7 +237,21 @@ def test_sparq_rejects_bad_arguments_without_launching(rkv):
     assert call(ws=16) == rkv.RKV_ERR_WORKSPACE
     assert call(cache=_fake_cache(rkv, max_pages=4096, num_phys_pages=8192)) == rkv.RKV_ERR_UNSUPPORTED  # 64K tokens
     assert call(cache=_fake_cache(rkv, page_size=8)) == rkv.RKV_ERR_UNSUPPORTED
+    # the channel-major key copy: too small, or misaligned
+    c = _fake_cache(rkv)
+    need = lib.rkv_sparq_keys_size(2, 2, c.max_pages, c.page_size)
+    assert call(keys=ctypes.c_void_p(0xC0000), keys_bytes=need - 1) == rkv.RKV_ERR_WORKSPACE
+    assert call(keys=ctypes.c_void_p(0xC0008), keys_bytes=need) == rkv.RKV_ERR_INVALID_ARG
     assert rkv.rkv_launch_count() == before
+
+
+def test_sparq_keys_size_is_the_record_and_a_block_per_unit(rkv):
+    """[B*Hkv] int32 lengths padded to 256 bytes, then [B*Hkv][128][max_pages*P] bf16."""
+    lib = rkv.lib()
+    for B, Hkv, mp, P in ((1, 2, 8, 16), (16, 8, 304, 32), (64, 8, 16384, 64)):
+        units = B * Hkv
+        assert lib.rkv_sparq_keys_size(B, Hkv, mp, P) == (units * 4 + 255) // 256 * 256 + units * 128 * mp * P * 2
+    assert lib.rkv_sparq_keys_size(0, 2, 8, 16) == 0
 
 
 def test_decode_step_host_rejects_bad_arguments_without_launching(rkv):

@@ -25,7 +25,17 @@ def rkv():
     return mod
 
 
-def _sparq_steps(rkv, wl, k_tokens, units=None, steps=None, seed=0x5EED, gen_device="cpu", tail="nan"):
+def _keys_block(rkv, run, keys_t, b, g):
+    """[128][n] channel-major view of unit (b, g) in the key copy (float64 on the CPU)."""
+    units = run.cache.B * run.cache.Hkv
+    cap = run.cache.max_pages * run.cache.page_size
+    off = (units * 4 + 255) // 256 * 256
+    blk = keys_t[off:].view(torch.bfloat16).view(units, 128, cap)
+    return f64(blk[b * run.cache.Hkv + g])
+
+
+def _sparq_steps(rkv, wl, k_tokens, units=None, steps=None, seed=0x5EED, gen_device="cpu", tail="nan",
+                 keys_t=False):
     run = GpuRun(wl, rkv, seed=seed, gen_device=gen_device, tail=tail)
     run.prefill()
     if units is None:
@@ -36,6 +46,7 @@ def _sparq_steps(rkv, wl, k_tokens, units=None, steps=None, seed=0x5EED, gen_dev
     G = wl.G
     ws = rkv.sparq_workspace(wl.B, wl.Hq, wl.Hkv, run.cache.max_pages, wl.page_size)
     stride = max(k_tokens) + 1
+    kt = rkv.sparq_keys(run.cache, run.dev) if keys_t else None
     errs = []
     for step in range(wl.steps if steps is None else steps):
         d = W.decode_tensors(wl, step, seed, 0, run.dev)
@@ -44,7 +55,8 @@ def _sparq_steps(rkv, wl, k_tokens, units=None, steps=None, seed=0x5EED, gen_dev
         out = torch.full((wl.B, wl.Hq, 128), float("nan"), dtype=torch.float32, device=run.dev)
         ch = torch.full((wl.B, wl.Hkv, 128), -9, dtype=torch.int32, device=run.dev)
         tk = torch.full((wl.B, wl.Hkv, stride), -9, dtype=torch.int32, device=run.dev)
-        rkv.rkv_decode_sparq(run.cache, d["q"], run.k1, k_tokens, out, sel_channels=ch, sel_tokens=tk, workspace=ws)
+        rkv.rkv_decode_sparq(run.cache, d["q"], run.k1, k_tokens, out, sel_channels=ch, sel_tokens=tk, workspace=ws,
+                             keys_t=kt)
         for u in checks:
             b, g = u.b, u.g
             u.Kc = np.concatenate([u.Kc[: u.n], f64(d["k_new"][b, g])[None]])
@@ -67,6 +79,8 @@ def _sparq_steps(rkv, wl, k_tokens, units=None, steps=None, seed=0x5EED, gen_dev
             err = float(np.abs(f64(out[b, g * G:(g + 1) * G]) - ref).max())
             errs.append(err)
             assert err <= ATOL_OUT, f"attention max-abs error {err}"
+            if kt is not None:  # the copy holds every cached key, bit for bit
+                np.testing.assert_array_equal(_keys_block(rkv, run, kt, b, g)[:, :u.n].T, u.Kc[:u.n])
     st, bits = run.status()
     assert st == rkv.RKV_OK, bits
     return max(errs)
@@ -84,10 +98,41 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("keys_t", [False, True], ids=["rows", "keys_t"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_sparq_small(rkv, name):
+def test_sparq_small(rkv, name, keys_t):
     wl, kt = SMALL[name]
-    _sparq_steps(rkv, wl, kt)
+    _sparq_steps(rkv, wl, kt, keys_t=keys_t)
+
+
+def test_sparq_keys_copy_restarts_when_its_record_is_ahead(rkv):
+    """A record above the cache's length (the cache was refilled shorter) makes the
+    next call copy every position again; a zeroed copy is rebuilt the same way."""
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=2,
+                  pool_kernel=5)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    kt = rkv.sparq_keys(run.cache, run.dev)
+    units = wl.B * wl.Hkv
+    cap = run.cache.max_pages * wl.page_size
+    d = W.decode_tensors(wl, 0, run.seed, 0, run.dev)
+    out = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=run.dev)
+    rkv.rkv_decode_sparq(run.cache, d["q"], run.k1, [64, 64], out, keys_t=kt)
+    n = run.cache.seq_len.cpu().numpy()
+    rec = kt[:units * 4].view(torch.int32)
+    assert rec.cpu().tolist() == [int(n[u // wl.Hkv]) for u in range(units)]
+    ref = kt.clone()
+    # scramble the block and push every record past the end: the next call recopies all
+    off = (units * 4 + 255) // 256 * 256
+    kt[off:] = 0x55
+    rec.fill_(cap)
+    rkv.rkv_decode_sparq(run.cache, d["q"], run.k1, [64, 64], out, keys_t=kt)
+    for b in range(wl.B):
+        for g in range(wl.Hkv):
+            nb = int(n[b])
+            np.testing.assert_array_equal(_keys_block(rkv, run, kt, b, g)[:, :nb], _keys_block(rkv, run, ref, b, g)[:, :nb])
+    assert rec.cpu().tolist() == [int(n[u // wl.Hkv]) for u in range(units)]
+    assert run.status()[0] == rkv.RKV_OK
 
 
 def test_sparq_every_token_is_dense_attention(rkv):
@@ -127,8 +172,21 @@ def test_sparq_workload2_sampled(rkv):
     _sparq_steps(rkv, wl, [512], units=[(0, 0), (0, 6)], gen_device="cuda", tail="zero")
 
 
+def test_sparq_workload2_keys_t_sampled(rkv):
+    wl = W.workload(2)
+    wl.steps = 3
+    _sparq_steps(rkv, wl, [512], units=[(0, 1), (0, 7)], gen_device="cuda", tail="zero", keys_t=True)
+
+
 def test_sparq_workload4_sampled(rkv):
     wl = W.workload(4)
     wl.steps = 2
     longest = int(np.argmax(wl.prompt_lens))
     _sparq_steps(rkv, wl, [2048] * wl.B, units=[(longest, 3), (0, 0)], gen_device="cuda", tail="zero")
+
+
+def test_sparq_workload4_keys_t_sampled(rkv):
+    wl = W.workload(4)
+    wl.steps = 2
+    longest = int(np.argmax(wl.prompt_lens))
+    _sparq_steps(rkv, wl, [2048] * wl.B, units=[(longest, 5), (3, 2)], gen_device="cuda", tail="zero", keys_t=True)

@@ -127,7 +127,8 @@ const char* kernel_name(int kind) {
       "append_small", "append_pages", "append_advance", "snap_stats",  "snap_stats_combine",
       "snap_colsum",  "snap_pool",    "snap_select",    "snap_compact", "hsa_score",
       "hsa_topk",     "hsa_attend",   "hsa_combine",    "hsa_step",     "recall",
-      "chunk_gather", "sparq_score",  "sparq_topk",     "sparq_attend", "wait_selftest"};
+      "chunk_gather", "sparq_score",  "sparq_topk",     "sparq_attend", "wait_selftest",
+      "sparq_keys_sync"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : nullptr;
 }
 
@@ -471,10 +472,15 @@ size_t rkv_sparq_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t max_
   return rkv::sparq_ws_bytes(B, Hq, Hkv, max_pages, page_size);
 }
 
+size_t rkv_sparq_keys_size(int32_t B, int32_t Hkv, int32_t max_pages, int32_t page_size) {
+  if (B < 1 || Hkv < 1 || max_pages < 1 || page_size < 1) return 0;
+  return rkv::sparq_keys_bytes(B, Hkv, max_pages, page_size);
+}
+
 rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t Hq, const int32_t* k1,
                             const int32_t* k_tokens, float scale, float* out, int32_t* sel_channels,
-                            int32_t* sel_tokens, int32_t sel_tokens_stride, void* workspace, size_t workspace_bytes,
-                            void* stream) {
+                            int32_t* sel_tokens, int32_t sel_tokens_stride, void* keys_t, size_t keys_t_bytes,
+                            void* workspace, size_t workspace_bytes, void* stream) {
   const NvtxRange nvtx_range("rkv_decode_sparq");
   rkv_status st = check_cache(cache);
   if (st != RKV_OK) return st;
@@ -500,6 +506,11 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
   const size_t need = rkv::sparq_ws_bytes(cache->B, Hq, cache->Hkv, cache->max_pages, cache->page_size);
   if (workspace_bytes < need)
     return fail(RKV_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (keys_t) {
+    if (!al16(keys_t)) return fail(RKV_ERR_INVALID_ARG, "keys_t must be 16-byte aligned");
+    const size_t kneed = rkv::sparq_keys_bytes(cache->B, cache->Hkv, cache->max_pages, cache->page_size);
+    if (keys_t_bytes < kneed) return fail(RKV_ERR_WORKSPACE, "keys_t %zu bytes < %zu needed", keys_t_bytes, kneed);
+  }
   rkv::DecodeArgs a;
   a.cache = *cache;
   a.q = q;
@@ -517,6 +528,7 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
   a.sel_pages_stride = sel_tokens_stride;
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
+  a.keys_t = keys_t;
   return cuda_status(rkv::launch_sparq(a, static_cast<cudaStream_t>(stream)), "rkv_decode_sparq launch");
 }
 

@@ -4,8 +4,8 @@
 // "Where it sits -- the mechanism gap" (Quest-style paged element-wise max/min
 // summaries along the sequence) and section "Evidence" (the incremental update at
 // decode equals a rebuild of the summaries, bit for bit).  Min and max of bf16
-// values are exact, so recomputing a touched page from its tokens is bit-identical
-// to any rebuild order.
+// values are exact, so folding new tokens into a page's stored summary, or
+// recomputing the page from its tokens, is bit-identical to any rebuild order.
 #include "rkv_device.cuh"
 #include "rkv_internal.h"
 
@@ -47,6 +47,34 @@ __device__ __forceinline__ void summarize_pair(const AppendParams& p, int b, int
   p.kmin[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mn1) >> 16);
 }
 
+// Folds new tokens [s0, s1) of page `pg` of (b, g) into the page's summary for the
+// channel pair (2*c2, 2*c2+1); the keys come from k_new (token t is its row t - n).
+// A page that held tokens before s0 starts from its stored summary.
+__device__ __forceinline__ void fold_new_pair(const AppendParams& p, int b, int g, int pg, int n, int s0, int s1,
+                                              int c2) {
+  const size_t row = ((size_t)(b * p.Hkv + g) * 128 + 2 * c2) * p.max_pages + pg;
+  float mx0 = -INFINITY, mx1 = -INFINITY, mn0 = INFINITY, mn1 = INFINITY;
+  if (s0 > pg * p.P) {
+    mx0 = bf16_f(p.kmax[row]);
+    mx1 = bf16_f(p.kmax[row + p.max_pages]);
+    mn0 = bf16_f(p.kmin[row]);
+    mn1 = bf16_f(p.kmin[row + p.max_pages]);
+  }
+  const rkv_bf16* src = p.k_new + ((size_t)(b * p.Hkv + g) * p.n_new) * 128 + 2 * c2;
+  for (int t = s0; t < s1; ++t) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(src + (size_t)(t - n) * 128);
+    const float x0 = bf16_lo(u), x1 = bf16_hi(u);
+    mx0 = fmaxf(mx0, x0);
+    mx1 = fmaxf(mx1, x1);
+    mn0 = fminf(mn0, x0);
+    mn1 = fminf(mn1, x1);
+  }
+  p.kmax[row] = (rkv_bf16)(__float_as_uint(mx0) >> 16);
+  p.kmax[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mx1) >> 16);
+  p.kmin[row] = (rkv_bf16)(__float_as_uint(mn0) >> 16);
+  p.kmin[row + p.max_pages] = (rkv_bf16)(__float_as_uint(mn1) >> 16);
+}
+
 __device__ __forceinline__ bool phys_ok(const AppendParams& p, int phys) {
   if (phys < 0 || phys >= p.num_phys) {
     flag_error(p.err, RKV_DEVERR_PAGE_ID);
@@ -56,7 +84,9 @@ __device__ __forceinline__ bool phys_ok(const AppendParams& p, int phys) {
 }
 
 // Few tokens per sequence (decode): one CTA per sequence does copy, summaries and
-// the length update.  grid B, 256 threads.
+// the length update.  With the new keys given, the touched pages' summaries fold
+// them in (no page is re-read); without (the tokens were written by the caller),
+// each touched page is recomputed from its tokens.  grid B, 256 threads.
 __global__ void __launch_bounds__(256) append_small_kernel(const __grid_constant__ AppendParams p) {
   __shared__ int s_n;
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -83,16 +113,24 @@ __global__ void __launch_bounds__(256) append_small_kernel(const __grid_constant
       *reinterpret_cast<uint32_t*>(p.v_pages + dst) = *reinterpret_cast<const uint32_t*>(p.v_new + src);
     }
   }
-  __syncthreads();  // the block's page writes are visible to the block
   const int end = n + p.n_new;
   const int first = n / p.P, last = (end - 1) / p.P;
   const int per = (last - first + 1) * 64;
-  for (int e = tid; e < p.Hkv * per; e += 256) {
-    const int g = e / per, pg = first + (e / 64) % (last - first + 1), c2 = e % 64;
-    const int phys = ptab[pg];
-    if (!phys_ok(p, phys)) continue;
-    const int cnt = min(p.P, end - pg * p.P);
-    summarize_pair(p, b, g, pg, phys, cnt, c2);
+  if (p.k_new) {
+    for (int e = tid; e < p.Hkv * per; e += 256) {
+      const int g = e / per, pg = first + (e / 64) % (last - first + 1), c2 = e % 64;
+      if (!phys_ok(p, ptab[pg])) continue;
+      fold_new_pair(p, b, g, pg, n, max(n, pg * p.P), min(end, (pg + 1) * p.P), c2);
+    }
+  } else {
+    __syncthreads();
+    for (int e = tid; e < p.Hkv * per; e += 256) {
+      const int g = e / per, pg = first + (e / 64) % (last - first + 1), c2 = e % 64;
+      const int phys = ptab[pg];
+      if (!phys_ok(p, phys)) continue;
+      const int cnt = min(p.P, end - pg * p.P);
+      summarize_pair(p, b, g, pg, phys, cnt, c2);
+    }
   }
   __syncthreads();
   if (tid == 0) p.seq_len[b] = end;

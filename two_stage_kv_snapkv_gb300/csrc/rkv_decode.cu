@@ -1091,6 +1091,151 @@ __global__ void __launch_bounds__(kScoreThreads) sparq_score_kernel(const __grid
   }
 }
 
+// Token path with the channel-major key copy (SparQ's own layout: the keys stored
+// once more along the head dimension, so scoring reads only the chosen channels;
+// "RocketKV-adapted", "Where it sits -- the mechanism gap", SparQ-style channels).
+// Per unit (b, g) the copy holds a [128][cap] bf16 block, cap = max_pages * P, row c
+// = channel c of every position; a [units] int32 record counts the positions copied.
+struct KeysT {
+  rkv_bf16* kt;  // [units][128][cap]
+  int32_t* len;  // [units]
+  int32_t* chan; // [units][128] the chosen channels (workspace, this call)
+  float* qs;     // [units][128] their sums of q over the group
+};
+
+// Step 0: the copy catches up with the cache: positions [len, n) of every unit (from
+// len rounded down to 8, so every store is a whole 16-byte group; a record above n
+// restarts at 0).  grid (units, kKtSplit), 256 threads; CTA y takes the 64-position
+// tiles y, y + kKtSplit, ...  A tile's key rows are staged in shared memory, then each
+// thread writes 8 positions of two channels as two 16-byte stores.  CTA 0 of a unit
+// also chooses the unit's channels (into the workspace, for step 1).  The record is
+// advanced by step 1, which runs after every CTA here has read it.
+constexpr int kKtTile = 64, kKtSplit = 8;
+__global__ void __launch_bounds__(256) sparq_keys_sync_kernel(const __grid_constant__ HsaParams p, KeysT kt) {
+  __shared__ __align__(16) uint32_t tile[kKtTile][68];  // a position's 64 channel pairs (+4 pad words)
+  __shared__ ChanSmem cs;
+  __shared__ float qf[8][128];
+  const int unit = blockIdx.x, b = unit / p.Hkv, g = unit % p.Hkv;
+  const int tid = threadIdx.x;
+  const int n = seq_length(p, b);
+  if (blockIdx.y == 0) {
+    const int G = p.G;
+    const rkv_bf16* qg = p.q + ((size_t)b * p.Hq + (size_t)g * G) * 128;
+    for (int i = tid; i < G * 128; i += 256) qf[i >> 7][i & 127] = bf16_f(qg[i]);
+    const int k1 = p.k1[b];
+    select_channels(qf, cs, G, k1);
+    if (tid < 128) {
+      if (p.sel_channels) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
+      kt.chan[unit * 128 + tid] = tid < k1 ? cs.chan[tid] : 0;
+      kt.qs[unit * 128 + tid] = tid < k1 ? cs.qpos[tid] + cs.qneg[tid] : 0.f;  // the group's sum of q
+    }
+  }
+  int m = kt.len[unit];
+  if (m < 0 || m > n) m = 0;
+  const size_t cap = (size_t)p.max_pages * p.P;
+  rkv_bf16* dst = kt.kt + (size_t)unit * 128 * cap;
+  for (int t0 = (m & ~7) + blockIdx.y * kKtTile; t0 < n; t0 += kKtSplit * kKtTile) {
+    for (int e = tid; e < kKtTile * 16; e += 256) {  // 16-byte pieces of the tile's key rows
+      const int r = e >> 4, piece = e & 15, t = t0 + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < n) {
+        const int phys = p.page_table[(size_t)b * p.max_pages + t / p.P];
+        if (phys >= 0 && phys < p.num_phys)
+          v = reinterpret_cast<const uint4*>(p.k_pages + (((size_t)phys * p.Hkv + g) * p.P + t % p.P) * 128)[piece];
+        else if (piece == 0)
+          flag_error(p.err, RKV_DEVERR_PAGE_ID);
+      }
+      *reinterpret_cast<uint4*>(&tile[r][piece * 4]) = v;
+    }
+    __syncthreads();
+    const int ngrp = (min(kKtTile, n - t0) + 7) >> 3;
+    for (int e = tid; e < 64 * ngrp; e += 256) {  // lanes take consecutive channel pairs
+      const int c2 = e & 63, grp = e >> 6;
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = tile[grp * 8 + j][c2];
+      uint4 lo, hi;  // channel 2 c2, channel 2 c2 + 1: positions in ascending order
+      lo.x = (w[0] & 0xffffu) | (w[1] << 16);
+      lo.y = (w[2] & 0xffffu) | (w[3] << 16);
+      lo.z = (w[4] & 0xffffu) | (w[5] << 16);
+      lo.w = (w[6] & 0xffffu) | (w[7] << 16);
+      hi.x = (w[0] >> 16) | (w[1] & 0xffff0000u);
+      hi.y = (w[2] >> 16) | (w[3] & 0xffff0000u);
+      hi.z = (w[4] >> 16) | (w[5] & 0xffff0000u);
+      hi.w = (w[6] >> 16) | (w[7] & 0xffff0000u);
+      rkv_bf16* col = dst + (size_t)(2 * c2) * cap + t0 + grp * 8;
+      *reinterpret_cast<uint4*>(col) = lo;
+      *reinterpret_cast<uint4*>(col + cap) = hi;
+    }
+    __syncthreads();
+  }
+}
+
+// Step 1 with the copy: s_t over the chosen channels (chosen in step 0), each one's
+// row read from the copy.  grid (ceil(max tokens / 1024), units), 256 threads = 4
+// channel groups x 64 threads of 2 x 8 positions (16-byte loads); the four groups'
+// partial sums add in shared memory.  Group r takes the chosen channels r, r + 4, ...,
+// four at a time (eight loads in flight a thread); the channels past k1 weigh 0.
+// Positions at or past n read whatever the copy holds there (finite: keys or zeros)
+// and are not written out; columns past the block's end are clamped into it.
+constexpr int kTokScoreT = 1024;
+__global__ void __launch_bounds__(kScoreThreads) sparq_score_t_kernel(const __grid_constant__ HsaParams p, KeysT kt) {
+  __shared__ int chan[128];
+  __shared__ float qs[128];
+  __shared__ __align__(16) float part[4][kTokScoreT];
+  const int unit = blockIdx.y, b = unit / p.Hkv;
+  const int tid = threadIdx.x;
+  const int n = seq_length(p, b);
+  const int t0 = blockIdx.x * kTokScoreT;
+  if (blockIdx.x == 0 && tid == 0) kt.len[unit] = n;  // every position below n is in the copy
+  if (t0 >= n) return;
+  const int k1 = p.k1[b];
+  if (tid < 128) {
+    chan[tid] = tid < k1 ? kt.chan[unit * 128 + tid] : 0;
+    qs[tid] = tid < k1 ? kt.qs[unit * 128 + tid] : 0.f;
+  }
+  __syncthreads();
+  const int cap = p.max_pages * p.P;
+  const rkv_bf16* blk = kt.kt + (size_t)unit * 128 * cap;
+  const int grp = tid >> 6, j = tid & 63;
+  const int c0 = min(t0 + 8 * j, cap - 8), c1 = min(t0 + 512 + 8 * j, cap - 8);
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  const int k1r = (k1 + 15) & ~15;
+#pragma unroll 1
+  for (int kk = grp; kk < k1r; kk += 16) {
+    uint4 u[4], v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const rkv_bf16* row = blk + (size_t)chan[kk + 4 * i] * cap;
+      u[i] = *reinterpret_cast<const uint4*>(row + c0);
+      v[i] = *reinterpret_cast<const uint4*>(row + c1);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float q = qs[kk + 4 * i];
+      const uint32_t w[8] = {u[i].x, u[i].y, u[i].z, u[i].w, v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[2 * e] = fmaf(q, bf16_lo(w[e]), acc[2 * e]);
+        acc[2 * e + 1] = fmaf(q, bf16_hi(w[e]), acc[2 * e + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    part[grp][8 * j + e] = acc[e];
+    part[grp][512 + 8 * j + e] = acc[8 + e];
+  }
+  __syncthreads();
+  float* sg = p.sigma + (size_t)unit * p.tok_stride;
+  for (int i = tid; i < kTokScoreT; i += kScoreThreads) {
+    const int t = t0 + i;
+    if (t < n) sg[t] = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
+  }
+}
+
 // Token path, step 2: top-k2 tokens, ascending.  grid B*Hkv, 1024 threads, dynamic
 // shared memory = the sequence's token count of keys (at most kTokMax).
 constexpr int kTokMax = 32768;
@@ -1395,10 +1540,15 @@ size_t sparq_ws_bytes(int B, int Hq, int Hkv, int max_pages, int page_size) {
   const size_t units = (size_t)B * Hkv;
   const size_t tok = (size_t)max_pages * page_size;
   return align256(units * tok * 4) * 2 + align256((size_t)B * Hq * kMaxSplit * 128 * 4) +
-         align256((size_t)B * Hq * kMaxSplit * 8);
+         align256((size_t)B * Hq * kMaxSplit * 8) + units * 128 * 8;
 }
 
 int sparq_max_tokens() { return kTokMax; }
+
+size_t sparq_keys_bytes(int B, int Hkv, int max_pages, int page_size) {
+  const size_t units = (size_t)B * Hkv;
+  return align256(units * 4) + units * 128 * (size_t)max_pages * page_size * 2;
+}
 
 cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s) {
   bool ok = false;
@@ -1429,9 +1579,26 @@ cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s) {
     attrs = true;
   }
   const int ntok = p.tok_stride < kTokMax ? p.tok_stride : kTokMax;
-  launch_begin(K_SPARQ_SCORE, s);
-  sparq_score_kernel<<<dim3((ntok + kTokScore - 1) / kTokScore, (unsigned)units), kScoreThreads, 0, s>>>(p);
-  launch_end(K_SPARQ_SCORE, s);
+  const dim3 score_grid((ntok + kTokScore - 1) / kTokScore, (unsigned)units);
+  if (a.keys_t) {
+    KeysT kt;
+    kt.len = static_cast<int32_t*>(a.keys_t);
+    kt.kt = reinterpret_cast<rkv_bf16*>(static_cast<uint8_t*>(a.keys_t) + align256(units * 4));
+    uint8_t* chw = w + 2 * sg + align256((size_t)c.B * a.Hq * kMaxSplit * 128 * 4) +
+                   align256((size_t)c.B * a.Hq * kMaxSplit * 8);
+    kt.chan = reinterpret_cast<int32_t*>(chw);
+    kt.qs = reinterpret_cast<float*>(chw + units * 128 * 4);
+    launch_begin(K_SPARQ_KEYS_SYNC, s);
+    sparq_keys_sync_kernel<<<dim3((unsigned)units, kKtSplit), 256, 0, s>>>(p, kt);
+    launch_end(K_SPARQ_KEYS_SYNC, s);
+    launch_begin(K_SPARQ_SCORE, s);
+    sparq_score_t_kernel<<<dim3((ntok + kTokScoreT - 1) / kTokScoreT, (unsigned)units), kScoreThreads, 0, s>>>(p, kt);
+    launch_end(K_SPARQ_SCORE, s);
+  } else {
+    launch_begin(K_SPARQ_SCORE, s);
+    sparq_score_kernel<<<score_grid, kScoreThreads, 0, s>>>(p);
+    launch_end(K_SPARQ_SCORE, s);
+  }
   launch_begin(K_SPARQ_TOPK, s);
   sparq_topk_kernel<<<(unsigned)units, kTopkThreads, (size_t)ntok * 4, s>>>(p);
   launch_end(K_SPARQ_TOPK, s);

@@ -32,6 +32,7 @@ enum KernelKind {
   K_SPARQ_TOPK,
   K_SPARQ_ATTEND,
   K_WAIT_SELFTEST,
+  K_SPARQ_KEYS_SYNC,
   K_NUM_KINDS
 };
 const char* kernel_name(int kind);
@@ -110,11 +111,13 @@ struct DecodeArgs {
   int sel_pages_stride;
   void* ws;
   size_t ws_bytes;
+  void* keys_t = nullptr;  // token path: the channel-major key copy, or null
 };
 size_t decode_ws_bytes(int B, int Hq, int Hkv, int max_pages);
 // Token path (SparQ-only): k2 counts tokens; k_new must be null.
 size_t sparq_ws_bytes(int B, int Hq, int Hkv, int max_pages, int page_size);
 int sparq_max_tokens();
+size_t sparq_keys_bytes(int B, int Hkv, int max_pages, int page_size);
 cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s);
 bool decode_fused_ok(const rkv_cache& c);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

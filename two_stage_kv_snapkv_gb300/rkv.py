@@ -100,7 +100,9 @@ _lib.rkv_decode_step_host.restype = _i32
 _lib.rkv_sparq_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.rkv_sparq_workspace_size.restype = _sz
 _lib.rkv_decode_sparq.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _i32p, _i32p, _f32, _vp, _vp, _vp, _i32,
-                                  _vp, _sz, _vp]
+                                  _vp, _sz, _vp, _sz, _vp]
+_lib.rkv_sparq_keys_size.argtypes = [_i32, _i32, _i32, _i32]
+_lib.rkv_sparq_keys_size.restype = _sz
 _lib.rkv_decode_sparq.restype = _i32
 _lib.rkv_exact_topk_recall.argtypes = [ctypes.POINTER(RkvCacheStruct), _vp, _i32, _vp, _i32, _i32p, _f32, _vp, _vp,
                                        _vp]
@@ -127,7 +129,8 @@ _lib.rkv_profile_read.restype = ctypes.c_char_p
 EXPORTED = ["rkv_split_ratio", "rkv_split_ratio_mt", "rkv_prefill_workspace_size", "rkv_prefill_evict",
             "rkv_prefill_chunk_workspace_size", "rkv_prefill_chunk", "rkv_append_page_summary",
             "rkv_decode_workspace_size", "rkv_decode_hsa", "rkv_decode_hsa_noalloc", "rkv_decode_step",
-            "rkv_decode_path", "rkv_step_host_staging_size", "rkv_decode_step_host", "rkv_sparq_workspace_size", "rkv_decode_sparq", "rkv_exact_topk_recall", "rkv_selftest_bounded_wait", "rkv_get_device_status", "rkv_last_error",
+            "rkv_decode_path", "rkv_step_host_staging_size", "rkv_decode_step_host", "rkv_sparq_workspace_size", "rkv_decode_sparq", "rkv_sparq_keys_size",
+            "rkv_exact_topk_recall", "rkv_selftest_bounded_wait", "rkv_get_device_status", "rkv_last_error",
             "rkv_launch_count", "rkv_profile_enable", "rkv_profile_accumulate", "rkv_profile_release",
             "rkv_profile_reset", "rkv_profile_read"]
 
@@ -349,21 +352,29 @@ def sparq_workspace(B: int, Hq: int, Hkv: int, max_pages: int, page_size: int, d
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def sparq_keys(cache: "PagedCache", device="cuda") -> torch.Tensor:
+    """A zero-filled (empty) channel-major key copy for rkv_decode_sparq's keys_t."""
+    n = _lib.rkv_sparq_keys_size(cache.B, cache.Hkv, cache.max_pages, cache.page_size)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def rkv_decode_sparq(cache: PagedCache, q: torch.Tensor, k1: Sequence[int], k_tokens: Sequence[int],
                      out: torch.Tensor, sel_channels: Optional[torch.Tensor] = None,
                      sel_tokens: Optional[torch.Tensor] = None, scale: Optional[float] = None,
-                     workspace: Optional[torch.Tensor] = None, stream=None):
+                     workspace: Optional[torch.Tensor] = None, keys_t: Optional[torch.Tensor] = None, stream=None):
     """SparQ-only step (HSA with one-token pages): k_tokens tokens by their partial dot
-    products over the top-k1 channels, then exact attention over them."""
+    products over the top-k1 channels, then exact attention over them.  keys_t (from
+    sparq_keys) is the channel-major key copy to score from, kept between calls."""
     B, Hq, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if workspace is None:
         workspace = sparq_workspace(B, Hq, cache.Hkv, cache.max_pages, cache.page_size, q.device)
     stride = sel_tokens.shape[-1] if sel_tokens is not None else 0
+    kt_bytes = keys_t.numel() * keys_t.element_size() if keys_t is not None else 0
     _check(_lib.rkv_decode_sparq(ctypes.byref(cache.struct), _ptr(q), Hq, _host_i32(k1), _host_i32(k_tokens), scale,
-                                 _ptr(out), _ptr(sel_channels), _ptr(sel_tokens), stride, _ptr(workspace),
-                                 workspace.numel(), _stream(stream)))
+                                 _ptr(out), _ptr(sel_channels), _ptr(sel_tokens), stride, _ptr(keys_t), kt_bytes,
+                                 _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def rkv_exact_topk_recall(cache: PagedCache, q: torch.Tensor, sel_pages: torch.Tensor, k_tokens: Sequence[int],
