@@ -1266,11 +1266,13 @@ __global__ void __launch_bounds__(kTopkThreads) sparq_topk_kernel(const __grid_c
 // grid (nsplit, B*Hkv), 128 threads.  Dynamic shared memory: the ring (1024-aligned),
 // then the CTA's token rows (at most kTokRowItems chunks of 16).
 constexpr int kTokRowItems = 512;
-constexpr int kTokAttendSmem = 1024 + ring_bytes(kSplitStages) + 1024 + kTokRowItems * kChunkTok * 4;
-static_assert(ring_bytes(kSplitStages) >= kWarpCombineBytes, "the ring doubles as the warp-combine buffer");
+constexpr int kTokStages = 2;  // 2 CTAs an SM (3 stages fit one): at batch 16, 41 us a step against 59
+constexpr int kTokAttendSmem = 1024 + ring_bytes(kTokStages) + 1024 + kTokRowItems * kChunkTok * 4;
+static_assert(ring_bytes(kTokStages) >= kWarpCombineBytes, "the ring doubles as the warp-combine buffer");
+static_assert(kTokMax / kChunkTok / kTokRowItems <= kMaxSplit, "the largest selection splits into few enough CTAs");
 __global__ void __launch_bounds__(kThreads) sparq_attend_kernel(const __grid_constant__ HsaParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ AttnSmem<kSplitStages> as;
+  __shared__ AttnSmem<kTokStages> as;
   const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv, split = blockIdx.x;
   const int n = min(seq_length(p, b), kTokMax);
   const int k = min(p.k2[b], n);
@@ -1279,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads) sparq_attend_kernel(const __grid_con
   const int it0 = min(items, split * ips), it1 = min(items, it0 + ips);
   // this CTA's tokens as rows of the K/V pools, resolved once (the chunk loop then
   // issues its copies without waiting on the list or the page table)
-  int32_t* rows = reinterpret_cast<int32_t*>(align1024(smem) + ring_bytes(kSplitStages) + 1024);
+  int32_t* rows = reinterpret_cast<int32_t*>(align1024(smem) + ring_bytes(kTokStages) + 1024);
   const int r0 = it0 * kChunkTok, r1 = min(k, it1 * kChunkTok);
   const int32_t* list = p.selp + (size_t)unit * p.tok_stride;
   const int32_t* prow = p.page_table + (size_t)b * p.max_pages;
@@ -1292,7 +1294,7 @@ __global__ void __launch_bounds__(kThreads) sparq_attend_kernel(const __grid_con
   }
   __syncthreads();
   int to = 0;
-  const CtaPart* part = attend_cta<kSplitStages, true>(p, rows - r0, nullptr, b, g, k, it0, it1, align1024(smem), as,
+  const CtaPart* part = attend_cta<kTokStages, true>(p, rows - r0, nullptr, b, g, k, it0, it1, align1024(smem), as,
                                                        -1, nullptr, &to);
   const int c = threadIdx.x;
   for (int h = 0; h < p.G; ++h) {
@@ -1565,7 +1567,18 @@ cudaError_t launch_sparq(const DecodeArgs& a, cudaStream_t s) {
   for (int b = 0; b < c.B; ++b) kmax = a.k2[b] > kmax ? a.k2[b] : kmax;
   kmax = kmax < p.tok_stride ? kmax : p.tok_stride;
   const int items = (kmax + kChunkTok - 1) / kChunkTok;
-  int nsplit = (4 * num_sms() + (int)units - 1) / (int)units;
+  // CTAs per unit: as many as fill one wave of resident CTAs (more waves each pay the
+  // ring's fill and drain again), at most one per 4 chunks, and enough that no CTA
+  // resolves more than kTokRowItems chunks' rows
+  static int occ = 0;
+  if (occ == 0) {
+    cudaFuncSetAttribute(sparq_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTokAttendSmem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparq_attend_kernel, kThreads, kTokAttendSmem) !=
+            cudaSuccess ||
+        occ < 1)
+      occ = 1;
+  }
+  int nsplit = occ * num_sms() / (int)units;
   const int by_items = (items + kAtWarps - 1) / kAtWarps;
   nsplit = nsplit < by_items ? nsplit : by_items;
   const int by_rows = (items + kTokRowItems - 1) / kTokRowItems;  // a CTA resolves at most 512 items' rows
