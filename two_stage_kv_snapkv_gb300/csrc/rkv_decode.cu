@@ -1502,17 +1502,20 @@ cudaError_t launch_split(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
   const rkv_cache& c = a.cache;
   const size_t units = (size_t)c.B * c.Hkv;
   const int items = max_items(a);
-  int nsplit = (4 * num_sms() + (int)units - 1) / (int)units;
+  static int occ = 0;
+  if (occ == 0) {
+    cudaFuncSetAttribute(hsa_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+    cudaFuncSetAttribute(hsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, hsa_attend_kernel, kThreads, kSplitSmem) != cudaSuccess ||
+        occ < 1)
+      occ = 1;
+  }
+  // CTAs per unit: as many as fill one wave of resident CTAs, at most one per 4 chunks
+  int nsplit = occ * num_sms() / (int)units;
   const int by_items = (items + kAtWarps - 1) / kAtWarps;
   nsplit = nsplit < by_items ? nsplit : by_items;
   nsplit = nsplit < 1 ? 1 : (nsplit > kMaxSplit ? kMaxSplit : nsplit);
   p.nsplit = nsplit;
-  static bool attrs = false;
-  if (!attrs) {
-    cudaFuncSetAttribute(hsa_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
-    cudaFuncSetAttribute(hsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 16384 * 4);
-    attrs = true;
-  }
   launch_begin(K_HSA_SCORE, s);
   hsa_score_kernel<<<dim3((c.max_pages + kScorePages - 1) / kScorePages, (unsigned)units), kScoreThreads, 0, s>>>(p);
   launch_end(K_HSA_SCORE, s);
