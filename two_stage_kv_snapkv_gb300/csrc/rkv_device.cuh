@@ -122,6 +122,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 
 // Bulk copy (TMA engine) of `bytes` (multiple of 16, 16-B aligned ends) from global to
 // this CTA's shared memory; completion is signalled on `bar` as transaction bytes.
+// A hint: fetch [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+// Nothing waits for it, and L2 never serves stale data, so it may run before the
+// writes it would otherwise have to follow.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
