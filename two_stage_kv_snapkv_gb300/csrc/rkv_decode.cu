@@ -687,11 +687,11 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   }
   if (do_append && tid < 32) *reinterpret_cast<uint4*>(new_kv + tid * 16) = nkv;
 
-  // 5. channels (every CTA)
+  // 4. channels (every CTA)
   const int k1 = p.k1[b];
   select_channels(qf, cs, G, k1);
 
-  // 6. page bounds of this CTA's slice [p0, p1).  Staged rows: all 128 channels' Kmax
+  // 5. page bounds of this CTA's slice [p0, p1).  Staged rows: all 128 channels' Kmax
   // then Kmin (rows ch and 128 + ch), or the k1 chosen channels' (rows kk and k1 + kk,
   // copied per tile now, the region holding the whole slice whenever it fits).  The
   // appended token is folded into its
@@ -831,11 +831,11 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
 
   // the arrival count of sequence b's clusters: every CTA of this cluster has read the
   // length by now (before its second barrier), so the last cluster of b to count here
-  // may advance seq_len (step 12).  Only the result waits, until the end.
+  // may advance seq_len (step 11).  Only the result waits, until the end.
   int arrivals = -1;
   if (do_append && rank == 0 && tid == 0) arrivals = atomicAdd(&p.sync[b], 1);
 
-  // 7. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
+  // 6. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
   // 128 pages by counting each key's rank, beyond that the histogram select written
   // without divergent per-key branches (on GB300 it took 2.6 us over 1212 keys where
   // the branchy looping form took 4.3 us, both with warm instruction caches).  The list
@@ -866,14 +866,14 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // the next kernel on the stream may start launching its CTAs into the slots this one
   // frees (it waits for this grid's completion before touching memory)
   grid_launch_dependents();
-  // 8. attention over this CTA's share of the selected chunks
+  // 7. attention over this CTA's share of the selected chunks
   const int items = k * (P / kChunkTok);
   const int ips = (items + C - 1) / C;
   const int it0 = min(items, rank * ips), it1 = min(items, it0 + ips);
   int to = 0;
   const CtaPart* part = attend_cta<STAGES>(p, sel, ptab, b, g, n, it0, it1, ring, as, do_append ? n0 : -1, new_kv, &to);
 
-  // 9. each head's partial state goes to the CTA that finishes the head (h % C), slot
+  // 8. each head's partial state goes to the CTA that finishes the head (h % C), slot
   // [rank][h / C] of its inbox
   for (int h = 0; h < G; ++h) {
     float* dst = cluster.map_shared_rank(inbox, h % C) + ((size_t)rank * hpc + h / C) * 130;
@@ -886,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
 
   cluster.sync();  // every inbox is filled; no shared memory is touched remotely after this
 
-  // 10. merge this CTA's heads
+  // 9. merge this CTA's heads
   for (int h = rank; h < G; h += C) {
     float M = -1e30f;
     for (int r = 0; r < C; ++r) M = fmaxf(M, inbox[((size_t)r * hpc + h / C) * 130]);
@@ -900,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     p.out[((size_t)b * p.Hq + (size_t)g * G + h) * 128 + tid] = L > 0.f ? O / L : 0.f;
   }
 
-  // 11. the append's stores: the token's K and V into its slot (its physical page from
+  // 10. the append's stores: the token's K and V into its slot (its physical page from
   // the page-table row), its key into the page's Kmax/Kmin
   if (appender) {
     const int app_phys = ptab[app_page];
@@ -925,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
       flag_error(p.err, RKV_DEVERR_PAGE_ID);
     }
   }
-  // 12. the last cluster of sequence b to count advances seq_len (every CTA of every
+  // 11. the last cluster of sequence b to count advances seq_len (every CTA of every
   // cluster of b read it before that cluster counted); nothing in this launch reads it
   // again, and the next launch sees it
   if (arrivals == p.Hkv - 1) {
