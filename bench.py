@@ -6,8 +6,10 @@ workload: the adaptive split, stage-1 SnapKV++ eviction of the prompt
 (rkv_prefill_evict, which also builds the page summaries), then every decode step
 (rkv_decode_step: append the new token + the HSA step, one launch).  Inputs are seeded,
 synthetic and resident in HBM before timing.  L2 is flushed (a 256 MB write)
-before the prefill and before every decode step, outside the timed intervals:
-each timed interval starts with a cold L2, as a layer of a full model would.
+before the prefill, and before every decode step whose compulsory bytes fit in L2,
+outside the timed intervals.  Steps that read more than L2 holds (the batch-16
+workloads) and the multi-layer workload, whose layers stream far more than L2
+between two steps of a layer, run back to back: their inputs are larger than L2.
 
 The metric is decode steps per second per layer over the whole job, prefill time
 included: decode_steps * K / sum(pass time).  Each pass's prefill and decode
@@ -54,6 +56,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-decode-steps", type=int, default=0, help="decode steps per oracle sample (0: all)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="repeat the oracle sample until this much CPU time")
+    ap.add_argument("--flush-steps", choices=["auto", "always"], default="auto",
+                    help="flush L2 before every decode step of a one-layer workload: always, or (auto) only when a "
+                         "step's compulsory bytes fit in L2")
     ap.add_argument("--flush", choices=["write", "clean"], default="write",
                     help="L2 flush before timed intervals: write a 256 MB buffer (default), or write it and then read "
                          "another 256 MB buffer so no dirty line is left for the timed kernel to write back (clean)")
@@ -525,13 +530,21 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * (wl.steps + 1))]
 
-    def one_pass(pre, dec):
+    # Between decode steps L2 is flushed unless a step's compulsory bytes exceed L2 (the
+    # timing rule's other option: inputs larger than L2), or the layers evict it: several
+    # layers stream far more than L2 between two steps of a layer.  A flush before every
+    # step also leaves L2 full of the flush's dirty lines, which the step then writes back.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    step_mb = statistics.mean(setup.decode_bytes(t)["step_total"] for t in range(wl.steps)) / 1e6
+    flush_steps = not multi and (args.flush_steps == "always" or step_mb * 1e6 <= l2_bytes)
+
+    def one_pass(pre, dec, flush_each=flush_steps):
         setup.flush()
         ev[0].record(stream)
         pre.replay()
         ev[1].record(stream)
         for t in range(wl.steps):
-            if not multi:   # one layer: every step starts cold; several: the other layers evict it
+            if flush_each:   # one layer whose steps fit in L2: every step starts cold
                 setup.flush()
             ev[2 + 2 * t].record(stream)
             dec[t].replay()
@@ -617,7 +630,7 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
         ms_per_step=round(statistics.mean(pass_ms), 4), higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="bf16", data="synthetic (seeded normal bf16 with the workload's shapes, outlier channels, sinks and needles)",
         config=workload_config(wl, setup.keep1, setup.k1, setup.k2, setup.kp, args.decode_path, world, nl,
-                               args.mode, args.flush),
+                               args.mode, args.flush, None if flush_steps else (step_mb, l2_bytes / 1e6)),
         prefill_evict_ms=round(pre_layer_ms, 4),
         decode_us_per_step=round(dec_mean_ms * 1e3, 3),
         decode_achieved_gbs=round(step_total / (dec_mean_ms * 1e-3) / 1e9, 1),
@@ -629,6 +642,12 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
         clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"],
                     samples=clocks["samples"]),
     )
+    if not multi and not flush_steps:
+        # the same passes with L2 flushed before every decode step too, for comparison
+        dec_fl = []
+        for _ in range(args.steps):
+            dec_fl += one_pass(g_pre, g_dec, flush_each=True)[1]
+        res["decode_us_per_step_l2_flushed"] = round(statistics.mean(dec_fl) * 1e3, 3)
     if multi:
         res["prefill_all_layers_ms"] = round(statistics.mean(pre_all), 4)
         res["decode_all_layers_us_per_step"] = round(dec_mean_ms * nl * 1e3, 3)
@@ -661,7 +680,7 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
 
 
 def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: int, layers: int = 1,
-                    mode: str = "hsa", flush: str = "write") -> dict:
+                    mode: str = "hsa", flush: str = "write", step_over_l2=None) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
     how = ("256 MB write, then a 256 MB read of another buffer, so no dirty line is left for the timed work "
            "to write back" if flush == "clean" else "256 MB write")
@@ -670,6 +689,11 @@ def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: 
                 f"(append + HSA for each layer in turn); value counts layer-steps")
         l2 = (f"flushed ({how}) before the prefill; not between decode steps: each step streams "
               f"{layers} layers' caches, far more than L2, so every layer starts cold; flush not timed")
+    elif step_over_l2:
+        step = "one request: split + prefill evict + every decode step (append + HSA)"
+        l2 = (f"flushed ({how}) before the prefill; not between decode steps: a step's compulsory bytes "
+              f"({step_over_l2[0]:.1f} MB) exceed L2 ({step_over_l2[1]:.1f} MB), so its inputs are larger than "
+              f"L2; flush not timed (decode_us_per_step_l2_flushed: the same steps with a flush before each)")
     else:
         step = "one request: split + prefill evict + every decode step (append + HSA)"
         l2 = f"flushed ({how}) before the prefill and before every decode step; flush not timed"
@@ -869,6 +893,8 @@ def main():
                                     ms_per_step=w4["ms_per_step"], decode_us_per_step=w4["decode_us_per_step"],
                                     prefill_evict_ms=w4["prefill_evict_ms"],
                                     decode_achieved_gbs=w4["decode_achieved_gbs"], roofline=w4["roofline"],
+                                    l2=w4["config"]["l2"],
+                                    decode_us_per_step_l2_flushed=w4.get("decode_us_per_step_l2_flushed"),
                                     clocks=w4["clocks"], gpu_launches=w4["gpu_launches"])
     if rank == 0 and res:
         print(json.dumps(res))
