@@ -153,7 +153,11 @@ size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t wi
  * 0..keep1-1), their Kmax/Kmin summaries are built and seq_len[b] = keep1[b].
  *   q_win  : device [B][Hq][window][128] bf16, the last `window` queries.
  *   k, v   : device [B][Hkv][max_prompt_len][128] bf16; rows >= prompt_len[b]
- *            are never read.
+ *            are never read.  v may instead be pinned host memory (cudaHostAlloc or
+ *            registered, mapped into the device's address space; 16-byte aligned):
+ *            only the kept rows of V are read, once, through the mapping, so a
+ *            prompt that lives on the host needs only q_win and k copied to the
+ *            device (the kernels read nothing else of v).
  *   prompt_len, keep1, pool_kernel : host [B]; window <= keep1[b] <= prompt_len[b]
  *            <= max_prompt_len; pool_kernel odd in [1, 255]; G * window <= 128.
  *   scale  : softmax scale (1/sqrt(128) for the standard one).

@@ -432,6 +432,39 @@ def test_workload6_mt_batched_sampled(rkv):
     assert _sampled_full(rkv, 6, [(longest, 2), (0, 5)], {0, 255}) <= ATOL_OUT
 
 
+@pytest.mark.parametrize("name", ["gqa4_ragged", "no_eviction"])
+def test_prefill_with_host_v_matches(rkv, name):
+    """rkv_prefill_evict with V in pinned host memory (read through its device mapping)
+    fills the cache exactly as with V on the device; a host K is refused."""
+    wl = SMALL[name]
+    runs = [GpuRun(wl, rkv), GpuRun(wl, rkv)]
+    runs[0].prefill()
+    g = runs[1].gpu_in
+    v_host = runs[1].inputs["v"].contiguous().pin_memory()
+    rkv.rkv_prefill_evict(g["q_win"], g["k"], v_host, g["prompt_len"], runs[1].keep1, runs[1].kp, runs[1].cache,
+                          runs[1].kept, pooled_scores=runs[1].pooled)
+    torch.cuda.synchronize()
+    a, b = runs[0].cache, runs[1].cache
+    assert torch.equal(runs[0].kept, runs[1].kept)
+    assert torch.equal(a.seq_len, b.seq_len)
+    for x, y in ((a.kmax, b.kmax), (a.kmin, b.kmin)):
+        assert torch.equal(x.nan_to_num(), y.nan_to_num())
+    # every page a sequence uses holds the same K and V rows
+    for bb in range(wl.B):
+        n = int(a.seq_len[bb])
+        for pg in range((n + wl.page_size - 1) // wl.page_size):
+            phys = int(a.page_table[bb, pg])
+            cnt = min(wl.page_size, n - pg * wl.page_size)
+            assert torch.equal(a.k_pages[phys, :, :cnt], b.k_pages[phys, :, :cnt])
+            assert torch.equal(a.v_pages[phys, :, :cnt], b.v_pages[phys, :, :cnt])
+    k_host = runs[1].inputs["k"].contiguous().pin_memory()
+    with pytest.raises(rkv.RkvError):
+        rkv.rkv_prefill_evict(g["q_win"], k_host, v_host, g["prompt_len"], runs[1].keep1, runs[1].kp,
+                              runs[1].cache, runs[1].kept)
+    for r in runs:
+        assert r.status()[0] == rkv.RKV_OK
+
+
 def test_decode_step_from_host_buffers_matches(rkv):
     """rkv_decode_step_host (host inputs and output) computes what rkv_decode_step does."""
     wl = SMALL["gqa4_ragged"]

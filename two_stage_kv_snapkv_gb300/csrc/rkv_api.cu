@@ -261,6 +261,27 @@ size_t rkv_prefill_workspace_size(int32_t B, int32_t Hq, int32_t Hkv, int32_t wi
   return rkv::prefill_ws_bytes(B, Hq, Hkv, window, max_prompt_len);
 }
 
+// Device address of pinned host memory mapped into the device's address space, else null.
+// True when p is known to be host memory (pinned or not); false for device or managed
+// memory, and when the query itself fails (then the launch reports any fault).
+static bool host_side(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
+static const void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // unregistered memory: clear the sticky query error
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv_bf16* v, int32_t B, int32_t Hq,
                              int32_t window, int32_t max_prompt_len, const int32_t* prompt_len, const int32_t* keep1,
                              const int32_t* pool_kernel, float scale, const rkv_cache* cache, int32_t* kept_idx,
@@ -298,7 +319,13 @@ rkv_status rkv_prefill_evict(const rkv_bf16* q_win, const rkv_bf16* k, const rkv
   rkv::PrefillArgs a;
   a.q_win = q_win;
   a.k = k;
-  a.v = v;
+  // pinned host V: the compaction reads the kept rows through the device mapping.  q_win
+  // and k are read by the tensor engine and must be device memory.
+  if (host_side(q_win) || host_side(k)) return fail(RKV_ERR_INVALID_ARG, "q_win and k must be device memory");
+  const void* vmap = mapped_host(v);
+  if (!vmap && host_side(v)) return fail(RKV_ERR_INVALID_ARG, "v is host memory that is not pinned and mapped");
+  a.v = vmap ? static_cast<const rkv_bf16*>(vmap) : v;
+  if (!al16(a.v)) return fail(RKV_ERR_INVALID_ARG, "v's device mapping must be 16-byte aligned");
   a.B = B;
   a.Hq = Hq;
   a.Hkv = cache->Hkv;
@@ -532,15 +559,6 @@ rkv_status rkv_decode_sparq(const rkv_cache* cache, const rkv_bf16* q, int32_t H
   return cuda_status(rkv::launch_sparq(a, static_cast<cudaStream_t>(stream)), "rkv_decode_sparq launch");
 }
 
-// Device address of pinned host memory mapped into the device's address space, else null.
-static const void* mapped_host(const void* p) {
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-    cudaGetLastError();  // unregistered memory: clear the sticky query error
-    return nullptr;
-  }
-  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
-}
 
 size_t rkv_step_host_staging_size(int32_t B, int32_t Hq, int32_t Hkv) {
   if (B < 1 || Hq < 1 || Hkv < 1) return 0;
