@@ -12,9 +12,10 @@ workloads) and the multi-layer workload, whose layers stream far more than L2
 between two steps of a layer, run back to back: their inputs are larger than L2.
 
 The metric is decode steps per second per layer over the whole job, prefill time
-included: decode_steps * K / sum(pass time).  Each pass's prefill and decode
-steps run as CUDA graphs (one per decode step) timed with CUDA events on the
-launching stream.
+included: decode_steps * K / sum(pass time).  Each pass's prefill runs as a CUDA
+graph; its decode steps run as one graph (the decode loop) where they run back to
+back, else one graph a step with the L2 flush between them.  CUDA events on the
+launching stream time each graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2]
     python bench.py --impl reference     # the CPU oracle, timed on this host
@@ -538,11 +539,24 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
     step_mb = statistics.mean(setup.decode_bytes(t)["step_total"] for t in range(wl.steps)) / 1e6
     flush_steps = not multi and (args.flush_steps == "always" or step_mb * 1e6 <= l2_bytes)
 
-    def one_pass(pre, dec, flush_each=flush_steps):
+    # Steps that run back to back also run as one graph, the decode loop: every step of
+    # every layer, each launch chained to the one before by programmatic launch, as a
+    # serving engine replays its decode graphs.  One graph a step instead adds a graph
+    # launch (a few us) to every step of a single-layer workload.
+    g_loop = None if flush_steps else capture(lambda: [decode_all(t) for t in range(wl.steps)], stream)
+
+    def one_pass(pre, dec, flush_each=flush_steps, loop=None):
         setup.flush()
         ev[0].record(stream)
         pre.replay()
         ev[1].record(stream)
+        if loop is not None:
+            ev[2].record(stream)
+            loop.replay()
+            ev[3].record(stream)
+            stream.synchronize()
+            per = ev[2].elapsed_time(ev[3]) / wl.steps
+            return ev[0].elapsed_time(ev[1]), [per] * wl.steps
         for t in range(wl.steps):
             if flush_each:   # one layer whose steps fit in L2: every step starts cold
                 setup.flush()
@@ -555,14 +569,14 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
         return pre_ms, dec_ms
 
     for _ in range(args.warmup):
-        one_pass(g_pre, g_dec)
+        one_pass(g_pre, g_dec, loop=g_loop)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     pre_all, dec_all = [], []
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         for _ in range(args.steps):
-            p, d = one_pass(g_pre, g_dec)
+            p, d = one_pass(g_pre, g_dec, loop=g_loop)
             pre_all.append(p)
             dec_all.append(d)
         torch.cuda.synchronize()
@@ -599,15 +613,15 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
         kernels[k] = dict(launches=n, avg_us=round(avg_ms * 1e3, 3), share=round(ms / sum(v[1] for v in prof.values()), 4),
                           algo_bytes=ab, achieved_gbs=(round(ab / (avg_ms * 1e-3) / 1e9, 1) if ab else None))
     dec_mean_ms = statistics.mean(x for d in dec_all for x in d) / nl   # one layer's decode step
-    if multi and launches_per_step == nl and "hsa_step" in kernels:
-        # the decode graphs hold only hsa_step launches, back to back: their event time
+    if g_loop is not None and launches_per_step == nl and "hsa_step" in kernels:
+        # the decode loop holds only hsa_step launches, back to back: its event time
         # divided by the launches is the kernel's own average duration, which the event
         # nodes of the instrumented copy (one per launch) would serialise and inflate
         hk = kernels["hsa_step"]
         hk["avg_us_instrumented"] = hk["avg_us"]
         hk["avg_us"] = round(dec_mean_ms * 1e3, 3)
         hk["achieved_gbs"] = round(hk["algo_bytes"] / (dec_mean_ms * 1e-3) / 1e9, 1)
-        hk["duration_from"] = "uninstrumented decode graphs: event time / hsa_step launches"
+        hk["duration_from"] = "uninstrumented decode loop graph: event time / hsa_step launches"
     dominant = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches"])
     dk = kernels[dominant]
     traffic = None
@@ -642,8 +656,14 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
         clocks=dict(sm_mhz=clocks["sm_mhz"], sm_max_mhz=clocks["sm_max_mhz"], reasons=clocks["reasons"],
                     samples=clocks["samples"]),
     )
+    if g_loop is not None:
+        # the same steps as one graph each (a graph launch before every step), and for a
+        # single layer with L2 flushed before every step too, for comparison
+        dec_g = []
+        for _ in range(args.steps):
+            dec_g += one_pass(g_pre, g_dec, flush_each=False)[1]
+        res["decode_us_per_step_graph_per_step"] = round(statistics.mean(dec_g) * 1e3 / nl, 3)
     if not multi and not flush_steps:
-        # the same passes with L2 flushed before every decode step too, for comparison
         dec_fl = []
         for _ in range(args.steps):
             dec_fl += one_pass(g_pre, g_dec, flush_each=True)[1]
@@ -702,7 +722,11 @@ def workload_config(wl: W.Workload, keep1, k1, k2, kp, decode_path: str, world: 
                 window=wl.window, page_size=wl.page_size, decode_steps=wl.steps, layers=layers,
                 keep1=self_or_range(keep1), k1=self_or_range(k1), k2=self_or_range(k2),
                 pool_kernel=self_or_range(kp), split="RocketKV-MT (nothing evicted)" if wl.mt else "two-stage",
-                step=step, l2=l2, timing="CUDA graphs per prefill / decode step, CUDA events on the launching stream",
+                step=step, l2=l2, timing=("CUDA graphs: the prefill, then the decode loop (every step of every layer, "
+                                          "launches chained by programmatic launch); CUDA events on the launching "
+                                          "stream around each" if step_over_l2 or layers > 1 else
+                                          "CUDA graphs: the prefill, then one per decode step (L2 flushed between "
+                                          "them); CUDA events on the launching stream around each"),
                 decode_path=decode_path, parallelism=f"replica x{world}" if world > 1 else "single GPU",
                 mode={"hsa": "HSA", "quest": "Quest-only (HSA, k1 = every channel)",
                       "sparq": "SparQ-only (one-token pages, k2 x P tokens)"}[mode])
