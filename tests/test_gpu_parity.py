@@ -235,6 +235,59 @@ def test_deterministic(rkv, path):
         assert torch.equal(a.nan_to_num(), b.nan_to_num())
 
 
+def test_decode_loop_graph_matches_eager(rkv, path):
+    """Every decode step of two layers captured as one CUDA graph (as the bench replays
+    the decode loop; the fused steps chained by programmatic launch, each step of a
+    layer reading the cache the previous one appended to) gives the eager results bit
+    for bit: outputs, selections and the cache with its summaries."""
+    wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=12,
+                  pool_kernel=5)
+
+    def setup():
+        runs = [GpuRun(wl, rkv, layer=layer) for layer in range(2)]
+        for r in runs:
+            r.prefill()
+        ins = [[W.decode_tensors(wl, t, r.seed, r.layer, r.dev) for t in range(wl.steps)] for r in runs]
+        outs = [[(torch.full((wl.B, wl.Hq, 128), float("nan"), dtype=torch.float32, device=r.dev),
+                  torch.full((wl.B, wl.Hkv, 128), -9, dtype=torch.int32, device=r.dev),
+                  torch.full((wl.B, wl.Hkv, max(r.k2) + 1), -9, dtype=torch.int32, device=r.dev))
+                 for _ in range(wl.steps)] for r in runs]
+        torch.cuda.synchronize()
+        return runs, ins, outs
+
+    def loop(runs, ins, outs):
+        for t in range(wl.steps):
+            for r, i, o in zip(runs, ins, outs):
+                d = i[t]
+                rkv.rkv_decode_step(r.cache, d["q"], d["k_new"], d["v_new"], r.k1, r.k2, o[t][0],
+                                    sel_channels=o[t][1], sel_pages=o[t][2], workspace=r.dws)
+
+    eager = setup()
+    loop(*eager)
+    torch.cuda.synchronize()
+
+    graph = setup()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        loop(*graph)
+    g.replay()
+    torch.cuda.synchronize()
+
+    def bits(t):   # bitwise view: NaN fills compare equal to themselves
+        return t.view({torch.bfloat16: torch.int16, torch.float32: torch.int32}.get(t.dtype, t.dtype))
+
+    for re, rg in zip(eager[0], graph[0]):
+        assert re.status()[0] == rkv.RKV_OK and rg.status()[0] == rkv.RKV_OK
+        for name in ("k_pages", "v_pages", "kmax", "kmin", "seq_len"):
+            assert torch.equal(bits(getattr(re.cache, name)), bits(getattr(rg.cache, name))), name
+    for oe, og in zip(eager[2], graph[2]):
+        for t, (te, tg) in enumerate(zip(oe, og)):
+            for a, b in zip(te, tg):
+                assert torch.equal(bits(a), bits(b)), t
+
+
 def test_bad_page_id_is_flagged_not_faulted(rkv, path):
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
     run = GpuRun(wl, rkv)

@@ -265,11 +265,12 @@ __device__ __forceinline__ void flag_error(int32_t* word, int32_t bit) {
 // called several times for each i in [0, n); every thread of the block calls this.
 constexpr int kTkBins = 1024;
 constexpr int kTkCand = 32;
+constexpr int kTkCandFlat = 64;  // the candidate cap of topk_flat (two ranking warps)
 template <int NT, int NBINS = kTkBins>
 struct TopkSmem {
   alignas(16) uint32_t hist[NBINS];
-  int cand[kTkCand];
-  uint32_t ckey[kTkCand];
+  alignas(16) int cand[kTkCandFlat];
+  alignas(16) uint32_t ckey[kTkCandFlat];
   uint32_t wlo[NT / 32], whi[NT / 32];
   int wa[NT / 32], wb[NT / 32];
   int ncand, bstar, need, nb, tidx;
@@ -473,392 +474,6 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
   });
 }
 
-// The same select with every thread's keys held in registers: thread t owns keys
-// [t KPT, t KPT + KPT) of a shared-memory array (read once, by 16-byte loads when KPT
-// is a multiple of 4), so each pass is an unrolled loop over registers instead of a
-// chain of shared-memory loads; the candidates are ranked by warp 0 with shuffles.
-// Needs n <= NT * KPT, `keys` 16-byte aligned and readable up to NT * KPT entries
-// (entries from n on are ignored).  Every thread of the block calls this.
-template <int NT, int KPT, int NBINS = kTkBins>
-__device__ void topk_regs(const uint32_t* keys, int n, int k, TopkSmem<NT, NBINS>& ts, int32_t* out) {
-  static_assert(NT % 32 == 0 && NBINS % NT == 0 && (NBINS / NT) % 4 == 0, "bins must split into uint4s");
-  static_assert((NBINS & (NBINS - 1)) == 0 && NBINS >= 1024, "a power of two of at least 1024 bins");
-  constexpr unsigned FULL = 0xffffffffu;
-  constexpr int NW = NT / 32;
-  constexpr int BPT = NBINS / NT;
-  constexpr int LOG_BINS = NBINS == 1024 ? 10 : (NBINS == 2048 ? 11 : (NBINS == 4096 ? 12 : 13));
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i0 = tid * KPT;
-  uint32_t kv[KPT];
-  if (i0 < n) {
-    if constexpr (KPT % 4 == 0) {
-#pragma unroll
-      for (int j = 0; j < KPT; j += 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(keys + i0 + j);
-        kv[j] = v.x;
-        kv[j + 1] = v.y;
-        kv[j + 2] = v.z;
-        kv[j + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) kv[j] = keys[i0 + j];
-    }
-  }
-  const int nv = max(0, min(KPT, n - i0));  // valid keys of this thread: kv[0 .. nv)
-  uint4* h4 = reinterpret_cast<uint4*>(ts.hist);
-  for (int j = tid; j < NBINS / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) ts.ncand = 0;
-
-  // 1. the key range
-  uint32_t lo = 0xffffffffu, hi = 0u;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j)
-    if (j < nv) {
-      lo = min(lo, kv[j]);
-      hi = max(hi, kv[j]);
-    }
-  lo = __reduce_min_sync(FULL, lo);
-  hi = __reduce_max_sync(FULL, hi);
-  if (lane == 0) {
-    ts.wlo[warp] = lo;
-    ts.whi[warp] = hi;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    lo = min(lo, ts.wlo[w]);
-    hi = max(hi, ts.whi[w]);
-  }
-
-  // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
-  int need = k, nin = n;
-  bool cleared = true;
-  while (nin > kTkCand && lo != hi) {
-    if (!cleared) {
-      for (int j = tid; j < NBINS / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
-      __syncthreads();
-    }
-    cleared = false;
-    const uint32_t range = hi - lo;
-    const int shift = range < (uint32_t)NBINS ? 0 : (32 - __clz(range)) - LOG_BINS;
-    int run_bin = -1, run = 0;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const uint32_t u = kv[j];
-      const int bin = (j < nv && u >= lo && u <= hi) ? (int)((u - lo) >> shift) : -1;
-      if (bin != run_bin) {
-        if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
-        run_bin = bin;
-        run = 0;
-      }
-      ++run;
-    }
-    if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
-    __syncthreads();
-    uint32_t c[BPT];
-#pragma unroll
-    for (int j = 0; j < BPT; j += 4) {
-      const uint4 v = h4[(tid * BPT + j) >> 2];
-      c[j] = v.x;
-      c[j + 1] = v.y;
-      c[j + 2] = v.z;
-      c[j + 3] = v.w;
-    }
-    int sum = 0;
-#pragma unroll
-    for (int j = 0; j < BPT; ++j) sum += (int)c[j];
-    int incl = sum;  // over the lanes >= this one
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_down_sync(FULL, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    if (lane == 0) ts.wa[warp] = incl;
-    __syncthreads();
-    int above = incl - sum;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-      if (w > warp) above += ts.wa[w];
-    if (above < need && above + sum >= need) {
-      int acc = above;
-#pragma unroll
-      for (int j = BPT - 1; j >= 0; --j) {
-        if (acc + (int)c[j] >= need) {
-          ts.bstar = tid * BPT + j;
-          ts.need = need - acc;
-          ts.nb = (int)c[j];
-          break;
-        }
-        acc += (int)c[j];
-      }
-    }
-    __syncthreads();
-    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
-    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
-    lo = nlo;
-    need = ts.need;
-    nin = ts.nb;
-  }
-
-  // 3. the boundary pair (T, t): candidates gathered by one atomic per thread that has
-  // any, ranked by warp 0 (lane l holds candidate l) with shuffles
-  const bool all_in = need == nin;                // every key in [lo, hi] is taken
-  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
-  if (!by_index && !all_in) {
-    int cnt = 0;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) cnt += j < nv && kv[j] >= lo && kv[j] <= hi;
-    if (cnt > 0) {
-      int slot = atomicAdd(&ts.ncand, cnt);
-#pragma unroll
-      for (int j = 0; j < KPT; ++j)
-        if (j < nv && kv[j] >= lo && kv[j] <= hi) {
-          if (slot < kTkCand) {
-            ts.cand[slot] = i0 + j;
-            ts.ckey[slot] = kv[j];
-          }
-          ++slot;
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int nc = min(ts.ncand, kTkCand);
-      const int ci = lane < nc ? ts.cand[lane] : 0;
-      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
-      int r = 0;
-#pragma unroll 4  // runs once per select: a short body fetches fewer cold instructions
-      for (int m = 0; m < 32; ++m) {
-        const uint32_t a = __shfl_sync(FULL, cu, m);
-        const int cm = __shfl_sync(FULL, ci, m);
-        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
-      }
-      if (lane < nc && r == need - 1) {
-        ts.tkey = cu;
-        ts.tidx = ci;
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
-  const int tI = (by_index || all_in) ? n : ts.tidx;  // all_in: every key >= lo is taken
-
-  // 4. ascending compaction: 0 not taken, 1 taken, 2 a boundary key taken by index
-  int pk[KPT];
-  int c1 = 0, c2 = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const uint32_t u = kv[j];
-    int t = 0;
-    if (j < nv) {
-      if (u > hi) t = 1;
-      else if (u >= lo) t = by_index ? 2 : ((u > T || (u == T && i0 + j <= tI)) ? 1 : 0);
-    }
-    pk[j] = t;
-    c1 += t == 1;
-    c2 += t == 2;
-  }
-  int x1 = c1, x2 = c2;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y1 = __shfl_up_sync(FULL, x1, o), y2 = __shfl_up_sync(FULL, x2, o);
-    if (lane >= o) {
-      x1 += y1;
-      x2 += y2;
-    }
-  }
-  if (lane == 31) {
-    ts.wa[warp] = x1;
-    ts.wb[warp] = x2;
-  }
-  __syncthreads();
-  int base = x1 - c1, bseen = x2 - c2;
-#pragma unroll
-  for (int w = 0; w < NW; ++w)
-    if (w < warp) {
-      base += ts.wa[w];
-      bseen += ts.wb[w];
-    }
-  int o = base + min(need, bseen);
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const int t = pk[j];
-    if (t == 1 || (t == 2 && bseen < need)) {
-      if (o < k) out[o] = i0 + j;
-      ++o;
-    }
-    bseen += t == 2;
-  }
-  __syncthreads();  // the scratch may be reused right after
-}
-
-// The same selection computed by every warp on its own, with warp primitives only:
-// lane l reads keys l, l + 32, l + 64, ... (one coalesced 128-byte row per round), so a
-// warp sweeps all n keys per pass with no block barrier between the passes.  Each
-// warp finds the key range, builds its private 1024-bin histogram over it (refining
-// while the boundary bin holds more than kTkCand keys), ranks the boundary bin's keys
-// and derives the same boundary (T, t); the ascending list is written by ballots in
-// index order, warp w storing the rounds r with r % NW == w.  One block barrier at
-// the end publishes the list.  For 1 <= k < n; every thread of the block calls this.
-struct TopkWarpSmem {
-  alignas(16) uint32_t hist[kTkBins];
-  uint32_t ckey[kTkCand];
-  int cidx[kTkCand];
-};
-
-template <int NT>
-__device__ void topk_warp(const uint32_t* keys, int n, int k, TopkWarpSmem* wsm, int32_t* out) {
-  constexpr unsigned FULL = 0xffffffffu;
-  constexpr int NW = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt = (1u << lane) - 1u;
-  TopkWarpSmem& ws = wsm[warp];
-  const int R = (n + 31) >> 5;  // rounds of 32 keys
-  auto key_at = [&](int r) -> uint32_t {
-    const int i = r * 32 + lane;
-    return i < n ? keys[i] : 0u;
-  };
-
-  // 1. key range
-  uint32_t lo = 0xffffffffu, hi = 0u;
-#pragma unroll 4
-  for (int r = 0; r < R; ++r) {
-    if (r * 32 + lane < n) {
-      const uint32_t u = keys[r * 32 + lane];
-      lo = min(lo, u);
-      hi = max(hi, u);
-    }
-  }
-  lo = __reduce_min_sync(FULL, lo);
-  hi = __reduce_max_sync(FULL, hi);
-
-  // 2. shrink [lo, hi] to the bin holding the k-th key; `need` of its `nin` keys are taken
-  int need = k, nin = n;
-  while (nin > kTkCand && lo != hi) {
-    const uint32_t range = hi - lo;
-    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
-    uint4* h4 = reinterpret_cast<uint4*>(ws.hist);
-#pragma unroll
-    for (int j = 0; j < kTkBins / 128; ++j) h4[lane + 32 * j] = make_uint4(0, 0, 0, 0);
-    __syncwarp();
-#pragma unroll 4
-    for (int r = 0; r < R; ++r) {
-      const uint32_t u = key_at(r);
-      if (r * 32 + lane < n && u >= lo && u <= hi) atomicAdd(&ws.hist[(u - lo) >> shift], 1u);
-    }
-    __syncwarp();
-    // lane l holds bins [32 l, 32 l + 32)
-    uint32_t c[32];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint4 v = h4[lane * 8 + j];
-      c[4 * j] = v.x;
-      c[4 * j + 1] = v.y;
-      c[4 * j + 2] = v.z;
-      c[4 * j + 3] = v.w;
-    }
-    int sum = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) sum += (int)c[j];
-    int incl = sum;  // keys in this lane's bins and every higher lane's
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_down_sync(FULL, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    const int above = incl - sum;
-    int bstar = 0, nneed = 0, nb = 0;
-    const bool mine = above < need && above + sum >= need;
-    if (mine) {
-      int acc = above;
-#pragma unroll
-      for (int j = 31; j >= 0; --j) {
-        if (acc + (int)c[j] >= need && nb == 0) {
-          bstar = lane * 32 + j;
-          nneed = need - acc;
-          nb = (int)c[j];
-        }
-        acc += (int)c[j];
-      }
-    }
-    const int src = __ffs(__ballot_sync(FULL, mine)) - 1;
-    bstar = __shfl_sync(FULL, bstar, src);
-    nneed = __shfl_sync(FULL, nneed, src);
-    nb = __shfl_sync(FULL, nb, src);
-    const uint32_t nlo = lo + ((uint32_t)bstar << shift);
-    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
-    lo = nlo;
-    need = nneed;
-    nin = nb;
-    __syncwarp();  // the histogram is read before the next round clears it
-  }
-
-  // 3. boundary pair (T, t) among at most kTkCand keys of [lo, hi]
-  const bool all_in = need == nin;                // every key in [lo, hi] is taken
-  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi: the first `need` by index
-  uint32_t T = lo;
-  int tI = n;
-  if (!all_in && !by_index) {
-    int cnt = 0;
-#pragma unroll 4
-    for (int r = 0; r < R; ++r) {
-      const uint32_t u = key_at(r);
-      const bool f = r * 32 + lane < n && u >= lo && u <= hi;
-      const unsigned m = __ballot_sync(FULL, f);
-      if (f) {
-        const int slot = cnt + __popc(m & lt);
-        ws.ckey[slot] = u;
-        ws.cidx[slot] = r * 32 + lane;
-      }
-      cnt += __popc(m);
-    }
-    __syncwarp();
-    const uint32_t cu = lane < nin ? ws.ckey[lane] : 0u;
-    const int ci = lane < nin ? ws.cidx[lane] : 0;
-    int rank = 0;
-#pragma unroll 8
-    for (int m = 0; m < kTkCand; ++m) {
-      if (m < nin) {
-        const uint32_t a = ws.ckey[m];
-        const int am = ws.cidx[m];
-        rank += (a > cu) | ((a == cu) & (am < ci));
-      }
-    }
-    const bool is_t = lane < nin && rank == need - 1;
-    const int tl = __ffs(__ballot_sync(FULL, is_t)) - 1;
-    T = __shfl_sync(FULL, cu, tl);
-    tI = __shfl_sync(FULL, ci, tl);
-  }
-
-  // 4. ascending list: rounds in index order, a ballot per round
-  int base = 0, eq_seen = 0;
-#pragma unroll 2
-  for (int r = 0; r < R; ++r) {
-    const int i = r * 32 + lane;
-    const uint32_t u = key_at(r);
-    bool f = false, eq = false;
-    if (i < n) {
-      if (u > hi) f = true;
-      else if (u >= lo) {
-        if (by_index) eq = true;
-        else f = u > T || (u == T && i <= tI);
-      }
-    }
-    if (by_index) {  // the first `need` keys equal to lo, by index
-      const unsigned me = __ballot_sync(FULL, eq);
-      f = f || (eq && eq_seen + __popc(me & lt) < need);
-      eq_seen += __popc(me);
-    }
-    const unsigned m = __ballot_sync(FULL, f);
-    if (f && (r % NW) == warp) {
-      const int pos = base + __popc(m & lt);
-      if (pos < k) out[pos] = i;
-    }
-    base += __popc(m);
-  }
-  __syncthreads();  // the list is complete and every warp's scratch is free
-}
-
 // The same selection written without divergent branches in its per-key work: on this
 // GPU a data-dependent branch inside an unrolled per-key loop costs on the order of
 // a hundred cycles (measured: the compaction's two passes took 4,800 cycles with
@@ -866,7 +481,7 @@ __device__ void topk_warp(const uint32_t* keys, int n, int k, TopkWarpSmem* wsm,
 // Thread t owns the contiguous keys [t S, t S + S), S a multiple of 4 (16-byte loads,
 // index-ordered compaction by one block scan); every thread runs the same trip counts.
 // Boundary candidates are gathered by a block scan instead of shared atomics.  Needs
-// n <= NT * S with `keys` 16-byte aligned and readable up to NT * S entries (entries
+// n < 65536, n <= NT * S with `keys` 16-byte aligned and readable up to NT * S entries (entries
 // from n on are ignored).  For 1 <= k < n; every thread of the block calls this.
 template <int NT>
 __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
@@ -937,7 +552,7 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
   int need = k, nin = n;
   bool cleared = true;
-  while (nin > kTkCand && lo != hi) {
+  while (nin > kTkCandFlat && lo != hi) {
     if (!cleared) {
       for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
       __syncthreads();
@@ -1002,10 +617,11 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
     // the next round's first barrier orders these reads before the next writes
   }
 
-  // 3. the boundary pair (T, t) among at most kTkCand candidates, gathered in index
-  // order by a block scan and ranked by warp 0
-  const bool all_in = need == nin;                // every key in [lo, hi] is taken
-  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
+  // 3. the boundary pair (T, t) among at most kTkCandFlat candidates, gathered in
+  // index order by a block scan and ranked by warps 0 and 1 (one candidate a lane,
+  // compared with the others four at a time, over the gathered ones only)
+  const bool all_in = need == nin;                    // every key in [lo, hi] is taken
+  const bool by_index = !all_in && nin > kTkCandFlat;  // then lo == hi
   if (!by_index && !all_in) {
     int cnt = 0;
 #pragma unroll 1
@@ -1027,7 +643,7 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
       for (int e = 0; e < 4; ++e) {
         const uint32_t u = u4[e];
         const bool f = (i0 + 4 * q + e < n) & (u >= lo) & (u <= hi);
-        if (f & (slot < kTkCand)) {
+        if (f & (slot < kTkCandFlat)) {
           ts.cand[slot] = i0 + 4 * q + e;
           ts.ckey[slot] = u;
         }
@@ -1035,18 +651,26 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
       }
     }
     __syncthreads();
-    if (warp == 0) {
-      const int nc = min(nin, kTkCand);
-      const int ci = lane < nc ? ts.cand[lane] : 0;
-      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
+    static_assert(kTkCandFlat <= NT && kTkCandFlat % 32 == 0, "one candidate a lane");
+    if (warp < kTkCandFlat / 32) {
+      const int nc = nin;  // <= kTkCandFlat here
+      const int me = warp * 32 + lane;
+      const int ci = me < nc ? ts.cand[me] : 0;
+      const uint32_t cu = me < nc ? ts.ckey[me] : 0u;
+      const uint4* a4 = reinterpret_cast<const uint4*>(ts.ckey);
+      const int4* c4 = reinterpret_cast<const int4*>(ts.cand);
       int r = 0;
-#pragma unroll 8
-      for (int m = 0; m < kTkCand; ++m) {
-        const uint32_t a = ts.ckey[m];
-        const int cm = ts.cand[m];
-        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
+#pragma unroll 1
+      for (int m4 = 0; m4 < (nc + 3) >> 2; ++m4) {  // entries from nc on are ignored
+        const uint4 a = a4[m4];
+        const int4 c = c4[m4];
+        const int m = 4 * m4;
+        r += (m < nc) & ((a.x > cu) | ((a.x == cu) & (c.x < ci)));
+        r += (m + 1 < nc) & ((a.y > cu) | ((a.y == cu) & (c.y < ci)));
+        r += (m + 2 < nc) & ((a.z > cu) | ((a.z == cu) & (c.z < ci)));
+        r += (m + 3 < nc) & ((a.w > cu) | ((a.w == cu) & (c.w < ci)));
       }
-      if ((lane < nc) & (r == need - 1)) {
+      if ((me < nc) & (r == need - 1)) {
         ts.tkey = cu;
         ts.tidx = ci;
       }
@@ -1075,9 +699,11 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
     c1 += (int)((a & 1u) + (b & 1u) + (c & 1u) + (d & 1u));
     c2 += (int)((a >> 1) + (b >> 1) + (c >> 1) + (d >> 1));
   }
-  int tot1, tot2;
-  const int base = block_scan(c1, 1, tot1);
-  int bseen = block_scan(c2, 0, tot2);
+  // both prefixes in one scan, one count in each 16-bit half (every count is <= n < 2^16)
+  int tot;
+  const int both = block_scan(c1 | (c2 << 16), 1, tot);
+  const int base = both & 0xffff;
+  int bseen = both >> 16;
   int o = base + min(need, bseen);
 #pragma unroll 1
   for (int q = 0; q < Q; ++q) {
@@ -1163,247 +789,6 @@ __device__ void topk_rank(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
     }
   }
   __syncthreads();  // the list is complete and the scratch may be reused
-}
-
-// The select of topk_regs with the keys left in shared memory, for n beyond a few keys
-// per thread: thread t owns the 4 G consecutive keys from 4 G t (G = ceil(n / 4 NT)
-// groups of four, each read by one 16-byte load), and every pass is a short loop over
-// its groups.  A block runs the select once, so each of its instructions is fetched
-// cold; past four keys a thread, the unrolled passes of topk_regs cost more in
-// instruction fetches than their register-resident keys save.  Needs `keys` 16-byte
-// aligned; reads keys[0, n rounded up to a multiple of 4) only (entries from n on are
-// ignored).  Every thread of the block calls this.
-template <int NT>
-__device__ void topk_loop(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
-  static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
-  constexpr unsigned FULL = 0xffffffffu;
-  constexpr int NW = NT / 32;
-  constexpr int BPT = kTkBins / NT;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = (n + 4 * NT - 1) / (4 * NT);
-  const int i0 = tid * 4 * G;
-  const int nv = max(0, min(4 * G, n - i0));  // valid keys of this thread: i0 .. i0 + nv - 1
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys + i0);
-  // Each pass below walks this thread's valid keys in ascending order: group q (one
-  // 16-byte load), then its members e = 0..3, key offset j = 4 q + e from i0.
-  uint4* h4 = reinterpret_cast<uint4*>(ts.hist);
-  for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) ts.ncand = 0;
-
-  // 1. the key range
-  uint32_t lo = 0xffffffffu, hi = 0u;
-#pragma unroll 1
-  for (int q = 0; 4 * q < nv; ++q) {
-    const uint4 v = k4[q];
-    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (4 * q + e < nv) {
-        lo = min(lo, u4[e]);
-        hi = max(hi, u4[e]);
-      }
-  }
-  lo = __reduce_min_sync(FULL, lo);
-  hi = __reduce_max_sync(FULL, hi);
-  if (lane == 0) {
-    ts.wlo[warp] = lo;
-    ts.whi[warp] = hi;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int w = 0; w < NW; ++w) {
-    lo = min(lo, ts.wlo[w]);
-    hi = max(hi, ts.whi[w]);
-  }
-
-  // 2. shrink [lo, hi]; `need` of the `nin` keys inside it are taken
-  int need = k, nin = n;
-  bool cleared = true;
-  while (nin > kTkCand && lo != hi) {
-    if (!cleared) {
-      for (int j = tid; j < kTkBins / 4; j += NT) h4[j] = make_uint4(0, 0, 0, 0);
-      __syncthreads();
-    }
-    cleared = false;
-    const uint32_t range = hi - lo;
-    const int shift = range < (uint32_t)kTkBins ? 0 : (32 - __clz(range)) - 10;
-    int run_bin = -1, run = 0;  // a run of keys in one bin adds to it once
-#pragma unroll 1
-    for (int q = 0; 4 * q < nv; ++q) {
-      const uint4 v = k4[q];
-      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t u = u4[e];
-        const int bin = (4 * q + e < nv && u >= lo && u <= hi) ? (int)((u - lo) >> shift) : -1;
-        if (bin != run_bin) {
-          if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
-          run_bin = bin;
-          run = 0;
-        }
-        ++run;
-      }
-    }
-    if (run_bin >= 0) atomicAdd(&ts.hist[run_bin], (uint32_t)run);
-    __syncthreads();
-    uint32_t c[BPT];
-#pragma unroll
-    for (int j = 0; j < BPT; j += 4) {
-      const uint4 v = h4[(tid * BPT + j) >> 2];
-      c[j] = v.x;
-      c[j + 1] = v.y;
-      c[j + 2] = v.z;
-      c[j + 3] = v.w;
-    }
-    int sum = 0;
-#pragma unroll
-    for (int j = 0; j < BPT; ++j) sum += (int)c[j];
-    int incl = sum;  // over the lanes >= this one
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_down_sync(FULL, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    if (lane == 0) ts.wa[warp] = incl;
-    __syncthreads();
-    int above = incl - sum;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-      if (w > warp) above += ts.wa[w];
-    if (above < need && above + sum >= need) {
-      int acc = above;
-#pragma unroll
-      for (int j = BPT - 1; j >= 0; --j) {
-        if (acc + (int)c[j] >= need) {
-          ts.bstar = tid * BPT + j;
-          ts.need = need - acc;
-          ts.nb = (int)c[j];
-          break;
-        }
-        acc += (int)c[j];
-      }
-    }
-    __syncthreads();
-    const uint32_t nlo = lo + ((uint32_t)ts.bstar << shift);
-    hi = shift == 0 ? nlo : min(hi, nlo + ((1u << shift) - 1u));
-    lo = nlo;
-    need = ts.need;
-    nin = ts.nb;
-  }
-
-  // 3. the boundary pair (T, t), as in topk_regs
-  const bool all_in = need == nin;                // every key in [lo, hi] is taken
-  const bool by_index = !all_in && nin > kTkCand;  // then lo == hi
-  if (!by_index && !all_in) {
-    int cnt = 0;
-#pragma unroll 1
-    for (int q = 0; 4 * q < nv; ++q) {
-      const uint4 v = k4[q];
-      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) cnt += 4 * q + e < nv && u4[e] >= lo && u4[e] <= hi;
-    }
-    if (cnt > 0) {
-      int slot = atomicAdd(&ts.ncand, cnt);
-#pragma unroll 1
-      for (int q = 0; 4 * q < nv; ++q) {
-        const uint4 v = k4[q];
-        const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (4 * q + e < nv && u4[e] >= lo && u4[e] <= hi) {
-            if (slot < kTkCand) {
-              ts.cand[slot] = i0 + 4 * q + e;
-              ts.ckey[slot] = u4[e];
-            }
-            ++slot;
-          }
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int nc = min(ts.ncand, kTkCand);
-      const int ci = lane < nc ? ts.cand[lane] : 0;
-      const uint32_t cu = lane < nc ? ts.ckey[lane] : 0u;
-      int r = 0;
-#pragma unroll 4
-      for (int m = 0; m < 32; ++m) {
-        const uint32_t a = __shfl_sync(FULL, cu, m);
-        const int cm = __shfl_sync(FULL, ci, m);
-        r += (m < nc) & ((a > cu) | ((a == cu) & (cm < ci)));
-      }
-      if (lane < nc && r == need - 1) {
-        ts.tkey = cu;
-        ts.tidx = ci;
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t T = (by_index || all_in) ? lo : ts.tkey;
-  const int tI = (by_index || all_in) ? n : ts.tidx;  // all_in: every key >= lo is taken
-
-  // 4. ascending compaction: 0 not taken, 1 taken, 2 a boundary key taken by index
-  int c1 = 0, c2 = 0;
-#pragma unroll 1
-  for (int q = 0; 4 * q < nv; ++q) {
-    const uint4 v = k4[q];
-    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t u = u4[e];
-      const int i = i0 + 4 * q + e;
-      const int t = 4 * q + e >= nv ? 0
-                    : u > hi        ? 1
-                    : u < lo        ? 0
-                    : by_index      ? 2
-                                    : ((u > T || (u == T && i <= tI)) ? 1 : 0);
-      c1 += t == 1;
-      c2 += t == 2;
-    }
-  }
-  int x1 = c1, x2 = c2;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y1 = __shfl_up_sync(FULL, x1, o), y2 = __shfl_up_sync(FULL, x2, o);
-    if (lane >= o) {
-      x1 += y1;
-      x2 += y2;
-    }
-  }
-  if (lane == 31) {
-    ts.wa[warp] = x1;
-    ts.wb[warp] = x2;
-  }
-  __syncthreads();
-  int base = x1 - c1, bseen = x2 - c2;
-#pragma unroll
-  for (int w = 0; w < NW; ++w)
-    if (w < warp) {
-      base += ts.wa[w];
-      bseen += ts.wb[w];
-    }
-  int o = base + min(need, bseen);
-#pragma unroll 1
-  for (int q = 0; 4 * q < nv; ++q) {
-    const uint4 v = k4[q];
-    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t u = u4[e];
-      const int i = i0 + 4 * q + e;
-      const int t = 4 * q + e >= nv ? 0
-                    : u > hi        ? 1
-                    : u < lo        ? 0
-                    : by_index      ? 2
-                                    : ((u > T || (u == T && i <= tI)) ? 1 : 0);
-      if (t == 1 || (t == 2 && bseen < need)) {
-        if (o < k) out[o] = i;
-        ++o;
-      }
-      bseen += t == 2;
-    }
-  }
-  __syncthreads();  // the scratch may be reused right after
 }
 
 }  // namespace rkv
