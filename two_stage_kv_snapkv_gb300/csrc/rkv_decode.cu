@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // 6. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
   // 128 pages by counting each key's rank, beyond that the histogram select written
   // without divergent per-key branches (on GB300 it took 2.6 us over 1212 keys where
-  // the branchy looping form took 4.3 us, both with warm instruction caches).  The list
+  // a form with per-key branches took 4.3 us, both with warm instruction caches).  The list
   // is ascending.  The scratch lives in the region, free between the scoring and the
   // attention.  (The key array is 16-byte aligned and followed by the list, the
   // page-table row and the inbox, so the select's reads up to 512 entries past NP stay
