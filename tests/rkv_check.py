@@ -62,7 +62,7 @@ class GpuRun:
     """One layer of a workload on the GPU: inputs, cache, prefill, decode steps."""
 
     def __init__(self, wl: W.Workload, rkv, seed: int = 0x5EED, layer: int = 0, gen_device="cpu",
-                 tail="nan", fill=float("nan"), api: str = "step"):
+                 tail="nan", fill=float("nan"), api: str = "step", max_pages_req: int = 0):
         self.wl, self.rkv, self.seed, self.layer = wl, rkv, seed, layer
         self.api = api   # "step": rkv_decode_step; "separate": rkv_append_page_summary + rkv_decode_hsa
         self.dev = torch.device("cuda")
@@ -76,6 +76,8 @@ class GpuRun:
         P = wl.page_size
         max_pages = (max(self.keep1) + wl.steps + P - 1) // P
         max_pages = (max_pages + 7) // 8 * 8
+        if max_pages_req:   # a larger page capacity than the request needs
+            max_pages = max(max_pages, (max_pages_req + 7) // 8 * 8)
         spare = 5
         pt = W.page_table(wl.B, max_pages, seed, self.dev, spare=spare)
         self.cache = rkv.PagedCache(wl.B, wl.Hkv, P, max_pages, self.dev, page_table=pt,

@@ -235,6 +235,27 @@ def test_deterministic(rkv, path):
         assert torch.equal(a.nan_to_num(), b.nan_to_num())
 
 
+def test_long_slices_with_few_pages(rkv, path):
+    """A page capacity of 1024 makes every launch take the long-slice kernel (chosen
+    channels staged after the select, the histogram top-k2) while the sequences hold
+    40-70 pages: short slices and small page counts through that kernel, every unit
+    checked against the oracle at every step."""
+    wl = W.custom(B=4, Hq=8, Hkv=2, prompt_lens=[3000, 2200, 1500, 700], budget=256, window=8, page_size=16,
+                  steps=4, pool_kernel=7)
+    run = GpuRun(wl, rkv, max_pages_req=1024)
+    assert run.cache.max_pages >= 1024
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in units:
+            assert u.step(run, d, out, ch, pg, check_cache=True)["err"] <= ATOL_OUT
+    assert run.status()[0] == rkv.RKV_OK
+    assert max(run.k2) < min((k + wl.steps) // wl.page_size for k in run.keep1)   # a real page selection
+
+
 def test_decode_loop_graph_matches_eager(rkv, path):
     """Every decode step of two layers captured as one CUDA graph (as the bench replays
     the decode loop; the fused steps chained by programmatic launch, each step of a

@@ -536,6 +536,11 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
 
 // ---------------------------------------------------------------------------
 // Fused decode step.  grid (C, B*Hkv), cluster (C, 1, 1), 128 threads.
+// Two instances: kShort for launches whose every slice holds under 64 pages (all
+// channels staged early; top-k2 by counting ranks up to 128 pages, else the histogram
+// select), and the long one (chosen channels staged after the select; the histogram
+// select).  Each holds only its own once-per-CTA code, which runs cold: on GB300 one
+// kernel holding both was 0.2-0.8 us a step slower at 150-1212 pages.
 // Dynamic shared memory (1024-aligned start):
 //   region [region_bytes]: the query, then the staged summaries, then the K/V ring
 //                          (STAGES x 4 warps x 8 KB) and the warp partials;
@@ -565,7 +570,7 @@ __device__ __forceinline__ void summary_fold(rkv_bf16* mx, rkv_bf16* mn, rkv_bf1
                : "memory");
 }
 
-template <int STAGES, class Params>
+template <int STAGES, class Params, bool kShort>
 __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ChanSmem cs;
@@ -648,17 +653,21 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   const bool appender = do_append && rank == 0 && tid < 64;
   const int app_page = n0 / P;
   const size_t app_row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + app_page;
-  // this CTA's slice [p0, p1) of the pages (8-page aligned).  Short slices (under 64
-  // pages) have the summaries of all 128 channels staged right away, in 16-byte
-  // cp.async pieces (Kmax rows 0-127, Kmin rows 128-255), while the query arrives and
-  // the channels are chosen; longer ones stage only the chosen channels' rows, after
-  // the select (on GB300: early all-channel staging saved 0.5 us a step at 26 pages a
-  // slice; at 150-300 pages, waiting for the chosen half saved 0.5-2.9 us).  The
-  // page-table row (needed after the select) comes by bulk copy.
+  // this CTA's slice [p0, p1) of the pages (8-page aligned).  The short instance
+  // (every slice under 64 pages) stages the summaries of all 128 channels right away,
+  // in 16-byte cp.async pieces (Kmax rows 0-127, Kmin rows 128-255), while the query
+  // arrives and the channels are chosen; the long one stages only the chosen
+  // channels' rows, one bulk copy per row, after the select (on GB300: early
+  // all-channel staging saved 0.5 us a step at 26 pages a slice; at 150-300 pages,
+  // waiting for the chosen half saved 0.5-2.9 us).  The page-table row (needed after
+  // the select) comes by bulk copy.
   const int per = ((NP + C - 1) / C + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
   const int slice8 = (p1 - p0 + 7) & ~7;
-  const bool all_ch = p1 > p0 && slice8 < 64 && 2 * 128 * slice8 * 2 <= p.region_bytes;
+  // The short instance is launched only when every CTA's slice qualifies: a slice
+  // never exceeds the one the launch computed from max_pages (the length is clamped to
+  // the capacity above).  The long one never stages all channels.
+  const bool all_ch = kShort && p1 > p0 && slice8 < 64 && 2 * 128 * slice8 * 2 <= p.region_bytes;
   if (all_ch) {
     const int cpr = slice8 >> 3;
     for (int e = tid; e < 256 * cpr; e += kThreads) {
@@ -708,36 +717,25 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     const int cnt = min(tcap, p1 - t0);
     const int cnt8 = (cnt + 7) & ~7;  // t0 + cnt8 <= max_pages since both are multiples of 8
     __syncthreads();  // the previous tile is consumed
-    if (all_ch) {  // the one tile, staged at the start
+    if constexpr (kShort) {  // the one tile, staged at the start
+      if (!all_ch) {  // cannot happen (see the launch); no scores rather than an overrun
+        if (tid == 0) flag_error(p.err, RKV_DEVERR_CAPACITY);
+        break;
+      }
       cp_async_wait<0>();
     } else {
-      if (cnt8 <= 256) {
-        // the chosen channels' rows in 16-byte pieces (one warp instruction moves 512
-        // B; on GB300 0.3-0.6 us a step faster than a bulk copy per row at 150-160 pages)
-        const int cpr = cnt8 >> 3;
-        for (int e = tid; e < 2 * k1 * cpr; e += kThreads) {
-          const int i = e / cpr, c = e - i * cpr;
-          const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
-          const int ch = cs.chan[i < k1 ? i : i - k1];
-          cp_async16(ring + (size_t)i * cnt8 * 2 + c * 16,
-                     base + ((size_t)unit * 128 + ch) * p.max_pages + t0 + c * 8, 16u);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-      } else {
-        // one bulk copy per row (long rows: 0.2 us faster than pieces at 384 pages)
-        fence_proxy_async_smem();
-        if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
-        __syncthreads();
-        for (int i = tid; i < 2 * k1; i += kThreads) {
-          const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
-          const int ch = cs.chan[i < k1 ? i : i - k1];
-          bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0,
-                   (uint32_t)cnt8 * 2, &sbar);
-        }
-        if (!mbar_wait(&sbar, (uint32_t)(stile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
-        ++stile;
+      // the chosen channels' rows, one bulk copy per row
+      fence_proxy_async_smem();
+      if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
+      __syncthreads();
+      for (int i = tid; i < 2 * k1; i += kThreads) {
+        const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
+        const int ch = cs.chan[i < k1 ? i : i - k1];
+        bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0,
+                 (uint32_t)cnt8 * 2, &sbar);
       }
+      if (!mbar_wait(&sbar, (uint32_t)(stile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
+      ++stile;
     }
     __syncthreads();
     if (pnew >= t0 && pnew < t0 + cnt) {
@@ -820,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
         }
       }
     };
-    if (all_ch)
+    if constexpr (kShort)
       score(std::true_type{});
     else
       score_pairs();
@@ -847,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   TopkSmem<kThreads>& tks = *reinterpret_cast<TopkSmem<kThreads>*>(ring);
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
-  } else if (NP <= kThreads) {
+  } else if (kShort && NP <= kThreads) {
     topk_rank<kThreads, 1>(keys, NP, k, tks, sel);
   } else {
     topk_flat<kThreads>(keys, NP, k, tks, sel);
@@ -1386,18 +1384,33 @@ size_t fused_smem_bytes(int region, int max_pages) {
   return 1024 + (size_t)region + 3 * (size_t)max_pages * 4 + (size_t)(8 + kMaxCluster) * 130 * 4;
 }
 
-template <int STAGES, class Params>
+template <int STAGES, class Params, bool kShort>
 int fused_blocks_per_sm(size_t smem) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(hsa_step_kernel<STAGES, Params>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(hsa_step_kernel<STAGES, Params, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         200 * 1024);
     attr = true;
   }
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, hsa_step_kernel<STAGES, Params>, kThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, hsa_step_kernel<STAGES, Params, kShort>, kThreads, smem) !=
       cudaSuccess)
     nb = 0;
   return nb;
+}
+
+// Launch of one instance (its shared-memory attribute set on first use).
+template <int STAGES, class Params, bool kShort>
+cudaError_t launch_step(const cudaLaunchConfig_t& cfg, const Params& p) {
+  fused_blocks_per_sm<STAGES, Params, kShort>(cfg.dynamicSmemBytes);
+  return cudaLaunchKernelEx(&cfg, hsa_step_kernel<STAGES, Params, kShort>, p);
+}
+
+template <class Params>
+cudaError_t launch_step_as(const cudaLaunchConfig_t& cfg, const Params& p, int stages, bool short_slices) {
+  if (stages == 3)
+    return short_slices ? launch_step<3, Params, true>(cfg, p) : launch_step<3, Params, false>(cfg, p);
+  return short_slices ? launch_step<2, Params, true>(cfg, p) : launch_step<2, Params, false>(cfg, p);
 }
 
 // The parameter block with 16-entry k1 / k2 arrays (batches of at most 16).
@@ -1452,7 +1465,8 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
       if (C > 1 && C > by_items) break;
       const int region = region_for(st, C);
       const size_t smem = fused_smem_bytes(region, a.cache.max_pages);
-      const int occ = st == 3 ? fused_blocks_per_sm<3, HsaParams>(smem) : fused_blocks_per_sm<2, HsaParams>(smem);
+      const int occ = st == 3 ? fused_blocks_per_sm<3, HsaParams, false>(smem)
+                              : fused_blocks_per_sm<2, HsaParams, false>(smem);
       if (occ < 1) continue;
       const long ctas = (long)units * C;
       if (C > 1 && ctas > (long)occ * num_sms()) continue;
@@ -1493,21 +1507,16 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  // the short instance when every slice (at most the one computed from max_pages) has
+  // under 64 pages and all 128 channels' summaries of it fit the region
+  const int per_max = ((a.cache.max_pages + best_C - 1) / best_C + 7) & ~7;
+  const bool short_slices = per_max < 64 && 2 * 128 * per_max * 2 <= p.region_bytes;
   cudaError_t e;
   launch_begin(K_HSA_STEP, s);
-  if (a.cache.B <= 16) {
-    const HsaParamsSmall q = small_params(p);
-    if (best_st == 3) {
-      fused_blocks_per_sm<3, HsaParamsSmall>(best_smem);  // sets the shared-memory attribute once
-      e = cudaLaunchKernelEx(&cfg, hsa_step_kernel<3, HsaParamsSmall>, q);
-    } else {
-      fused_blocks_per_sm<2, HsaParamsSmall>(best_smem);
-      e = cudaLaunchKernelEx(&cfg, hsa_step_kernel<2, HsaParamsSmall>, q);
-    }
-  } else {
-    e = best_st == 3 ? cudaLaunchKernelEx(&cfg, hsa_step_kernel<3, HsaParams>, p)
-                     : cudaLaunchKernelEx(&cfg, hsa_step_kernel<2, HsaParams>, p);
-  }
+  if (a.cache.B <= 16)
+    e = launch_step_as(cfg, small_params(p), best_st, short_slices);
+  else
+    e = launch_step_as(cfg, p, best_st, short_slices);
   launch_end(K_HSA_STEP, s);
   return e;
 }
