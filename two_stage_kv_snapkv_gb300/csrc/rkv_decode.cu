@@ -52,6 +52,8 @@ constexpr int kAtWarps = 4;
 constexpr int kThreads = kAtWarps * 32;
 constexpr int kSplitStages = 3;
 constexpr int kFusedStages = 2;
+// instances of the fused step (see hsa_step_kernel)
+constexpr int kStepShortRank = 0, kStepShortFlat = 1, kStepLong = 2;
 constexpr int kChunkTok = 16;                 // tokens per pipeline stage
 constexpr int kHalfBytes = kChunkTok * 128;   // one 16-token x 64-channel box (128-B rows)
 constexpr int kStageBytes = 4 * kHalfBytes;   // K lo, K hi, V lo, V hi
@@ -536,11 +538,12 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
 
 // ---------------------------------------------------------------------------
 // Fused decode step.  grid (C, B*Hkv), cluster (C, 1, 1), 128 threads.
-// Two instances: kShort for launches whose every slice holds under 64 pages (all
-// channels staged early; top-k2 by counting ranks up to 128 pages, else the histogram
-// select), and the long one (chosen channels staged after the select; the histogram
-// select).  Each holds only its own once-per-CTA code, which runs cold: on GB300 one
-// kernel holding both was 0.2-0.8 us a step slower at 150-1212 pages.
+// Three instances (kMode), so that each launch holds only the once-per-CTA code it
+// runs, which is fetched cold (on GB300 one kernel holding every path was 0.3-2.1 us
+// a step slower): for launches whose every slice holds under 64 pages, all channels
+// staged early and the top-k2 by counting ranks (at most 128 pages: kStepShortRank)
+// or by the histogram select (kStepShortFlat); otherwise the chosen channels staged
+// after the select and the histogram select (kStepLong).
 // Dynamic shared memory (1024-aligned start):
 //   region [region_bytes]: the query, then the staged summaries, then the K/V ring
 //                          (STAGES x 4 warps x 8 KB) and the warp partials;
@@ -570,8 +573,9 @@ __device__ __forceinline__ void summary_fold(rkv_bf16* mx, rkv_bf16* mn, rkv_bf1
                : "memory");
 }
 
-template <int STAGES, class Params, bool kShort>
+template <int STAGES, class Params, int kMode>
 __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_constant__ Params p) {
+  constexpr bool kShort = kMode != kStepLong;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ ChanSmem cs;
   __shared__ AttnSmem<STAGES> as;
@@ -845,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   TopkSmem<kThreads>& tks = *reinterpret_cast<TopkSmem<kThreads>*>(ring);
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
-  } else if (kShort && NP <= kThreads) {
+  } else if constexpr (kMode == kStepShortRank) {  // NP <= max_pages <= kThreads
     topk_rank<kThreads, 1>(keys, NP, k, tks, sel);
   } else {
     topk_flat<kThreads>(keys, NP, k, tks, sel);
@@ -1384,33 +1388,38 @@ size_t fused_smem_bytes(int region, int max_pages) {
   return 1024 + (size_t)region + 3 * (size_t)max_pages * 4 + (size_t)(8 + kMaxCluster) * 130 * 4;
 }
 
-template <int STAGES, class Params, bool kShort>
+template <int STAGES, class Params, int kMode>
 int fused_blocks_per_sm(size_t smem) {
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(hsa_step_kernel<STAGES, Params, kShort>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(hsa_step_kernel<STAGES, Params, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          200 * 1024);
     attr = true;
   }
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, hsa_step_kernel<STAGES, Params, kShort>, kThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, hsa_step_kernel<STAGES, Params, kMode>, kThreads, smem) !=
       cudaSuccess)
     nb = 0;
   return nb;
 }
 
 // Launch of one instance (its shared-memory attribute set on first use).
-template <int STAGES, class Params, bool kShort>
+template <int STAGES, class Params, int kMode>
 cudaError_t launch_step(const cudaLaunchConfig_t& cfg, const Params& p) {
-  fused_blocks_per_sm<STAGES, Params, kShort>(cfg.dynamicSmemBytes);
-  return cudaLaunchKernelEx(&cfg, hsa_step_kernel<STAGES, Params, kShort>, p);
+  fused_blocks_per_sm<STAGES, Params, kMode>(cfg.dynamicSmemBytes);
+  return cudaLaunchKernelEx(&cfg, hsa_step_kernel<STAGES, Params, kMode>, p);
+}
+
+template <int STAGES, class Params>
+cudaError_t launch_step_mode(const cudaLaunchConfig_t& cfg, const Params& p, int mode) {
+  if (mode == kStepShortRank) return launch_step<STAGES, Params, kStepShortRank>(cfg, p);
+  if (mode == kStepShortFlat) return launch_step<STAGES, Params, kStepShortFlat>(cfg, p);
+  return launch_step<STAGES, Params, kStepLong>(cfg, p);
 }
 
 template <class Params>
-cudaError_t launch_step_as(const cudaLaunchConfig_t& cfg, const Params& p, int stages, bool short_slices) {
-  if (stages == 3)
-    return short_slices ? launch_step<3, Params, true>(cfg, p) : launch_step<3, Params, false>(cfg, p);
-  return short_slices ? launch_step<2, Params, true>(cfg, p) : launch_step<2, Params, false>(cfg, p);
+cudaError_t launch_step_as(const cudaLaunchConfig_t& cfg, const Params& p, int stages, int mode) {
+  return stages == 3 ? launch_step_mode<3, Params>(cfg, p, mode) : launch_step_mode<2, Params>(cfg, p, mode);
 }
 
 // The parameter block with 16-entry k1 / k2 arrays (batches of at most 16).
@@ -1465,8 +1474,8 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
       if (C > 1 && C > by_items) break;
       const int region = region_for(st, C);
       const size_t smem = fused_smem_bytes(region, a.cache.max_pages);
-      const int occ = st == 3 ? fused_blocks_per_sm<3, HsaParams, false>(smem)
-                              : fused_blocks_per_sm<2, HsaParams, false>(smem);
+      const int occ = st == 3 ? fused_blocks_per_sm<3, HsaParams, kStepLong>(smem)
+                              : fused_blocks_per_sm<2, HsaParams, kStepLong>(smem);
       if (occ < 1) continue;
       const long ctas = (long)units * C;
       if (C > 1 && ctas > (long)occ * num_sms()) continue;
@@ -1507,16 +1516,18 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  // the short instance when every slice (at most the one computed from max_pages) has
-  // under 64 pages and all 128 channels' summaries of it fit the region
+  // a short instance when every slice (at most the one computed from max_pages) has
+  // under 64 pages and all 128 channels' summaries of it fit the region; counting
+  // ranks when no sequence can hold more than 128 pages
   const int per_max = ((a.cache.max_pages + best_C - 1) / best_C + 7) & ~7;
   const bool short_slices = per_max < 64 && 2 * 128 * per_max * 2 <= p.region_bytes;
+  const int mode = !short_slices ? kStepLong : (a.cache.max_pages <= kThreads ? kStepShortRank : kStepShortFlat);
   cudaError_t e;
   launch_begin(K_HSA_STEP, s);
   if (a.cache.B <= 16)
-    e = launch_step_as(cfg, small_params(p), best_st, short_slices);
+    e = launch_step_as(cfg, small_params(p), best_st, mode);
   else
-    e = launch_step_as(cfg, p, best_st, short_slices);
+    e = launch_step_as(cfg, p, best_st, mode);
   launch_end(K_HSA_STEP, s);
   return e;
 }
