@@ -219,6 +219,36 @@ def test_channel_ties_go_to_lower_channels(rkv, path):
     assert run.status()[0] == rkv.RKV_OK
 
 
+def test_channel_scores_beyond_fp32_are_ranked_exactly(rkv, path):
+    """In every channel one query head of a group holds 1.0 and the other 2^-30 (1 + c % 7):
+    the fp32 sums all round to 1.0, so the channels are ranked on their exact (fp64)
+    sums, as the oracle ranks them: the k1 chosen channels are those with the largest
+    c % 7, ties to the lower channel."""
+    wl = W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[700, 900], budget=64, window=8, page_size=16, steps=2,
+                  pool_kernel=5)
+    run = GpuRun(wl, rkv)
+    run.prefill()
+    units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
+    for u in units:
+        u.check_prefill(run)
+    tiny = torch.tensor([2.0 ** -30 * (1 + c % 7) for c in range(128)])
+
+    def split_q(d):
+        q = torch.empty_like(d["q"])
+        q[:, 0::2] = 1.0
+        q[:, 1::2] = tiny.to(q.dtype).to(q.device)
+        d["q"] = q
+
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step, edit=split_q)
+        for u in units:
+            u.step(run, d, out, ch, pg)
+            k1 = run.k1[u.b]
+            want = sorted(sorted(range(128), key=lambda c: (-(c % 7), c))[:k1])
+            np.testing.assert_array_equal(ch[u.b, u.g, :k1].cpu().numpy(), np.array(want))
+    assert run.status()[0] == rkv.RKV_OK
+
+
 def test_deterministic(rkv, path):
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[900, 700], budget=64, window=8, page_size=16, steps=3,
                   pool_kernel=5)
