@@ -49,10 +49,13 @@ constexpr int kSelectSliceMax = 48 * 1024;  // keys a select CTA stages (192 KB 
 
 struct SnapParams {
   CUtensorMap tmk;        // k as [B*Hkv*Lmax rows][128] bf16, 128-row x 64-channel boxes, 128-B swizzle
+  CUtensorMap tmq;        // q_win as [B*Hq*w rows][128] bf16, the same boxes
   const rkv_bf16* q_win;
   const rkv_bf16* k;
   const rkv_bf16* v;
   int B, Hq, Hkv, G, w, R, Lmax, nsplit;
+  int flat;               // the scoring passes' split: 0 per unit (grid nsplit x units), 1 flat (grid N)
+  int flat_ctas;          // N of pass 1 in the flat split (the combine finds each unit's slots from it)
   int item_keys;          // keys per scoring CTA (a multiple of 128)
   int cgroup;             // pages per compaction CTA (1 .. 8)
   float scale_log2;
@@ -75,44 +78,119 @@ struct SnapParams {
   int32_t kp[RKV_MAX_BATCH];
 };
 
-// Byte offset of 16-byte piece `piece` (channels 8*piece .. +7) of row `row` in an
-// operand laid out as TMA writes it: two 128-row x 64-channel boxes (channels 0-63,
-// 64-127) of 128-byte rows, each piece XOR-ed with row % 8.
-__device__ __forceinline__ uint32_t tc_swz(int row, int piece) {
-  return (uint32_t)((piece >> 3) * (kTcOperandBytes / 2) + row * 128 + ((((piece & 7) ^ (row & 7))) << 4));
+// Key tiles of sequence b in a pass (pass 1: all L keys; pass 2: the L - w prefix).
+template <bool kStats>
+__device__ __forceinline__ int seq_tiles(const SnapParams& p, int b) {
+  const int n = kStats ? p.L[b] : p.L[b] - p.w;
+  return n > 0 ? (n + kTcTile - 1) / kTcTile : 0;
+}
+
+// The pass's key tiles, unit after unit (b major, then g), as one sequence; the
+// cursor walks it and names each tile's unit and its index in that unit.
+template <bool kStats>
+struct TileCursor {
+  int b, g, unit, local, ut;  // the tile's unit, its index there, the unit's tile count
+  long first;                 // sequence index of the unit's first tile
+  __device__ void start(const SnapParams& p, long x) {
+    b = 0;
+    first = 0;
+    for (;;) {
+      ut = seq_tiles<kStats>(p, b);
+      const long n = (long)p.Hkv * ut;
+      if (x - first < n || b == p.B - 1) break;
+      first += n;
+      ++b;
+    }
+    g = ut > 0 ? (int)((x - first) / ut) : 0;
+    first += (long)g * ut;
+    local = (int)(x - first);
+    unit = b * p.Hkv + g;
+  }
+  __device__ void next(const SnapParams& p) {  // past the last tile it stays in the last sequence
+    if (++local < ut) return;
+    first += ut;
+    local = 0;
+    if (++g == p.Hkv) {
+      g = 0;
+      while (b + 1 < p.B) {
+        ut = seq_tiles<kStats>(p, ++b);
+        if (ut > 0) break;
+      }
+    }
+    unit = b * p.Hkv + g;
+  }
+};
+
+// In the flat split (gridDim.x = N CTAs over the T tiles of the sequence), CTA i takes
+// tiles [i T / N, (i + 1) T / N); the CTA holding tile x is ceil((x + 1) N / T) - 1.
+__device__ __forceinline__ int flat_cta_of(long x, long T, int N) { return (int)(((x + 1) * N - 1) / T); }
+
+template <bool kStats>
+__device__ __forceinline__ long pass_tiles_total(const SnapParams& p) {
+  long T = 0;
+  for (int b = 0; b < p.B; ++b) T += (long)p.Hkv * seq_tiles<kStats>(p, b);
+  return T;
 }
 
 // ---------------------------------------------------------------------------
-// Both passes.  grid (nsplit, B*Hkv), 192 threads, dynamic smem kTcSmem; CTA
-// `split` scores keys [split * item_keys, ...) of its unit (pass 1: all L keys; pass 2:
-// the L - w prefix keys).
-//   warp 4 (one lane): TMA loads of the K tiles into a two-stage ring;
+// Both passes, 192 threads, dynamic smem kTcSmem.  Split per unit (flat == 0): grid
+// (nsplit, B*Hkv), CTA `split` scores tiles [split * item_keys / 128, ...) of its unit.
+// Flat split (flat == 1): grid (N), CTA i scores its equal share of the pass's tiles
+// taken unit after unit, so that every resident-CTA slot is used when the units do
+// not divide the slots; a share may run across units (the query tile is then
+// reloaded and, in pass 1, the row statistics are written per unit).  Pass 1 scores
+// all L keys, pass 2 the L - w prefix keys.
+//   warp 4 (one lane): TMA loads of each unit's query tile and of the K tiles into a
+//                      two-stage ring;
 //   warp 5 (one lane): per tile, eight K=16 MMAs into accumulator (tile % 2) of TMEM;
 //   warps 0-3: read the accumulator (thread = TMEM lane) and fold it.
-// Barriers: full[s] (TMA -> MMA, transaction bytes), empty[s] (MMA commit -> TMA),
-// tfull[d] (MMA commit -> epilogue), tempty[d] (128 epilogue arrivals -> MMA).  Every
-// wait is bounded; a wait that runs out flags RKV_DEVERR_TIMEOUT, stops every role
-// and the CTA drains what it issued before freeing TMEM.
+// Barriers: qfull (query TMA -> MMA, one phase per unit), full[s] (TMA -> MMA,
+// transaction bytes), empty[s] (MMA commit -> TMA; it also tells the TMA warp that
+// the query tile is free), tfull[d] (MMA commit -> epilogue), tempty[d] (128 epilogue
+// arrivals -> MMA).  Every wait is bounded; a wait that runs out flags
+// RKV_DEVERR_TIMEOUT, stops every role and the CTA drains what it issued before
+// freeing TMEM.  The query tile is the unit's R = G w rows (row r = head * w + j) and
+// then whatever follows them in q_win (zero past its end): pass 1 masks rows from R
+// on, pass 2 weighs them by 2^-inf = 0.
 // ---------------------------------------------------------------------------
 template <bool kStats>
 __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_constant__ SnapParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t full_b[kTcStages], empty_b[kTcStages], tfull_b[2], tempty_b[2];
+  __shared__ uint64_t full_b[kTcStages], empty_b[kTcStages], tfull_b[2], tempty_b[2], qfull_b;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
-  __shared__ __align__(16) float rs[128];  // pass 2: lse_r = M_r + log2(l_r) (base 2)
+  __shared__ __align__(16) float rs[4][128];  // pass 2: lse_r = M_r + log2(l_r) (base 2), per epilogue warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int unit = blockIdx.y, b = unit / p.Hkv, g = unit % p.Hkv, split = blockIdx.x;
-  const int L = p.L[b];
-  const int col_end = kStats ? L : L - p.w;  // keys scored by this pass
-  const int t_begin = split * p.item_keys;
-  const int t_end = min(col_end, t_begin + p.item_keys);
-  const int ntiles = t_end > t_begin ? (t_end - t_begin + kTcTile - 1) / kTcTile : 0;
+  // this CTA's run of tiles: ntiles from the cursor's start
+  TileCursor<kStats> cur0;
+  int ntiles, split = 0;
+  long T = 0;
+  if (p.flat) {
+    T = pass_tiles_total<kStats>(p);
+    const int N = gridDim.x, i = blockIdx.x;
+    const long g0 = (long)i * T / N, g1 = (long)(i + 1) * T / N;
+    ntiles = (int)(g1 - g0);
+    if (ntiles > 0) cur0.start(p, g0);
+  } else {
+    const int unit = blockIdx.y, b = unit / p.Hkv;
+    split = blockIdx.x;
+    const int ut = seq_tiles<kStats>(p, b), per = p.item_keys / kTcTile;
+    ntiles = max(0, min(per, ut - split * per));
+    cur0.b = b;
+    cur0.g = unit % p.Hkv;
+    cur0.unit = unit;
+    cur0.ut = ut;
+    cur0.local = split * per;
+    cur0.first = 0;  // unused: the run stays in its unit
+  }
   if (ntiles == 0) {
-    if (kStats && tid < 128) p.part[((size_t)unit * p.nsplit + split) * 128 + tid] = make_float2(-1e30f, 0.f);
+    if (kStats && !p.flat && tid < 128)
+      p.part[((size_t)blockIdx.y * p.nsplit + split) * 128 + tid] = make_float2(-1e30f, 0.f);
     return;
   }
+  // pass-1 slot of this CTA's statistics for the unit whose first tile is `first`
+  auto slot_of = [&](long first) { return p.flat ? blockIdx.x - flat_cta_of(first, T, gridDim.x) : split; };
   uint8_t* qs = align1024(smem);
   uint8_t* ks = qs + kTcOperandBytes;
 
@@ -125,6 +203,7 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
       mbar_init(&tfull_b[d], 1);
       mbar_init(&tempty_b[d], 128);
     }
+    mbar_init(&qfull_b, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -132,48 +211,60 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
     tmem_alloc(&tmem_base, kTcTmemCols);
     tmem_relinquish();
   }
-  // the unit's query rows (row r = head * w + j), zero from row R on
-  for (int e = tid; e < 128 * 16; e += kTcThreads) {
-    const int r = e >> 4, piece = e & 15;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < p.R)
-      v = *reinterpret_cast<const uint4*>(
-          p.q_win + (((size_t)b * p.Hq + (size_t)g * p.G + r / p.w) * p.w + r % p.w) * 128 + piece * 8);
-    *reinterpret_cast<uint4*>(qs + tc_swz(r, piece)) = v;
-  }
-  if (!kStats)
-    for (int r = tid; r < 128; r += kTcThreads) rs[r] = p.rowlse[(size_t)unit * 128 + r];
-  fence_proxy_async_smem();  // the generic writes of Q, before the MMAs read it
+  if (!kStats && warp < 4)
+    for (int r = lane; r < 128; r += 32) rs[warp][r] = p.rowlse[(size_t)cur0.unit * 128 + r];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-  int issued = 0, committed = -1;  // TMA tiles issued (warp 4); last tile committed (warp 5)
+  int issued = 0, committed = -1, qissued = 0;  // K tiles issued, query tiles issued (warp 4); last tile committed (warp 5)
+  // first query row of a unit in q_win ([B][Hq][w][128])
+  auto qrow0 = [&](int b, int g) { return ((b * p.Hq + g * p.G) * p.w); };
 
   if (warp == 4) {
     if (lane == 0) {
-      const int row0 = unit * p.Lmax + t_begin;  // rows past the unit are masked, past the array zero
+      TileCursor<kStats> c = cur0;
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % kTcStages;
+        const bool new_unit = i == 0 || c.local == 0;
         if (i >= kTcStages && !mbar_wait(&empty_b[s], (uint32_t)((i / kTcStages - 1) & 1))) {
           flag_error(p.err, RKV_DEVERR_TIMEOUT);
           abort_flag = 1;
         }
         if (abort_flag) break;
         uint8_t* st = ks + s * kTcOperandBytes;
+        const int row = c.unit * p.Lmax + c.local * kTcTile;  // rows past the unit are masked, past the array zero
         mbar_arrive_expect_tx(&full_b[s], kTcOperandBytes);
-        tma_load_2d(st, &p.tmk, 0, row0 + i * kTcTile, &full_b[s]);
-        tma_load_2d(st + kTcOperandBytes / 2, &p.tmk, 64, row0 + i * kTcTile, &full_b[s]);
+        tma_load_2d(st, &p.tmk, 0, row, &full_b[s]);
+        tma_load_2d(st + kTcOperandBytes / 2, &p.tmk, 64, row, &full_b[s]);
         issued = i + 1;
+        if (new_unit) {
+          // the query tile is free once the previous tile's MMAs have completed
+          if (i > 0 && !mbar_wait(&empty_b[(i - 1) % kTcStages], (uint32_t)(((i - 1) / kTcStages) & 1))) {
+            flag_error(p.err, RKV_DEVERR_TIMEOUT);
+            abort_flag = 1;
+            break;
+          }
+          const int qr = qrow0(c.b, c.g);
+          mbar_arrive_expect_tx(&qfull_b, kTcOperandBytes);
+          tma_load_2d(qs, &p.tmq, 0, qr, &qfull_b);
+          tma_load_2d(qs + kTcOperandBytes / 2, &p.tmq, 64, qr, &qfull_b);
+          ++qissued;
+        }
+        c.next(p);
       }
     }
   } else if (warp == 5) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
       const uint32_t q32 = smem_u32(qs), k32 = smem_u32(ks);
+      TileCursor<kStats> c = cur0;
+      int qseen = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int s = i % kTcStages, d = i & 1;
-        bool ok = mbar_wait(&full_b[s], (uint32_t)((i / kTcStages) & 1));
+        bool ok = true;
+        if (i == 0 || c.local == 0) ok = mbar_wait(&qfull_b, (uint32_t)(qseen++ & 1));
+        if (ok) ok = mbar_wait(&full_b[s], (uint32_t)((i / kTcStages) & 1));
         if (ok && i >= 2) ok = mbar_wait(&tempty_b[d], (uint32_t)(((i >> 1) - 1) & 1));
         if (!ok) {
           flag_error(p.err, RKV_DEVERR_TIMEOUT);
@@ -191,6 +282,7 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
         tc_commit(&empty_b[s]);
         tc_commit(&tfull_b[d]);
         committed = i;
+        c.next(p);
       }
       // the last tile's stage release lands before the CTA may exit
       if (committed >= 0 && !abort_flag)
@@ -201,7 +293,10 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl = p.scale_log2;
     float m_run = -1e30f, l_run = 0.f;
-    const int lim = (kStats && tid < p.R) ? L - p.w + tid % p.w : -1;  // last key row tid sees
+    TileCursor<kStats> c = cur0;
+    // the last key row tid sees in its unit (-1: a row past R, which sees none)
+    auto last_key = [&](int b) { return (kStats && tid < p.R) ? p.L[b] - p.w + tid % p.w : -1; };
+    int lim = last_key(c.b);
     for (int i = 0; i < ntiles; ++i) {
       const int d = i & 1;
       const bool late = !mbar_wait(&tfull_b[d], (uint32_t)((i >> 1) & 1));
@@ -211,15 +306,15 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
       }
       if (__any_sync(0xffffffffu, late || abort_flag)) break;  // warp-uniform: the TMEM loads are .aligned
       tc_fence_after();
-      const int t0 = t_begin + i * kTcTile;
+      const int t0 = c.local * kTcTile;
       if (kStats) {
-        const int vis = min(t_end, lim + 1) - t0;  // keys of this tile the row sees: [0, vis)
+        const int vis = lim + 1 - t0;  // keys of this tile the row sees: [0, vis)
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t v[32];
-          tc_ld32_wait(lane_addr + d * 128 + c * 32, v);
+          tc_ld32_wait(lane_addr + d * 128 + cc * 32, v);
           float s0 = 0.f, s1 = 0.f, m_new;
-          if (c * 32 + 32 <= vis) {  // the row sees the whole chunk: no mask; sl > 0, so max(v)*sl = max(v*sl)
+          if (cc * 32 + 32 <= vis) {  // the row sees the whole chunk: no mask; sl > 0, so max(v)*sl = max(v*sl)
             float mx = __uint_as_float(v[0]);
 #pragma unroll
             for (int j = 1; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
@@ -234,7 +329,7 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
             float mx = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              z[j] = (c * 32 + j < vis) ? __uint_as_float(v[j]) * sl : -INFINITY;
+              z[j] = (cc * 32 + j < vis) ? __uint_as_float(v[j]) * sl : -INFINITY;
               mx = fmaxf(mx, z[j]);
             }
             m_new = fmaxf(m_run, mx);
@@ -250,12 +345,12 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
       } else {
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 4 && c * 32 < p.R; ++c) {
+        for (int cc = 0; cc < 4 && cc * 32 < p.R; ++cc) {
           uint32_t v[32];
-          tc_ld32_wait(lane_addr + d * 128 + c * 32, v);
+          tc_ld32_wait(lane_addr + d * 128 + cc * 32, v);
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {  // p = 2^(z - M_r) / l_r = 2^(z - lse_r)
-            const float4 a = *reinterpret_cast<const float4*>(&rs[c * 32 + j]);
+            const float4 a = *reinterpret_cast<const float4*>(&rs[warp][cc * 32 + j]);
             s0 += ex2_approx(fmaf(__uint_as_float(v[j]), sl, -a.x));
             s1 += ex2_approx(fmaf(__uint_as_float(v[j + 1]), sl, -a.y));
             s0 += ex2_approx(fmaf(__uint_as_float(v[j + 2]), sl, -a.z));
@@ -263,21 +358,40 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
           }
         }
         const int t = t0 + tid;
-        if (t < t_end) p.S[(size_t)unit * p.Lmax + t] = s0 + s1;
+        if (t < p.L[c.b] - p.w) p.S[(size_t)c.unit * p.Lmax + t] = s0 + s1;
       }
       tc_fence_before();
       mbar_arrive(&tempty_b[d]);
+      // the unit's last tile of this run: pass 1 writes the unit's row statistics;
+      // pass 2 takes the next unit's row log-sum-exps (this warp's copy)
+      const bool unit_done = c.local + 1 == c.ut || i + 1 == ntiles;
+      if (unit_done && kStats) {
+        p.part[((size_t)c.unit * p.nsplit + slot_of(c.first)) * 128 + tid] = make_float2(m_run, l_run);
+        m_run = -1e30f;
+        l_run = 0.f;
+      }
+      c.next(p);
+      if (unit_done && i + 1 < ntiles) {
+        if (kStats) {
+          lim = last_key(c.b);
+        } else {
+          __syncwarp();  // every lane has read this warp's copy for the previous unit
+          for (int r = lane; r < 128; r += 32) rs[warp][r] = p.rowlse[(size_t)c.unit * 128 + r];
+          __syncwarp();
+        }
+      }
     }
-    if (kStats) p.part[((size_t)unit * p.nsplit + split) * 128 + tid] = make_float2(m_run, l_run);
   }
 
   // teardown: after a timeout, wait (bounded) for the copies and MMAs still in flight
   tc_fence_before();
   __syncthreads();
   if (abort_flag) {
-    if (warp == 4 && lane == 0)
+    if (warp == 4 && lane == 0) {
       for (int i = max(0, issued - kTcStages); i < issued; ++i)
         mbar_wait(&full_b[i % kTcStages], (uint32_t)((i / kTcStages) & 1));
+      if (qissued > 0) mbar_wait(&qfull_b, (uint32_t)((qissued - 1) & 1));
+    }
     if (warp == 5 && lane == 0 && committed >= 0)
       mbar_wait(&tfull_b[committed & 1], (uint32_t)((committed >> 1) & 1));
     __syncthreads();
@@ -292,10 +406,20 @@ __global__ void __launch_bounds__(kTcThreads) snap_score_kernel(const __grid_con
 __global__ void __launch_bounds__(128) snap_stats_combine_kernel(const __grid_constant__ SnapParams p) {
   const int unit = blockIdx.x, r = threadIdx.x;
   const float2* pp = p.part + (size_t)unit * p.nsplit * 128 + r;
+  int nparts = p.nsplit;  // split per unit: every slot written
+  if (p.flat) {           // the CTAs whose runs meet this unit's pass-1 tiles
+    const int b = unit / p.Hkv, g = unit % p.Hkv;
+    long first = 0;
+    for (int bb = 0; bb < b; ++bb) first += (long)p.Hkv * seq_tiles<true>(p, bb);
+    const int ut = seq_tiles<true>(p, b);
+    first += (long)g * ut;
+    const long T = pass_tiles_total<true>(p);
+    nparts = flat_cta_of(first + ut - 1, T, p.flat_ctas) - flat_cta_of(first, T, p.flat_ctas) + 1;
+  }
   float M = -1e30f;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, pp[(size_t)s * 128].x);
+  for (int s = 0; s < nparts; ++s) M = fmaxf(M, pp[(size_t)s * 128].x);
   float l = 0.f;
-  for (int s = 0; s < p.nsplit; ++s) l += pp[(size_t)s * 128].y * exp2f(pp[(size_t)s * 128].x - M);
+  for (int s = 0; s < nparts; ++s) l += pp[(size_t)s * 128].y * exp2f(pp[(size_t)s * 128].x - M);
   // rows without keys (r >= R) get +inf, so 2^(z - lse) = 0 and they add nothing
   p.rowlse[(size_t)unit * 128 + r] = (r < p.R && l > 0.f) ? M + log2f(l) : INFINITY;
 }
@@ -784,14 +908,44 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
       if (items <= slots) break;  // one wave: larger CTAs only lengthen it
     }
     p.item_keys = best_t * kTcTile;
+    // The flat split: N <= slots CTAs of equal shares of all the units' tiles (at
+    // least 4 each), one wave; a share that runs into the next unit reloads the query
+    // tile, worth ~1.5 tiles.  Taken when the model ranks it first: when the units'
+    // tiles do not divide into the slots (64 units of 512 tiles fill 256 of 304).
+    long T1 = 0;
+    for (int b = 0; b < a.B; ++b) T1 += (long)a.Hkv * ((a.prompt_len[b] + kTcTile - 1) / kTcTile);
+    int N = (int)(T1 / 4 < slots ? T1 / 4 : slots);
+    // every unit's pass-1 statistics must fit its kMaxSnapSplit slots
+    auto parts_fit = [&](int n) {
+      long first = 0;
+      for (int b = 0; b < a.B; ++b) {
+        const long ut = (a.prompt_len[b] + kTcTile - 1) / kTcTile;
+        for (int g = 0; g < a.Hkv; ++g, first += ut) {
+          const long c0 = ((first + 1) * n - 1) / T1, c1 = ((first + ut) * n - 1) / T1;
+          if (c1 - c0 + 1 > kMaxSnapSplit) return false;
+        }
+      }
+      return true;
+    };
+    while (N > 1 && !parts_fit(N)) --N;
+    p.flat = 0;
+    p.flat_ctas = 0;
+    if (N >= 1 && (double)T1 / N + 2.4 + 1.5 < best_cost) {
+      p.flat = 1;
+      p.flat_ctas = N;
+    }
   }
-  p.nsplit = (Lmax_seen + p.item_keys - 1) / p.item_keys;
+  p.nsplit = p.flat ? kMaxSnapSplit : (Lmax_seen + p.item_keys - 1) / p.item_keys;
   if (p.nsplit > kMaxSnapSplit) {
     set_last_error("prompt longer than the scoring kernels' split table (524288 tokens)");
     return cudaErrorInvalidValue;
   }
   if (!encode_rows_map(&p.tmk, a.k, (uint64_t)a.B * a.Hkv * a.Lmax, kTcTile)) {
     set_last_error("cuTensorMapEncodeTiled failed for the prompt keys");
+    return cudaErrorInvalidValue;
+  }
+  if (!encode_rows_map(&p.tmq, a.q_win, (uint64_t)a.B * a.Hq * a.w, kTcTile)) {
+    set_last_error("cuTensorMapEncodeTiled failed for the window queries");
     return cudaErrorInvalidValue;
   }
   static bool attrs = false;
@@ -804,7 +958,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   // so the scoring passes are skipped and the select only writes the identity
   bool evicts = false;
   for (int b = 0; b < a.B; ++b) evicts |= a.keep1[b] < a.prompt_len[b];
-  const dim3 sgrid(p.nsplit, (unsigned)units);
+  // pass 2 scores the L - w prefix keys: in the flat split, at most one CTA a tile
+  long T2 = 0;
+  for (int b = 0; b < a.B; ++b)
+    T2 += (long)a.Hkv * (a.prompt_len[b] > a.w ? (a.prompt_len[b] - a.w + kTcTile - 1) / kTcTile : 0);
+  const dim3 sgrid = p.flat ? dim3((unsigned)p.flat_ctas) : dim3(p.nsplit, (unsigned)units);
+  const dim3 sgrid2 = p.flat ? dim3((unsigned)(T2 < p.flat_ctas ? T2 : p.flat_ctas)) : sgrid;
   if (evicts) {
     launch_begin(K_SNAP_STATS, s);
     snap_score_kernel<true><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
@@ -813,7 +972,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     snap_stats_combine_kernel<<<(unsigned)units, 128, 0, s>>>(p);
     launch_end(K_SNAP_STATS_COMBINE, s);
     launch_begin(K_SNAP_COLSUM, s);
-    snap_score_kernel<false><<<sgrid, kTcThreads, kTcSmem, s>>>(p);
+    if (sgrid2.x > 0) snap_score_kernel<false><<<sgrid2, kTcThreads, kTcSmem, s>>>(p);
     launch_end(K_SNAP_COLSUM, s);
     launch_begin(K_SNAP_POOL, s);
     snap_pool_kernel<<<dim3((Lmax_seen + kPoolTile - 1) / kPoolTile, (unsigned)units), kPoolThreads, 0, s>>>(p);
