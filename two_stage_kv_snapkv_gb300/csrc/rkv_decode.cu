@@ -302,8 +302,11 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
                                const uint8_t* new_kv, int* timed_out_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = p.P, G = kG > 0 ? kG : p.G;  // kG > 0: the group size known at compile time
-  const int NP = (n + P - 1) / P;
-  const int cpp = P / kChunkTok;
+  // page sizes are powers of two (16, 32 or 64, checked on the host): shifts, not divisions
+  const int lg_p = __ffs(P) - 1;
+  const int NP = (n + P - 1) >> lg_p;
+  const int cpp = P / kChunkTok, lg_cpp = lg_p - 4;
+  static_assert(kChunkTok == 16, "chunks of 16 tokens: cpp = P >> 4");
   const int mine = it1 - it0 - warp;
   const int nj = mine > 0 ? (mine + kAtWarps - 1) / kAtWarps : 0;
   uint8_t* wbuf = ring + warp * (STAGES * kStageBytes);
@@ -344,8 +347,8 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
       __syncwarp();
       return;
     }
-    int page = sel[it / cpp];
-    const int chunk = it % cpp;
+    int page = sel[it >> lg_cpp];
+    const int chunk = it & (cpp - 1);
     const bool page_ok = page >= 0 && page < NP;  // always true for the select's output
     page = page_ok ? page : 0;
     int phys = ptab[page];
@@ -647,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     do_append = false;
   }
   const int n = n0 + (do_append ? 1 : 0);
-  const int NP = (n + P - 1) / P;
+  const int lg_p = __ffs(P) - 1;  // page sizes are powers of two (16, 32 or 64, checked on the host)
+  const int NP = (n + P - 1) >> lg_p;
   // 2. the append (rank 0, threads 0-63: channels 2t and 2t + 1) writes the token into
   // its slot and folds its key into its page's Kmax/Kmin.  Within this step every CTA
   // takes the token from new_kv, so nothing waits for these writes, and they need no
@@ -657,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // summaries during the selection held rank 0, and with it the cluster, up by about
   // a microsecond.)
   const bool appender = do_append && rank == 0 && tid < 64;
-  const int app_page = n0 / P;
+  const int app_page = n0 >> lg_p;
   const size_t app_row = ((size_t)unit * 128 + 2 * tid) * p.max_pages + app_page;
   // this CTA's slice [p0, p1) of the pages (8-page aligned).  The short instance
   // (every slice under 64 pages) stages the summaries of all 128 channels right away,
@@ -716,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   const int lo_row0 = all_ch ? 128 : k1;  // Kmin row of chosen channel kk: lo_row0 + hi row
   const int tcap = all_ch ? slice8 : (p.region_bytes / (4 * k1)) & ~7;
   rkv_bf16* stg = reinterpret_cast<rkv_bf16*>(ring);
-  const int pnew = do_append ? n0 / P : -1;
+  const int pnew = do_append ? n0 >> lg_p : -1;
   bool waited = false;
   int stile = 0;  // bulk-staged tiles so far (phase of sbar)
   for (int t0 = p0; t0 < p1; t0 += tcap) {
@@ -746,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     __syncthreads();
     if (pnew >= t0 && pnew < t0 + cnt) {
       const int j = pnew - t0;
-      const bool first = (n0 % P) == 0;
+      const bool first = (n0 & (P - 1)) == 0;
       const rkv_bf16* kn = reinterpret_cast<const rkv_bf16*>(new_kv);
       const int nrows = all_ch ? 128 : k1;
       for (int r = tid; r < nrows; r += kThreads) {
@@ -912,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     const uint32_t app_k = reinterpret_cast<const uint32_t*>(new_kv)[tid];
     const uint32_t app_v = reinterpret_cast<const uint32_t*>(new_kv)[64 + tid];
     if (app_phys >= 0 && app_phys < p.num_phys) {
-      const int slot = n0 % P;
+      const int slot = n0 & (P - 1);
       const size_t dst = (((size_t)app_phys * p.Hkv + g) * P + slot) * 128 + 2 * tid;
       *reinterpret_cast<uint32_t*>(p.k_pages + dst) = app_k;
       *reinterpret_cast<uint32_t*>(p.v_pages + dst) = app_v;
