@@ -95,6 +95,7 @@ struct HsaParamsT {
   int32_t* sel_pages;
   int sel_pages_stride;
   int B, Hkv, Hq, G, P, max_pages, num_phys, nsplit, cluster, region_bytes;
+  uint32_t c_mag;  // ceil(2^32 / cluster) for cluster > 1 (x / cluster as a multiply-high)
   int tok_stride;          // row stride of sigma / selp on the token path (max_pages * P)
   float scale_log2;
   int32_t k1[NB];
@@ -598,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   int32_t* sel = reinterpret_cast<int32_t*>(keys + p.max_pages);
   int32_t* ptab = sel + p.max_pages;
   float* inbox = reinterpret_cast<float*>(ptab + p.max_pages);
-  const int hpc = (G + C - 1) / C;  // heads finished per CTA
+  const int hpc = C > 1 ? (int)__umulhi((uint32_t)(G + C - 1), p.c_mag) : G;  // heads finished per CTA
   // the query as floats, in the inbox (idle until the partial states arrive), so the
   // whole region is free for the summaries from the start
   float(*qf)[128] = reinterpret_cast<float(*)[128]>(inbox);
@@ -671,7 +672,9 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // all-channel staging saved 0.5 us a step at 26 pages a slice; at 150-300 pages,
   // waiting for the chosen half saved 0.5-2.9 us).  The page-table row (needed after
   // the select) comes by bulk copy.
-  const int per = ((NP + C - 1) / C + 7) & ~7;
+  // x / C by a multiply (c_mag = ceil(2^32 / C) from the host; exact for x < 2^31)
+  auto div_c = [&](int x) { return C > 1 ? (int)__umulhi((uint32_t)x, p.c_mag) : x; };
+  const int per = (div_c(NP + C - 1) + 7) & ~7;
   const int p0 = min(NP, rank * per), p1 = min(NP, p0 + per);
   const int slice8 = (p1 - p0 + 7) & ~7;
   // The short instance is launched only when every CTA's slice qualifies: a slice
@@ -679,11 +682,10 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // the capacity above).  The long one never stages all channels.
   const bool all_ch = kShort && p1 > p0 && slice8 < 64 && 2 * 128 * slice8 * 2 <= p.region_bytes;
   if (all_ch) {
-    const int cpr = slice8 >> 3;
-    for (int e = tid; e < 256 * cpr; e += kThreads) {
-      const int i = e / cpr, c = e - i * cpr;
-      cp_async16(ring + (size_t)i * slice8 * 2 + c * 16,
-                 (i < 128 ? p.kmax : p.kmin) + ((size_t)unit * 128 + (i & 127)) * p.max_pages + p0 + c * 8, 16u);
+    const int cpr = slice8 >> 3;  // 16-byte pieces a row
+    for (int i = tid; i < 256; i += kThreads) {
+      const rkv_bf16* src = (i < 128 ? p.kmax : p.kmin) + ((size_t)unit * 128 + (i & 127)) * p.max_pages + p0;
+      for (int c = 0; c < cpr; ++c) cp_async16(ring + (size_t)i * slice8 * 2 + c * 16, src + c * 8, 16u);
     }
     cp_async_commit();
   }
@@ -876,32 +878,33 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   grid_launch_dependents();
   // 7. attention over this CTA's share of the selected chunks
   const int items = k * (P / kChunkTok);
-  const int ips = (items + C - 1) / C;
+  const int ips = div_c(items + C - 1);
   const int it0 = min(items, rank * ips), it1 = min(items, it0 + ips);
   int to = 0;
   const CtaPart* part =
       attend_cta<STAGES, false, Params, kG>(p, sel, ptab, b, g, n, it0, it1, ring, as, do_append ? n0 : -1, new_kv, &to);
 
   // 8. each head's partial state goes to the CTA that finishes the head (h % C), slot
-  // [rank][h / C] of its inbox
-  for (int h = 0; h < G; ++h) {
-    float* dst = cluster.map_shared_rank(inbox, h % C) + ((size_t)rank * hpc + h / C) * 130;
-    dst[2 + tid] = part->O[h][tid];
-    if (tid == 0) {
-      dst[0] = part->M[h];
-      dst[1] = part->L[h];
+  // [rank][h / C] of its inbox (h = j C + r)
+  for (int j = 0, h = 0; h < G; ++j)
+    for (int r = 0; r < C && h < G; ++r, ++h) {
+      float* dst = cluster.map_shared_rank(inbox, r) + ((size_t)rank * hpc + j) * 130;
+      dst[2 + tid] = part->O[h][tid];
+      if (tid == 0) {
+        dst[0] = part->M[h];
+        dst[1] = part->L[h];
+      }
     }
-  }
 
   cluster.sync();  // every inbox is filled; no shared memory is touched remotely after this
 
-  // 9. merge this CTA's heads
-  for (int h = rank; h < G; h += C) {
+  // 9. merge this CTA's heads (h = j C + rank)
+  for (int j = 0, h = rank; h < G; ++j, h += C) {
     float M = -1e30f;
-    for (int r = 0; r < C; ++r) M = fmaxf(M, inbox[((size_t)r * hpc + h / C) * 130]);
+    for (int r = 0; r < C; ++r) M = fmaxf(M, inbox[((size_t)r * hpc + j) * 130]);
     float L = 0.f, O = 0.f;
     for (int r = 0; r < C; ++r) {
-      const float* src = inbox + ((size_t)r * hpc + h / C) * 130;
+      const float* src = inbox + ((size_t)r * hpc + j) * 130;
       const float f = exp2f(src[0] - M);
       L += src[1] * f;
       O += src[2 + tid] * f;
@@ -1511,6 +1514,7 @@ cudaError_t launch_fused(HsaParams& p, const DecodeArgs& a, cudaStream_t s) {
   }
   if (!cached) last = {units, a.cache.max_pages, k1max, by_items, dev, best_C, best_st, best_smem};
   p.cluster = best_C;
+  p.c_mag = best_C > 1 ? 0xFFFFFFFFu / (uint32_t)best_C + 1u : 0u;
   p.region_bytes = region_for(best_st, best_C);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(best_C, (unsigned)units, 1);
