@@ -471,9 +471,11 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const float m_new = fmaxf(m_run, mx);
-    const float alpha = exp2f(m_run - m_new);
-    const float p0 = exp2f(z0 - m_new), p1 = exp2f(z1 - m_new);
-    const float p2 = exp2f(z2 - m_new), p3 = exp2f(z3 - m_new);
+    // one special-function instruction each (ex2.approx: a few ulps, results below
+    // 2^-126 flushed to zero; -inf gives 0)
+    const float alpha = ex2_approx(m_run - m_new);
+    const float p0 = ex2_approx(z0 - m_new), p1 = ex2_approx(z1 - m_new);
+    const float p2 = ex2_approx(z2 - m_new), p3 = ex2_approx(z3 - m_new);
     l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
     m_run = m_new;
 #pragma unroll
@@ -526,7 +528,7 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
     float L = 0.f, O = 0.f;
 #pragma unroll
     for (int w = 0; w < kAtWarps; ++w) {
-      const float f = exp2f(cm[w * 8 + h] - M);
+      const float f = ex2_approx(cm[w * 8 + h] - M);
       L += cl[w * 8 + h] * f;
       O += co[(w * 8 + h) * 128 + c] * f;
     }
@@ -905,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     float L = 0.f, O = 0.f;
     for (int r = 0; r < C; ++r) {
       const float* src = inbox + ((size_t)r * hpc + j) * 130;
-      const float f = exp2f(src[0] - M);
+      const float f = ex2_approx(src[0] - M);
       L += src[1] * f;
       O += src[2 + tid] * f;
     }

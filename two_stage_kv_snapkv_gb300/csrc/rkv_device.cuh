@@ -155,7 +155,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
 
 // 2^x by the special function unit's single instruction (PTX ex2.approx.ftz.f32):
 // relative error of a few ulps, results below 2^-126 flushed to zero.  Used where the
-// exponential is the inner loop's cost (the scoring epilogues).
+// exponential is the inner loop's cost (the scoring epilogues, the attention's online
+// softmax) and in the merges of partial softmax states.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
