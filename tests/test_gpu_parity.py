@@ -458,6 +458,28 @@ def test_workload4_batched_ragged(rkv, path):
     assert _sampled_full(rkv, 4, [(longest, 1), (shortest, 6)], {0, 255}) <= ATOL_OUT
 
 
+def test_flat_scoring_split_with_a_window_only_prompt(rkv):
+    """128 units whose key tiles do not divide into the resident slots take the flat
+    scoring split (equal shares of all units' tiles, runs crossing unit boundaries); one
+    prompt is only its window, so it has no pass-2 tiles at all.  The units on both
+    sides of it and that unit itself match the oracle (kept sets, pooled scores, cache,
+    decode steps)."""
+    lens = [8192] * 7 + [32] + [8192] * 8
+    wl = W.custom(B=16, Hq=32, Hkv=8, prompt_lens=lens, budget=1024, window=32, page_size=16, steps=2,
+                  pool_kernel=15)
+    run = GpuRun(wl, rkv, gen_device="cuda", tail="zero")
+    run.prefill()
+    checks = [OracleUnit(run, b, g) for b, g in [(6, 7), (7, 0), (7, 7), (8, 0), (15, 7)]]
+    for u in checks:
+        u.check_prefill(run)
+        u.check_cache(run)
+    for step in range(wl.steps):
+        d, out, ch, pg = run.decode_step(step)
+        for u in checks:
+            assert u.step(run, d, out, ch, pg, check_cache=True)["err"] <= ATOL_OUT
+    assert run.status()[0] == rkv.RKV_OK
+
+
 def test_workload5_one_layer_sampled(rkv):
     assert _sampled_full(rkv, 5, [(0, 0), (7, 7)], {0, 63}) <= ATOL_OUT
 
