@@ -9,10 +9,11 @@
 // Two implementations of the same step:
 //
 // * hsa_step_kernel (fused, one launch): one thread-block cluster per (sequence, KV
-//   head).  Optionally appends the new token first.  Every CTA selects the
-//   channels; each CTA stages the summaries of its slice of pages into shared
-//   memory (all channels early for short slices, the chosen ones after the select
-//   for long slices) and bounds those pages; the page
+//   head).  Optionally appends the new token (every CTA takes it from shared memory
+//   within the step; its K/V and summary updates are stored at the end).  Every CTA
+//   selects the channels; each CTA stages the summaries of its slice of pages into
+//   shared memory (all channels early for short slices, the chosen ones after the
+//   select for long slices: two compiled instances) and bounds those pages; the page
 //   scores are shared through distributed shared memory; every CTA runs the same
 //   top-k2 select, attends over its share of the selected pages, and the CTAs'
 //   partial softmax states are merged through distributed shared memory.  Used
