@@ -481,9 +481,11 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
 // branches and 1,700 with the decisions as bit arithmetic and predicated stores).
 // Thread t owns the contiguous keys [t S, t S + S), S a multiple of 4 (16-byte loads,
 // index-ordered compaction by one block scan); every thread runs the same trip counts.
-// Boundary candidates are gathered by a block scan instead of shared atomics.  Needs
-// n < 65536, n <= NT * S with `keys` 16-byte aligned and readable up to NT * S entries (entries
-// from n on are ignored).  For 1 <= k < n; every thread of the block calls this.
+// Boundary candidates are gathered by a block scan instead of shared atomics, and the
+// gather and the compaction visit only the keys they keep (bit masks of a thread's at
+// most 32 keys).  Needs n <= 32 NT, with `keys` 16-byte aligned and readable up to
+// NT * S entries (entries from n on are ignored).  For 1 <= k < n; every thread of the
+// block calls this.
 template <int NT>
 __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
   static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
@@ -624,32 +626,28 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
   const bool all_in = need == nin;                    // every key in [lo, hi] is taken
   const bool by_index = !all_in && nin > kTkCandFlat;  // then lo == hi
   if (!by_index && !all_in) {
-    int cnt = 0;
+    // this thread's keys inside [lo, hi] as a bit mask (S <= 32 keys a thread)
+    uint32_t fm = 0;
 #pragma unroll 1
     for (int q = 0; q < Q; ++q) {
       const uint4 v = k4[q];
       const int j = i0 + 4 * q;
-      cnt += (j < n) & (v.x >= lo) & (v.x <= hi);
-      cnt += (j + 1 < n) & (v.y >= lo) & (v.y <= hi);
-      cnt += (j + 2 < n) & (v.z >= lo) & (v.z <= hi);
-      cnt += (j + 3 < n) & (v.w >= lo) & (v.w <= hi);
+      const uint32_t f = (uint32_t)((j < n) & (v.x >= lo) & (v.x <= hi)) |
+                         ((uint32_t)((j + 1 < n) & (v.y >= lo) & (v.y <= hi)) << 1) |
+                         ((uint32_t)((j + 2 < n) & (v.z >= lo) & (v.z <= hi)) << 2) |
+                         ((uint32_t)((j + 3 < n) & (v.w >= lo) & (v.w <= hi)) << 3);
+      fm |= f << (4 * q);
     }
     int total;
-    int slot = block_scan(cnt, 0, total);
-#pragma unroll 1
-    for (int q = 0; q < Q; ++q) {
-      const uint4 v = k4[q];
-      const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t u = u4[e];
-        const bool f = (i0 + 4 * q + e < n) & (u >= lo) & (u <= hi);
-        if (f & (slot < kTkCandFlat)) {
-          ts.cand[slot] = i0 + 4 * q + e;
-          ts.ckey[slot] = u;
-        }
-        slot += f;
+    int slot = block_scan(__popc(fm), 0, total);
+    while (fm) {  // the few candidates, in index order
+      const int e = __ffs(fm) - 1;
+      fm &= fm - 1;
+      if (slot < kTkCandFlat) {
+        ts.cand[slot] = i0 + e;
+        ts.ckey[slot] = keys[i0 + e];
       }
+      ++slot;
     }
     __syncthreads();
     static_assert(kTkCandFlat <= NT && kTkCandFlat % 32 == 0, "one candidate a lane");
@@ -691,34 +689,31 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
     const unsigned tk = above | (inr & (bi ^ 1u) & ((unsigned)(u > T) | ((unsigned)(u == T) & (unsigned)(i <= tI))));
     return (0u - valid) & (tk | ((inr & bi) << 1));  // all bits of the class, or none
   };
-  int c1 = 0, c2 = 0;
+  // this thread's taken keys (tm) and boundary keys taken by index (bm) as bit masks
+  uint32_t tm = 0, bm = 0;
 #pragma unroll 1
   for (int q = 0; q < Q; ++q) {
     const uint4 v = k4[q];
     const int j = i0 + 4 * q;
     const unsigned a = cls(v.x, j), b = cls(v.y, j + 1), c = cls(v.z, j + 2), d = cls(v.w, j + 3);
-    c1 += (int)((a & 1u) + (b & 1u) + (c & 1u) + (d & 1u));
-    c2 += (int)((a >> 1) + (b >> 1) + (c >> 1) + (d >> 1));
+    tm |= ((a & 1u) | ((b & 1u) << 1) | ((c & 1u) << 2) | ((d & 1u) << 3)) << (4 * q);
+    bm |= ((a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2) | ((d >> 1) << 3)) << (4 * q);
   }
   // both prefixes in one scan, one count in each 16-bit half (every count is <= n < 2^16)
   int tot;
-  const int both = block_scan(c1 | (c2 << 16), 1, tot);
+  const int both = block_scan(__popc(tm) | (__popc(bm) << 16), 1, tot);
   const int base = both & 0xffff;
   int bseen = both >> 16;
   int o = base + min(need, bseen);
-#pragma unroll 1
-  for (int q = 0; q < Q; ++q) {
-    const uint4 v = k4[q];
-    const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = i0 + 4 * q + e;
-      const unsigned t = cls(u4[e], i);
-      const bool take = (t & 1u) | ((t >> 1) & (unsigned)(bseen < need));
-      if (take & (o < k)) out[o] = i;
-      o += take;
-      bseen += (int)(t >> 1);
-    }
+  uint32_t any = tm | bm;
+  while (any) {  // this thread's taken keys, in index order
+    const int e = __ffs(any) - 1;
+    any &= any - 1;
+    const unsigned isb = (bm >> e) & 1u;
+    const bool take = (isb ^ 1u) | (unsigned)(bseen < need);
+    if (take & (o < k)) out[o] = i0 + e;
+    o += take;
+    bseen += (int)isb;
   }
   __syncthreads();  // the list is complete and the scratch may be reused
 }
