@@ -58,7 +58,7 @@ def splits_for(wl: W.Workload, rkv) -> list:
     return out
 
 
-class GpuRun:
+class DeviceRun:
     """One layer of a workload on the GPU: inputs, cache, prefill, decode steps."""
 
     def __init__(self, wl: W.Workload, rkv, seed: int = 0x5EED, layer: int = 0, gen_device="cpu",
@@ -118,7 +118,7 @@ class OracleUnit:
     """The oracle's view of one (sequence, KV head): stage 1 on the prompt, then the
     compressed cache built from the GPU's (validated) kept set and grown per step."""
 
-    def __init__(self, run: GpuRun, b: int, g: int):
+    def __init__(self, run: DeviceRun, b: int, g: int):
         wl = run.wl
         self.b, self.g, self.wl = b, g, wl
         G = wl.G
@@ -131,7 +131,7 @@ class OracleUnit:
         self.res = O.prefill_evict_unit(q, k, run.keep1[b], run.kp[b])
         self.keep1 = run.keep1[b]
 
-    def check_prefill(self, run: GpuRun) -> int:
+    def check_prefill(self, run: DeviceRun) -> int:
         wl, b, g = self.wl, self.b, self.g
         Lp = self.L - wl.window
         gp = run.pooled[b, g, :Lp].double().cpu().numpy()
@@ -152,7 +152,7 @@ class OracleUnit:
         self.n = self.keep1
         return swaps
 
-    def check_cache(self, run: GpuRun):
+    def check_cache(self, run: DeviceRun):
         """Cache pages and summaries equal the oracle's, bit for bit."""
         b, g, P = self.b, self.g, self.wl.page_size
         K, V = run.cache.token_kv(b, self.n)
@@ -164,7 +164,7 @@ class OracleUnit:
         np.testing.assert_array_equal(f64(run.cache.kmin[b, g, :, :NP]), kmin)
         assert int(run.cache.seq_len[b].item()) == self.n
 
-    def step(self, run: GpuRun, d: dict, out, ch, pg, check_cache=False) -> dict:
+    def step(self, run: DeviceRun, d: dict, out, ch, pg, check_cache=False) -> dict:
         wl, b, g, P = self.wl, self.b, self.g, self.wl.page_size
         G = wl.G
         self.Kc = np.concatenate([self.Kc[: self.n], f64(d["k_new"][b, g])[None]])

@@ -12,7 +12,7 @@ import torch
 from oracle import rkv_oracle as O
 from two_stage_kv_snapkv_gb300 import workloads as W
 
-from rkv_check import ATOL_OUT, GpuRun, OracleUnit, f64
+from rkv_check import ATOL_OUT, DeviceRun, OracleUnit, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def path(rkv, request):
 
 
 def _run_small(rkv, wl, check_every=1, api="step"):
-    run = GpuRun(wl, rkv, api=api)
+    run = DeviceRun(wl, rkv, api=api)
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     for u in units:
@@ -88,7 +88,7 @@ def test_small_end_to_end(rkv, path, name, api):
 def test_tiny_workload_end_to_end(rkv, path):
     """Workload 1: 4K prompt, GQA 4, needles, 16 decode steps, every step checked."""
     wl = W.workload(1)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     units = [OracleUnit(run, 0, g) for g in range(wl.Hkv)]
     for u in units:
@@ -107,7 +107,7 @@ def test_full_selection_is_dense_attention(rkv, path):
     """k1 = 128 and k2 >= pages: HSA is exact attention over every cached token."""
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[600, 450], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.k1 = [128, 128]
     run.k2 = [4096, 4096]
     run.prefill()
@@ -127,7 +127,7 @@ def test_append_equals_rebuild_on_gpu(rkv, path):
     """Incremental appends, then a from-scratch rebuild by the library: bit-identical summaries."""
     wl = W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[600, 600], budget=64, window=8, page_size=16, steps=37,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     for step in range(wl.steps):
         run.decode_step(step)
@@ -152,7 +152,7 @@ def test_prefill_select_with_large_tie_groups(rkv, L):
     """Prompt keys take only two values, so hundreds of scores tie exactly at the top-k
     boundary: the kept set must be exactly the oracle's (ties go to lower positions)."""
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[L], budget=128, window=8, page_size=16, steps=1, pool_kernel=1)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     k = run.inputs["k"]
     a, bvec = k[0, 0, 0].clone(), k[0, 0, 1].clone()
     pattern = (torch.arange(L) % 3 == 0)
@@ -176,7 +176,7 @@ def test_decode_select_with_tied_page_scores(rkv, path, L, budget):
     in the oracle."""
     wl = W.custom(B=1, Hq=8, Hkv=2, prompt_lens=[L], budget=budget, window=16, page_size=16, steps=2,
                   pool_kernel=3)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     k = run.inputs["k"]
     k[0, :, :L] = k[0, :, :1].clone()
     run.gpu_in["k"] = k.to(run.dev)
@@ -201,7 +201,7 @@ def test_channel_ties_go_to_lower_channels(rkv, path):
     128 channel scores tie exactly: the channel set must be channels 0 .. k1-1."""
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 900], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     for u in units:
@@ -226,7 +226,7 @@ def test_channel_scores_beyond_fp32_are_ranked_exactly(rkv, path):
     c % 7, ties to the lower channel."""
     wl = W.custom(B=2, Hq=4, Hkv=2, prompt_lens=[700, 900], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     for u in units:
@@ -254,7 +254,7 @@ def test_deterministic(rkv, path):
                   pool_kernel=5)
     outs = []
     for _ in range(2):
-        run = GpuRun(wl, rkv)
+        run = DeviceRun(wl, rkv)
         run.prefill()
         res = [run.kept.clone(), run.pooled.clone()]
         for s in range(wl.steps):
@@ -272,7 +272,7 @@ def test_long_slices_with_few_pages(rkv, path):
     checked against the oracle at every step."""
     wl = W.custom(B=4, Hq=8, Hkv=2, prompt_lens=[3000, 2200, 1500, 700], budget=256, window=8, page_size=16,
                   steps=4, pool_kernel=7)
-    run = GpuRun(wl, rkv, max_pages_req=1024)
+    run = DeviceRun(wl, rkv, max_pages_req=1024)
     assert run.cache.max_pages >= 1024
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
@@ -295,7 +295,7 @@ def test_decode_loop_graph_matches_eager(rkv, path):
                   pool_kernel=5)
 
     def setup():
-        runs = [GpuRun(wl, rkv, layer=layer) for layer in range(2)]
+        runs = [DeviceRun(wl, rkv, layer=layer) for layer in range(2)]
         for r in runs:
             r.prefill()
         ins = [[W.decode_tensors(wl, t, r.seed, r.layer, r.dev) for t in range(wl.steps)] for r in runs]
@@ -341,7 +341,7 @@ def test_decode_loop_graph_matches_eager(rkv, path):
 
 def test_bad_page_id_is_flagged_not_faulted(rkv, path):
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     assert run.status()[0] == rkv.RKV_OK
     run.k2 = [1000]        # every page is attended, so the bad entry is used
@@ -354,7 +354,7 @@ def test_bad_page_id_is_flagged_not_faulted(rkv, path):
 
 def test_capacity_overflow_is_flagged(rkv, path):
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     cap = run.cache.max_pages * 16
     run.cache.seq_len.fill_(cap)
@@ -369,7 +369,7 @@ def test_bounded_wait_runs_out_and_reports_timeout(rkv):
     arrives on runs out, sets the timeout bit, and the host reads RKV_ERR_TIMEOUT; the
     context stays usable and the next decode step is clean and correct."""
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[400], budget=64, window=8, page_size=16, steps=1, pool_kernel=3)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     unit = OracleUnit(run, 0, 0)
     unit.check_prefill(run)
@@ -392,7 +392,7 @@ def test_quest_only_small(rkv, path, name):
     the pages (k1 = 128) while only k2 < NP pages are attended.  Channel and page sets
     and the output against the oracle's HSA at k1 = d."""
     wl = SMALL[name]
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.k1 = [128] * wl.B
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
@@ -418,7 +418,7 @@ def test_quest_only_workload4_sampled(rkv, path):
 # ------------------------------------------------------------------ full-size workloads
 def _sampled_full(rkv, n, units, steps_checked, gen_device="cuda", layer=0, k1=None):
     wl = W.workload(n)
-    run = GpuRun(wl, rkv, gen_device=gen_device, tail="zero", layer=layer)
+    run = DeviceRun(wl, rkv, gen_device=gen_device, tail="zero", layer=layer)
     if k1 is not None:
         run.k1 = [k1] * wl.B
     run.prefill()
@@ -467,7 +467,7 @@ def test_flat_scoring_split_with_a_window_only_prompt(rkv):
     lens = [8192] * 7 + [32] + [8192] * 8
     wl = W.custom(B=16, Hq=32, Hkv=8, prompt_lens=lens, budget=1024, window=32, page_size=16, steps=2,
                   pool_kernel=15)
-    run = GpuRun(wl, rkv, gen_device="cuda", tail="zero")
+    run = DeviceRun(wl, rkv, gen_device="cuda", tail="zero")
     run.prefill()
     checks = [OracleUnit(run, b, g) for b, g in [(6, 7), (7, 0), (7, 7), (8, 0), (15, 7)]]
     for u in checks:
@@ -496,7 +496,7 @@ def test_exact_topk_recall_matches_oracle(rkv, name):
     after every decode step.  The top-K may differ only by tokens whose exact score is
     within 1e-5 relative of the K-th score."""
     wl = SMALL[name]
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
     for u in units:
@@ -524,7 +524,7 @@ def test_exact_topk_recall_full_selection_is_one(rkv):
     """Every page selected (k2 >= pages): recall and mass are exactly one."""
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[600, 450], budget=64, window=8, page_size=16, steps=1,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.k2 = [4096, 4096]
     run.prefill()
     d, out, ch, pg = run.decode_step(0)
@@ -537,7 +537,7 @@ def test_mt_small_end_to_end(rkv, path):
     """RocketKV-MT: nothing evicted, HSA over the whole prompt plus the new tokens."""
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=12,
                   pool_kernel=5, mt=True, name="mt_small")
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     assert run.keep1 == [700, 1000]
     run.prefill()
     units = [OracleUnit(run, b, g) for b in range(wl.B) for g in range(wl.Hkv)]
@@ -563,7 +563,7 @@ def test_prefill_with_host_v_matches(rkv, name):
     """rkv_prefill_evict with V in pinned host memory (read through its device mapping)
     fills the cache exactly as with V on the device; a host K is refused."""
     wl = SMALL[name]
-    runs = [GpuRun(wl, rkv), GpuRun(wl, rkv)]
+    runs = [DeviceRun(wl, rkv), DeviceRun(wl, rkv)]
     runs[0].prefill()
     g = runs[1].gpu_in
     v_host = runs[1].inputs["v"].contiguous().pin_memory()
@@ -594,7 +594,7 @@ def test_prefill_with_host_v_matches(rkv, name):
 def test_decode_step_from_host_buffers_matches(rkv):
     """rkv_decode_step_host (host inputs and output) computes what rkv_decode_step does."""
     wl = SMALL["gqa4_ragged"]
-    runs = [GpuRun(wl, rkv), GpuRun(wl, rkv)]
+    runs = [DeviceRun(wl, rkv), DeviceRun(wl, rkv)]
     for r in runs:
         r.prefill()
     staging = rkv.step_host_staging(wl.B, wl.Hq, wl.Hkv)

@@ -10,7 +10,7 @@ import torch
 from oracle import rkv_oracle as O
 from two_stage_kv_snapkv_gb300 import workloads as W
 
-from rkv_check import ATOL_OUT, GpuRun, OracleUnit, check_topk, f64
+from rkv_check import ATOL_OUT, DeviceRun, OracleUnit, check_topk, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def _keys_block(rkv, run, keys_t, b, g):
 
 def _sparq_steps(rkv, wl, k_tokens, units=None, steps=None, seed=0x5EED, gen_device="cpu", tail="nan",
                  keys_t=False):
-    run = GpuRun(wl, rkv, seed=seed, gen_device=gen_device, tail=tail)
+    run = DeviceRun(wl, rkv, seed=seed, gen_device=gen_device, tail=tail)
     run.prefill()
     if units is None:
         units = [(b, g) for b in range(wl.B) for g in range(wl.Hkv)]
@@ -110,7 +110,7 @@ def test_sparq_keys_copy_restarts_when_its_record_is_ahead(rkv):
     next call copy every position again; a zeroed copy is rebuilt the same way."""
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     kt = rkv.sparq_keys(run.cache, run.dev)
     units = wl.B * wl.Hkv
@@ -144,7 +144,7 @@ def test_sparq_every_token_is_dense_attention(rkv):
 def test_sparq_ties_go_to_lower_tokens(rkv):
     """Every prompt key is the same vector, so all but the appended tokens tie."""
     wl = W.custom(B=1, Hq=4, Hkv=1, prompt_lens=[800], budget=64, window=8, page_size=16, steps=2, pool_kernel=3)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     k = run.inputs["k"]
     k[0, :, :800] = k[0, :, :1].clone()
     run.gpu_in["k"] = k.to(run.dev)

@@ -16,7 +16,7 @@ import torch
 
 from two_stage_kv_snapkv_gb300 import workloads as W
 
-from rkv_check import ATOL_OUT, GpuRun
+from rkv_check import ATOL_OUT, DeviceRun
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def test_noalloc_matches_workspace_decode_two_calls(rkv):
 def _compare_two_calls(rkv):
     wl = W.custom(B=2, Hq=8, Hkv=2, prompt_lens=[700, 1000], budget=64, window=8, page_size=16, steps=2,
                   pool_kernel=5)
-    run = GpuRun(wl, rkv)
+    run = DeviceRun(wl, rkv)
     run.prefill()
     dev = run.dev
     for step in range(2):   # two calls in a row share the same scratch
