@@ -134,8 +134,13 @@ struct ChanSmem {
 // (x + y) - x == y); then the fp32 bit patterns rank like the exact sums.  Otherwise
 // the block sums in fp64 (as the oracle does) and ranks on the fp64 bit patterns,
 // high words first.  Every thread of a block of >= 128 threads calls this after
-// filling qf[G][128].
-__device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int k1) {
+// filling qf[G][128].  on_chosen(pos, channel) runs in the thread of each chosen
+// channel as soon as its place pos in the ascending list is known.
+struct NoChosenHook {
+  __device__ void operator()(int, int) const {}
+};
+template <class OnChosen = NoChosenHook>
+__device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int k1, OnChosen on_chosen = {}) {
   const int tid = threadIdx.x;
   __syncthreads();
   float sf = 0.f;
@@ -227,6 +232,7 @@ __device__ void select_channels(const float (*qf)[128], ChanSmem& cs, int G, int
       sn += fminf(x, 0.f);
     }
     if (sel) {
+      on_chosen(pos, tid);  // the caller may start copying this channel's rows now
       cs.chan[pos] = tid;
       cs.qpos[pos] = sp;
       cs.qneg[pos] = sn;
@@ -711,9 +717,20 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   }
   if (do_append && tid < 32) *reinterpret_cast<uint4*>(new_kv + tid * 16) = nkv;
 
-  // 4. channels (every CTA)
+  // 4. channels (every CTA).  The long instance copies the first tile of its slice's
+  // chosen rows as each channel's place becomes known, inside the select.
   const int k1 = p.k1[b];
-  select_channels(qf, cs, G, k1);
+  const int tcap = kShort ? slice8 : (p.region_bytes / (4 * k1)) & ~7;  // pages a staged tile holds
+  const int cnt0_8 = (min(tcap, p1 - p0) + 7) & ~7;
+  const bool early_rows = !kShort && p1 > p0;
+  if (early_rows && tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt0_8 * 2));
+  select_channels(qf, cs, G, k1, [&](int pos, int ch) {
+    if (early_rows) {
+      const size_t row = ((size_t)unit * 128 + ch) * p.max_pages + p0;
+      bulk_g2s(ring + (size_t)pos * cnt0_8 * 2, p.kmax + row, (uint32_t)cnt0_8 * 2, &sbar);
+      bulk_g2s(ring + (size_t)(k1 + pos) * cnt0_8 * 2, p.kmin + row, (uint32_t)cnt0_8 * 2, &sbar);
+    }
+  });
 
   // 5. page bounds of this CTA's slice [p0, p1).  Staged rows: all 128 channels' Kmax
   // then Kmin (rows ch and 128 + ch), or the k1 chosen channels' (rows kk and k1 + kk,
@@ -723,7 +740,6 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // nothing: max and min are idempotent); then every thread bounds pages from shared
   // memory, and the scores go to every CTA's key array.
   const int lo_row0 = all_ch ? 128 : k1;  // Kmin row of chosen channel kk: lo_row0 + hi row
-  const int tcap = all_ch ? slice8 : (p.region_bytes / (4 * k1)) & ~7;
   rkv_bf16* stg = reinterpret_cast<rkv_bf16*>(ring);
   const int pnew = do_append ? n0 >> lg_p : -1;
   bool waited = false;
@@ -739,15 +755,18 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
       }
       cp_async_wait<0>();
     } else {
-      // the chosen channels' rows, one bulk copy per row
-      fence_proxy_async_smem();
-      if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
-      __syncthreads();
-      for (int i = tid; i < 2 * k1; i += kThreads) {
-        const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
-        const int ch = cs.chan[i < k1 ? i : i - k1];
-        bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0,
-                 (uint32_t)cnt8 * 2, &sbar);
+      // the chosen channels' rows, one bulk copy per row (the first tile's are on their
+      // way since the channel select)
+      if (t0 != p0) {
+        fence_proxy_async_smem();
+        if (tid == 0) mbar_arrive_expect_tx(&sbar, (uint32_t)(2 * k1 * cnt8 * 2));
+        __syncthreads();
+        for (int i = tid; i < 2 * k1; i += kThreads) {
+          const rkv_bf16* base = i < k1 ? p.kmax : p.kmin;
+          const int ch = cs.chan[i < k1 ? i : i - k1];
+          bulk_g2s(ring + (size_t)i * cnt8 * 2, base + ((size_t)unit * 128 + ch) * p.max_pages + t0,
+                   (uint32_t)cnt8 * 2, &sbar);
+        }
       }
       if (!mbar_wait(&sbar, (uint32_t)(stile & 1))) flag_error(p.err, RKV_DEVERR_TIMEOUT);
       ++stile;
