@@ -304,10 +304,40 @@ static_assert((int)sizeof(TopkSmem<kThreads>) <= ring_bytes(kFusedStages), "ring
 // sel[j] is token j's row in the K/V pools (-1: zero-filled and masked), gathered row
 // by row with 16-byte cp.async into the same swizzled stage layout the tiled TMA
 // loads produce (rows past n are zero-filled too).
+// The tiled TMA loads of chunk `chunk` of selected page `page` (of NP) into stage s of
+// warp w's ring; one thread calls this.  A page id outside [0, NP) or a page-table
+// entry outside the pool is flagged and its chunk masked (t0 past every token).
+template <int STAGES, class Params>
+__device__ __forceinline__ void load_chunk(const Params& p, AttnSmem<STAGES>& a, uint8_t* ring, int w, int s,
+                                           int page, int chunk, int NP, const int32_t* ptab, int g) {
+  const int P = p.P;
+  const bool page_ok = page >= 0 && page < NP;  // always true for the select's output
+  page = page_ok ? page : 0;
+  int phys = ptab[page];
+  int t0 = page * P + chunk * kChunkTok;
+  if (!page_ok || phys < 0 || phys >= p.num_phys) {
+    flag_error(p.err, RKV_DEVERR_PAGE_ID);
+    phys = 0;
+    t0 = INT_MAX / 2;  // every token of this chunk is masked
+  }
+  const int y = (phys * p.Hkv + g) * P + chunk * kChunkTok;
+  a.tstart[w][s] = t0;
+  uint8_t* st = ring + (w * STAGES + s) * kStageBytes;
+  mbar_arrive_expect_tx(&a.bars[w][s], kStageBytes);
+  tma_load_2d(st, &p.tmk, 0, y, &a.bars[w][s]);
+  tma_load_2d(st + kHalfBytes, &p.tmk, 64, y, &a.bars[w][s]);
+  tma_load_2d(st + 2 * kHalfBytes, &p.tmv, 0, y, &a.bars[w][s]);
+  tma_load_2d(st + 3 * kHalfBytes, &p.tmv, 64, y, &a.bars[w][s]);
+}
+
+// bars_ready: the ring's barriers were initialised by the caller.  pre_issued: the
+// caller already issued every warp's first STAGES chunks except warp kAtWarps - 1's
+// last one.
 template <int STAGES, bool kTok = false, class Params = HsaParams, int kG = 0>
 __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_t* ptab, int b, int g, int n,
                                int it0, int it1, uint8_t* ring, AttnSmem<STAGES>& a, int new_pos,
-                               const uint8_t* new_kv, int* timed_out_out) {
+                               const uint8_t* new_kv, int* timed_out_out, bool bars_ready = false,
+                               bool pre_issued = false) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = p.P, G = kG > 0 ? kG : p.G;  // kG > 0: the group size known at compile time
   // page sizes are powers of two (16, 32 or 64, checked on the host): shifts, not divisions
@@ -328,7 +358,7 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
     qa0[kk] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * q4) : 0u;
     qa2[kk] = hv ? *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * q4) : 0u;
   }
-  if (lane == 0) {
+  if (!bars_ready && lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) mbar_init(&a.bars[warp][s], 1);
     fence_mbar_init();
@@ -355,27 +385,7 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
       __syncwarp();
       return;
     }
-    int page = sel[it >> lg_cpp];
-    const int chunk = it & (cpp - 1);
-    const bool page_ok = page >= 0 && page < NP;  // always true for the select's output
-    page = page_ok ? page : 0;
-    int phys = ptab[page];
-    int t0 = page * P + chunk * kChunkTok;
-    if (!page_ok || phys < 0 || phys >= p.num_phys) {
-      flag_error(p.err, RKV_DEVERR_PAGE_ID);
-      phys = 0;
-      t0 = INT_MAX / 2;  // every token of this chunk is masked
-    }
-    const int y = (phys * p.Hkv + g) * P + chunk * kChunkTok;
-    if (lane == 0) {
-      a.tstart[warp][s] = t0;
-      uint8_t* st = wbuf + s * kStageBytes;
-      mbar_arrive_expect_tx(&a.bars[warp][s], kStageBytes);
-      tma_load_2d(st, &p.tmk, 0, y, &a.bars[warp][s]);
-      tma_load_2d(st + kHalfBytes, &p.tmk, 64, y, &a.bars[warp][s]);
-      tma_load_2d(st + 2 * kHalfBytes, &p.tmv, 0, y, &a.bars[warp][s]);
-      tma_load_2d(st + 3 * kHalfBytes, &p.tmv, 64, y, &a.bars[warp][s]);
-    }
+    if (lane == 0) load_chunk<STAGES>(p, a, ring, warp, s, sel[it >> lg_cpp], it & (cpp - 1), NP, ptab, g);
     __syncwarp();
   };
 
@@ -385,7 +395,8 @@ __device__ CtaPart* attend_cta(const Params& p, const int32_t* sel, const int32_
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
   const int pre = min(nj, STAGES);
-  for (int j = 0; j < pre; ++j) issue(j);
+  for (int j = 0; j < pre; ++j)
+    if (!pre_issued || (warp == kAtWarps - 1 && j == STAGES - 1)) issue(j);
   if constexpr (kTok)  // one cp.async group per ring slot, empty or not, so waits count evenly
     for (int j = pre; j < STAGES; ++j) cp_async_commit();
   int issued = pre, consumed = 0, timed_out = 0;
@@ -620,6 +631,8 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   if (tid == 0) {
     mbar_init(&sbar, 1);
     mbar_init(&pbar, 1);
+    for (int w = 0; w < kAtWarps; ++w)  // the attention ring's (the top-k2 may fill it)
+      for (int st = 0; st < STAGES; ++st) mbar_init(&as.bars[w][st], 1);
     fence_mbar_init();
   }
   // The launch may overlap the end of the previous kernel on the stream (programmatic
@@ -875,14 +888,33 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // attention.  (The key array is 16-byte aligned and followed by the list, the
   // page-table row and the inbox, so the select's reads up to 512 entries past NP stay
   // inside this CTA's shared memory.)
+  // The histogram select also starts the attention: as the compaction places each
+  // selected page, the thread placing it issues the TMA loads of the page's chunks that
+  // fall in this CTA's first ring fill (every warp's first STAGES chunks but the last
+  // stage of the last warp, which holds the select's scratch meanwhile).
   const int k = min(p.k2[b], NP);
-  TopkSmem<kThreads>& tks = *reinterpret_cast<TopkSmem<kThreads>*>(ring);
+  const int cpp = P >> 4;  // 16-token chunks a page
+  const int items = k * cpp;
+  const int ips = div_c(items + C - 1);
+  const int it0 = min(items, rank * ips), it1 = min(items, it0 + ips);
+  static_assert(sizeof(TopkSmem<kThreads>) <= kStageBytes, "the select's scratch fits one ring stage");
+  TopkSmem<kThreads>& tks =
+      *reinterpret_cast<TopkSmem<kThreads>*>(ring + (kAtWarps * STAGES - 1) * kStageBytes);
+  if (!mbar_wait(&pbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);  // the page-table row, for the loads
+  bool pre_issued = false;
   if (k >= NP) {
     for (int i = tid; i < NP; i += kThreads) sel[i] = i;
   } else if constexpr (kMode == kStepShortRank) {  // NP <= max_pages <= kThreads
     topk_rank<kThreads, 1>(keys, NP, k, tks, sel);
   } else {
-    topk_flat<kThreads>(keys, NP, k, tks, sel);
+    topk_flat<kThreads>(keys, NP, k, tks, sel, [&](int o, int page) {
+      for (int c = 0; c < cpp; ++c) {
+        const int rel = o * cpp + c - it0;
+        if (rel >= 0 && o * cpp + c < it1 && rel < kAtWarps * STAGES - 1)
+          load_chunk<STAGES>(p, as, ring, rel & (kAtWarps - 1), rel / kAtWarps, page, c, NP, ptab, g);
+      }
+    });
+    pre_issued = true;
   }
   if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;
   __syncthreads();
@@ -892,19 +924,16 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
     if (tid == 0 && k < p.sel_pages_stride) user_pages[k] = -1;
   }
   fence_proxy_async_smem();  // generic writes to the region before the attention's TMA loads
-  if (!mbar_wait(&pbar, 0)) flag_error(p.err, RKV_DEVERR_TIMEOUT);
   __syncthreads();
 
   // the next kernel on the stream may start launching its CTAs into the slots this one
   // frees (it waits for this grid's completion before touching memory)
   grid_launch_dependents();
   // 7. attention over this CTA's share of the selected chunks
-  const int items = k * (P / kChunkTok);
-  const int ips = div_c(items + C - 1);
-  const int it0 = min(items, rank * ips), it1 = min(items, it0 + ips);
   int to = 0;
   const CtaPart* part =
-      attend_cta<STAGES, false, Params, kG>(p, sel, ptab, b, g, n, it0, it1, ring, as, do_append ? n0 : -1, new_kv, &to);
+      attend_cta<STAGES, false, Params, kG>(p, sel, ptab, b, g, n, it0, it1, ring, as, do_append ? n0 : -1, new_kv, &to,
+                                            true, pre_issued);
 
   // 8. each head's partial state goes to the CTA that finishes the head (h % C), slot
   // [rank][h / C] of its inbox (h = j C + r)
