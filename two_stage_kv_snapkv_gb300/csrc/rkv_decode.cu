@@ -888,12 +888,12 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   // attention.  (The key array is 16-byte aligned and followed by the list, the
   // page-table row and the inbox, so the select's reads up to 512 entries past NP stay
   // inside this CTA's shared memory.)
-  // The histogram select also starts the attention: as the compaction places each
-  // selected page, the thread placing it issues the TMA loads of the page's chunks that
-  // fall in this CTA's first ring fill (every warp's first STAGES chunks but the last
-  // stage of the last warp, which holds the select's scratch meanwhile).
+  // After the histogram select the CTA's first ring fill is issued at once, one chunk a
+  // thread, before the list's other uses.  The select's scratch lives in the ring's
+  // last stage, which its warp fills with the rest of the attention's loads.
   const int k = min(p.k2[b], NP);
   const int cpp = P >> 4;  // 16-token chunks a page
+  const int warp_id = tid >> 5;
   const int items = k * cpp;
   const int ips = div_c(items + C - 1);
   const int it0 = min(items, rank * ips), it1 = min(items, it0 + ips);
@@ -907,13 +907,14 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   } else if constexpr (kMode == kStepShortRank) {  // NP <= max_pages <= kThreads
     topk_rank<kThreads, 1>(keys, NP, k, tks, sel);
   } else {
-    topk_flat<kThreads>(keys, NP, k, tks, sel, [&](int o, int page) {
-      for (int c = 0; c < cpp; ++c) {
-        const int rel = o * cpp + c - it0;
-        if (rel >= 0 && o * cpp + c < it1 && rel < kAtWarps * STAGES - 1)
-          load_chunk<STAGES>(p, as, ring, rel & (kAtWarps - 1), rel / kAtWarps, page, c, NP, ptab, g);
-      }
-    });
+    topk_flat<kThreads>(keys, NP, k, tks, sel);
+    // the first ring fill at once, lane s of warp w issuing warp w's chunk s (but the
+    // last stage of the last warp: the select's scratch, written through the generic
+    // proxy, is refilled only after the fence and barrier below)
+    const int rel = warp_id + kAtWarps * (tid & 31);
+    if ((tid & 31) < STAGES && rel < kAtWarps * STAGES - 1 && it0 + rel < it1)
+      load_chunk<STAGES>(p, as, ring, warp_id, tid & 31, sel[(it0 + rel) >> (lg_p - 4)], (it0 + rel) & (cpp - 1), NP,
+                         ptab, g);
     pre_issued = true;
   }
   if (rank == 0 && p.sel_channels && tid < 128) p.sel_channels[(size_t)unit * 128 + tid] = tid < k1 ? cs.chan[tid] : -1;

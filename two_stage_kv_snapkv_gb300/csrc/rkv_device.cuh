@@ -483,15 +483,11 @@ __device__ void topk_adaptive(int n, int k, KeyFn key, TopkSmem<NT>& ts, int32_t
 // index-ordered compaction by one block scan); every thread runs the same trip counts.
 // Boundary candidates are gathered by a block scan instead of shared atomics, and the
 // gather and the compaction visit only the keys they keep (bit masks of a thread's at
-// most 32 keys).  on_taken(o, i) runs in the thread that writes out[o] = i.  Needs n <= 32 NT, with `keys` 16-byte aligned and readable up to
+// most 32 keys).  Needs n <= 32 NT, with `keys` 16-byte aligned and readable up to
 // NT * S entries (entries from n on are ignored).  For 1 <= k < n; every thread of the
 // block calls this.
-struct NoTakenHook {
-  __device__ void operator()(int, int) const {}
-};
-template <int NT, class OnTaken = NoTakenHook>
-__device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out,
-                          OnTaken on_taken = {}) {
+template <int NT>
+__device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, int32_t* out) {
   static_assert(NT % 32 == 0 && kTkBins % NT == 0 && (kTkBins / NT) % 4 == 0, "bins must split into uint4s");
   constexpr unsigned FULL = 0xffffffffu;
   constexpr int NW = NT / 32;
@@ -715,10 +711,7 @@ __device__ void topk_flat(const uint32_t* keys, int n, int k, TopkSmem<NT>& ts, 
     any &= any - 1;
     const unsigned isb = (bm >> e) & 1u;
     const bool take = (isb ^ 1u) | (unsigned)(bseen < need);
-    if (take & (o < k)) {
-      out[o] = i0 + e;
-      on_taken(o, i0 + e);  // the caller may start using list entry o now
-    }
+    if (take & (o < k)) out[o] = i0 + e;
     o += take;
     bseen += (int)isb;
   }
