@@ -880,17 +880,17 @@ __global__ void __launch_bounds__(kThreads, 2) hsa_step_kernel(const __grid_cons
   int arrivals = -1;
   if (do_append && rank == 0 && tid == 0) arrivals = atomicAdd(&p.sync[b], 1);
 
-  // 6. top-k2: every CTA runs the same select over all keys (no exchange needed): up to
-  // 128 pages by counting each key's rank, beyond that the histogram select written
-  // without divergent per-key branches (on GB300 it took 2.6 us over 1212 keys where
-  // a form with per-key branches took 4.3 us, both with warm instruction caches).  The list
-  // is ascending.  The scratch lives in the region, free between the scoring and the
-  // attention.  (The key array is 16-byte aligned and followed by the list, the
-  // page-table row and the inbox, so the select's reads up to 512 entries past NP stay
-  // inside this CTA's shared memory.)
-  // After the histogram select the CTA's first ring fill is issued at once, one chunk a
-  // thread, before the list's other uses.  The select's scratch lives in the ring's
-  // last stage, which its warp fills with the rest of the attention's loads.
+  // 6. top-k2: every CTA runs the same select over all keys (no exchange needed): by
+  // counting each key's rank when the cache holds at most 128 pages, else the histogram
+  // select written without divergent per-key branches (on GB300 it took 2.6 us over
+  // 1212 keys where a form with per-key branches took 4.3 us, both with warm
+  // instruction caches).  The list is ascending.  The select's scratch lives in the
+  // ring's last stage (free between the scoring and the attention; that stage's warp
+  // fills it with the rest of the attention's loads).  (The key array is 16-byte
+  // aligned and followed by the list, the page-table row and the inbox, so the
+  // select's reads up to 512 entries past NP stay inside this CTA's shared memory.)
+  // After the histogram select the CTA's first ring fill is issued at once, one chunk
+  // a thread, before the list's other uses.
   const int k = min(p.k2[b], NP);
   const int cpp = P >> 4;  // 16-token chunks a page
   const int warp_id = tid >> 5;
