@@ -624,14 +624,7 @@ def run_ours(args, rank: int, world: int, dev, workload: int = 0, extras: bool =
         hk["duration_from"] = "uninstrumented decode loop graph: event time / hsa_step launches"
     dominant = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches"])
     dk = kernels[dominant]
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            tj = json.load(f)
-        ent = tj.get(str(wl.name), {}).get(dominant)
-        if ent and ent.get("source_sha") == _source_sha(ent.get("source_file", "")):
-            traffic = ent["bytes_per_launch"]
+    traffic = recorded_traffic(str(wl.name), dominant)
     roofline = dict(bound="hbm", kernel=dominant, achieved=dk["achieved_gbs"], peak=peaks["hbm_gbs"],
                     unit="GB/s", frac=(round(dk["achieved_gbs"] / peaks["hbm_gbs"], 4) if dk["achieved_gbs"] else None),
                     traffic=traffic, peak_source=peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
@@ -771,6 +764,20 @@ def _source_sha(rel: str) -> str:
         with open(path, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16] if rel else ""
+
+
+def recorded_traffic(workload: str, kernel: str, path: str = "") -> int | None:
+    """DRAM bytes per launch of `kernel` at `workload` from the committed ncu record
+    (profiles/traffic.json), or None when there is no entry or the kernel's sources
+    have changed since it was captured."""
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        ent = json.load(f).get(workload, {}).get(kernel)
+    if not ent or ent.get("source_sha") != _source_sha(ent.get("source_file", "")):
+        return None
+    return ent["bytes_per_launch"]
 
 
 def run_e2e(setup: Setup, args, stream, rkv) -> dict:
